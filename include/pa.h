@@ -1,0 +1,184 @@
+/*
+ * pa.h -- C ABI of the GB300 (sm_103a) paged KV-cache library.
+ *
+ * PagedAttention keeps each sequence's K/V cache in fixed-size physical blocks
+ * of block_size tokens and reaches them through a per-sequence block table
+ * (CS349E Lecture 7 notes "KV Cache Management", §4.1; Month 2 · PagedAttention,
+ * infra learning path, §5.2). The pages name three fused GPU operations around
+ * it (CS349E Lecture 7 notes, §4.3): writing new tokens' K/V into their slots,
+ * attention that reads through the block table, and one batched copy of the
+ * blocks that copy-on-write duplicates. This header exposes those operations,
+ * plus a split (partitioned) variant of the attention for long contexts.
+ *
+ * Conventions for every call:
+ *   - Every pointer argument is device memory owned by the caller, unless the
+ *     argument says "host". The library allocates nothing and keeps no pointer
+ *     after a call returns.
+ *   - Calls are asynchronous on `stream` (0 = the legacy default stream); the
+ *     status they return reports argument checks and launch errors only.
+ *   - Arguments are checked on the host before anything is launched; a bad
+ *     argument returns PA_ERR_INVALID_ARG or PA_ERR_UNSUPPORTED and launches
+ *     nothing.
+ *   - Values that live in device memory (block ids, slots, context lengths,
+ *     copy pairs) are checked by the kernels: an out-of-range value is skipped
+ *     (never dereferenced) and recorded in a device error word that
+ *     pa_get_error() reads. The kernels never trap.
+ *   - Layouts are dense and row-major. The KV pool layout is HND:
+ *     cache[num_blocks][num_kv_heads][block_size][head_dim]; token t of a
+ *     sequence lives in physical block block_table[t / block_size], row
+ *     t % block_size. Query head h reads kv head h / (num_heads / num_kv_heads).
+ *   - q, out, key, value and the caches must be 16-byte aligned.
+ *   - Supported: head_dim 64 or 128; block_size 16 or 32; num_heads /
+ *     num_kv_heads from 1 to 8; element types PA_F32, PA_F16, PA_BF16.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1, /* null / misaligned pointer, negative or inconsistent size */
+  PA_ERR_UNSUPPORTED = 2, /* valid but outside what this build implements */
+  PA_ERR_OUT_OF_RANGE = 3, /* (pa_get_error) a device-side value was out of range */
+  PA_ERR_CUDA = 4          /* a CUDA runtime call or launch failed */
+} pa_status;
+
+typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 } pa_dtype;
+
+/* Bits of the device error word returned by pa_get_error(). */
+#define PA_DEVERR_BLOCK_ID 1u /* a block-table entry outside [0, num_blocks) was skipped */
+#define PA_DEVERR_SLOT 2u     /* a slot outside [-1, num_blocks * block_size) was skipped */
+#define PA_DEVERR_CONTEXT 4u  /* a context length < 0 or beyond the table / workspace was clamped */
+#define PA_DEVERR_PAIR 8u     /* a copy pair with an id outside [0, num_blocks) was skipped */
+#define PA_DEVERR_TIMEOUT 16u /* an internal wait ran past its limit; the results are undefined */
+
+/*
+ * Write each new token's K and V into the cache slot the block manager chose
+ * for it (CS349E Lecture 7 notes §4.1 and §4.3: the slot is a row of a physical
+ * block; CMU 15-779 Lecture 16 notes §3.3: new tokens fill the last block).
+ *
+ *   key, value    [num_tokens][num_kv_heads][head_dim], element type `dtype`
+ *   k_cache,
+ *   v_cache       [num_blocks][num_kv_heads][block_size][head_dim], `dtype`
+ *   slot_mapping  int64 [num_tokens]; token t goes to block slot / block_size,
+ *                 row slot % block_size; a negative slot means "skip" (padding)
+ *
+ * The copy is bit-exact. Slots must be distinct (two tokens writing the same
+ * slot race). Slots >= num_blocks * block_size are skipped and recorded.
+ */
+pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
+                               const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                               int head_dim, int block_size, int64_t num_blocks, pa_dtype dtype,
+                               cudaStream_t stream);
+
+/*
+ * Decode attention over a paged KV cache: for every sequence s and query head h
+ * (Month 2 · PagedAttention §2.1 and §5.4; CS349E Lecture 7 notes §4.2)
+ *
+ *   out[s][h] = sum_{t < context_lens[s]} softmax_t(scale * q[s][h] . K_s[t]) V_s[t]
+ *
+ * with K_s[t] = k_cache[block_tables[s][t / block_size]][h / group][t % block_size]
+ * and group = num_heads / num_kv_heads.
+ *
+ *   out           [num_seqs][num_heads][head_dim], element type `out_dtype`
+ *                 (`dtype` or PA_F32; accumulation is always fp32)
+ *   q             [num_seqs][num_heads][head_dim], `dtype`
+ *   block_tables  int32 [num_seqs][max_blocks_per_seq]; only the first
+ *                 ceil(context_lens[s] / block_size) entries of a row are read
+ *   context_lens  int32 [num_seqs]; the new token is included (it must already
+ *                 be in the cache). 0 gives an all-zero output row.
+ *
+ * Context lengths beyond max_blocks_per_seq * block_size are clamped and recorded.
+ */
+pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                    int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                    int64_t num_blocks, float scale, pa_dtype dtype, pa_dtype out_dtype,
+                    cudaStream_t stream);
+
+/*
+ * Workspace size for pa_decode_split: with P = max(1, ceil(max_context_len /
+ * partition_tokens)), it holds
+ *   o  float [num_seqs][num_heads][P][head_dim]   normalised partial outputs
+ *   m  float [num_seqs][num_heads][P]             partition max score, base-2 units
+ *                                                 (scale * q . k * log2(e))
+ *   l  float [num_seqs][num_heads][P]             sum of 2^(score - m) over the partition
+ * each section starting on a 256-byte boundary, in that order. Returns 0 for
+ * invalid sizes.
+ */
+size_t pa_decode_split_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_context_len,
+                                       int partition_tokens);
+
+/*
+ * Decode attention for long contexts, in two launches on `stream`:
+ *   1. every (sequence, kv head, partition of partition_tokens tokens) is an
+ *      independent work item that writes its partition's softmax statistics and
+ *      normalised partial output into `workspace` (layout above);
+ *   2. a reduce kernel merges the partitions of each (sequence, head) with
+ *      log-sum-exp weights: M = max_p m_p, w_p = l_p 2^(m_p - M),
+ *      out = sum_p w_p o_p / sum_p w_p -- the merge rule under which blockwise
+ *      attention equals attention over the whole context (CMU 15-779 Lecture 16
+ *      notes §3.3).
+ * Arguments as pa_decode, plus:
+ *   max_context_len   host int >= every context length (sizes the workspace;
+ *                     longer contexts are clamped and recorded)
+ *   partition_tokens  a positive multiple of block_size
+ *   workspace         device scratch of at least workspace_bytes =
+ *                     pa_decode_split_workspace_bytes(...), 16-byte aligned,
+ *                     owned by the caller; its contents on entry are ignored and
+ *                     after return hold the partition results
+ * num_seqs may be at most 2048.
+ */
+pa_status pa_decode_split(void* out, const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_tables, int max_blocks_per_seq,
+                          const int32_t* context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                          int head_dim, int block_size, int64_t num_blocks, float scale, pa_dtype dtype,
+                          pa_dtype out_dtype, int max_context_len, int partition_tokens, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Batched copy-on-write block copies (CS349E Lecture 7 notes §5.1 and §4.3: a
+ * sample about to write into a shared block first gets its own copy; all copies
+ * pending for a step go in one launch). For every pair p and every layer l:
+ *   k_caches[l][block_pairs[p][1]] = k_caches[l][block_pairs[p][0]]   (all heads, rows)
+ *   v_caches[l][block_pairs[p][1]] = v_caches[l][block_pairs[p][0]]
+ *
+ *   k_caches, v_caches  HOST arrays of num_layers device pointers, each a pool
+ *                       [num_blocks][num_kv_heads][block_size][head_dim] of `dtype`
+ *   block_pairs         int64 [num_pairs][2] (src, dst)
+ *
+ * The copy is bit-exact. Destinations must be distinct and no destination may
+ * also be a source (the copies run in parallel). Pairs with an id outside
+ * [0, num_blocks) are skipped and recorded.
+ */
+pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers,
+                         const int64_t* block_pairs, int num_pairs, int num_kv_heads, int head_dim,
+                         int block_size, int64_t num_blocks, pa_dtype dtype, cudaStream_t stream);
+
+/*
+ * Read and clear the calling device's error word (PA_DEVERR_* bits) after the
+ * work already queued on `stream` has finished. *error_bits (host) receives the
+ * bits. Returns PA_ERR_OUT_OF_RANGE when any bit was set, PA_OK otherwise. It
+ * synchronises `stream`.
+ */
+pa_status pa_get_error(uint32_t* error_bits, cudaStream_t stream);
+
+/* A static, human-readable name for a status. */
+const char* pa_status_string(pa_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

@@ -1,0 +1,201 @@
+"""GB300 paged KV-cache library: Python binding of the C ABI in ``include/pa.h``.
+
+The functions below carry the C entry points' names and only marshal
+arguments (shapes, dtypes, data pointers, the current CUDA stream); every step
+of the computation runs in the CUDA kernels of ``libpa.so``. There is no CPU
+fallback: if the library is missing or cannot load, every call raises.
+
+Tensors are ``torch`` CUDA tensors in the layouts the header documents:
+
+* ``q``, ``out``                 ``[num_seqs, num_heads, head_dim]``
+* ``k_cache``, ``v_cache``       ``[num_blocks, num_kv_heads, block_size, head_dim]``
+* ``block_tables``               int32 ``[num_seqs, max_blocks_per_seq]``
+* ``context_lens``               int32 ``[num_seqs]``
+* ``key``, ``value``             ``[num_tokens, num_kv_heads, head_dim]``
+* ``slot_mapping``               int64 ``[num_tokens]``
+* ``block_pairs``                int64 ``[num_pairs, 2]``
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "PAError", "library", "library_path", "pa_reshape_and_cache", "pa_decode", "pa_decode_split",
+    "pa_decode_split_workspace_bytes", "pa_copy_blocks", "pa_get_error", "pa_version",
+    "PA_DEVERR_BLOCK_ID", "PA_DEVERR_SLOT", "PA_DEVERR_CONTEXT", "PA_DEVERR_PAIR", "PA_DEVERR_TIMEOUT",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "libpa.so")
+
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_OUT_OF_RANGE, PA_ERR_CUDA = range(5)
+PA_F32, PA_F16, PA_BF16 = 0, 1, 2
+PA_DEVERR_BLOCK_ID, PA_DEVERR_SLOT, PA_DEVERR_CONTEXT, PA_DEVERR_PAIR, PA_DEVERR_TIMEOUT = 1, 2, 4, 8, 16
+
+_lib = None
+
+
+class PAError(RuntimeError):
+    def __init__(self, func, status, detail=""):
+        names = {1: "invalid argument", 2: "unsupported configuration", 3: "device-side value out of range",
+                 4: "CUDA error"}
+        super().__init__(f"{func}: {names.get(status, status)}{(' (' + detail + ')') if detail else ''}")
+        self.status = status
+
+
+def library():
+    """Load ``libpa.so`` (raises if it is absent: build it with ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(library_path):
+        raise PAError("load", PA_ERR_CUDA, f"{library_path} not built")
+    lib = ctypes.CDLL(library_path)
+    P, I, I64, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    lib.pa_reshape_and_cache.argtypes = [P, P, P, P, P, I, I, I, I, I64, I, P]
+    lib.pa_decode.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I64, F, I, I, P]
+    lib.pa_decode_split_workspace_bytes.argtypes = [I, I, I, I, I]
+    lib.pa_decode_split_workspace_bytes.restype = SZ
+    lib.pa_decode_split.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I64, F, I, I, I, I, P, SZ, P]
+    lib.pa_copy_blocks.argtypes = [P, P, I, P, I, I, I, I, I64, I, P]
+    lib.pa_get_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), P]
+    lib.pa_status_string.argtypes = [I]
+    lib.pa_status_string.restype = ctypes.c_char_p
+    lib.pa_version.argtypes = []
+    for f in ("pa_reshape_and_cache", "pa_decode", "pa_decode_split", "pa_copy_blocks", "pa_get_error",
+              "pa_version"):
+        getattr(lib, f).restype = I
+    _lib = lib
+    return lib
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t):
+    torch = _torch()
+    codes = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16}
+    if t.dtype not in codes:
+        raise PAError("dtype", PA_ERR_UNSUPPORTED, str(t.dtype))
+    return codes[t.dtype]
+
+
+def _stream(stream):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _need(cond, func, what):
+    if not cond:
+        raise PAError(func, PA_ERR_INVALID_ARG, what)
+
+
+def _dev(func, *ts):
+    for t in ts:
+        _need(t.is_cuda and t.is_contiguous(), func, "tensors must be contiguous CUDA tensors")
+
+
+def _check(func, status):
+    if status != PA_OK:
+        raise PAError(func, status)
+
+
+def pa_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, stream=None):
+    """Write each new token's K/V into ``k_cache`` / ``v_cache`` at its slot (negative slot: skip)."""
+    f = "pa_reshape_and_cache"
+    torch = _torch()
+    _dev(f, key, value, k_cache, v_cache, slot_mapping)
+    _need(slot_mapping.dtype == torch.int64, f, "slot_mapping must be int64")
+    _need(key.dtype == value.dtype == k_cache.dtype == v_cache.dtype, f, "dtype mismatch")
+    N, G, d = key.shape
+    nb, G2, B, d2 = k_cache.shape
+    _need(value.shape == key.shape and v_cache.shape == k_cache.shape and G2 == G and d2 == d, f, "shapes")
+    _need(slot_mapping.shape == (N,), f, "slot_mapping shape")
+    _check(f, library().pa_reshape_and_cache(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
+                                             _ptr(slot_mapping), N, G, d, B, nb, _dtype_code(key),
+                                             _stream(stream)))
+
+
+def _decode_args(f, out, q, k_cache, v_cache, block_tables, context_lens):
+    torch = _torch()
+    _dev(f, out, q, k_cache, v_cache, block_tables, context_lens)
+    _need(block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32, f,
+          "block_tables and context_lens must be int32")
+    _need(q.dtype == k_cache.dtype == v_cache.dtype, f, "q / cache dtype mismatch")
+    S, H, d = q.shape
+    nb, G, B, d2 = k_cache.shape
+    _need(v_cache.shape == k_cache.shape and d2 == d and out.shape == q.shape, f, "shapes")
+    _need(block_tables.dim() == 2 and block_tables.shape[0] == S and context_lens.shape == (S,), f,
+          "table shapes")
+    return S, H, G, d, B, nb, int(block_tables.shape[1])
+
+
+def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, stream=None):
+    """``out[s, h] = softmax(scale * q[s, h] K_s^T) V_s`` over each sequence's paged context."""
+    f = "pa_decode"
+    S, H, G, d, B, nb, maxb = _decode_args(f, out, q, k_cache, v_cache, block_tables, context_lens)
+    _check(f, library().pa_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                  maxb, _ptr(context_lens), S, H, G, d, B, nb, float(scale),
+                                  _dtype_code(q), _dtype_code(out), _stream(stream)))
+
+
+def pa_decode_split_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len, partition_tokens):
+    return int(library().pa_decode_split_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len,
+                                                         partition_tokens))
+
+
+def pa_decode_split(out, q, k_cache, v_cache, block_tables, context_lens, scale, max_context_len,
+                    partition_tokens, workspace, stream=None):
+    """Partitioned decode (per-partition softmax, then a log-sum-exp reduce) into ``out``.
+
+    ``workspace`` is a CUDA tensor of at least ``pa_decode_split_workspace_bytes(...)`` bytes.
+    """
+    f = "pa_decode_split"
+    S, H, G, d, B, nb, maxb = _decode_args(f, out, q, k_cache, v_cache, block_tables, context_lens)
+    _dev(f, workspace)
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(f, library().pa_decode_split(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                        maxb, _ptr(context_lens), S, H, G, d, B, nb, float(scale),
+                                        _dtype_code(q), _dtype_code(out), int(max_context_len),
+                                        int(partition_tokens), _ptr(workspace), nbytes, _stream(stream)))
+
+
+def pa_copy_blocks(k_caches, v_caches, block_pairs, stream=None):
+    """For every (src, dst) pair and layer: ``cache[dst] = cache[src]`` for K and V."""
+    f = "pa_copy_blocks"
+    torch = _torch()
+    k_caches, v_caches = list(k_caches), list(v_caches)
+    _need(len(k_caches) == len(v_caches) and k_caches, f, "one K and one V pool per layer")
+    _dev(f, block_pairs, *k_caches, *v_caches)
+    _need(block_pairs.dtype == torch.int64 and block_pairs.dim() == 2 and block_pairs.shape[1] == 2, f,
+          "block_pairs must be int64 [P, 2]")
+    shape, dt = k_caches[0].shape, k_caches[0].dtype
+    for t in k_caches + v_caches:
+        _need(t.shape == shape and t.dtype == dt, f, "all pools must share shape and dtype")
+    nb, G, B, d = shape
+    L = len(k_caches)
+    karr = (ctypes.c_void_p * L)(*[t.data_ptr() for t in k_caches])
+    varr = (ctypes.c_void_p * L)(*[t.data_ptr() for t in v_caches])
+    _check(f, library().pa_copy_blocks(karr, varr, L, _ptr(block_pairs), int(block_pairs.shape[0]), G, d, B,
+                                       nb, _dtype_code(k_caches[0]), _stream(stream)))
+
+
+def pa_get_error(stream=None) -> int:
+    """Read and clear the device error word (``PA_DEVERR_*`` bits); synchronises the stream."""
+    bits = ctypes.c_uint32(0)
+    st = library().pa_get_error(ctypes.byref(bits), _stream(stream))
+    if st not in (PA_OK, PA_ERR_OUT_OF_RANGE):
+        raise PAError("pa_get_error", st)
+    return int(bits.value)
+
+
+def pa_version() -> int:
+    return int(library().pa_version())

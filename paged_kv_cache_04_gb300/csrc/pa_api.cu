@@ -1,0 +1,284 @@
+// C ABI entry points for decode attention, argument checks, TMA descriptor set-up
+// and the device error word.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "pa_decode.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+// The device error word: kernels OR PA_DEVERR_* bits into it; pa_get_error
+// reads and clears it. One copy per device that loads the library.
+__device__ unsigned g_error_word;
+
+constexpr int kMaxDevices = 64;
+struct DeviceState {
+  bool ready = false;
+  unsigned* err = nullptr;
+  int sms = 0;
+};
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+int esize(pa_dtype dt) { return dt == PA_F32 ? 4 : 2; }
+bool valid_dtype(pa_dtype dt) { return dt == PA_F32 || dt == PA_F16 || dt == PA_BF16; }
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+pa_status encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_encode) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return PA_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  *out = g_encode;
+  return PA_OK;
+}
+
+// A 2-D view of a KV pool: rows = num_blocks * num_kv_heads * block_size, each
+// head_dim elements. One TMA box is 128 bytes of a row x block_size rows, staged
+// with 128-byte swizzling.
+pa_status make_pool_map(CUtensorMap* map, const void* base, pa_dtype dt, int D, int BS, long long rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+  pa_status st = encoder(&enc);
+  if (st != PA_OK) return st;
+  const int e = esize(dt);
+  const CUtensorMapDataType t = dt == PA_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                : dt == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                               : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)D * e};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / e), (cuuint32_t)BS};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, t, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+struct DecodeArgs {
+  void* out;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  int max_blocks;
+  const int32_t* context_lens;
+  int S, H, G, D, BS;
+  long long num_blocks;
+  float scale;
+  pa_dtype dt, odt;
+};
+
+pa_status check_decode(const DecodeArgs& a) {
+  if (a.S < 0 || a.H <= 0 || a.G <= 0 || a.D <= 0 || a.BS <= 0 || a.num_blocks <= 0 || a.max_blocks <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (a.H % a.G || !valid_dtype(a.dt) || !valid_dtype(a.odt) || !std::isfinite(a.scale)) return PA_ERR_INVALID_ARG;
+  if (a.S == 0) return PA_OK;
+  if (!a.out || !a.q || !a.k_cache || !a.v_cache || !a.block_tables || !a.context_lens) return PA_ERR_INVALID_ARG;
+  if (!aligned16(a.out) || !aligned16(a.q) || !aligned16(a.k_cache) || !aligned16(a.v_cache) ||
+      (reinterpret_cast<uintptr_t>(a.block_tables) & 3u) || (reinterpret_cast<uintptr_t>(a.context_lens) & 3u))
+    return PA_ERR_INVALID_ARG;
+  if ((a.D != 64 && a.D != 128) || (a.BS != 16 && a.BS != 32) || a.H / a.G > kMaxGroup) return PA_ERR_UNSUPPORTED;
+  if (a.odt != a.dt && a.odt != PA_F32) return PA_ERR_UNSUPPORTED;
+  // TMA row coordinates are 32-bit
+  if ((long long)a.num_blocks * a.G * a.BS > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+  return PA_OK;
+}
+
+template <typename DT, typename OT, int D, int BS>
+pa_status dispatch_path(const CUtensorMap& km, const CUtensorMap& vm, const DecodeParams& p, int sms,
+                        long long items, bool split, cudaStream_t st) {
+  const bool mma = sizeof(DT) == 2 && p.group >= 4;
+  if (split) {
+    if constexpr (sizeof(DT) == 2) {
+      if (mma) return launch_decode<DT, float, D, BS, true, true>(km, vm, p, sms, items, st);
+    }
+    return launch_decode<DT, float, D, BS, false, true>(km, vm, p, sms, items, st);
+  }
+  if constexpr (sizeof(DT) == 2) {
+    if (mma) return launch_decode<DT, OT, D, BS, true, false>(km, vm, p, sms, items, st);
+  }
+  return launch_decode<DT, OT, D, BS, false, false>(km, vm, p, sms, items, st);
+}
+
+template <typename DT, typename OT>
+pa_status dispatch_shape(const CUtensorMap& km, const CUtensorMap& vm, const DecodeParams& p, int D, int BS,
+                         int sms, long long items, bool split, cudaStream_t st) {
+  if (D == 64 && BS == 16) return dispatch_path<DT, OT, 64, 16>(km, vm, p, sms, items, split, st);
+  if (D == 64 && BS == 32) return dispatch_path<DT, OT, 64, 32>(km, vm, p, sms, items, split, st);
+  if (D == 128 && BS == 16) return dispatch_path<DT, OT, 128, 16>(km, vm, p, sms, items, split, st);
+  if (D == 128 && BS == 32) return dispatch_path<DT, OT, 128, 32>(km, vm, p, sms, items, split, st);
+  return PA_ERR_UNSUPPORTED;
+}
+
+template <typename OT>
+pa_status dispatch_reduce(const DecodeParams& p, int D, cudaStream_t st) {
+  return D == 64 ? launch_lse_reduce<OT, 64>(p, st) : launch_lse_reduce<OT, 128>(p, st);
+}
+
+pa_status run_decode(const DecodeArgs& a, bool split, int partition, int max_partitions, void* ws,
+                     cudaStream_t st) {
+  unsigned* err = nullptr;
+  int sms = 0;
+  pa_status s = device_state(&err, &sms);
+  if (s != PA_OK) return s;
+  const long long rows = (long long)a.num_blocks * a.G * a.BS;
+  CUtensorMap km, vm;
+  if ((s = make_pool_map(&km, a.k_cache, a.dt, a.D, a.BS, rows)) != PA_OK) return s;
+  if ((s = make_pool_map(&vm, a.v_cache, a.dt, a.D, a.BS, rows)) != PA_OK) return s;
+
+  DecodeParams p{};
+  p.out = a.out;
+  p.q = a.q;
+  p.block_tables = a.block_tables;
+  p.context_lens = a.context_lens;
+  p.max_blocks = a.max_blocks;
+  p.block_size = a.BS;
+  p.S = a.S;
+  p.H = a.H;
+  p.G = a.G;
+  p.group = a.H / a.G;
+  p.num_blocks = a.num_blocks;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.err = err;
+  long long items = (long long)a.S * a.G;
+  if (split) {
+    p.partition = partition;
+    p.max_partitions = max_partitions;
+    const size_t o_bytes = (size_t)a.S * a.H * max_partitions * a.D * 4;
+    const size_t m_bytes = (size_t)a.S * a.H * max_partitions * 4;
+    p.ws_o = static_cast<float*>(ws);
+    p.ws_m = reinterpret_cast<float*>(static_cast<char*>(ws) + align256(o_bytes));
+    p.ws_l = reinterpret_cast<float*>(static_cast<char*>(ws) + align256(o_bytes) + align256(m_bytes));
+    items *= max_partitions;
+  }
+  switch (a.dt) {
+    case PA_BF16:
+      s = a.odt == PA_F32 ? dispatch_shape<__nv_bfloat16, float>(km, vm, p, a.D, a.BS, sms, items, split, st)
+                          : dispatch_shape<__nv_bfloat16, __nv_bfloat16>(km, vm, p, a.D, a.BS, sms, items, split, st);
+      break;
+    case PA_F16:
+      s = a.odt == PA_F32 ? dispatch_shape<__half, float>(km, vm, p, a.D, a.BS, sms, items, split, st)
+                          : dispatch_shape<__half, __half>(km, vm, p, a.D, a.BS, sms, items, split, st);
+      break;
+    default:
+      s = dispatch_shape<float, float>(km, vm, p, a.D, a.BS, sms, items, split, st);
+  }
+  if (s != PA_OK || !split) return s;
+  switch (a.odt) {
+    case PA_BF16: return dispatch_reduce<__nv_bfloat16>(p, a.D, st);
+    case PA_F16: return dispatch_reduce<__half>(p, a.D, st);
+    default: return dispatch_reduce<float>(p, a.D, st);
+  }
+}
+
+}  // namespace
+
+pa_status device_state(unsigned** err, int* num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& d = g_dev[dev];
+  if (!d.ready) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_error_word) != cudaSuccess) return PA_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+      return PA_ERR_CUDA;
+    d.err = static_cast<unsigned*>(ptr);
+    d.sms = sms;
+    d.ready = true;
+  }
+  *err = d.err;
+  *num_sms = d.sms;
+  return PA_OK;
+}
+
+}  // namespace pa
+
+extern "C" pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                               int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                               int64_t num_blocks, float scale, pa_dtype dtype, pa_dtype out_dtype,
+                               cudaStream_t stream) {
+  using namespace pa;
+  const DecodeArgs a{out,      q,         k_cache,      v_cache,  block_tables, max_blocks_per_seq,
+                     context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                     (long long)num_blocks, scale, dtype, out_dtype};
+  pa_status s = check_decode(a);
+  if (s != PA_OK || num_seqs == 0) return s;
+  return run_decode(a, false, 0, 0, nullptr, stream);
+}
+
+extern "C" size_t pa_decode_split_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_context_len,
+                                                  int partition_tokens) {
+  if (num_seqs < 0 || num_heads <= 0 || head_dim <= 0 || max_context_len < 0 || partition_tokens <= 0) return 0;
+  const long long P = std::max(1LL, ((long long)max_context_len + partition_tokens - 1) / partition_tokens);
+  const size_t rows = (size_t)num_seqs * num_heads * P;
+  return pa::align256(rows * head_dim * 4) + 2 * pa::align256(rows * 4);
+}
+
+extern "C" pa_status pa_decode_split(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                     const int32_t* block_tables, int max_blocks_per_seq,
+                                     const int32_t* context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                                     int head_dim, int block_size, int64_t num_blocks, float scale,
+                                     pa_dtype dtype, pa_dtype out_dtype, int max_context_len,
+                                     int partition_tokens, void* workspace, size_t workspace_bytes,
+                                     cudaStream_t stream) {
+  using namespace pa;
+  const DecodeArgs a{out,      q,         k_cache,      v_cache,  block_tables, max_blocks_per_seq,
+                     context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                     (long long)num_blocks, scale, dtype, out_dtype};
+  pa_status s = check_decode(a);
+  if (s != PA_OK) return s;
+  if (max_context_len < 0 || partition_tokens <= 0 || partition_tokens % block_size) return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PA_OK;
+  if (num_seqs > kSplitMaxSeqs) return PA_ERR_UNSUPPORTED;
+  const size_t need =
+      pa_decode_split_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len, partition_tokens);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < need || need == 0) return PA_ERR_INVALID_ARG;
+  const long long P = std::max(1LL, ((long long)max_context_len + partition_tokens - 1) / partition_tokens);
+  if ((long long)num_seqs * num_kv_heads * P > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+  return run_decode(a, true, partition_tokens, (int)P, workspace, stream);
+}
+
+extern "C" pa_status pa_get_error(uint32_t* error_bits, cudaStream_t stream) {
+  if (!error_bits) return PA_ERR_INVALID_ARG;
+  unsigned* err = nullptr;
+  int sms = 0;
+  pa_status s = pa::device_state(&err, &sms);
+  if (s != PA_OK) return s;
+  unsigned host = 0;
+  if (cudaMemcpyAsync(&host, err, sizeof(unsigned), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (cudaMemsetAsync(err, 0, sizeof(unsigned), stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return PA_ERR_CUDA;
+  *error_bits = host;
+  return host ? PA_ERR_OUT_OF_RANGE : PA_OK;
+}
+
+extern "C" const char* pa_status_string(pa_status status) {
+  switch (status) {
+    case PA_OK: return "ok";
+    case PA_ERR_INVALID_ARG: return "invalid argument";
+    case PA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PA_ERR_OUT_OF_RANGE: return "device-side value out of range";
+    case PA_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+extern "C" int pa_version(void) { return 100; }

@@ -1,0 +1,145 @@
+// The two kernels that keep the paged KV cache current (CS349E Lecture 7 notes,
+// §4.3: one fused write of new tokens into their block slots, one batched copy
+// of the blocks copy-on-write must duplicate). Both are pure data movement:
+// 16-byte vector loads and stores, bit-exact, bounds-checked against the pool.
+#include <algorithm>
+#include <cstdint>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+// One thread per 16-byte vector of a (token, K-or-V, kv head) row.
+__global__ void __launch_bounds__(256)
+    reshape_and_cache_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value, uint4* k_cache,
+                             uint4* v_cache, const int64_t* __restrict__ slot_mapping, int num_tokens, int G,
+                             int vpr, int BS, long long num_slots, unsigned* err) {
+  const long long total = (long long)num_tokens * 2 * G * vpr;
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int v = (int)(idx % vpr);
+    long long rest = idx / vpr;
+    const int h = (int)(rest % G);
+    rest /= G;
+    const int which = (int)(rest & 1);
+    const long long t = rest >> 1;
+    const long long slot = __ldg(slot_mapping + t);
+    if (slot < 0) continue;
+    if (slot >= num_slots) {
+      if (v == 0 && h == 0 && which == 0) atomicOr(err, kErrSlot);
+      continue;
+    }
+    const long long blk = slot / BS, row = slot - blk * BS;
+    const uint4* src = which ? value : key;
+    uint4* dst = which ? v_cache : k_cache;
+    dst[((blk * G + h) * BS + row) * vpr + v] = __ldg(src + (t * G + h) * vpr + v);
+  }
+}
+
+constexpr int kMaxLayersPerLaunch = 64;
+struct LayerPtrs {
+  uint4* k[kMaxLayersPerLaunch];
+  uint4* v[kMaxLayersPerLaunch];
+};
+
+// grid = (pairs, layers, 2): one CTA copies one K or V block of one layer.
+template <int VPT>
+__global__ void __launch_bounds__(256)
+    copy_blocks_kernel(const LayerPtrs ptrs, const int64_t* __restrict__ pairs, long long num_blocks,
+                       int vpb, unsigned* err) {
+  const long long src = __ldg(pairs + 2 * (long long)blockIdx.x);
+  const long long dst = __ldg(pairs + 2 * (long long)blockIdx.x + 1);
+  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+    if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) atomicOr(err, kErrPair);
+    return;
+  }
+  uint4* base = blockIdx.z ? ptrs.v[blockIdx.y] : ptrs.k[blockIdx.y];
+  const uint4* s = base + src * vpb;
+  uint4* d = base + dst * vpb;
+  for (int i0 = threadIdx.x; i0 < vpb; i0 += 256 * VPT) {
+    uint4 r[VPT];
+#pragma unroll
+    for (int u = 0; u < VPT; ++u) {
+      const int i = i0 + u * 256;
+      if (i < vpb) r[u] = __ldcs(s + i);
+    }
+#pragma unroll
+    for (int u = 0; u < VPT; ++u) {
+      const int i = i0 + u * 256;
+      if (i < vpb) __stcs(d + i, r[u]);
+    }
+  }
+}
+
+int esize(pa_dtype dt) { return dt == PA_F32 ? 4 : 2; }
+bool valid_dtype(pa_dtype dt) { return dt == PA_F32 || dt == PA_F16 || dt == PA_BF16; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace pa
+
+extern "C" pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
+                                          const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                                          int head_dim, int block_size, int64_t num_blocks, pa_dtype dtype,
+                                          cudaStream_t stream) {
+  using namespace pa;
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0 ||
+      !valid_dtype(dtype))
+    return PA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+  if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+    return PA_ERR_INVALID_ARG;
+  const int row_bytes = head_dim * esize(dtype);
+  if (row_bytes % 16) return PA_ERR_UNSUPPORTED;
+  unsigned* err = nullptr;
+  int sms = 0;
+  pa_status st = device_state(&err, &sms);
+  if (st != PA_OK) return st;
+  const int vpr = row_bytes / 16;
+  const long long total = (long long)num_tokens * 2 * num_kv_heads * vpr;
+  const long long want = (total + 255) / 256;
+  const unsigned grid = (unsigned)std::min<long long>(want, (long long)sms * 16);
+  reshape_and_cache_kernel<<<grid, 256, 0, stream>>>(
+      static_cast<const uint4*>(key), static_cast<const uint4*>(value), static_cast<uint4*>(k_cache),
+      static_cast<uint4*>(v_cache), slot_mapping, num_tokens, num_kv_heads, vpr, block_size,
+      (long long)num_blocks * block_size, err);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+extern "C" pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers,
+                                    const int64_t* block_pairs, int num_pairs, int num_kv_heads, int head_dim,
+                                    int block_size, int64_t num_blocks, pa_dtype dtype, cudaStream_t stream) {
+  using namespace pa;
+  if (num_layers < 0 || num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+      num_blocks <= 0 || !valid_dtype(dtype))
+    return PA_ERR_INVALID_ARG;
+  if (num_layers == 0 || num_pairs == 0) return PA_OK;
+  if (!k_caches || !v_caches || !block_pairs || (reinterpret_cast<uintptr_t>(block_pairs) & 7u))
+    return PA_ERR_INVALID_ARG;
+  for (int l = 0; l < num_layers; ++l)
+    if (!k_caches[l] || !v_caches[l] || !aligned16(k_caches[l]) || !aligned16(v_caches[l]))
+      return PA_ERR_INVALID_ARG;
+  const long long block_bytes = (long long)num_kv_heads * block_size * head_dim * esize(dtype);
+  if (block_bytes % 16 || block_bytes / 16 > (1LL << 30) || num_pairs > 0x7fffffff / 2) return PA_ERR_UNSUPPORTED;
+  unsigned* err = nullptr;
+  int sms = 0;
+  pa_status st = device_state(&err, &sms);
+  if (st != PA_OK) return st;
+  const int vpb = (int)(block_bytes / 16);
+  for (int l0 = 0; l0 < num_layers; l0 += kMaxLayersPerLaunch) {
+    const int nl = std::min(kMaxLayersPerLaunch, num_layers - l0);
+    LayerPtrs ptrs;
+    for (int i = 0; i < kMaxLayersPerLaunch; ++i) {
+      ptrs.k[i] = i < nl ? static_cast<uint4*>(k_caches[l0 + i]) : nullptr;
+      ptrs.v[i] = i < nl ? static_cast<uint4*>(v_caches[l0 + i]) : nullptr;
+    }
+    dim3 grid((unsigned)num_pairs, (unsigned)nl, 2);
+    copy_blocks_kernel<8><<<grid, 256, 0, stream>>>(ptrs, block_pairs, (long long)num_blocks, vpb, err);
+    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  }
+  return PA_OK;
+}

@@ -1,0 +1,723 @@
+// Paged decode attention: one query token per sequence attends to its whole
+// context, whose K/V rows sit in fixed-size physical blocks reached through a
+// per-sequence block table.
+//
+// What is computed (Month 2 · PagedAttention, infra learning path, §2.1 and
+// §5.4; CS349E Lecture 7 notes, §4.2): for sequence s, query head h and kv head
+// kv = h / (H / G),
+//     out[s][h] = sum_t softmax_t(scale * q[s][h] . K[s][t]) V[s][t],  t < ctx[s],
+// where K[s][t] = k_cache[block_tables[s][t / B]][kv][t % B] (HND pool layout).
+// Blockwise evaluation with an online softmax merge gives the same result as a
+// contiguous cache (CMU 15-779 Lecture 16 notes, §3.3).
+//
+// Design (one launch, persistent CTAs):
+//   * a work item is (sequence, kv head[, partition]); every CTA walks a fixed
+//     list of items, dealt out in a serpentine order over the grid, longest
+//     contexts first (sequences sorted by 512-token length buckets);
+//   * the item's blocks are dealt round-robin to the CTA's W warps; each warp
+//     keeps R (K, V) tile stages of its own in shared memory, filled by TMA
+//     tensor copies with 128-byte swizzling and completed on an mbarrier, so a
+//     warp always has R - 1 blocks in flight while it computes one;
+//   * a KV block is read once for all H / G query heads of its kv head: with a
+//     group of >= 4 heads on 16-bit data the step is a small dense contraction
+//     and runs on mma.sync m16n8k16 (tokens x heads for q K^T, d x heads for
+//     P V); otherwise (MHA, fp32) lanes split head_dim and use FFMA;
+//   * the softmax is online, in fp32, base 2, with warp shuffles for the block
+//     maxima; at the end of an item the W warps' partial (max, sum, output)
+//     triples are merged through shared memory;
+//   * split mode writes the normalised partial output and its (max, sum) to a
+//     caller workspace; a second kernel merges partitions with log-sum-exp
+//     weights.
+#pragma once
+
+#include "pa_device.cuh"
+
+namespace pa {
+
+constexpr int kMaxGroup = 8;         // query heads per kv head
+constexpr int kSortMaxSeqs = 1024;   // longest-first ordering up to this batch size
+constexpr int kSplitMaxSeqs = 2048;  // split mode keeps per-sequence offsets in shared memory
+constexpr int kLenBucketShift = 9;   // sort key: context length / 512
+
+struct DecodeParams {
+  void* out;                    // [S][H][D] out dtype (non-split)
+  const void* q;                // [S][H][D]
+  const int32_t* block_tables;  // [S][max_blocks]
+  const int32_t* context_lens;  // [S]
+  int max_blocks;
+  int block_size;
+  int S, H, G, group;
+  long long num_blocks;
+  float scale_log2;             // scale * log2(e)
+  int partition;                // split mode: tokens per partition (multiple of the block size)
+  int max_partitions;           // split mode: workspace partition dimension
+  float* ws_o;                  // [S][H][P][D]
+  float* ws_m;                  // [S][H][P]  (max score, base-2 units)
+  float* ws_l;                  // [S][H][P]
+  unsigned* err;
+};
+
+struct SmemLayout {
+  unsigned stage_bytes, bars_off, merge_off, q_off, sched_off, misc_off, total;
+};
+
+__host__ __device__ inline unsigned round_up(unsigned x, unsigned a) { return (x + a - 1) / a * a; }
+
+// Shared-memory map, computed identically on the host (launch size) and device.
+__host__ __device__ inline SmemLayout make_layout(int W, int R, int D, int BS, int esize, int group, bool vec,
+                                                  bool split, int S) {
+  SmemLayout L;
+  L.stage_bytes = 2u * BS * D * esize;
+  unsigned off = W * R * L.stage_bytes;
+  L.bars_off = off;
+  off += W * R * 8;
+  off = round_up(off, 16);
+  L.merge_off = off;
+  off += W * group * D * 4 + W * kMaxGroup * 2 * 4;
+  L.q_off = off;
+  if (vec) off += W * group * D * 4;
+  L.sched_off = off;
+  if (split)
+    off += (2 * S + 1) * 4;
+  else if (S <= kSortMaxSeqs)
+    off += 2 * S * 4;
+  off = round_up(off, 16);
+  L.misc_off = off;
+  off += 16;
+  L.total = off + 1024;  // slack to align the dynamic window to 1024 bytes
+  return L;
+}
+
+template <typename DT, int D, int BS, bool MMA>
+struct StageCfg {
+  static constexpr int E = sizeof(DT);
+  static constexpr int kStage = 2 * BS * D * E;
+  static constexpr int W = 4;
+  static constexpr int R = kStage <= 4096 ? 4 : (kStage <= 16384 ? 3 : 1);
+};
+
+struct Item {
+  int s, kv, t0, t1, part;
+};
+
+// Context length of sequence s, clamped to what the table (and, in split mode,
+// the workspace) can describe; out-of-range values are recorded.
+__device__ __forceinline__ int clamp_ctx(const DecodeParams& p, int s, bool split) {
+  int c = __ldg(p.context_lens + s);
+  long long lim = (long long)p.max_blocks * p.block_size;
+  if (split) {
+    long long lp = (long long)p.max_partitions * p.partition;
+    lim = lp < lim ? lp : lim;
+  }
+  if (c < 0 || c > lim) {
+    atomicOr(p.err, kErrContext);
+    c = c < 0 ? 0 : (int)lim;
+  }
+  return c;
+}
+
+template <bool SPLIT>
+struct Schedule {
+  const int* ctx;    // clamped context lengths (shared memory) or nullptr
+  const int* aux;    // order[] (decode) or pstart[] (split)
+  int num_items;
+
+  __device__ __forceinline__ int seq_ctx(const DecodeParams& p, int s, int BS) const {
+    return ctx ? ctx[s] : clamp_ctx(p, s, SPLIT);
+  }
+
+  // k-th item of this CTA (serpentine deal over the grid).
+  __device__ __forceinline__ bool get(const DecodeParams& p, int BS, int k, Item& it) const {
+    const int pos = (k & 1) ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x;
+    const long long i = (long long)k * gridDim.x + pos;
+    if (i >= num_items) return false;
+    const int ii = (int)i;
+    it.kv = ii % p.G;
+    const int qi = ii / p.G;
+    if (SPLIT) {
+      int lo = 0, hi = p.S - 1;  // last s with pstart[s] <= qi
+      while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (aux[mid] <= qi) lo = mid; else hi = mid - 1;
+      }
+      it.s = lo;
+      it.part = qi - aux[lo];
+      const int c = ctx[lo];
+      it.t0 = it.part * p.partition;
+      it.t1 = min(it.t0 + p.partition, c);
+    } else {
+      it.s = aux ? aux[qi] : qi;
+      it.part = 0;
+      it.t0 = 0;
+      it.t1 = seq_ctx(p, it.s, BS);
+    }
+    return true;
+  }
+};
+
+template <typename DT, typename OT, int D, int BS, bool MMA, bool SPLIT>
+__global__ void __launch_bounds__(StageCfg<DT, D, BS, MMA>::W * 32)
+    paged_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                        const DecodeParams p) {
+  using Cfg = StageCfg<DT, D, BS, MMA>;
+  constexpr int W = Cfg::W, R = Cfg::R, E = Cfg::E;
+  constexpr int TILE = BS * D * E;
+  constexpr int NCH = D * E / 16;     // 16-byte chunks per row
+  constexpr int NREG = D * E / 128;   // 128-byte column regions (one TMA box each)
+  constexpr int BOX_X = 128 / E;
+  static_assert(NREG >= 1 && D * E % 128 == 0, "head_dim * element size must be a multiple of 128 bytes");
+  static_assert(!MMA || (sizeof(DT) == 2 && BS % 16 == 0 && D % 16 == 0), "mma path needs 16-bit data");
+
+  extern __shared__ uint8_t smem_raw[];
+  // TMA 128-byte swizzling needs 1024-byte aligned destinations: align the shared-window offset.
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const SmemLayout L = make_layout(W, R, D, BS, E, p.group, !MMA, SPLIT, p.S);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars_off);
+  float* mrg_o = reinterpret_cast<float*>(smem + L.merge_off);        // [W][group][D]
+  float* mrg_ml = mrg_o + W * p.group * D;                             // [W][kMaxGroup][2]
+  float* qs_all = reinterpret_cast<float*>(smem + L.q_off);            // [W][group][D] (vector path)
+  int* sched = reinterpret_cast<int*>(smem + L.sched_off);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc_off);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x, nthreads = W * 32;
+
+  if (tid == 0) {
+    for (int i = 0; i < W * R; ++i) mbar_init(&bars[i], 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (tid == 32) {
+    prefetch_tensormap(&kmap);
+    prefetch_tensormap(&vmap);
+  }
+
+  // ---- schedule tables -----------------------------------------------------
+  Schedule<SPLIT> sch;
+  sch.ctx = nullptr;
+  sch.aux = nullptr;
+  if (SPLIT) {
+    int* ctxs = sched;
+    int* pstart = sched + p.S;
+    for (int s = tid; s < p.S; s += nthreads) ctxs[s] = clamp_ctx(p, s, true);
+    __syncthreads();
+    if (warp == 0) {
+      // exclusive scan of ceil(ctx / partition) over sequences, lane-chunked
+      const int per = (p.S + 31) / 32;
+      const int b = lane * per, e = min(p.S, b + per);
+      int local = 0;
+      for (int s = b; s < e; ++s) local += (ctxs[s] + p.partition - 1) / p.partition;
+      int incl = local;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      int run = incl - local;
+      for (int s = b; s < e; ++s) {
+        pstart[s] = run;
+        run += (ctxs[s] + p.partition - 1) / p.partition;
+      }
+      if (lane == 31) pstart[p.S] = incl;
+    }
+    __syncthreads();
+    sch.ctx = ctxs;
+    sch.aux = pstart;
+    sch.num_items = pstart[p.S] * p.G;
+  } else {
+    sch.num_items = p.S * p.G;
+    if (p.S <= kSortMaxSeqs) {
+      int* ctxs = sched;
+      int* order = sched + p.S;
+      for (int s = tid; s < p.S; s += nthreads) ctxs[s] = clamp_ctx(p, s, false);
+      __syncthreads();
+      // rank by (length bucket descending, index ascending); ties keep batch order
+      for (int s = tid; s < p.S; s += nthreads) {
+        const int key = ctxs[s] >> kLenBucketShift;
+        int rank = 0;
+        for (int o = 0; o < p.S; ++o) {
+          const int ko = ctxs[o] >> kLenBucketShift;
+          rank += (ko > key) | ((ko == key) & (o < s));
+        }
+        order[rank] = s;
+      }
+      __syncthreads();
+      sch.ctx = ctxs;
+      sch.aux = order;
+    } else {
+      __syncthreads();
+    }
+  }
+
+  // ---- per-warp issue cursor ------------------------------------------------
+  uint8_t* my_stages = smem + warp * R * L.stage_bytes;
+  uint64_t* my_bars = bars + warp * R;
+
+  struct Cursor {
+    int k, j, je;
+    Item it;
+    bool valid;
+  };
+  auto cursor_settle = [&](Cursor& c) {
+    while (c.valid && c.j >= c.je) {
+      ++c.k;
+      if (!sch.get(p, BS, c.k, c.it)) {
+        c.valid = false;
+        break;
+      }
+      c.j = c.it.t0 / BS + warp;
+      c.je = (c.it.t1 + BS - 1) / BS;
+    }
+  };
+  Cursor ic;
+  ic.k = 0;
+  ic.valid = sch.get(p, BS, 0, ic.it);
+  if (ic.valid) {
+    ic.j = ic.it.t0 / BS + warp;
+    ic.je = (ic.it.t1 + BS - 1) / BS;
+    cursor_settle(ic);
+  }
+
+  auto issue = [&](const Cursor& c, int n) {
+    if (lane == 0) {
+      const int stage = n % R;
+      uint64_t* bar = &my_bars[stage];
+      const long long phys = __ldg(p.block_tables + (long long)c.it.s * p.max_blocks + c.j);
+      if (phys < 0 || phys >= p.num_blocks) {
+        atomicOr(p.err, kErrBlockId);
+        mbar_arrive(bar);  // completes the phase with no data; the consumer skips the block
+      } else {
+        uint8_t* kdst = my_stages + stage * L.stage_bytes;
+        uint8_t* vdst = kdst + TILE;
+        const int row = (int)((phys * p.G + c.it.kv) * BS);
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(bar, 2 * TILE);
+#pragma unroll
+        for (int rg = 0; rg < NREG; ++rg) {
+          tma_load_2d(kdst + rg * BS * 128, &kmap, rg * BOX_X, row, bar);
+          tma_load_2d(vdst + rg * BS * 128, &vmap, rg * BOX_X, row, bar);
+        }
+      }
+    }
+  };
+
+  __syncthreads();  // barrier inits visible before the first copy
+
+  int n_issue = 0;
+#pragma unroll 1
+  for (int r = 0; r < R && ic.valid; ++r) {
+    issue(ic, n_issue++);
+    ic.j += W;
+    cursor_settle(ic);
+  }
+
+  // ---- consume -----------------------------------------------------------------
+  int n_done = 0;
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  Item it;
+#pragma unroll 1
+  for (int k = 0; sch.get(p, BS, k, it); ++k) {
+    const int hq0 = it.kv * p.group;  // first query head of this kv head
+    const DT* qrow = reinterpret_cast<const DT*>(p.q) + ((long long)it.s * p.H + hq0) * D;
+    const int jb = it.t0 / BS, je = (it.t1 + BS - 1) / BS;
+
+    if constexpr (MMA) {
+      // ---------------- tensor-core path: group >= 4, 16-bit data ----------------
+      const int g = lane >> 2, t4 = lane & 3;
+      uint32_t qf[D / 16][2];
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        if (g < p.group) {
+          const DT* qr = qrow + (long long)g * D + ks * 16 + 2 * t4;
+          qf[ks][0] = __ldg(reinterpret_cast<const uint32_t*>(qr));
+          qf[ks][1] = __ldg(reinterpret_cast<const uint32_t*>(qr + 8));
+        } else {
+          qf[ks][0] = 0u;
+          qf[ks][1] = 0u;
+        }
+      }
+      float o[D / 16][4];
+#pragma unroll
+      for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+      float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
+
+#pragma unroll 1
+      for (int j = jb + warp; j < je; j += W) {
+        const int stage = n_done % R;
+        bool ok = mbar_wait_bounded(&my_bars[stage], (n_done / R) & 1, abort_flag, p.err, kWaitLimitNs);
+        ok = __all_sync(0xffffffffu, ok);
+        const long long phys = __ldg(p.block_tables + (long long)it.s * p.max_blocks + j);
+        if (ok && phys >= 0 && phys < p.num_blocks) {
+          const uint32_t kt = smem_u32(my_stages + stage * L.stage_bytes);
+          const uint32_t vt = kt + TILE;
+          const int nv = min(BS, it.t1 - j * BS);
+          constexpr int NSUB = BS / 16;
+          float sc[NSUB][4];
+#pragma unroll
+          for (int sub = 0; sub < NSUB; ++sub) {
+            sc[sub][0] = sc[sub][1] = sc[sub][2] = sc[sub][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+              uint32_t a[4];
+              ldsm_x4(a, kt + sw128_offset(sub * 16 + (lane & 15), ks * 2 + (lane >> 4), BS));
+              Mma<DT>::run(sc[sub], a, qf[ks][0], qf[ks][1]);
+            }
+          }
+          float mx0 = NEG_INF, mx1 = NEG_INF;
+#pragma unroll
+          for (int sub = 0; sub < NSUB; ++sub) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int tok = sub * 16 + g + ((e >> 1) << 3);
+              const float z = tok < nv ? sc[sub][e] * p.scale_log2 : NEG_INF;
+              sc[sub][e] = z;
+              if (e & 1) mx1 = fmaxf(mx1, z); else mx0 = fmaxf(mx0, z);
+            }
+          }
+#pragma unroll
+          for (int o2 = 4; o2 < 32; o2 <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o2));
+          }
+          const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+          const float c0 = exp2f(m0 - mn0), c1 = exp2f(m1 - mn1);
+          m0 = mn0;
+          m1 = mn1;
+          float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+          for (int sub = 0; sub < NSUB; ++sub) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float pv = exp2f(sc[sub][e] - ((e & 1) ? mn1 : mn0));
+              sc[sub][e] = pv;
+              if (e & 1) s1 += pv; else s0 += pv;
+            }
+          }
+          l0 = l0 * c0 + s0;
+          l1 = l1 * c1 + s1;
+#pragma unroll
+          for (int mt = 0; mt < D / 16; ++mt) {
+            o[mt][0] *= c0;
+            o[mt][2] *= c0;
+            o[mt][1] *= c1;
+            o[mt][3] *= c1;
+          }
+          // P enters the P V product as a 16-bit operand (both operands of one MMA
+          // share a type). Rounding P to bf16 alone costs up to 2^-9 relative per
+          // weight, too coarse for a 2e-3 bound when a few tokens dominate, so P is
+          // split into hi + lo 16-bit parts (P - hi - lo is below 2^-17 P) and each
+          // part gets its own MMA into the same fp32 accumulator.
+#pragma unroll
+          for (int sub = 0; sub < NSUB; ++sub) {
+            const uint32_t h01 = Mma<DT>::pack(sc[sub][0], sc[sub][1]);
+            const uint32_t h23 = Mma<DT>::pack(sc[sub][2], sc[sub][3]);
+            float r0, r1, r2, r3;
+            unpack2(h01, (DT*)nullptr, r0, r1);
+            unpack2(h23, (DT*)nullptr, r2, r3);
+            const uint32_t b0 = movmatrix_trans(h01);
+            const uint32_t b1 = movmatrix_trans(h23);
+            const uint32_t c0 = movmatrix_trans(Mma<DT>::pack(sc[sub][0] - r0, sc[sub][1] - r1));
+            const uint32_t c1 = movmatrix_trans(Mma<DT>::pack(sc[sub][2] - r2, sc[sub][3] - r3));
+            const int vtok = sub * 16 + ((lane >> 4) << 3) + (lane & 7);
+            // tokens held by this lane's A fragments: lo pair (a0, a1), hi pair (a2, a3)
+            const int tlo = sub * 16 + 2 * t4;
+            const uint32_t mlo = (tlo < nv ? 0x0000ffffu : 0u) | (tlo + 1 < nv ? 0xffff0000u : 0u);
+            const uint32_t mhi = (tlo + 8 < nv ? 0x0000ffffu : 0u) | (tlo + 9 < nv ? 0xffff0000u : 0u);
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+              uint32_t a[4];
+              ldsm_x4_trans(a, vt + sw128_offset(vtok, mt * 2 + ((lane >> 3) & 1), BS));
+              a[0] &= mlo;
+              a[1] &= mlo;
+              a[2] &= mhi;
+              a[3] &= mhi;
+              Mma<DT>::run(o[mt], a, b0, b1);
+              Mma<DT>::run(o[mt], a, c0, c1);
+            }
+          }
+        }
+        __syncwarp();
+        ++n_done;
+        if (ic.valid && !*abort_flag) {
+          issue(ic, n_issue++);
+          ic.j += W;
+          cursor_settle(ic);
+        }
+      }
+      // warp partials -> shared memory
+#pragma unroll
+      for (int o2 = 4; o2 < 32; o2 <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, o2);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, o2);
+      }
+      const int hA = 2 * t4, hB = hA + 1;
+      float* mo = mrg_o + warp * p.group * D;
+      if (hA < p.group) {
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+          mo[hA * D + mt * 16 + g] = o[mt][0];
+          mo[hA * D + mt * 16 + g + 8] = o[mt][2];
+        }
+      }
+      if (hB < p.group) {
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+          mo[hB * D + mt * 16 + g] = o[mt][1];
+          mo[hB * D + mt * 16 + g + 8] = o[mt][3];
+        }
+      }
+      if (g == 0) {
+        float* ml = mrg_ml + warp * kMaxGroup * 2;
+        ml[hA * 2 + 0] = m0;
+        ml[hA * 2 + 1] = l0;
+        ml[hB * 2 + 0] = m1;
+        ml[hB * 2 + 1] = l1;
+      }
+    } else {
+      // ---------------- vector path: lanes split head_dim, FFMA ----------------
+      constexpr int LPT = 32 / BS;        // lanes per token in q K^T
+      constexpr int CPL = NCH / LPT;      // 16-byte K chunks per lane
+      constexpr int EPC = 16 / E;         // elements per 16-byte chunk
+      constexpr int EPL = D / 32;         // output elements per lane in P V
+      constexpr int VB = EPL * E;         // V bytes per lane per row
+      static_assert(32 % BS == 0 || BS == 32, "block size must divide 32");
+      float* qs = qs_all + warp * p.group * D;
+      for (int i = lane; i < p.group * D; i += 32) qs[i] = to_f32(qrow[i]);
+      __syncwarp();
+      const int t = lane % BS, part = lane / BS;
+      float o[kMaxGroup][EPL];
+      float mr[kMaxGroup], lr[kMaxGroup];
+#pragma unroll
+      for (int h = 0; h < kMaxGroup; ++h) {
+        mr[h] = NEG_INF;
+        lr[h] = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) o[h][e] = 0.f;
+      }
+#pragma unroll 1
+      for (int j = jb + warp; j < je; j += W) {
+        const int stage = n_done % R;
+        bool ok = mbar_wait_bounded(&my_bars[stage], (n_done / R) & 1, abort_flag, p.err, kWaitLimitNs);
+        ok = __all_sync(0xffffffffu, ok);
+        const long long phys = __ldg(p.block_tables + (long long)it.s * p.max_blocks + j);
+        if (ok && phys >= 0 && phys < p.num_blocks) {
+          const uint8_t* kt = my_stages + stage * L.stage_bytes;
+          const uint8_t* vt = kt + TILE;
+          const int nv = min(BS, it.t1 - j * BS);
+          // this lane's K chunks (row t), as floats
+#pragma unroll
+          for (int h = 0; h < kMaxGroup; ++h) {
+            if (h >= p.group) break;
+            const float* qh = qs + h * D;
+            float z = 0.f;
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) {
+              const int ch = part * CPL + c;
+              const uint4 raw = *reinterpret_cast<const uint4*>(kt + sw128_offset(t, ch, BS));
+              const float4* qv = reinterpret_cast<const float4*>(qh + ch * EPC);
+              if constexpr (E == 4) {
+                const float4 qa = qv[0];
+                z = fmaf(qa.x, __uint_as_float(raw.x), z);
+                z = fmaf(qa.y, __uint_as_float(raw.y), z);
+                z = fmaf(qa.z, __uint_as_float(raw.z), z);
+                z = fmaf(qa.w, __uint_as_float(raw.w), z);
+              } else {
+                const float4 qa = qv[0], qb = qv[1];
+                float f0, f1, f2, f3, f4, f5, f6, f7;
+                unpack2(raw.x, (DT*)nullptr, f0, f1);
+                unpack2(raw.y, (DT*)nullptr, f2, f3);
+                unpack2(raw.z, (DT*)nullptr, f4, f5);
+                unpack2(raw.w, (DT*)nullptr, f6, f7);
+                z = fmaf(qa.x, f0, z);
+                z = fmaf(qa.y, f1, z);
+                z = fmaf(qa.z, f2, z);
+                z = fmaf(qa.w, f3, z);
+                z = fmaf(qb.x, f4, z);
+                z = fmaf(qb.y, f5, z);
+                z = fmaf(qb.z, f6, z);
+                z = fmaf(qb.w, f7, z);
+              }
+            }
+            if (LPT == 2) z += __shfl_xor_sync(0xffffffffu, z, 16);
+            z = t < nv ? z * p.scale_log2 : NEG_INF;
+            float mx = z;
+#pragma unroll
+            for (int o2 = 1; o2 < 32; o2 <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+            const float mn = fmaxf(mr[h], mx);
+            const float corr = exp2f(mr[h] - mn);
+            mr[h] = mn;
+            const float pt = exp2f(z - mn);
+            lr[h] = lr[h] * corr + (part == 0 ? pt : 0.f);
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) o[h][e] *= corr;
+#pragma unroll 4
+            for (int tt = 0; tt < nv; ++tt) {
+              const float w = __shfl_sync(0xffffffffu, pt, tt);
+              const int byte = lane * VB;
+              const uint8_t* src = vt + sw128_offset(tt, byte >> 4, BS) + (byte & 15);
+              if constexpr (E == 4) {
+                if constexpr (VB == 16) {
+                  const float4 v = *reinterpret_cast<const float4*>(src);
+                  o[h][0] = fmaf(w, v.x, o[h][0]);
+                  o[h][1] = fmaf(w, v.y, o[h][1]);
+                  o[h][2] = fmaf(w, v.z, o[h][2]);
+                  o[h][3] = fmaf(w, v.w, o[h][3]);
+                } else {
+                  const float2 v = *reinterpret_cast<const float2*>(src);
+                  o[h][0] = fmaf(w, v.x, o[h][0]);
+                  o[h][1] = fmaf(w, v.y, o[h][1]);
+                }
+              } else {
+                if constexpr (VB == 8) {
+                  const uint2 raw = *reinterpret_cast<const uint2*>(src);
+                  float f0, f1, f2, f3;
+                  unpack2(raw.x, (DT*)nullptr, f0, f1);
+                  unpack2(raw.y, (DT*)nullptr, f2, f3);
+                  o[h][0] = fmaf(w, f0, o[h][0]);
+                  o[h][1] = fmaf(w, f1, o[h][1]);
+                  o[h][2] = fmaf(w, f2, o[h][2]);
+                  o[h][3] = fmaf(w, f3, o[h][3]);
+                } else {
+                  const uint32_t raw = *reinterpret_cast<const uint32_t*>(src);
+                  float f0, f1;
+                  unpack2(raw, (DT*)nullptr, f0, f1);
+                  o[h][0] = fmaf(w, f0, o[h][0]);
+                  o[h][1] = fmaf(w, f1, o[h][1]);
+                }
+              }
+            }
+          }
+        }
+        __syncwarp();
+        ++n_done;
+        if (ic.valid && !*abort_flag) {
+          issue(ic, n_issue++);
+          ic.j += W;
+          cursor_settle(ic);
+        }
+      }
+      float* mo = mrg_o + warp * p.group * D;
+      float* ml = mrg_ml + warp * kMaxGroup * 2;
+#pragma unroll
+      for (int h = 0; h < kMaxGroup; ++h) {
+        if (h >= p.group) break;
+        float l = lr[h];
+#pragma unroll
+        for (int o2 = 1; o2 < 32; o2 <<= 1) l += __shfl_xor_sync(0xffffffffu, l, o2);
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) mo[h * D + lane * EPL + e] = o[h][e];
+        if (lane == 0) {
+          ml[h * 2 + 0] = mr[h];
+          ml[h * 2 + 1] = l;
+        }
+      }
+    }
+
+    // ---- merge the W warps' partials and write ---------------------------------
+    asm volatile("bar.sync 1, %0;" ::"n"(W * 32) : "memory");
+    for (int idx = tid; idx < p.group * D; idx += nthreads) {
+      const int h = idx / D, i = idx - h * D;
+      float M = NEG_INF;
+#pragma unroll
+      for (int w = 0; w < W; ++w) {
+        const float l = mrg_ml[(w * kMaxGroup + h) * 2 + 1];
+        if (l > 0.f) M = fmaxf(M, mrg_ml[(w * kMaxGroup + h) * 2 + 0]);
+      }
+      float Lsum = 0.f, O = 0.f;
+#pragma unroll
+      for (int w = 0; w < W; ++w) {
+        const float l = mrg_ml[(w * kMaxGroup + h) * 2 + 1];
+        if (l > 0.f) {
+          const float f = exp2f(mrg_ml[(w * kMaxGroup + h) * 2 + 0] - M);
+          Lsum = fmaf(l, f, Lsum);
+          O = fmaf(mrg_o[(w * p.group + h) * D + i], f, O);
+        }
+      }
+      const float res = Lsum > 0.f ? O / Lsum : 0.f;
+      const int hq = hq0 + h;
+      if (SPLIT) {
+        const long long row = ((long long)it.s * p.H + hq) * p.max_partitions + it.part;
+        p.ws_o[row * D + i] = res;
+        if (i == 0) {
+          p.ws_m[row] = M;
+          p.ws_l[row] = Lsum;
+        }
+      } else {
+        reinterpret_cast<OT*>(p.out)[((long long)it.s * p.H + hq) * D + i] = from_f32<OT>(res);
+      }
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(W * 32) : "memory");
+  }
+
+  // ---- let every copy this warp started land before the block exits ------------
+  if (lane == 0) {
+    const int first = n_issue - R > 0 ? n_issue - R : 0;
+    for (int n = first; n < n_issue; ++n)
+      mbar_wait_bounded(&my_bars[n % R], (n / R) & 1, nullptr, p.err, kDrainLimitNs);
+  }
+  __syncwarp();
+}
+
+// Pass 2 of split mode: merge the partitions of one (sequence, head) row with
+// log-sum-exp weights, w_p = l_p * 2^(m_p - M), out = sum_p w_p o_p / sum_p w_p.
+template <typename OT, int D>
+__global__ void __launch_bounds__(128) lse_reduce_kernel(const DecodeParams p) {
+  constexpr int EPL = D / 32;
+  const int row = blockIdx.x;  // s * H + h
+  const int s = row / p.H;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  const int c = clamp_ctx(p, s, true);
+  const int P = (c + p.partition - 1) / p.partition;
+  const long long base = (long long)row * p.max_partitions;
+  float M = NEG_INF, Lsum = 0.f, acc[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+#pragma unroll 4
+  for (int q = warp; q < P; q += 4) {
+    const float mq = __ldg(p.ws_m + base + q), lq = __ldg(p.ws_l + base + q);
+    if (!(lq > 0.f)) continue;
+    const float* oq = p.ws_o + (base + q) * D + lane * EPL;
+    float v[EPL];
+    if constexpr (EPL == 4) {
+      const float4 t4 = __ldg(reinterpret_cast<const float4*>(oq));
+      v[0] = t4.x; v[1] = t4.y; v[2] = t4.z; v[3] = t4.w;
+    } else {
+      const float2 t2 = __ldg(reinterpret_cast<const float2*>(oq));
+      v[0] = t2.x; v[1] = t2.y;
+    }
+    const float Mn = fmaxf(M, mq);
+    const float a = exp2f(M - Mn), b = lq * exp2f(mq - Mn);
+    Lsum = Lsum * a + b;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] = acc[e] * a + b * v[e];
+    M = Mn;
+  }
+  __shared__ float sh_ml[4][2];
+  __shared__ float sh_o[4][D];
+  if (lane == 0) {
+    sh_ml[warp][0] = M;
+    sh_ml[warp][1] = Lsum;
+  }
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) sh_o[warp][lane * EPL + e] = acc[e];
+  __syncthreads();
+  for (int i = threadIdx.x; i < D; i += 128) {
+    float Mx = NEG_INF;
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+      if (sh_ml[w][1] > 0.f) Mx = fmaxf(Mx, sh_ml[w][0]);
+    float Ls = 0.f, O = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      if (sh_ml[w][1] > 0.f) {
+        const float f = exp2f(sh_ml[w][0] - Mx);
+        Ls = fmaf(sh_ml[w][1], f, Ls);
+        O = fmaf(sh_o[w][i], f, O);
+      }
+    }
+    reinterpret_cast<OT*>(p.out)[(long long)row * D + i] = from_f32<OT>(Ls > 0.f ? O / Ls : 0.f);
+  }
+}
+
+}  // namespace pa

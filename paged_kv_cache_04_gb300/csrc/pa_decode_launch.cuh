@@ -1,0 +1,71 @@
+// Host launchers for the decode kernels (included by the per-dtype units).
+#pragma once
+
+#include <mutex>
+
+#include "pa_decode.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+template <typename DT, typename OT, int D, int BS, bool MMA, bool SPLIT>
+pa_status launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
+                        int num_sms, long long max_items, cudaStream_t stream) {
+  using Cfg = StageCfg<DT, D, BS, MMA>;
+  auto kern = paged_decode_kernel<DT, OT, D, BS, MMA, SPLIT>;
+  const SmemLayout L = make_layout(Cfg::W, Cfg::R, D, BS, Cfg::E, p.group, !MMA, SPLIT, p.S);
+  if (L.total > 227u * 1024u) return PA_ERR_UNSUPPORTED;
+
+  // Opt in to the dynamic shared memory once per device, and remember the
+  // occupancy for the last shared-memory size seen on that device.
+  static std::mutex mu;
+  static unsigned set_bytes[64] = {0};
+  static unsigned occ_bytes[64] = {0};
+  static int occ_blocks[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
+  int per_sm = 1;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (set_bytes[dev] < L.total) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total) != cudaSuccess)
+        return PA_ERR_CUDA;
+      set_bytes[dev] = L.total;
+    }
+    if (occ_bytes[dev] != L.total) {
+      int n = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, Cfg::W * 32, L.total) != cudaSuccess)
+        return PA_ERR_CUDA;
+      occ_bytes[dev] = L.total;
+      occ_blocks[dev] = n;
+    }
+    per_sm = occ_blocks[dev];
+  }
+  if (per_sm < 1) return PA_ERR_UNSUPPORTED;
+  long long grid = (long long)num_sms * per_sm;
+  if (max_items < grid) grid = max_items;
+  if (grid <= 0) return PA_OK;
+  kern<<<(unsigned)grid, Cfg::W * 32, L.total, stream>>>(kmap, vmap, p);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+template <typename OT, int D>
+pa_status launch_lse_reduce(const DecodeParams& p, cudaStream_t stream) {
+  const long long rows = (long long)p.S * p.H;
+  if (rows <= 0) return PA_OK;
+  lse_reduce_kernel<OT, D><<<(unsigned)rows, 128, 0, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace pa
+
+// Explicit instantiations for one element type DT (the tensor-core path only
+// exists for 16-bit types).
+#define PA_INSTANTIATE_DECODE(DT, OT, D, BS, MMA)                                                        \
+  template pa_status pa::launch_decode<DT, OT, D, BS, MMA, false>(const CUtensorMap&, const CUtensorMap&, \
+                                                                  const pa::DecodeParams&, int, long long, \
+                                                                  cudaStream_t);
+#define PA_INSTANTIATE_SPLIT(DT, D, BS, MMA)                                                               \
+  template pa_status pa::launch_decode<DT, float, D, BS, MMA, true>(const CUtensorMap&, const CUtensorMap&, \
+                                                                    const pa::DecodeParams&, int, long long, \
+                                                                    cudaStream_t);

@@ -1,0 +1,26 @@
+// Host-side helpers shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime_api.h>
+
+#include "pa.h"
+
+namespace pa {
+
+struct DecodeParams;
+
+// Per-device state, set up on the first call on a device: the device address
+// of the error word and the SM count. Returns PA_ERR_CUDA if CUDA fails.
+pa_status device_state(unsigned** err, int* num_sms);
+
+// Launchers, one per (element type, output type, head_dim, block_size, path,
+// split) combination, instantiated in pa_decode_{f32,f16,bf16}.cu.
+template <typename DT, typename OT, int D, int BS, bool MMA, bool SPLIT>
+pa_status launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
+                        int num_sms, long long max_items, cudaStream_t stream);
+
+template <typename OT, int D>
+pa_status launch_lse_reduce(const DecodeParams& p, cudaStream_t stream);
+
+}  // namespace pa

@@ -149,15 +149,19 @@ def _tables(bm: BlockManager, seq_ids, B) -> tuple:
 
 def batch_with_new_tokens(name, S, H, G, d, B, dtype, ctx, num_blocks, device,
                           new_token=True, scale=None, partition_tokens=None, meta=None,
-                          pool_fill=None) -> Workload:
+                          pool_fill=None, rotate=0) -> Workload:
     """Independent sequences of lengths ``ctx`` scattered over a shuffled pool.
 
     With ``new_token`` the last position of every sequence is left for
     reshape_and_cache (its K/V are in ``new_key`` / ``new_value`` and its slot
-    in ``slot_mapping``); the pool holds the earlier positions.
+    in ``slot_mapping``); the pool holds the earlier positions. ``rotate``
+    starts handing out blocks ``rotate`` places into the shuffled free list, so
+    two batches drawn with rotations far enough apart use disjoint blocks.
     """
     ctx = [int(c) for c in ctx]
     perm = torch.randperm(num_blocks, generator=_gen(SEED_PERM)).tolist()
+    if rotate:
+        perm = perm[rotate:] + perm[:rotate]
     bm = BlockManager(num_blocks, B, free_order=perm)
     slots = []
     for s, c in enumerate(ctx):
@@ -209,10 +213,10 @@ def opt13b(device="cpu", S=64, new_token=True) -> Workload:
                                  meta={"pool_reading": "max(763, blocks needed)"})
 
 
-def llama8b(device="cpu", S=256, num_blocks=100_000, new_token=True) -> Workload:
+def llama8b(device="cpu", S=256, num_blocks=100_000, new_token=True, rotate=0) -> Workload:
     ctx = uniform_lengths(S, 512, 4096, _gen(SEED_CTX)).tolist()
     return batch_with_new_tokens("llama8b", S, 32, 8, 128, 16, torch.bfloat16, ctx, num_blocks,
-                                 device, new_token=new_token)
+                                 device, new_token=new_token, rotate=rotate)
 
 
 def long70b(device="cpu", S=8, B=16, lo=32768, hi=131072, partition_tokens=512,
