@@ -145,6 +145,45 @@ pa_status pa_decode_split(void* out, const void* q, const void* k_cache, const v
                           size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Size of the scratch array built into the library for pa_decode_split_static:
+ * 16 MiB of device memory, held on every GPU that loads the library until the
+ * process exits.
+ */
+#define PA_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/*
+ * pa_decode_split without a workspace argument. The pages have no counterpart
+ * to this call: it exists for callers that cannot allocate device memory at
+ * the point they run attention -- for example a plugin whose host framework
+ * owns every device allocation and does not let it call cudaMalloc, or a
+ * serving loop that must stay out of the CUDA allocator (which can synchronise
+ * the device) once it is running. It computes exactly what pa_decode_split
+ * computes, with the same arguments minus `workspace` / `workspace_bytes`, and
+ * keeps the partition results in a scratch array of PA_STATIC_SCRATCH_BYTES
+ * inside the library instead. It calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *
+ *   - Size limit: pa_decode_split_workspace_bytes(num_seqs, num_heads,
+ *     head_dim, max_context_len, partition_tokens) must not exceed
+ *     PA_STATIC_SCRATCH_BYTES (e.g. 8 sequences x 64 heads x head_dim 128 fit
+ *     up to 63 partitions, 32,256 tokens at 512-token partitions); a larger
+ *     request returns PA_ERR_UNSUPPORTED and launches nothing -- use
+ *     pa_decode_split with a workspace for it.
+ *   - The first call on a device looks up the array's device address (once per
+ *     device, with that device current); make that first call before any
+ *     stream capture.
+ *   - Every call, on every stream, shares the one array and leaves its
+ *     contents behind: calls whose executions overlap on the GPU race and give
+ *     undefined results. Nothing in the array needs to start at zero.
+ */
+pa_status pa_decode_split_static(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                 const int32_t* block_tables, int max_blocks_per_seq,
+                                 const int32_t* context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                                 int head_dim, int block_size, int64_t num_blocks, float scale,
+                                 pa_dtype dtype, pa_dtype out_dtype, int max_context_len, int partition_tokens,
+                                 cudaStream_t stream);
+
+/*
  * Batched copy-on-write block copies (CS349E Lecture 7 notes §5.1 and §4.3: a
  * sample about to write into a shared block first gets its own copy; all copies
  * pending for a step go in one launch). For every pair p and every layer l:

@@ -22,7 +22,8 @@ import os
 
 __all__ = [
     "PAError", "library", "library_path", "pa_reshape_and_cache", "pa_decode", "pa_decode_split",
-    "pa_decode_split_workspace_bytes", "pa_copy_blocks", "pa_get_error", "pa_version",
+    "pa_decode_split_workspace_bytes", "pa_decode_split_static", "pa_copy_blocks", "pa_get_error",
+    "pa_version", "PA_STATIC_SCRATCH_BYTES",
     "PA_DEVERR_BLOCK_ID", "PA_DEVERR_SLOT", "PA_DEVERR_CONTEXT", "PA_DEVERR_PAIR", "PA_DEVERR_TIMEOUT",
 ]
 
@@ -32,6 +33,7 @@ library_path = os.path.join(_HERE, "libpa.so")
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_OUT_OF_RANGE, PA_ERR_CUDA = range(5)
 PA_F32, PA_F16, PA_BF16 = 0, 1, 2
 PA_DEVERR_BLOCK_ID, PA_DEVERR_SLOT, PA_DEVERR_CONTEXT, PA_DEVERR_PAIR, PA_DEVERR_TIMEOUT = 1, 2, 4, 8, 16
+PA_STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 _lib = None
 
@@ -58,13 +60,14 @@ def library():
     lib.pa_decode_split_workspace_bytes.argtypes = [I, I, I, I, I]
     lib.pa_decode_split_workspace_bytes.restype = SZ
     lib.pa_decode_split.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I64, F, I, I, I, I, P, SZ, P]
+    lib.pa_decode_split_static.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I64, F, I, I, I, I, P]
     lib.pa_copy_blocks.argtypes = [P, P, I, P, I, I, I, I, I64, I, P]
     lib.pa_get_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), P]
     lib.pa_status_string.argtypes = [I]
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_version.argtypes = []
-    for f in ("pa_reshape_and_cache", "pa_decode", "pa_decode_split", "pa_copy_blocks", "pa_get_error",
-              "pa_version"):
+    for f in ("pa_reshape_and_cache", "pa_decode", "pa_decode_split", "pa_decode_split_static",
+              "pa_copy_blocks", "pa_get_error", "pa_version"):
         getattr(lib, f).restype = I
     _lib = lib
     return lib
@@ -166,6 +169,25 @@ def pa_decode_split(out, q, k_cache, v_cache, block_tables, context_lens, scale,
                                         maxb, _ptr(context_lens), S, H, G, d, B, nb, float(scale),
                                         _dtype_code(q), _dtype_code(out), int(max_context_len),
                                         int(partition_tokens), _ptr(workspace), nbytes, _stream(stream)))
+
+
+def pa_decode_split_static(out, q, k_cache, v_cache, block_tables, context_lens, scale, max_context_len,
+                           partition_tokens, stream=None):
+    """``pa_decode_split`` for callers that cannot allocate: no workspace argument.
+
+    The partition results go to a scratch array inside the library
+    (``PA_STATIC_SCRATCH_BYTES`` per GPU, held until exit), so nothing is
+    allocated per call. Requests whose workspace would exceed that size raise
+    (status "unsupported"). All calls share the one array: calls that overlap
+    on the GPU race. The first call on a device looks up the array's address;
+    make it before any stream capture.
+    """
+    f = "pa_decode_split_static"
+    S, H, G, d, B, nb, maxb = _decode_args(f, out, q, k_cache, v_cache, block_tables, context_lens)
+    _check(f, library().pa_decode_split_static(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                               _ptr(block_tables), maxb, _ptr(context_lens), S, H, G, d, B,
+                                               nb, float(scale), _dtype_code(q), _dtype_code(out),
+                                               int(max_context_len), int(partition_tokens), _stream(stream)))
 
 
 def pa_copy_blocks(k_caches, v_caches, block_pairs, stream=None):
