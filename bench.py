@@ -52,6 +52,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
     ap.add_argument("--profile", action="store_true",
                     help="run only the step's kernels on a 64-sequence batch of the same shape (for ncu)")
+    ap.add_argument("--workload", default="llama8b",
+                    choices=["llama8b", "tiny", "opt13b", "shared", "shared_cow", "long70b_b16", "long70b_b32"],
+                    help="the other workload shapes give a device-timed line of their own (no e2e / CPU legs)")
     return ap.parse_args()
 
 
@@ -431,6 +434,94 @@ def run_reference(args, rank, world, local):
     }
 
 
+def run_workload(args):
+    """Device-timed step of one of the other workload shapes (single GPU)."""
+    import torch
+    import paged_kv_cache_04_gb300 as pa
+    from paged_kv_cache_04_gb300 import _build, roofline, workloads
+    _build.ensure_built()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    name = args.workload
+    split, T = False, None
+    if name == "tiny":
+        wl = workloads.tiny(device=dev)
+    elif name == "opt13b":
+        wl = workloads.opt13b(device=dev)
+    elif name.startswith("shared"):
+        wl = workloads.shared_prefix(device=dev, cow=name == "shared_cow")
+        # set-up: the CoW copies and every appended token, once; a timed step then
+        # repeats the copies and writes each sample's newest token before decoding
+        if wl.copy_pairs.numel():
+            pa.pa_copy_blocks([wl.k_cache], [wl.v_cache], wl.copy_pairs)
+        pa.pa_reshape_and_cache(wl.new_key, wl.new_value, wl.k_cache, wl.v_cache, wl.slot_mapping)
+        last = torch.tensor([int(wl.block_tables[s, (int(c) - 1) // wl.B]) * wl.B + (int(c) - 1) % wl.B
+                             for s, c in enumerate(wl.context_lens.tolist())], dtype=torch.int64, device=dev)
+        wl.slot_mapping = last
+        wl.new_key, wl.new_value = wl.new_key[:wl.S].contiguous(), wl.new_value[:wl.S].contiguous()
+    else:
+        B = 16 if name.endswith("16") else 32
+        wl = workloads.long70b(device=dev, B=B)
+        split, T = True, 512
+    out = torch.empty_like(wl.q)
+    ws = None
+    if split:
+        ws = torch.empty(pa.pa_decode_split_workspace_bytes(wl.S, wl.H, wl.d, wl.max_context, T),
+                         dtype=torch.uint8, device=dev)
+    # a buffer larger than L2, rewritten between timed steps
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    pairs = wl.copy_pairs if wl.copy_pairs is not None and wl.copy_pairs.numel() else None
+
+    def step():
+        if pairs is not None:
+            pa.pa_copy_blocks([wl.k_cache], [wl.v_cache], pairs)
+        if wl.slot_mapping is not None:
+            pa.pa_reshape_and_cache(wl.new_key, wl.new_value, wl.k_cache, wl.v_cache, wl.slot_mapping)
+        if split:
+            pa.pa_decode_split(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale,
+                               wl.max_context, T, ws)
+        else:
+            pa.pa_decode(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(args.steps):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        times.append((a, b))
+    torch.cuda.synchronize()
+    ms = statistics.mean(x.elapsed_time(y) for x, y in times)
+    e = wl.q.element_size()
+    ctx = wl.context_lens.tolist()
+    dec = roofline.decode_bytes(ctx, wl.H, wl.G, wl.d, e)
+    extra = 0
+    if wl.slot_mapping is not None:
+        extra += roofline.reshape_and_cache_bytes(wl.slot_mapping.numel(), wl.G, wl.d, e)
+    if pairs is not None:
+        extra += roofline.copy_blocks_bytes(pairs.shape[0], 1, wl.B, wl.G, wl.d, e)
+    unique = None
+    if name.startswith("shared"):
+        unique = wl.meta["unique_tokens"] * roofline.kv_bytes_per_token(1, wl.G, wl.d, e) + 2 * wl.S * wl.H * wl.d * e
+    peak, _ = measured_hbm_peak()
+    line = {"workload": name, "ms_per_step": round(ms, 5), "seqs_per_s": round(wl.S / (ms * 1e-3), 1),
+            "kv_tokens_per_s": round(sum(ctx) / (ms * 1e-3), 1),
+            "algorithmic_GBps": round((dec + extra) / (ms * 1e-3) / 1e9, 1),
+            "frac_of_measured_peak": round((dec + extra) / (ms * 1e-3) / 1e9 / peak, 4),
+            "bytes_per_step": dec + extra, "l2": "512 MiB buffer rewritten between timed steps",
+            "device_errors": pa.pa_get_error()}
+    if unique is not None:
+        line["unique_GBps"] = round((unique + extra) / (ms * 1e-3) / 1e9, 1)
+        line["unique_frac_of_measured_peak"] = round((unique + extra) / (ms * 1e-3) / 1e9 / peak, 4)
+        line["copy_pairs"] = 0 if pairs is None else int(pairs.shape[0])
+    print(json.dumps(line), flush=True)
+
+
 def run_profile_case(args):
     """The step's kernels on a 64-sequence batch of the workload's shape (~0.6 GB of K/V per
     step, still larger than L2; ~1 GB pool), sized so that an ncu capture stays small."""
@@ -455,6 +546,9 @@ def main():
     args = parse()
     if args.profile:
         run_profile_case(args)
+        return
+    if args.workload != "llama8b":
+        run_workload(args)
         return
     rank, world, local = dist_init(args.gpus)
     if args.impl == "reference":
