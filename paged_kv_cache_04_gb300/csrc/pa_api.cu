@@ -48,8 +48,8 @@ pa_status encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
 }
 
 // A 2-D view of a KV pool: rows = num_blocks * num_kv_heads * block_size, each
-// head_dim elements. One TMA box is 128 bytes of a row x block_size rows, staged
-// with 128-byte swizzling.
+// head_dim elements. One TMA box is 128 bytes of a row x 16 rows (one job),
+// staged with 128-byte swizzling.
 pa_status make_pool_map(CUtensorMap* map, const void* base, pa_dtype dt, int D, int BS, long long rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
   pa_status st = encoder(&enc);
@@ -60,7 +60,7 @@ pa_status make_pool_map(CUtensorMap* map, const void* base, pa_dtype dt, int D, 
                                                : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)D * e};
-  cuuint32_t box[2] = {(cuuint32_t)(128 / e), (cuuint32_t)BS};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / e), (cuuint32_t)kJobTokens};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, t, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -98,29 +98,27 @@ pa_status check_decode(const DecodeArgs& a) {
   return PA_OK;
 }
 
-template <typename DT, typename OT, int D, int BS>
+template <typename DT, typename OT, int D>
 pa_status dispatch_path(const CUtensorMap& km, const CUtensorMap& vm, const DecodeParams& p, int sms,
                         long long items, bool split, cudaStream_t st) {
   const bool mma = sizeof(DT) == 2 && p.group >= 4;
   if (split) {
     if constexpr (sizeof(DT) == 2) {
-      if (mma) return launch_decode<DT, float, D, BS, true, true>(km, vm, p, sms, items, st);
+      if (mma) return launch_decode<DT, float, D, true, true>(km, vm, p, sms, items, st);
     }
-    return launch_decode<DT, float, D, BS, false, true>(km, vm, p, sms, items, st);
+    return launch_decode<DT, float, D, false, true>(km, vm, p, sms, items, st);
   }
   if constexpr (sizeof(DT) == 2) {
-    if (mma) return launch_decode<DT, OT, D, BS, true, false>(km, vm, p, sms, items, st);
+    if (mma) return launch_decode<DT, OT, D, true, false>(km, vm, p, sms, items, st);
   }
-  return launch_decode<DT, OT, D, BS, false, false>(km, vm, p, sms, items, st);
+  return launch_decode<DT, OT, D, false, false>(km, vm, p, sms, items, st);
 }
 
 template <typename DT, typename OT>
-pa_status dispatch_shape(const CUtensorMap& km, const CUtensorMap& vm, const DecodeParams& p, int D, int BS,
-                         int sms, long long items, bool split, cudaStream_t st) {
-  if (D == 64 && BS == 16) return dispatch_path<DT, OT, 64, 16>(km, vm, p, sms, items, split, st);
-  if (D == 64 && BS == 32) return dispatch_path<DT, OT, 64, 32>(km, vm, p, sms, items, split, st);
-  if (D == 128 && BS == 16) return dispatch_path<DT, OT, 128, 16>(km, vm, p, sms, items, split, st);
-  if (D == 128 && BS == 32) return dispatch_path<DT, OT, 128, 32>(km, vm, p, sms, items, split, st);
+pa_status dispatch_shape(const CUtensorMap& km, const CUtensorMap& vm, const DecodeParams& p, int D, int sms,
+                         long long items, bool split, cudaStream_t st) {
+  if (D == 64) return dispatch_path<DT, OT, 64>(km, vm, p, sms, items, split, st);
+  if (D == 128) return dispatch_path<DT, OT, 128>(km, vm, p, sms, items, split, st);
   return PA_ERR_UNSUPPORTED;
 }
 
@@ -147,6 +145,7 @@ pa_status run_decode(const DecodeArgs& a, bool split, int partition, int max_par
   p.context_lens = a.context_lens;
   p.max_blocks = a.max_blocks;
   p.block_size = a.BS;
+  p.block_shift = a.BS == 32 ? 5 : 4;
   p.S = a.S;
   p.H = a.H;
   p.G = a.G;
@@ -167,15 +166,15 @@ pa_status run_decode(const DecodeArgs& a, bool split, int partition, int max_par
   }
   switch (a.dt) {
     case PA_BF16:
-      s = a.odt == PA_F32 ? dispatch_shape<__nv_bfloat16, float>(km, vm, p, a.D, a.BS, sms, items, split, st)
-                          : dispatch_shape<__nv_bfloat16, __nv_bfloat16>(km, vm, p, a.D, a.BS, sms, items, split, st);
+      s = a.odt == PA_F32 ? dispatch_shape<__nv_bfloat16, float>(km, vm, p, a.D, sms, items, split, st)
+                          : dispatch_shape<__nv_bfloat16, __nv_bfloat16>(km, vm, p, a.D, sms, items, split, st);
       break;
     case PA_F16:
-      s = a.odt == PA_F32 ? dispatch_shape<__half, float>(km, vm, p, a.D, a.BS, sms, items, split, st)
-                          : dispatch_shape<__half, __half>(km, vm, p, a.D, a.BS, sms, items, split, st);
+      s = a.odt == PA_F32 ? dispatch_shape<__half, float>(km, vm, p, a.D, sms, items, split, st)
+                          : dispatch_shape<__half, __half>(km, vm, p, a.D, sms, items, split, st);
       break;
     default:
-      s = dispatch_shape<float, float>(km, vm, p, a.D, a.BS, sms, items, split, st);
+      s = dispatch_shape<float, float>(km, vm, p, a.D, sms, items, split, st);
   }
   if (s != PA_OK || !split) return s;
   switch (a.odt) {

@@ -11,41 +11,47 @@
 // contiguous cache (CMU 15-779 Lecture 16 notes, §3.3).
 //
 // Design (one launch, persistent CTAs):
-//   * a work item is (sequence, kv head[, partition]); every CTA walks a fixed
-//     list of items, dealt out in a serpentine order over the grid, longest
-//     contexts first (sequences sorted by 512-token length buckets);
-//   * the item's blocks are dealt round-robin to the CTA's W warps; each warp
-//     keeps R (K, V) tile stages of its own in shared memory, filled by TMA
-//     tensor copies with 128-byte swizzling and completed on an mbarrier, so a
-//     warp always has R - 1 blocks in flight while it computes one;
-//   * a KV block is read once for all H / G query heads of its kv head: with a
+//   * the unit of data movement is a 16-token job: one (K, V) pair of TMA
+//     boxes of 16 rows x head_dim, taken from one physical block (a 32-token
+//     block is two jobs). Each warp owns R job stages in shared memory, filled
+//     by TMA tensor copies with 128-byte swizzling that complete on the
+//     stage's mbarrier, so a warp always has R - 1 jobs in flight while it
+//     computes one;
+//   * plain mode: a work item is (sequence, kv head); items are dealt to CTAs
+//     in a serpentine order, longest contexts first (512-token length buckets,
+//     ties in batch order), and an item's jobs go round-robin to the CTA's W
+//     warps, whose partial (max, sum, output) triples are merged through shared
+//     memory at the end of the item;
+//   * split mode: an item is (sequence, kv head, W consecutive partitions) and
+//     warp w handles partition w of it alone, writing its normalised partial
+//     output and (max, sum) to the caller's workspace -- no merge inside the
+//     CTA; a second kernel merges partitions with log-sum-exp weights;
+//   * a KV job is read once for all H / G query heads of its kv head: with a
 //     group of >= 4 heads on 16-bit data the step is a small dense contraction
 //     and runs on mma.sync m16n8k16 (tokens x heads for q K^T, d x heads for
 //     P V); otherwise (MHA, fp32) lanes split head_dim and use FFMA;
-//   * the softmax is online, in fp32, base 2, with warp shuffles for the block
-//     maxima; at the end of an item the W warps' partial (max, sum, output)
-//     triples are merged through shared memory;
-//   * split mode writes the normalised partial output and its (max, sum) to a
-//     caller workspace; a second kernel merges partitions with log-sum-exp
-//     weights.
+//   * the softmax is online, in fp32, base 2, with warp shuffles for the maxima.
 #pragma once
 
 #include "pa_device.cuh"
 
 namespace pa {
 
-constexpr int kMaxGroup = 8;         // query heads per kv head
-constexpr int kSortMaxSeqs = 1024;   // longest-first ordering up to this batch size
-constexpr int kSplitMaxSeqs = 2048;  // split mode keeps per-sequence offsets in shared memory
-constexpr int kLenBucketShift = 9;   // sort key: context length / 512
+constexpr int kMaxGroup = 8;          // query heads per kv head
+constexpr int kSortMaxSeqs = 2048;    // longest-first ordering up to this batch size
+constexpr int kSplitMaxSeqs = 2048;   // split mode keeps per-sequence offsets in shared memory
+constexpr int kLenBucketShift = 9;    // sort key: context length / 512
+constexpr int kNumBuckets = 1024;     // longer contexts share the top bucket
+constexpr int kJobTokens = 16;        // tokens per TMA job
 
 struct DecodeParams {
-  void* out;                    // [S][H][D] out dtype (non-split)
+  void* out;                    // [S][H][D] out dtype (plain mode)
   const void* q;                // [S][H][D]
   const int32_t* block_tables;  // [S][max_blocks]
   const int32_t* context_lens;  // [S]
   int max_blocks;
-  int block_size;
+  int block_size;               // 16 or 32
+  int block_shift;              // log2(block_size)
   int S, H, G, group;
   long long num_blocks;
   float scale_log2;             // scale * log2(e)
@@ -58,29 +64,30 @@ struct DecodeParams {
 };
 
 struct SmemLayout {
-  unsigned stage_bytes, bars_off, merge_off, q_off, sched_off, misc_off, total;
+  unsigned stage_bytes, bars_off, ok_off, merge_off, q_off, sched_off, misc_off, total;
 };
 
 __host__ __device__ inline unsigned round_up(unsigned x, unsigned a) { return (x + a - 1) / a * a; }
 
 // Shared-memory map, computed identically on the host (launch size) and device.
-__host__ __device__ inline SmemLayout make_layout(int W, int R, int D, int BS, int esize, int group, bool vec,
-                                                  bool split, int S) {
+__host__ __device__ inline SmemLayout make_layout(int W, int R, int D, int esize, int group, bool vec, bool split,
+                                                  int S) {
   SmemLayout L;
-  L.stage_bytes = 2u * BS * D * esize;
+  L.stage_bytes = 2u * kJobTokens * D * esize;
   unsigned off = W * R * L.stage_bytes;
   L.bars_off = off;
   off += W * R * 8;
-  off = round_up(off, 16);
+  L.ok_off = off;
+  off = round_up(off + W * R, 16);
   L.merge_off = off;
-  off += W * group * D * 4 + W * kMaxGroup * 2 * 4;
+  if (!split) off += W * group * D * 4 + W * kMaxGroup * 2 * 4;
   L.q_off = off;
   if (vec) off += W * group * D * 4;
   L.sched_off = off;
   if (split)
-    off += (2 * S + 1) * 4;
+    off += (S + 1) * 4;
   else if (S <= kSortMaxSeqs)
-    off += 2 * S * 4;
+    off += S * 2;
   off = round_up(off, 16);
   L.misc_off = off;
   off += 16;
@@ -88,16 +95,18 @@ __host__ __device__ inline SmemLayout make_layout(int W, int R, int D, int BS, i
   return L;
 }
 
-template <typename DT, int D, int BS, bool MMA>
+template <typename DT, int D, bool MMA>
 struct StageCfg {
   static constexpr int E = sizeof(DT);
-  static constexpr int kStage = 2 * BS * D * E;
+  static constexpr int TILE = kJobTokens * D * E;  // one K (or V) job tile
+  static constexpr int kStage = 2 * TILE;
   static constexpr int W = 4;
-  static constexpr int R = kStage <= 4096 ? 4 : (kStage <= 16384 ? 3 : 1);
+  static constexpr int R = kStage <= 4096 ? 4 : 3;
 };
 
 struct Item {
-  int s, kv, t0, t1, part;
+  int s, kv, part;   // part: split mode, this warp's partition (-1: none)
+  int t0, t1;        // this warp's token range (plain mode: the whole context)
 };
 
 // Context length of sequence s, clamped to what the table (and, in split mode,
@@ -116,18 +125,14 @@ __device__ __forceinline__ int clamp_ctx(const DecodeParams& p, int s, bool spli
   return c;
 }
 
-template <bool SPLIT>
+template <bool SPLIT, int W>
 struct Schedule {
-  const int* ctx;    // clamped context lengths (shared memory) or nullptr
-  const int* aux;    // order[] (decode) or pstart[] (split)
+  const uint16_t* order;  // plain mode: sequences longest-first (nullptr: batch order)
+  const int* pstart;      // split mode: first item of each sequence, [S + 1]
   int num_items;
 
-  __device__ __forceinline__ int seq_ctx(const DecodeParams& p, int s, int BS) const {
-    return ctx ? ctx[s] : clamp_ctx(p, s, SPLIT);
-  }
-
-  // k-th item of this CTA (serpentine deal over the grid).
-  __device__ __forceinline__ bool get(const DecodeParams& p, int BS, int k, Item& it) const {
+  // k-th item of this CTA (serpentine deal over the grid), as seen by `warp`.
+  __device__ __forceinline__ bool get(const DecodeParams& p, int k, int warp, Item& it) const {
     const int pos = (k & 1) ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x;
     const long long i = (long long)k * gridDim.x + pos;
     if (i >= num_items) return false;
@@ -137,46 +142,52 @@ struct Schedule {
     if (SPLIT) {
       int lo = 0, hi = p.S - 1;  // last s with pstart[s] <= qi
       while (lo < hi) {
-        int mid = (lo + hi + 1) >> 1;
-        if (aux[mid] <= qi) lo = mid; else hi = mid - 1;
+        const int mid = (lo + hi + 1) >> 1;
+        if (pstart[mid] <= qi) lo = mid; else hi = mid - 1;
       }
       it.s = lo;
-      it.part = qi - aux[lo];
-      const int c = ctx[lo];
-      it.t0 = it.part * p.partition;
-      it.t1 = min(it.t0 + p.partition, c);
+      const int c = clamp_ctx(p, lo, true);
+      const int nparts = (c + p.partition - 1) / p.partition;
+      const int part = (qi - pstart[lo]) * W + warp;
+      if (part < nparts) {
+        it.part = part;
+        it.t0 = part * p.partition;
+        it.t1 = min(it.t0 + p.partition, c);
+      } else {
+        it.part = -1;
+        it.t0 = it.t1 = 0;
+      }
     } else {
-      it.s = aux ? aux[qi] : qi;
+      it.s = order ? (int)order[qi] : qi;
       it.part = 0;
       it.t0 = 0;
-      it.t1 = seq_ctx(p, it.s, BS);
+      it.t1 = clamp_ctx(p, it.s, false);
     }
     return true;
   }
 };
 
-template <typename DT, typename OT, int D, int BS, bool MMA, bool SPLIT>
-__global__ void __launch_bounds__(StageCfg<DT, D, BS, MMA>::W * 32)
+template <typename DT, typename OT, int D, bool MMA, bool SPLIT>
+__global__ void __launch_bounds__(StageCfg<DT, D, MMA>::W * 32)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         const DecodeParams p) {
-  using Cfg = StageCfg<DT, D, BS, MMA>;
-  constexpr int W = Cfg::W, R = Cfg::R, E = Cfg::E;
-  constexpr int TILE = BS * D * E;
+  using Cfg = StageCfg<DT, D, MMA>;
+  constexpr int W = Cfg::W, R = Cfg::R, E = Cfg::E, TILE = Cfg::TILE, JT = kJobTokens;
   constexpr int NCH = D * E / 16;     // 16-byte chunks per row
   constexpr int NREG = D * E / 128;   // 128-byte column regions (one TMA box each)
   constexpr int BOX_X = 128 / E;
   static_assert(NREG >= 1 && D * E % 128 == 0, "head_dim * element size must be a multiple of 128 bytes");
-  static_assert(!MMA || (sizeof(DT) == 2 && BS % 16 == 0 && D % 16 == 0), "mma path needs 16-bit data");
+  static_assert(!MMA || (sizeof(DT) == 2 && D % 16 == 0), "mma path needs 16-bit data");
 
   extern __shared__ uint8_t smem_raw[];
   // TMA 128-byte swizzling needs 1024-byte aligned destinations: align the shared-window offset.
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const SmemLayout L = make_layout(W, R, D, BS, E, p.group, !MMA, SPLIT, p.S);
+  const SmemLayout L = make_layout(W, R, D, E, p.group, !MMA, SPLIT, p.S);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars_off);
-  float* mrg_o = reinterpret_cast<float*>(smem + L.merge_off);        // [W][group][D]
+  volatile uint8_t* stage_ok = smem + L.ok_off;                        // [W][R]
+  float* mrg_o = reinterpret_cast<float*>(smem + L.merge_off);        // [W][group][D] (plain mode)
   float* mrg_ml = mrg_o + W * p.group * D;                             // [W][kMaxGroup][2]
   float* qs_all = reinterpret_cast<float*>(smem + L.q_off);            // [W][group][D] (vector path)
-  int* sched = reinterpret_cast<int*>(smem + L.sched_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc_off);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -192,89 +203,116 @@ __global__ void __launch_bounds__(StageCfg<DT, D, BS, MMA>::W * 32)
     prefetch_tensormap(&vmap);
   }
 
-  // ---- schedule tables -----------------------------------------------------
-  Schedule<SPLIT> sch;
-  sch.ctx = nullptr;
-  sch.aux = nullptr;
+  // ---- schedule tables (the stage buffers are free until the first copy) ------
+  Schedule<SPLIT, W> sch;
+  sch.order = nullptr;
+  sch.pstart = nullptr;
   if (SPLIT) {
-    int* ctxs = sched;
-    int* pstart = sched + p.S;
-    for (int s = tid; s < p.S; s += nthreads) ctxs[s] = clamp_ctx(p, s, true);
-    __syncthreads();
+    int* pstart = reinterpret_cast<int*>(smem + L.sched_off);
     if (warp == 0) {
-      // exclusive scan of ceil(ctx / partition) over sequences, lane-chunked
+      // exclusive scan over sequences of ceil(partitions / W), lane-chunked
       const int per = (p.S + 31) / 32;
       const int b = lane * per, e = min(p.S, b + per);
+      auto items_of = [&](int s) {
+        const int c = clamp_ctx(p, s, true);
+        return ((c + p.partition - 1) / p.partition + W - 1) / W;
+      };
       int local = 0;
-      for (int s = b; s < e; ++s) local += (ctxs[s] + p.partition - 1) / p.partition;
+      for (int s = b; s < e; ++s) local += items_of(s);
       int incl = local;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        int v = __shfl_up_sync(0xffffffffu, incl, o);
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += v;
       }
       int run = incl - local;
       for (int s = b; s < e; ++s) {
         pstart[s] = run;
-        run += (ctxs[s] + p.partition - 1) / p.partition;
+        run += items_of(s);
       }
       if (lane == 31) pstart[p.S] = incl;
     }
     __syncthreads();
-    sch.ctx = ctxs;
-    sch.aux = pstart;
+    sch.pstart = pstart;
     sch.num_items = pstart[p.S] * p.G;
   } else {
     sch.num_items = p.S * p.G;
     if (p.S <= kSortMaxSeqs) {
-      int* ctxs = sched;
-      int* order = sched + p.S;
-      for (int s = tid; s < p.S; s += nthreads) ctxs[s] = clamp_ctx(p, s, false);
+      // stable counting sort of the sequences by length bucket, longest first
+      uint16_t* order = reinterpret_cast<uint16_t*>(smem + L.sched_off);
+      int* base = reinterpret_cast<int*>(smem);  // kNumBuckets counters, in stage memory
+      for (int b = tid; b < kNumBuckets; b += nthreads) base[b] = 0;
       __syncthreads();
-      // rank by (length bucket descending, index ascending); ties keep batch order
-      for (int s = tid; s < p.S; s += nthreads) {
-        const int key = ctxs[s] >> kLenBucketShift;
-        int rank = 0;
-        for (int o = 0; o < p.S; ++o) {
-          const int ko = ctxs[o] >> kLenBucketShift;
-          rank += (ko > key) | ((ko == key) & (o < s));
+      auto bucket = [&](int s) {  // ascending bucket index = descending length
+        const int key = min(clamp_ctx(p, s, false) >> kLenBucketShift, kNumBuckets - 1);
+        return kNumBuckets - 1 - key;
+      };
+      for (int s = tid; s < p.S; s += nthreads) atomicAdd(&base[bucket(s)], 1);
+      __syncthreads();
+      if (warp == 0) {
+        constexpr int PER = kNumBuckets / 32;
+        int local = 0;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) local += base[lane * PER + i];
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
         }
-        order[rank] = s;
+        int run = incl - local;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+          const int c = base[lane * PER + i];
+          base[lane * PER + i] = run;
+          run += c;
+        }
+        __syncwarp();
+        const unsigned lt = (1u << lane) - 1u;
+        for (int c0 = 0; c0 < p.S; c0 += 32) {
+          const int s = c0 + lane;
+          const int key = s < p.S ? bucket(s) : -1 - lane;  // padding lanes: keys of their own
+          const unsigned peers = __match_any_sync(0xffffffffu, key);
+          if (s < p.S) order[base[key] + __popc(peers & lt)] = (uint16_t)s;
+          __syncwarp();
+          if (s < p.S && (peers & lt) == 0) base[key] += __popc(peers);
+          __syncwarp();
+        }
       }
       __syncthreads();
-      sch.ctx = ctxs;
-      sch.aux = order;
+      sch.order = order;
     } else {
       __syncthreads();
     }
   }
 
-  // ---- per-warp issue cursor ------------------------------------------------
+  // ---- per-warp issue cursor over this warp's jobs ---------------------------
   uint8_t* my_stages = smem + warp * R * L.stage_bytes;
   uint64_t* my_bars = bars + warp * R;
+  volatile uint8_t* my_ok = stage_ok + warp * R;
+  const int job_step = SPLIT ? 1 : W;
 
   struct Cursor {
-    int k, j, je;
+    int k, u, ue;
     Item it;
     bool valid;
   };
+  auto cursor_range = [&](Cursor& c) {
+    c.u = c.it.t0 / JT + (SPLIT ? 0 : warp);
+    c.ue = (c.it.t1 + JT - 1) / JT;
+  };
   auto cursor_settle = [&](Cursor& c) {
-    while (c.valid && c.j >= c.je) {
+    while (c.valid && c.u >= c.ue) {
       ++c.k;
-      if (!sch.get(p, BS, c.k, c.it)) {
-        c.valid = false;
-        break;
-      }
-      c.j = c.it.t0 / BS + warp;
-      c.je = (c.it.t1 + BS - 1) / BS;
+      c.valid = sch.get(p, c.k, warp, c.it);
+      if (c.valid) cursor_range(c);
     }
   };
   Cursor ic;
   ic.k = 0;
-  ic.valid = sch.get(p, BS, 0, ic.it);
+  ic.valid = sch.get(p, 0, warp, ic.it);
   if (ic.valid) {
-    ic.j = ic.it.t0 / BS + warp;
-    ic.je = (ic.it.t1 + BS - 1) / BS;
+    cursor_range(ic);
     cursor_settle(ic);
   }
 
@@ -282,97 +320,144 @@ __global__ void __launch_bounds__(StageCfg<DT, D, BS, MMA>::W * 32)
     if (lane == 0) {
       const int stage = n % R;
       uint64_t* bar = &my_bars[stage];
-      const long long phys = __ldg(p.block_tables + (long long)c.it.s * p.max_blocks + c.j);
+      const int tok = c.u * JT;
+      const int blk = tok >> p.block_shift;
+      const long long phys = __ldg(p.block_tables + (long long)c.it.s * p.max_blocks + blk);
       if (phys < 0 || phys >= p.num_blocks) {
         atomicOr(p.err, kErrBlockId);
-        mbar_arrive(bar);  // completes the phase with no data; the consumer skips the block
+        my_ok[stage] = 0;
+        mbar_arrive(bar);  // completes the phase with no data; the consumer skips the job
       } else {
+        my_ok[stage] = 1;
         uint8_t* kdst = my_stages + stage * L.stage_bytes;
         uint8_t* vdst = kdst + TILE;
-        const int row = (int)((phys * p.G + c.it.kv) * BS);
+        const int row = (int)((phys * p.G + c.it.kv) << p.block_shift) + (tok - (blk << p.block_shift));
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(bar, 2 * TILE);
 #pragma unroll
         for (int rg = 0; rg < NREG; ++rg) {
-          tma_load_2d(kdst + rg * BS * 128, &kmap, rg * BOX_X, row, bar);
-          tma_load_2d(vdst + rg * BS * 128, &vmap, rg * BOX_X, row, bar);
+          tma_load_2d(kdst + rg * JT * 128, &kmap, rg * BOX_X, row, bar);
+          tma_load_2d(vdst + rg * JT * 128, &vmap, rg * BOX_X, row, bar);
         }
       }
     }
   };
 
-  __syncthreads();  // barrier inits visible before the first copy
+  fence_proxy_async_smem();  // generic writes to stage memory (sort counters) before TMA reuses it
+  __syncthreads();            // barrier inits and schedule tables visible; stage memory free again
 
   int n_issue = 0;
 #pragma unroll 1
   for (int r = 0; r < R && ic.valid; ++r) {
     issue(ic, n_issue++);
-    ic.j += W;
+    ic.u += job_step;
     cursor_settle(ic);
   }
 
   // ---- consume -----------------------------------------------------------------
   int n_done = 0;
   const float NEG_INF = -__int_as_float(0x7f800000);
-  Item it;
-#pragma unroll 1
-  for (int k = 0; sch.get(p, BS, k, it); ++k) {
-    const int hq0 = it.kv * p.group;  // first query head of this kv head
-    const DT* qrow = reinterpret_cast<const DT*>(p.q) + ((long long)it.s * p.H + hq0) * D;
-    const int jb = it.t0 / BS, je = (it.t1 + BS - 1) / BS;
+  auto next_job = [&](int& stage_out) -> bool {  // wait for this warp's next job
+    stage_out = n_done % R;
+    bool ok = mbar_wait_bounded(&my_bars[stage_out], (n_done / R) & 1, abort_flag, p.err, kWaitLimitNs);
+    ok = __all_sync(0xffffffffu, ok);
+    return ok && my_ok[stage_out];
+  };
+  auto job_done = [&]() {  // release the stage and refill it with the job R ahead
+    __syncwarp();
+    ++n_done;
+    if (ic.valid && !*abort_flag) {
+      issue(ic, n_issue++);
+      ic.u += job_step;
+      cursor_settle(ic);
+    }
+  };
+  // Plain mode: merge the W warps' partials of the current item and write it.
+  auto merge_and_write = [&](const Item& x) {
+    asm volatile("bar.sync 1, %0;" ::"n"(W * 32) : "memory");
+    const int hq0 = x.kv * p.group;
+    for (int idx = tid; idx < p.group * D; idx += nthreads) {
+      const int h = idx / D, i = idx - h * D;
+      float M = NEG_INF;
+#pragma unroll
+      for (int w = 0; w < W; ++w) {
+        if (mrg_ml[(w * kMaxGroup + h) * 2 + 1] > 0.f) M = fmaxf(M, mrg_ml[(w * kMaxGroup + h) * 2 + 0]);
+      }
+      float Lsum = 0.f, O = 0.f;
+#pragma unroll
+      for (int w = 0; w < W; ++w) {
+        const float l = mrg_ml[(w * kMaxGroup + h) * 2 + 1];
+        if (l > 0.f) {
+          const float f = exp2f(mrg_ml[(w * kMaxGroup + h) * 2 + 0] - M);
+          Lsum = fmaf(l, f, Lsum);
+          O = fmaf(mrg_o[(w * p.group + h) * D + i], f, O);
+        }
+      }
+      reinterpret_cast<OT*>(p.out)[((long long)x.s * p.H + hq0 + h) * D + i] =
+          from_f32<OT>(Lsum > 0.f ? O / Lsum : 0.f);
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(W * 32) : "memory");
+  };
 
-    if constexpr (MMA) {
-      // ---------------- tensor-core path: group >= 4, 16-bit data ----------------
-      const int g = lane >> 2, t4 = lane & 3;
-      uint32_t qf[D / 16][2];
+  Item it;
+  if constexpr (MMA) {
+    // ---------------- tensor-core path: group >= 4, 16-bit data ----------------
+    const int g = lane >> 2, t4 = lane & 3;
+    uint32_t qf[D / 16][2], qn[D / 16][2];
+    auto load_q = [&](const Item& x, uint32_t (&dst)[D / 16][2]) {
+      const DT* qrow = reinterpret_cast<const DT*>(p.q) + ((long long)x.s * p.H + x.kv * p.group) * D;
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
         if (g < p.group) {
           const DT* qr = qrow + (long long)g * D + ks * 16 + 2 * t4;
-          qf[ks][0] = __ldg(reinterpret_cast<const uint32_t*>(qr));
-          qf[ks][1] = __ldg(reinterpret_cast<const uint32_t*>(qr + 8));
+          dst[ks][0] = __ldg(reinterpret_cast<const uint32_t*>(qr));
+          dst[ks][1] = __ldg(reinterpret_cast<const uint32_t*>(qr + 8));
         } else {
-          qf[ks][0] = 0u;
-          qf[ks][1] = 0u;
+          dst[ks][0] = 0u;
+          dst[ks][1] = 0u;
         }
       }
+    };
+    bool have = sch.get(p, 0, warp, it);
+    if (have) load_q(it, qn);
+#pragma unroll 1
+    for (int k = 0; have; ++k) {
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        qf[ks][0] = qn[ks][0];
+        qf[ks][1] = qn[ks][1];
+      }
+      Item nx;
+      const bool have_next = sch.get(p, k + 1, warp, nx);
+      if (have_next) load_q(nx, qn);  // in flight while this item streams
+
       float o[D / 16][4];
 #pragma unroll
       for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
       float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
-
+      const int ub = it.t0 / JT + (SPLIT ? 0 : warp), ue = (it.t1 + JT - 1) / JT;
 #pragma unroll 1
-      for (int j = jb + warp; j < je; j += W) {
-        const int stage = n_done % R;
-        bool ok = mbar_wait_bounded(&my_bars[stage], (n_done / R) & 1, abort_flag, p.err, kWaitLimitNs);
-        ok = __all_sync(0xffffffffu, ok);
-        const long long phys = __ldg(p.block_tables + (long long)it.s * p.max_blocks + j);
-        if (ok && phys >= 0 && phys < p.num_blocks) {
+      for (int u = ub; u < ue; u += job_step) {
+        int stage;
+        if (next_job(stage)) {
           const uint32_t kt = smem_u32(my_stages + stage * L.stage_bytes);
           const uint32_t vt = kt + TILE;
-          const int nv = min(BS, it.t1 - j * BS);
-          constexpr int NSUB = BS / 16;
-          float sc[NSUB][4];
+          const int nv = min(JT, it.t1 - u * JT);
+          float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int sub = 0; sub < NSUB; ++sub) {
-            sc[sub][0] = sc[sub][1] = sc[sub][2] = sc[sub][3] = 0.f;
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-              uint32_t a[4];
-              ldsm_x4(a, kt + sw128_offset(sub * 16 + (lane & 15), ks * 2 + (lane >> 4), BS));
-              Mma<DT>::run(sc[sub], a, qf[ks][0], qf[ks][1]);
-            }
+          for (int ks = 0; ks < D / 16; ++ks) {
+            uint32_t a[4];
+            ldsm_x4(a, kt + sw128_offset(lane & 15, ks * 2 + (lane >> 4), JT));
+            Mma<DT>::run(sc, a, qf[ks][0], qf[ks][1]);
           }
+          // sc[e]: token g + 8*(e>>1), head 2*t4 + (e&1)
           float mx0 = NEG_INF, mx1 = NEG_INF;
 #pragma unroll
-          for (int sub = 0; sub < NSUB; ++sub) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int tok = sub * 16 + g + ((e >> 1) << 3);
-              const float z = tok < nv ? sc[sub][e] * p.scale_log2 : NEG_INF;
-              sc[sub][e] = z;
-              if (e & 1) mx1 = fmaxf(mx1, z); else mx0 = fmaxf(mx0, z);
-            }
+          for (int e = 0; e < 4; ++e) {
+            const int tok = g + ((e >> 1) << 3);
+            const float z = tok < nv ? sc[e] * p.scale_log2 : NEG_INF;
+            sc[e] = z;
+            if (e & 1) mx1 = fmaxf(mx1, z); else mx0 = fmaxf(mx0, z);
           }
 #pragma unroll
           for (int o2 = 4; o2 < 32; o2 <<= 1) {
@@ -383,18 +468,12 @@ __global__ void __launch_bounds__(StageCfg<DT, D, BS, MMA>::W * 32)
           const float c0 = exp2f(m0 - mn0), c1 = exp2f(m1 - mn1);
           m0 = mn0;
           m1 = mn1;
-          float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-          for (int sub = 0; sub < NSUB; ++sub) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float pv = exp2f(sc[sub][e] - ((e & 1) ? mn1 : mn0));
-              sc[sub][e] = pv;
-              if (e & 1) s1 += pv; else s0 += pv;
-            }
-          }
-          l0 = l0 * c0 + s0;
-          l1 = l1 * c1 + s1;
+          sc[0] = exp2f(sc[0] - mn0);
+          sc[1] = exp2f(sc[1] - mn1);
+          sc[2] = exp2f(sc[2] - mn0);
+          sc[3] = exp2f(sc[3] - mn1);
+          l0 = l0 * c0 + sc[0] + sc[2];
+          l1 = l1 * c1 + sc[1] + sc[3];
 #pragma unroll
           for (int mt = 0; mt < D / 16; ++mt) {
             o[mt][0] *= c0;
@@ -407,84 +486,111 @@ __global__ void __launch_bounds__(StageCfg<DT, D, BS, MMA>::W * 32)
           // weight, too coarse for a 2e-3 bound when a few tokens dominate, so P is
           // split into hi + lo 16-bit parts (P - hi - lo is below 2^-17 P) and each
           // part gets its own MMA into the same fp32 accumulator.
+          const uint32_t h01 = Mma<DT>::pack(sc[0], sc[1]);
+          const uint32_t h23 = Mma<DT>::pack(sc[2], sc[3]);
+          float r0, r1, r2, r3;
+          unpack2(h01, (DT*)nullptr, r0, r1);
+          unpack2(h23, (DT*)nullptr, r2, r3);
+          const uint32_t b0 = movmatrix_trans(h01);
+          const uint32_t b1 = movmatrix_trans(h23);
+          const uint32_t e0 = movmatrix_trans(Mma<DT>::pack(sc[0] - r0, sc[1] - r1));
+          const uint32_t e1 = movmatrix_trans(Mma<DT>::pack(sc[2] - r2, sc[3] - r3));
+          const int vtok = ((lane >> 4) << 3) + (lane & 7);
+          // tokens held by this lane's A fragments: lo pair (a0, a1), hi pair (a2, a3);
+          // rows past the context are zeroed so that 0 * (stale or NaN) cannot leak in
+          const int tlo = 2 * t4;
+          const uint32_t mlo = (tlo < nv ? 0x0000ffffu : 0u) | (tlo + 1 < nv ? 0xffff0000u : 0u);
+          const uint32_t mhi = (tlo + 8 < nv ? 0x0000ffffu : 0u) | (tlo + 9 < nv ? 0xffff0000u : 0u);
 #pragma unroll
-          for (int sub = 0; sub < NSUB; ++sub) {
-            const uint32_t h01 = Mma<DT>::pack(sc[sub][0], sc[sub][1]);
-            const uint32_t h23 = Mma<DT>::pack(sc[sub][2], sc[sub][3]);
-            float r0, r1, r2, r3;
-            unpack2(h01, (DT*)nullptr, r0, r1);
-            unpack2(h23, (DT*)nullptr, r2, r3);
-            const uint32_t b0 = movmatrix_trans(h01);
-            const uint32_t b1 = movmatrix_trans(h23);
-            const uint32_t c0 = movmatrix_trans(Mma<DT>::pack(sc[sub][0] - r0, sc[sub][1] - r1));
-            const uint32_t c1 = movmatrix_trans(Mma<DT>::pack(sc[sub][2] - r2, sc[sub][3] - r3));
-            const int vtok = sub * 16 + ((lane >> 4) << 3) + (lane & 7);
-            // tokens held by this lane's A fragments: lo pair (a0, a1), hi pair (a2, a3)
-            const int tlo = sub * 16 + 2 * t4;
-            const uint32_t mlo = (tlo < nv ? 0x0000ffffu : 0u) | (tlo + 1 < nv ? 0xffff0000u : 0u);
-            const uint32_t mhi = (tlo + 8 < nv ? 0x0000ffffu : 0u) | (tlo + 9 < nv ? 0xffff0000u : 0u);
-#pragma unroll
-            for (int mt = 0; mt < D / 16; ++mt) {
-              uint32_t a[4];
-              ldsm_x4_trans(a, vt + sw128_offset(vtok, mt * 2 + ((lane >> 3) & 1), BS));
-              a[0] &= mlo;
-              a[1] &= mlo;
-              a[2] &= mhi;
-              a[3] &= mhi;
-              Mma<DT>::run(o[mt], a, b0, b1);
-              Mma<DT>::run(o[mt], a, c0, c1);
-            }
+          for (int mt = 0; mt < D / 16; ++mt) {
+            uint32_t a[4];
+            ldsm_x4_trans(a, vt + sw128_offset(vtok, mt * 2 + ((lane >> 3) & 1), JT));
+            a[0] &= mlo;
+            a[1] &= mlo;
+            a[2] &= mhi;
+            a[3] &= mhi;
+            Mma<DT>::run(o[mt], a, b0, b1);
+            Mma<DT>::run(o[mt], a, e0, e1);
           }
         }
-        __syncwarp();
-        ++n_done;
-        if (ic.valid && !*abort_flag) {
-          issue(ic, n_issue++);
-          ic.j += W;
-          cursor_settle(ic);
-        }
+        job_done();
       }
-      // warp partials -> shared memory
 #pragma unroll
       for (int o2 = 4; o2 < 32; o2 <<= 1) {
         l0 += __shfl_xor_sync(0xffffffffu, l0, o2);
         l1 += __shfl_xor_sync(0xffffffffu, l1, o2);
       }
       const int hA = 2 * t4, hB = hA + 1;
-      float* mo = mrg_o + warp * p.group * D;
-      if (hA < p.group) {
+      if (SPLIT) {
+        if (it.part >= 0) {
+          const long long rowA = ((long long)it.s * p.H + it.kv * p.group + hA) * p.max_partitions + it.part;
+          const long long rowB = rowA + p.max_partitions;
+          const float iA = l0 > 0.f ? 1.f / l0 : 0.f, iB = l1 > 0.f ? 1.f / l1 : 0.f;
+          if (hA < p.group) {
 #pragma unroll
-        for (int mt = 0; mt < D / 16; ++mt) {
-          mo[hA * D + mt * 16 + g] = o[mt][0];
-          mo[hA * D + mt * 16 + g + 8] = o[mt][2];
-        }
-      }
-      if (hB < p.group) {
+            for (int mt = 0; mt < D / 16; ++mt) {
+              p.ws_o[rowA * D + mt * 16 + g] = o[mt][0] * iA;
+              p.ws_o[rowA * D + mt * 16 + g + 8] = o[mt][2] * iA;
+            }
+            if (g == 0) {
+              p.ws_m[rowA] = m0;
+              p.ws_l[rowA] = l0;
+            }
+          }
+          if (hB < p.group) {
 #pragma unroll
-        for (int mt = 0; mt < D / 16; ++mt) {
-          mo[hB * D + mt * 16 + g] = o[mt][1];
-          mo[hB * D + mt * 16 + g + 8] = o[mt][3];
+            for (int mt = 0; mt < D / 16; ++mt) {
+              p.ws_o[rowB * D + mt * 16 + g] = o[mt][1] * iB;
+              p.ws_o[rowB * D + mt * 16 + g + 8] = o[mt][3] * iB;
+            }
+            if (g == 0) {
+              p.ws_m[rowB] = m1;
+              p.ws_l[rowB] = l1;
+            }
+          }
         }
+      } else {
+        float* mo = mrg_o + warp * p.group * D;
+        if (hA < p.group) {
+#pragma unroll
+          for (int mt = 0; mt < D / 16; ++mt) {
+            mo[hA * D + mt * 16 + g] = o[mt][0];
+            mo[hA * D + mt * 16 + g + 8] = o[mt][2];
+          }
+        }
+        if (hB < p.group) {
+#pragma unroll
+          for (int mt = 0; mt < D / 16; ++mt) {
+            mo[hB * D + mt * 16 + g] = o[mt][1];
+            mo[hB * D + mt * 16 + g + 8] = o[mt][3];
+          }
+        }
+        if (g == 0) {
+          float* ml = mrg_ml + warp * kMaxGroup * 2;
+          ml[hA * 2 + 0] = m0;
+          ml[hA * 2 + 1] = l0;
+          ml[hB * 2 + 0] = m1;
+          ml[hB * 2 + 1] = l1;
+        }
+        merge_and_write(it);
       }
-      if (g == 0) {
-        float* ml = mrg_ml + warp * kMaxGroup * 2;
-        ml[hA * 2 + 0] = m0;
-        ml[hA * 2 + 1] = l0;
-        ml[hB * 2 + 0] = m1;
-        ml[hB * 2 + 1] = l1;
-      }
-    } else {
-      // ---------------- vector path: lanes split head_dim, FFMA ----------------
-      constexpr int LPT = 32 / BS;        // lanes per token in q K^T
-      constexpr int CPL = NCH / LPT;      // 16-byte K chunks per lane
-      constexpr int EPC = 16 / E;         // elements per 16-byte chunk
-      constexpr int EPL = D / 32;         // output elements per lane in P V
-      constexpr int VB = EPL * E;         // V bytes per lane per row
-      static_assert(32 % BS == 0 || BS == 32, "block size must divide 32");
-      float* qs = qs_all + warp * p.group * D;
+      have = have_next;
+      it = nx;
+    }
+  } else {
+    // ---------------- vector path: lanes split head_dim, FFMA ----------------
+    constexpr int LPT = 32 / JT;        // lanes per token in q K^T (2)
+    constexpr int CPL = NCH / LPT;      // 16-byte K chunks per lane
+    constexpr int EPC = 16 / E;         // elements per 16-byte chunk
+    constexpr int EPL = D / 32;         // output elements per lane in P V
+    constexpr int VB = EPL * E;         // V bytes per lane per row
+    float* qs = qs_all + warp * p.group * D;
+    const int t = lane % JT, part = lane / JT;
+#pragma unroll 1
+    for (int k = 0; sch.get(p, k, warp, it); ++k) {
+      const DT* qrow = reinterpret_cast<const DT*>(p.q) + ((long long)it.s * p.H + it.kv * p.group) * D;
       for (int i = lane; i < p.group * D; i += 32) qs[i] = to_f32(qrow[i]);
       __syncwarp();
-      const int t = lane % BS, part = lane / BS;
       float o[kMaxGroup][EPL];
       float mr[kMaxGroup], lr[kMaxGroup];
 #pragma unroll
@@ -494,17 +600,14 @@ __global__ void __launch_bounds__(StageCfg<DT, D, BS, MMA>::W * 32)
 #pragma unroll
         for (int e = 0; e < EPL; ++e) o[h][e] = 0.f;
       }
+      const int ub = it.t0 / JT + (SPLIT ? 0 : warp), ue = (it.t1 + JT - 1) / JT;
 #pragma unroll 1
-      for (int j = jb + warp; j < je; j += W) {
-        const int stage = n_done % R;
-        bool ok = mbar_wait_bounded(&my_bars[stage], (n_done / R) & 1, abort_flag, p.err, kWaitLimitNs);
-        ok = __all_sync(0xffffffffu, ok);
-        const long long phys = __ldg(p.block_tables + (long long)it.s * p.max_blocks + j);
-        if (ok && phys >= 0 && phys < p.num_blocks) {
+      for (int u = ub; u < ue; u += job_step) {
+        int stage;
+        if (next_job(stage)) {
           const uint8_t* kt = my_stages + stage * L.stage_bytes;
           const uint8_t* vt = kt + TILE;
-          const int nv = min(BS, it.t1 - j * BS);
-          // this lane's K chunks (row t), as floats
+          const int nv = min(JT, it.t1 - u * JT);
 #pragma unroll
           for (int h = 0; h < kMaxGroup; ++h) {
             if (h >= p.group) break;
@@ -513,7 +616,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, BS, MMA>::W * 32)
 #pragma unroll
             for (int c = 0; c < CPL; ++c) {
               const int ch = part * CPL + c;
-              const uint4 raw = *reinterpret_cast<const uint4*>(kt + sw128_offset(t, ch, BS));
+              const uint4 raw = *reinterpret_cast<const uint4*>(kt + sw128_offset(t, ch, JT));
               const float4* qv = reinterpret_cast<const float4*>(qh + ch * EPC);
               if constexpr (E == 4) {
                 const float4 qa = qv[0];
@@ -542,7 +645,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, BS, MMA>::W * 32)
             z = t < nv ? z * p.scale_log2 : NEG_INF;
             float mx = z;
 #pragma unroll
-            for (int o2 = 1; o2 < 32; o2 <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+            for (int o2 = 1; o2 < 16; o2 <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
             const float mn = fmaxf(mr[h], mx);
             const float corr = exp2f(mr[h] - mn);
             mr[h] = mn;
@@ -554,7 +657,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, BS, MMA>::W * 32)
             for (int tt = 0; tt < nv; ++tt) {
               const float w = __shfl_sync(0xffffffffu, pt, tt);
               const int byte = lane * VB;
-              const uint8_t* src = vt + sw128_offset(tt, byte >> 4, BS) + (byte & 15);
+              const uint8_t* src = vt + sw128_offset(tt, byte >> 4, JT) + (byte & 15);
               if constexpr (E == 4) {
                 if constexpr (VB == 16) {
                   const float4 v = *reinterpret_cast<const float4*>(src);
@@ -588,13 +691,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, BS, MMA>::W * 32)
             }
           }
         }
-        __syncwarp();
-        ++n_done;
-        if (ic.valid && !*abort_flag) {
-          issue(ic, n_issue++);
-          ic.j += W;
-          cursor_settle(ic);
-        }
+        job_done();
       }
       float* mo = mrg_o + warp * p.group * D;
       float* ml = mrg_ml + warp * kMaxGroup * 2;
@@ -604,49 +701,28 @@ __global__ void __launch_bounds__(StageCfg<DT, D, BS, MMA>::W * 32)
         float l = lr[h];
 #pragma unroll
         for (int o2 = 1; o2 < 32; o2 <<= 1) l += __shfl_xor_sync(0xffffffffu, l, o2);
+        if (SPLIT) {
+          if (it.part >= 0) {
+            const long long row = ((long long)it.s * p.H + it.kv * p.group + h) * p.max_partitions + it.part;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) mo[h * D + lane * EPL + e] = o[h][e];
-        if (lane == 0) {
-          ml[h * 2 + 0] = mr[h];
-          ml[h * 2 + 1] = l;
+            for (int e = 0; e < EPL; ++e) p.ws_o[row * D + lane * EPL + e] = o[h][e] * inv;
+            if (lane == 0) {
+              p.ws_m[row] = mr[h];
+              p.ws_l[row] = l;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) mo[h * D + lane * EPL + e] = o[h][e];
+          if (lane == 0) {
+            ml[h * 2 + 0] = mr[h];
+            ml[h * 2 + 1] = l;
+          }
         }
       }
+      if (!SPLIT) merge_and_write(it);
     }
-
-    // ---- merge the W warps' partials and write ---------------------------------
-    asm volatile("bar.sync 1, %0;" ::"n"(W * 32) : "memory");
-    for (int idx = tid; idx < p.group * D; idx += nthreads) {
-      const int h = idx / D, i = idx - h * D;
-      float M = NEG_INF;
-#pragma unroll
-      for (int w = 0; w < W; ++w) {
-        const float l = mrg_ml[(w * kMaxGroup + h) * 2 + 1];
-        if (l > 0.f) M = fmaxf(M, mrg_ml[(w * kMaxGroup + h) * 2 + 0]);
-      }
-      float Lsum = 0.f, O = 0.f;
-#pragma unroll
-      for (int w = 0; w < W; ++w) {
-        const float l = mrg_ml[(w * kMaxGroup + h) * 2 + 1];
-        if (l > 0.f) {
-          const float f = exp2f(mrg_ml[(w * kMaxGroup + h) * 2 + 0] - M);
-          Lsum = fmaf(l, f, Lsum);
-          O = fmaf(mrg_o[(w * p.group + h) * D + i], f, O);
-        }
-      }
-      const float res = Lsum > 0.f ? O / Lsum : 0.f;
-      const int hq = hq0 + h;
-      if (SPLIT) {
-        const long long row = ((long long)it.s * p.H + hq) * p.max_partitions + it.part;
-        p.ws_o[row * D + i] = res;
-        if (i == 0) {
-          p.ws_m[row] = M;
-          p.ws_l[row] = Lsum;
-        }
-      } else {
-        reinterpret_cast<OT*>(p.out)[((long long)it.s * p.H + hq) * D + i] = from_f32<OT>(res);
-      }
-    }
-    asm volatile("bar.sync 1, %0;" ::"n"(W * 32) : "memory");
   }
 
   // ---- let every copy this warp started land before the block exits ------------

@@ -8,12 +8,12 @@
 
 namespace pa {
 
-template <typename DT, typename OT, int D, int BS, bool MMA, bool SPLIT>
+template <typename DT, typename OT, int D, bool MMA, bool SPLIT>
 pa_status launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                         int num_sms, long long max_items, cudaStream_t stream) {
-  using Cfg = StageCfg<DT, D, BS, MMA>;
-  auto kern = paged_decode_kernel<DT, OT, D, BS, MMA, SPLIT>;
-  const SmemLayout L = make_layout(Cfg::W, Cfg::R, D, BS, Cfg::E, p.group, !MMA, SPLIT, p.S);
+  using Cfg = StageCfg<DT, D, MMA>;
+  auto kern = paged_decode_kernel<DT, OT, D, MMA, SPLIT>;
+  const SmemLayout L = make_layout(Cfg::W, Cfg::R, D, Cfg::E, p.group, !MMA, SPLIT, p.S);
   if (L.total > 227u * 1024u) return PA_ERR_UNSUPPORTED;
 
   // Opt in to the dynamic shared memory once per device, and remember the
@@ -61,11 +61,11 @@ pa_status launch_lse_reduce(const DecodeParams& p, cudaStream_t stream) {
 
 // Explicit instantiations for one element type DT (the tensor-core path only
 // exists for 16-bit types).
-#define PA_INSTANTIATE_DECODE(DT, OT, D, BS, MMA)                                                        \
-  template pa_status pa::launch_decode<DT, OT, D, BS, MMA, false>(const CUtensorMap&, const CUtensorMap&, \
-                                                                  const pa::DecodeParams&, int, long long, \
-                                                                  cudaStream_t);
-#define PA_INSTANTIATE_SPLIT(DT, D, BS, MMA)                                                               \
-  template pa_status pa::launch_decode<DT, float, D, BS, MMA, true>(const CUtensorMap&, const CUtensorMap&, \
-                                                                    const pa::DecodeParams&, int, long long, \
-                                                                    cudaStream_t);
+#define PA_INSTANTIATE_DECODE(DT, OT, D, MMA)                                                        \
+  template pa_status pa::launch_decode<DT, OT, D, MMA, false>(const CUtensorMap&, const CUtensorMap&, \
+                                                              const pa::DecodeParams&, int, long long, \
+                                                              cudaStream_t);
+#define PA_INSTANTIATE_SPLIT(DT, D, MMA)                                                               \
+  template pa_status pa::launch_decode<DT, float, D, MMA, true>(const CUtensorMap&, const CUtensorMap&, \
+                                                                const pa::DecodeParams&, int, long long, \
+                                                                cudaStream_t);
