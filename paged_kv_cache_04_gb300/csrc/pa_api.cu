@@ -101,17 +101,17 @@ pa_status check_decode(const DecodeArgs& a) {
 template <typename DT, typename OT, int D>
 pa_status dispatch_path(const CUtensorMap& km, const CUtensorMap& vm, const DecodeParams& p, int sms,
                         long long items, bool split, cudaStream_t st) {
-  const bool mma = sizeof(DT) == 2 && p.group >= 4;
-  if (split) {
-    if constexpr (sizeof(DT) == 2) {
-      if (mma) return launch_decode<DT, float, D, true, true>(km, vm, p, sms, items, st);
-    }
-    return launch_decode<DT, float, D, false, true>(km, vm, p, sms, items, st);
-  }
+  // group >= 4 on 16-bit data: tensor cores; MHA: vector path with q in registers
   if constexpr (sizeof(DT) == 2) {
-    if (mma) return launch_decode<DT, OT, D, true, false>(km, vm, p, sms, items, st);
+    if (p.group >= 4)
+      return split ? launch_decode<DT, float, D, kPathMma, true>(km, vm, p, sms, items, st)
+                   : launch_decode<DT, OT, D, kPathMma, false>(km, vm, p, sms, items, st);
   }
-  return launch_decode<DT, OT, D, false, false>(km, vm, p, sms, items, st);
+  if (p.group == 1)
+    return split ? launch_decode<DT, float, D, kPathVecMha, true>(km, vm, p, sms, items, st)
+                 : launch_decode<DT, OT, D, kPathVecMha, false>(km, vm, p, sms, items, st);
+  return split ? launch_decode<DT, float, D, kPathVec, true>(km, vm, p, sms, items, st)
+               : launch_decode<DT, OT, D, kPathVec, false>(km, vm, p, sms, items, st);
 }
 
 template <typename DT, typename OT>

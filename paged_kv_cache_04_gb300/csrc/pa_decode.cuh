@@ -24,8 +24,10 @@
 //     memory at the end of the item;
 //   * split mode: an item is (sequence, kv head, W consecutive partitions) and
 //     warp w handles partition w of it alone, writing its normalised partial
-//     output and (max, sum) to the caller's workspace -- no merge inside the
-//     CTA; a second kernel merges partitions with log-sum-exp weights;
+//     output and (max, sum) to the caller's workspace -- no merge or barrier
+//     inside the CTA (a shared-partition variant with a per-partition merge
+//     measured 40% slower on 32K-128K contexts); a second kernel merges
+//     partitions with log-sum-exp weights;
 //   * a KV job is read once for all H / G query heads of its kv head: with a
 //     group of >= 4 heads on 16-bit data the step is a small dense contraction
 //     and runs on mma.sync m16n8k16 (tokens x heads for q K^T, d x heads for
@@ -43,6 +45,11 @@ constexpr int kSplitMaxSeqs = 2048;   // split mode keeps per-sequence offsets i
 constexpr int kLenBucketShift = 9;    // sort key: context length / 512
 constexpr int kNumBuckets = 1024;     // longer contexts share the top bucket
 constexpr int kJobTokens = 16;        // tokens per TMA job
+
+// Compute paths of the decode kernel.
+constexpr int kPathVec = 0;     // lanes split head_dim, FFMA; any group, q staged in shared memory
+constexpr int kPathVecMha = 1;  // the same for group 1 (MHA), q held in registers
+constexpr int kPathMma = 2;     // group >= 4 on 16-bit data: mma.sync m16n8k16
 
 struct DecodeParams {
   void* out;                    // [S][H][D] out dtype (plain mode)
@@ -70,7 +77,7 @@ struct SmemLayout {
 __host__ __device__ inline unsigned round_up(unsigned x, unsigned a) { return (x + a - 1) / a * a; }
 
 // Shared-memory map, computed identically on the host (launch size) and device.
-__host__ __device__ inline SmemLayout make_layout(int W, int R, int D, int esize, int group, bool vec, bool split,
+__host__ __device__ inline SmemLayout make_layout(int W, int R, int D, int esize, int group, int path, bool split,
                                                   int S) {
   SmemLayout L;
   L.stage_bytes = 2u * kJobTokens * D * esize;
@@ -82,7 +89,8 @@ __host__ __device__ inline SmemLayout make_layout(int W, int R, int D, int esize
   L.merge_off = off;
   if (!split) off += W * group * D * 4 + W * kMaxGroup * 2 * 4;
   L.q_off = off;
-  if (vec) off += W * group * D * 4;
+  if (path == kPathVec) off += W * group * D * 4;            // fp32 q rows per warp
+  if (path == kPathVecMha) off += round_up(W * 2 * D * esize, 16);  // double-buffered raw q row per warp
   L.sched_off = off;
   if (split)
     off += (S + 1) * 4;
@@ -95,7 +103,7 @@ __host__ __device__ inline SmemLayout make_layout(int W, int R, int D, int esize
   return L;
 }
 
-template <typename DT, int D, bool MMA>
+template <typename DT, int D, int PATH>
 struct StageCfg {
   static constexpr int E = sizeof(DT);
   static constexpr int TILE = kJobTokens * D * E;  // one K (or V) job tile
@@ -167,11 +175,12 @@ struct Schedule {
   }
 };
 
-template <typename DT, typename OT, int D, bool MMA, bool SPLIT>
-__global__ void __launch_bounds__(StageCfg<DT, D, MMA>::W * 32)
+template <typename DT, typename OT, int D, int PATH, bool SPLIT>
+__global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         const DecodeParams p) {
-  using Cfg = StageCfg<DT, D, MMA>;
+  using Cfg = StageCfg<DT, D, PATH>;
+  constexpr bool MMA = PATH == kPathMma;
   constexpr int W = Cfg::W, R = Cfg::R, E = Cfg::E, TILE = Cfg::TILE, JT = kJobTokens;
   constexpr int NCH = D * E / 16;     // 16-byte chunks per row
   constexpr int NREG = D * E / 128;   // 128-byte column regions (one TMA box each)
@@ -182,12 +191,13 @@ __global__ void __launch_bounds__(StageCfg<DT, D, MMA>::W * 32)
   extern __shared__ uint8_t smem_raw[];
   // TMA 128-byte swizzling needs 1024-byte aligned destinations: align the shared-window offset.
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const SmemLayout L = make_layout(W, R, D, E, p.group, !MMA, SPLIT, p.S);
+  const SmemLayout L = make_layout(W, R, D, E, p.group, PATH, SPLIT, p.S);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars_off);
   volatile uint8_t* stage_ok = smem + L.ok_off;                        // [W][R]
   float* mrg_o = reinterpret_cast<float*>(smem + L.merge_off);        // [W][group][D] (plain mode)
   float* mrg_ml = mrg_o + W * p.group * D;                             // [W][kMaxGroup][2]
   float* qs_all = reinterpret_cast<float*>(smem + L.q_off);            // [W][group][D] (vector path)
+  uint8_t* qraw_all = smem + L.q_off;                                  // [W][2][D] raw (MHA path)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc_off);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -290,15 +300,17 @@ __global__ void __launch_bounds__(StageCfg<DT, D, MMA>::W * 32)
   uint8_t* my_stages = smem + warp * R * L.stage_bytes;
   uint64_t* my_bars = bars + warp * R;
   volatile uint8_t* my_ok = stage_ok + warp * R;
-  const int job_step = SPLIT ? 1 : W;
+  constexpr bool WARP_PARTS = SPLIT;  // split mode: each warp owns whole partitions
+  const int job_step = WARP_PARTS ? 1 : W;
 
   struct Cursor {
     int k, u, ue;
+    long long phys;  // block-table entry of job u, loaded one job ahead of its issue
     Item it;
     bool valid;
   };
   auto cursor_range = [&](Cursor& c) {
-    c.u = c.it.t0 / JT + (SPLIT ? 0 : warp);
+    c.u = c.it.t0 / JT + (WARP_PARTS ? 0 : warp);
     c.ue = (c.it.t1 + JT - 1) / JT;
   };
   auto cursor_settle = [&](Cursor& c) {
@@ -307,6 +319,8 @@ __global__ void __launch_bounds__(StageCfg<DT, D, MMA>::W * 32)
       c.valid = sch.get(p, c.k, warp, c.it);
       if (c.valid) cursor_range(c);
     }
+    if (c.valid)
+      c.phys = __ldg(p.block_tables + (long long)c.it.s * p.max_blocks + ((c.u * JT) >> p.block_shift));
   };
   Cursor ic;
   ic.k = 0;
@@ -322,7 +336,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, MMA>::W * 32)
       uint64_t* bar = &my_bars[stage];
       const int tok = c.u * JT;
       const int blk = tok >> p.block_shift;
-      const long long phys = __ldg(p.block_tables + (long long)c.it.s * p.max_blocks + blk);
+      const long long phys = c.phys;
       if (phys < 0 || phys >= p.num_blocks) {
         atomicOr(p.err, kErrBlockId);
         my_ok[stage] = 0;
@@ -435,7 +449,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, MMA>::W * 32)
 #pragma unroll
       for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
       float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
-      const int ub = it.t0 / JT + (SPLIT ? 0 : warp), ue = (it.t1 + JT - 1) / JT;
+      const int ub = it.t0 / JT + (WARP_PARTS ? 0 : warp), ue = (it.t1 + JT - 1) / JT;
 #pragma unroll 1
       for (int u = ub; u < ue; u += job_step) {
         int stage;
@@ -443,13 +457,18 @@ __global__ void __launch_bounds__(StageCfg<DT, D, MMA>::W * 32)
           const uint32_t kt = smem_u32(my_stages + stage * L.stage_bytes);
           const uint32_t vt = kt + TILE;
           const int nv = min(JT, it.t1 - u * JT);
-          float sc[4] = {0.f, 0.f, 0.f, 0.f};
+          // two independent accumulator chains over head_dim halve the MMA latency chain
+          float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            uint32_t a[4];
+          for (int ks = 0; ks < D / 16; ks += 2) {
+            uint32_t a[4], b[4];
             ldsm_x4(a, kt + sw128_offset(lane & 15, ks * 2 + (lane >> 4), JT));
+            ldsm_x4(b, kt + sw128_offset(lane & 15, ks * 2 + 2 + (lane >> 4), JT));
             Mma<DT>::run(sc, a, qf[ks][0], qf[ks][1]);
+            Mma<DT>::run(sd, b, qf[ks + 1][0], qf[ks + 1][1]);
           }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sc[e] += sd[e];
           // sc[e]: token g + 8*(e>>1), head 2*t4 + (e&1)
           float mx0 = NEG_INF, mx1 = NEG_INF;
 #pragma unroll
@@ -521,7 +540,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, MMA>::W * 32)
         l1 += __shfl_xor_sync(0xffffffffu, l1, o2);
       }
       const int hA = 2 * t4, hB = hA + 1;
-      if (SPLIT) {
+      if (WARP_PARTS) {
         if (it.part >= 0) {
           const long long rowA = ((long long)it.s * p.H + it.kv * p.group + hA) * p.max_partitions + it.part;
           const long long rowB = rowA + p.max_partitions;
@@ -579,28 +598,56 @@ __global__ void __launch_bounds__(StageCfg<DT, D, MMA>::W * 32)
     }
   } else {
     // ---------------- vector path: lanes split head_dim, FFMA ----------------
-    constexpr int LPT = 32 / JT;        // lanes per token in q K^T (2)
-    constexpr int CPL = NCH / LPT;      // 16-byte K chunks per lane
-    constexpr int EPC = 16 / E;         // elements per 16-byte chunk
-    constexpr int EPL = D / 32;         // output elements per lane in P V
-    constexpr int VB = EPL * E;         // V bytes per lane per row
+    constexpr bool MHA = PATH == kPathVecMha;
+    constexpr int GM = MHA ? 1 : kMaxGroup;  // heads held per warp
+    constexpr int LPT = 32 / JT;             // lanes per token in q K^T (2)
+    constexpr int CPL = NCH / LPT;           // 16-byte K chunks per lane
+    constexpr int EPC = 16 / E;              // elements per 16-byte chunk
+    constexpr int EPL = D / 32;              // output elements per lane in P V
+    constexpr int VB = EPL * E;              // V bytes per lane per row
+    constexpr int QCH = D * E / 16;          // 16-byte chunks of one q row
     float* qs = qs_all + warp * p.group * D;
+    uint8_t* qraw = qraw_all + warp * 2 * D * E;
     const int t = lane % JT, part = lane / JT;
+    float qreg[MHA ? CPL * EPC : 1];  // MHA: this lane's half of the q row
+    auto fetch_q_raw = [&](const Item& x, int buf) {  // MHA: next q row -> shared memory, async
+      const uint8_t* src = reinterpret_cast<const uint8_t*>(p.q) + ((long long)x.s * p.H + x.kv) * D * E;
+      for (int c = lane; c < QCH; c += 32) cp_async16(qraw + buf * D * E + c * 16, src + c * 16);
+      cp_async_commit();
+    };
+    int qbuf = 0;
+    if constexpr (MHA) {
+      if (sch.get(p, 0, warp, it)) fetch_q_raw(it, 0);
+    }
 #pragma unroll 1
     for (int k = 0; sch.get(p, k, warp, it); ++k) {
-      const DT* qrow = reinterpret_cast<const DT*>(p.q) + ((long long)it.s * p.H + it.kv * p.group) * D;
-      for (int i = lane; i < p.group * D; i += 32) qs[i] = to_f32(qrow[i]);
-      __syncwarp();
-      float o[kMaxGroup][EPL];
-      float mr[kMaxGroup], lr[kMaxGroup];
+      if constexpr (MHA) {
+        cp_async_wait_all();
+        __syncwarp();
+        const DT* qr = reinterpret_cast<const DT*>(qraw + qbuf * D * E);
 #pragma unroll
-      for (int h = 0; h < kMaxGroup; ++h) {
+        for (int c = 0; c < CPL; ++c)
+#pragma unroll
+          for (int e = 0; e < EPC; ++e) qreg[c * EPC + e] = to_f32(qr[(part * CPL + c) * EPC + e]);
+        __syncwarp();
+        Item nx;
+        if (sch.get(p, k + 1, warp, nx)) fetch_q_raw(nx, qbuf ^ 1);
+        qbuf ^= 1;
+      } else {
+        const DT* qrow = reinterpret_cast<const DT*>(p.q) + ((long long)it.s * p.H + it.kv * p.group) * D;
+        for (int i = lane; i < p.group * D; i += 32) qs[i] = to_f32(qrow[i]);
+        __syncwarp();
+      }
+      float o[GM][EPL];
+      float mr[GM], lr[GM];
+#pragma unroll
+      for (int h = 0; h < GM; ++h) {
         mr[h] = NEG_INF;
         lr[h] = 0.f;
 #pragma unroll
         for (int e = 0; e < EPL; ++e) o[h][e] = 0.f;
       }
-      const int ub = it.t0 / JT + (SPLIT ? 0 : warp), ue = (it.t1 + JT - 1) / JT;
+      const int ub = it.t0 / JT + (WARP_PARTS ? 0 : warp), ue = (it.t1 + JT - 1) / JT;
 #pragma unroll 1
       for (int u = ub; u < ue; u += job_step) {
         int stage;
@@ -609,38 +656,56 @@ __global__ void __launch_bounds__(StageCfg<DT, D, MMA>::W * 32)
           const uint8_t* vt = kt + TILE;
           const int nv = min(JT, it.t1 - u * JT);
 #pragma unroll
-          for (int h = 0; h < kMaxGroup; ++h) {
+          for (int h = 0; h < GM; ++h) {
             if (h >= p.group) break;
             const float* qh = qs + h * D;
-            float z = 0.f;
+            float zc[CPL];  // one partial sum per chunk: short, independent FMA chains
 #pragma unroll
             for (int c = 0; c < CPL; ++c) {
+              float z = 0.f;
               const int ch = part * CPL + c;
               const uint4 raw = *reinterpret_cast<const uint4*>(kt + sw128_offset(t, ch, JT));
-              const float4* qv = reinterpret_cast<const float4*>(qh + ch * EPC);
-              if constexpr (E == 4) {
-                const float4 qa = qv[0];
-                z = fmaf(qa.x, __uint_as_float(raw.x), z);
-                z = fmaf(qa.y, __uint_as_float(raw.y), z);
-                z = fmaf(qa.z, __uint_as_float(raw.z), z);
-                z = fmaf(qa.w, __uint_as_float(raw.w), z);
+              float qv[EPC];
+              if constexpr (MHA) {
+#pragma unroll
+                for (int e = 0; e < EPC; ++e) qv[e] = qreg[c * EPC + e];
               } else {
-                const float4 qa = qv[0], qb = qv[1];
+#pragma unroll
+                for (int e = 0; e < EPC; e += 4) {
+                  const float4 q4 = *reinterpret_cast<const float4*>(qh + ch * EPC + e);
+                  qv[e] = q4.x;
+                  qv[e + 1] = q4.y;
+                  qv[e + 2] = q4.z;
+                  qv[e + 3] = q4.w;
+                }
+              }
+              if constexpr (E == 4) {
+                z = fmaf(qv[0], __uint_as_float(raw.x), z);
+                z = fmaf(qv[1], __uint_as_float(raw.y), z);
+                z = fmaf(qv[2], __uint_as_float(raw.z), z);
+                z = fmaf(qv[3], __uint_as_float(raw.w), z);
+              } else {
                 float f0, f1, f2, f3, f4, f5, f6, f7;
                 unpack2(raw.x, (DT*)nullptr, f0, f1);
                 unpack2(raw.y, (DT*)nullptr, f2, f3);
                 unpack2(raw.z, (DT*)nullptr, f4, f5);
                 unpack2(raw.w, (DT*)nullptr, f6, f7);
-                z = fmaf(qa.x, f0, z);
-                z = fmaf(qa.y, f1, z);
-                z = fmaf(qa.z, f2, z);
-                z = fmaf(qa.w, f3, z);
-                z = fmaf(qb.x, f4, z);
-                z = fmaf(qb.y, f5, z);
-                z = fmaf(qb.z, f6, z);
-                z = fmaf(qb.w, f7, z);
+                z = fmaf(qv[0], f0, z);
+                z = fmaf(qv[1], f1, z);
+                z = fmaf(qv[2], f2, z);
+                z = fmaf(qv[3], f3, z);
+                z = fmaf(qv[4], f4, z);
+                z = fmaf(qv[5], f5, z);
+                z = fmaf(qv[6], f6, z);
+                z = fmaf(qv[7], f7, z);
               }
+              zc[c] = z;
             }
+#pragma unroll
+            for (int w2 = 1; w2 < CPL; w2 <<= 1)
+#pragma unroll
+              for (int c = 0; c + w2 < CPL; c += 2 * w2) zc[c] += zc[c + w2];
+            float z = zc[0];
             if (LPT == 2) z += __shfl_xor_sync(0xffffffffu, z, 16);
             z = t < nv ? z * p.scale_log2 : NEG_INF;
             float mx = z;
@@ -696,12 +761,12 @@ __global__ void __launch_bounds__(StageCfg<DT, D, MMA>::W * 32)
       float* mo = mrg_o + warp * p.group * D;
       float* ml = mrg_ml + warp * kMaxGroup * 2;
 #pragma unroll
-      for (int h = 0; h < kMaxGroup; ++h) {
+      for (int h = 0; h < GM; ++h) {
         if (h >= p.group) break;
         float l = lr[h];
 #pragma unroll
         for (int o2 = 1; o2 < 32; o2 <<= 1) l += __shfl_xor_sync(0xffffffffu, l, o2);
-        if (SPLIT) {
+        if (WARP_PARTS) {
           if (it.part >= 0) {
             const long long row = ((long long)it.s * p.H + it.kv * p.group + h) * p.max_partitions + it.part;
             const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -721,8 +786,9 @@ __global__ void __launch_bounds__(StageCfg<DT, D, MMA>::W * 32)
           }
         }
       }
-      if (!SPLIT) merge_and_write(it);
+      if (!WARP_PARTS) merge_and_write(it);
     }
+    if constexpr (MHA) cp_async_wait_all();
   }
 
   // ---- let every copy this warp started land before the block exits ------------
@@ -735,64 +801,87 @@ __global__ void __launch_bounds__(StageCfg<DT, D, MMA>::W * 32)
 }
 
 // Pass 2 of split mode: merge the partitions of one (sequence, head) row with
-// log-sum-exp weights, w_p = l_p * 2^(m_p - M), out = sum_p w_p o_p / sum_p w_p.
+// log-sum-exp weights, M = max_p m_p, w_p = l_p * 2^(m_p - M),
+// out = sum_p w_p o_p / sum_p w_p. One CTA per row; the row's partials are read
+// with every load of a thread issued before any is used, so the kernel costs a
+// few memory round trips rather than one per partition.
 template <typename OT, int D>
-__global__ void __launch_bounds__(128) lse_reduce_kernel(const DecodeParams p) {
-  constexpr int EPL = D / 32;
-  const int row = blockIdx.x;  // s * H + h
+__global__ void __launch_bounds__(256) lse_reduce_kernel(const DecodeParams p) {
+  constexpr int NT = 256;
+  constexpr int VPR = D / 4;        // float4 vectors per partial row
+  constexpr int PG = NT / VPR;      // partition groups (8 for D = 128, 16 for D = 64)
+  constexpr int BATCH = 8;          // loads in flight per thread
+  constexpr int CHUNK = 2048;       // partitions whose weights sit in shared memory at a time
+  const int row = blockIdx.x;       // s * H + h
   const int s = row / p.H;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const float NEG_INF = -__int_as_float(0x7f800000);
   const int c = clamp_ctx(p, s, true);
   const int P = (c + p.partition - 1) / p.partition;
   const long long base = (long long)row * p.max_partitions;
-  float M = NEG_INF, Lsum = 0.f, acc[EPL];
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-#pragma unroll 4
-  for (int q = warp; q < P; q += 4) {
-    const float mq = __ldg(p.ws_m + base + q), lq = __ldg(p.ws_l + base + q);
-    if (!(lq > 0.f)) continue;
-    const float* oq = p.ws_o + (base + q) * D + lane * EPL;
-    float v[EPL];
-    if constexpr (EPL == 4) {
-      const float4 t4 = __ldg(reinterpret_cast<const float4*>(oq));
-      v[0] = t4.x; v[1] = t4.y; v[2] = t4.z; v[3] = t4.w;
-    } else {
-      const float2 t2 = __ldg(reinterpret_cast<const float2*>(oq));
-      v[0] = t2.x; v[1] = t2.y;
-    }
-    const float Mn = fmaxf(M, mq);
-    const float a = exp2f(M - Mn), b = lq * exp2f(mq - Mn);
-    Lsum = Lsum * a + b;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) acc[e] = acc[e] * a + b * v[e];
-    M = Mn;
-  }
-  __shared__ float sh_ml[4][2];
-  __shared__ float sh_o[4][D];
-  if (lane == 0) {
-    sh_ml[warp][0] = M;
-    sh_ml[warp][1] = Lsum;
+  __shared__ float sh_w[CHUNK];
+  __shared__ float sh_red[NT / 32];
+  __shared__ float4 sh_acc[PG][VPR];
+
+  float mx = NEG_INF;
+  for (int q = tid; q < P; q += NT) {
+    const float l = __ldg(p.ws_l + base + q), m = __ldg(p.ws_m + base + q);
+    if (l > 0.f) mx = fmaxf(mx, m);
   }
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) sh_o[warp][lane * EPL + e] = acc[e];
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) sh_red[warp] = mx;
   __syncthreads();
-  for (int i = threadIdx.x; i < D; i += 128) {
-    float Mx = NEG_INF;
+  float M = sh_red[0];
 #pragma unroll
-    for (int w = 0; w < 4; ++w)
-      if (sh_ml[w][1] > 0.f) Mx = fmaxf(Mx, sh_ml[w][0]);
-    float Ls = 0.f, O = 0.f;
+  for (int w = 1; w < NT / 32; ++w) M = fmaxf(M, sh_red[w]);
+  __syncthreads();
+
+  const int v = tid % VPR, pg = tid / VPR;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float wsum = 0.f;
+  for (int q0 = 0; q0 < P; q0 += CHUNK) {
+    const int n = min(CHUNK, P - q0);
+    for (int q = tid; q < n; q += NT) {
+      const float l = __ldg(p.ws_l + base + q0 + q), m = __ldg(p.ws_m + base + q0 + q);
+      const float w = l > 0.f ? l * exp2f(m - M) : 0.f;
+      sh_w[q] = w;
+      wsum += w;
+    }
+    __syncthreads();
+    const float4* src = reinterpret_cast<const float4*>(p.ws_o + (base + q0) * D) + v;
+    for (int q = pg; q < n; q += PG * BATCH) {
+      float4 x[BATCH];
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      if (sh_ml[w][1] > 0.f) {
-        const float f = exp2f(sh_ml[w][0] - Mx);
-        Ls = fmaf(sh_ml[w][1], f, Ls);
-        O = fmaf(sh_o[w][i], f, O);
+      for (int b = 0; b < BATCH; ++b) {
+        const int qq = q + b * PG;
+        x[b] = qq < n ? __ldg(src + (long long)qq * VPR) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int b = 0; b < BATCH; ++b) {
+        const int qq = q + b * PG;
+        const float w = qq < n ? sh_w[qq] : 0.f;
+        acc.x = fmaf(w, x[b].x, acc.x);
+        acc.y = fmaf(w, x[b].y, acc.y);
+        acc.z = fmaf(w, x[b].z, acc.z);
+        acc.w = fmaf(w, x[b].w, acc.w);
       }
     }
-    reinterpret_cast<OT*>(p.out)[(long long)row * D + i] = from_f32<OT>(Ls > 0.f ? O / Ls : 0.f);
+    __syncthreads();
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+  if (lane == 0) sh_red[warp] = wsum;
+  sh_acc[pg][v] = acc;
+  __syncthreads();
+  float W = 0.f;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) W += sh_red[w];
+  for (int i = tid; i < D; i += NT) {
+    float O = 0.f;
+#pragma unroll
+    for (int g = 0; g < PG; ++g) O += reinterpret_cast<const float*>(&sh_acc[g][0])[i];
+    reinterpret_cast<OT*>(p.out)[(long long)row * D + i] = from_f32<OT>(W > 0.f ? O / W : 0.f);
   }
 }
 

@@ -105,6 +105,16 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ---------------------------------------------------------------------------
+// cp.async: 16-byte global -> shared copies that land without passing through
+// registers (used to fetch the next item's query row while the current streams)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Byte offset of the 16-byte chunk `c` of row `r` in a tile staged by TMA with
 // 128-byte swizzling: the tile is split into column regions of 128 bytes, each
 // region holds `rows` rows of 128 bytes, and inside a region the chunk index is

@@ -16,7 +16,7 @@ pa_status device_state(unsigned** err, int* num_sms);
 
 // Launchers, one per (element type, output type, head_dim, path, split)
 // combination, instantiated in pa_decode_{f32,f16,bf16}.cu.
-template <typename DT, typename OT, int D, bool MMA, bool SPLIT>
+template <typename DT, typename OT, int D, int PATH, bool SPLIT>
 pa_status launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                         int num_sms, long long max_items, cudaStream_t stream);
 
