@@ -203,6 +203,32 @@ pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches, int num_l
                          int block_size, int64_t num_blocks, pa_dtype dtype, cudaStream_t stream);
 
 /*
+ * Move KV blocks between two pools in one launch: the GPU <-> CPU swap of
+ * preempted sequences (CS349E Lecture 7 notes §6.2: a preempted sequence's
+ * blocks go to CPU memory and come back later; done as per-block copies each
+ * layer's K and V cost layers x 2 x blocks small transfers with a fixed
+ * overhead each). For every pair p and every layer l:
+ *   dst_k_caches[l][block_pairs[p][1]] = src_k_caches[l][block_pairs[p][0]]  (same for V)
+ *
+ *   dst_*_caches, src_*_caches  HOST arrays of num_layers pool pointers; a pool
+ *                               is [*_num_blocks][num_kv_heads][block_size][head_dim]
+ *                               of `dtype`, in device memory or in pinned host
+ *                               memory (cudaHostAlloc / cudaMallocHost), which
+ *                               the kernel reads or writes directly at its host
+ *                               address (unified addressing)
+ *   block_pairs                 int64 [num_pairs][2] (src id, dst id), device
+ *                               memory or pinned host memory
+ *
+ * Bit-exact. Destinations must be distinct and must not alias any source
+ * block. Ids outside their pool are skipped and recorded (PA_DEVERR_PAIR).
+ */
+pa_status pa_swap_blocks(void* const* dst_k_caches, void* const* dst_v_caches,
+                         const void* const* src_k_caches, const void* const* src_v_caches, int num_layers,
+                         const int64_t* block_pairs, int num_pairs, int num_kv_heads, int head_dim,
+                         int block_size, int64_t dst_num_blocks, int64_t src_num_blocks, pa_dtype dtype,
+                         cudaStream_t stream);
+
+/*
  * Read and clear the calling device's error word (PA_DEVERR_* bits) after the
  * work already queued on `stream` has finished. *error_bits (host) receives the
  * bits. Returns PA_ERR_OUT_OF_RANGE when any bit was set, PA_OK otherwise. It

@@ -7,12 +7,12 @@ shares no code with it.
 
 * :func:`decode` / :func:`partitions` / :func:`merge` -- float64 attention, in
   plain C (``pa_oracle.c``), reading the pool through the block table.
-* :func:`reshape_and_cache` / :func:`copy_blocks` -- the cache writes, element
+* :func:`reshape_and_cache` / :func:`copy_blocks` / :func:`swap_blocks` -- the cache writes, element
   by element on bit patterns (``cache_ops.py``).
 * :func:`kv_bytes_per_token` -- the per-token KV size formula.
 
 Every function cites the passage it follows; the pins in
 ``tests/test_oracle_pins.py`` tie each one to something other than itself.
 """
-from .cache_ops import copy_blocks, kv_bytes_per_token, reshape_and_cache  # noqa: F401
+from .cache_ops import copy_blocks, kv_bytes_per_token, reshape_and_cache, swap_blocks  # noqa: F401
 from .attention import decode, partitions, merge, f16_bits_to_f64, bf16_bits_to_f64, max_threads  # noqa: F401

@@ -85,6 +85,26 @@ def copy_blocks(k_caches, v_caches, block_pairs):
     return ks, vs
 
 
+def swap_blocks(dst_k_caches, dst_v_caches, src_k_caches, src_v_caches, block_pairs):
+    """Return new per-layer destination (k, v) bit arrays after moving blocks between pools.
+
+    For every pair (src, dst) and layer: dst_pool[dst] = src_pool[src], K and V
+    (CS349E Lecture 7 notes §6.2: a preempted sequence's blocks are copied to
+    CPU memory and later back). The source pools are not modified.
+    """
+    pairs = np.asarray(_bits(block_pairs), dtype=np.int64).reshape(-1, 2)
+    dks = [_bits(k) for k in dst_k_caches]
+    dvs = [_bits(v) for v in dst_v_caches]
+    for layer in range(len(dks)):
+        sk, sv = _bits(src_k_caches[layer]), _bits(src_v_caches[layer])
+        for src, dst in pairs:
+            if not (0 <= src < sk.shape[0] and 0 <= dst < dks[layer].shape[0]):
+                raise IndexError(f"pair ({src}, {dst}) outside its pool")
+            dks[layer][dst] = sk[src]
+            dvs[layer][dst] = sv[src]
+    return dks, dvs
+
+
 def kv_bytes_per_token(num_layers, num_kv_heads, head_dim, dtype_bytes):
     """KV-cache bytes one token occupies: 2 (K and V) x layers x kv heads x head dim x bytes.
 

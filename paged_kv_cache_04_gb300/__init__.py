@@ -22,7 +22,8 @@ import os
 
 __all__ = [
     "PAError", "library", "library_path", "pa_reshape_and_cache", "pa_decode", "pa_decode_split",
-    "pa_decode_split_workspace_bytes", "pa_decode_split_static", "pa_copy_blocks", "pa_get_error",
+    "pa_decode_split_workspace_bytes", "pa_decode_split_static", "pa_copy_blocks", "pa_swap_blocks",
+    "pa_get_error",
     "pa_version", "PA_STATIC_SCRATCH_BYTES",
     "PA_DEVERR_BLOCK_ID", "PA_DEVERR_SLOT", "PA_DEVERR_CONTEXT", "PA_DEVERR_PAIR", "PA_DEVERR_TIMEOUT",
 ]
@@ -62,12 +63,13 @@ def library():
     lib.pa_decode_split.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I64, F, I, I, I, I, P, SZ, P]
     lib.pa_decode_split_static.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I64, F, I, I, I, I, P]
     lib.pa_copy_blocks.argtypes = [P, P, I, P, I, I, I, I, I64, I, P]
+    lib.pa_swap_blocks.argtypes = [P, P, P, P, I, P, I, I, I, I, I64, I64, I, P]
     lib.pa_get_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), P]
     lib.pa_status_string.argtypes = [I]
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_version.argtypes = []
     for f in ("pa_reshape_and_cache", "pa_decode", "pa_decode_split", "pa_decode_split_static",
-              "pa_copy_blocks", "pa_get_error", "pa_version"):
+              "pa_copy_blocks", "pa_swap_blocks", "pa_get_error", "pa_version"):
         getattr(lib, f).restype = I
     _lib = lib
     return lib
@@ -208,6 +210,34 @@ def pa_copy_blocks(k_caches, v_caches, block_pairs, stream=None):
     varr = (ctypes.c_void_p * L)(*[t.data_ptr() for t in v_caches])
     _check(f, library().pa_copy_blocks(karr, varr, L, _ptr(block_pairs), int(block_pairs.shape[0]), G, d, B,
                                        nb, _dtype_code(k_caches[0]), _stream(stream)))
+
+
+def pa_swap_blocks(dst_k_caches, dst_v_caches, src_k_caches, src_v_caches, block_pairs, stream=None):
+    """For every (src, dst) pair and layer: ``dst[dst] = src[src]`` for K and V, in one launch.
+
+    Pools may be CUDA tensors or pinned CPU tensors (``pin_memory()``), which
+    the kernel reaches directly; ``block_pairs`` (int64 [P, 2]) likewise.
+    """
+    f = "pa_swap_blocks"
+    torch = _torch()
+    dk, dv, sk, sv = list(dst_k_caches), list(dst_v_caches), list(src_k_caches), list(src_v_caches)
+    L = len(dk)
+    _need(L > 0 and len(dv) == L and len(sk) == L and len(sv) == L, f, "one K and one V pool per layer")
+    for t in dk + dv + sk + sv + [block_pairs]:
+        _need(t.is_contiguous() and (t.is_cuda or t.is_pinned()), f, "tensors must be CUDA or pinned host memory")
+    _need(block_pairs.dtype == torch.int64 and block_pairs.dim() == 2 and block_pairs.shape[1] == 2, f,
+          "block_pairs must be int64 [P, 2]")
+    dshape, sshape, dt = dk[0].shape, sk[0].shape, dk[0].dtype
+    for t in dk + dv:
+        _need(t.shape == dshape and t.dtype == dt, f, "destination pools must share shape and dtype")
+    for t in sk + sv:
+        _need(t.shape == sshape and t.dtype == dt, f, "source pools must share shape and dtype")
+    _need(dshape[1:] == sshape[1:], f, "pools must share the block shape")
+    _, G, B, d = dshape
+    arr = lambda ts: (ctypes.c_void_p * L)(*[t.data_ptr() for t in ts])  # noqa: E731
+    _check(f, library().pa_swap_blocks(arr(dk), arr(dv), arr(sk), arr(sv), L, _ptr(block_pairs),
+                                       int(block_pairs.shape[0]), G, d, B, dshape[0], sshape[0], _dtype_code(dk[0]),
+                                       _stream(stream)))
 
 
 def pa_get_error(stream=None) -> int:

@@ -1,7 +1,8 @@
-// The two kernels that keep the paged KV cache current (CS349E Lecture 7 notes,
+// The kernels that keep the paged KV cache current (CS349E Lecture 7 notes,
 // §4.3: one fused write of new tokens into their block slots, one batched copy
-// of the blocks copy-on-write must duplicate). Both are pure data movement:
-// 16-byte vector loads and stores, bit-exact, bounds-checked against the pool.
+// of the blocks copy-on-write must duplicate; §6.2: swapping a preempted
+// sequence's blocks to CPU memory and back). All are pure data movement:
+// 16-byte vector loads and stores, bit-exact, bounds-checked against the pools.
 #include <algorithm>
 #include <cstdint>
 
@@ -58,6 +59,44 @@ __global__ void __launch_bounds__(256)
   uint4* base = blockIdx.z ? ptrs.v[blockIdx.y] : ptrs.k[blockIdx.y];
   const uint4* s = base + src * vpb;
   uint4* d = base + dst * vpb;
+  for (int i0 = threadIdx.x; i0 < vpb; i0 += 256 * VPT) {
+    uint4 r[VPT];
+#pragma unroll
+    for (int u = 0; u < VPT; ++u) {
+      const int i = i0 + u * 256;
+      if (i < vpb) r[u] = __ldcs(s + i);
+    }
+#pragma unroll
+    for (int u = 0; u < VPT; ++u) {
+      const int i = i0 + u * 256;
+      if (i < vpb) __stcs(d + i, r[u]);
+    }
+  }
+}
+
+constexpr int kMaxSwapLayers = 32;
+struct SwapPtrs {
+  const uint4* src_k[kMaxSwapLayers];
+  const uint4* src_v[kMaxSwapLayers];
+  uint4* dst_k[kMaxSwapLayers];
+  uint4* dst_v[kMaxSwapLayers];
+};
+
+// grid = (pairs, layers, 2): one CTA moves one K or V block of one layer from
+// the source pool to the destination pool (either may be pinned host memory,
+// reached directly through the unified address space).
+template <int VPT>
+__global__ void __launch_bounds__(256)
+    swap_blocks_kernel(const SwapPtrs ptrs, const int64_t* __restrict__ pairs, long long src_blocks,
+                       long long dst_blocks, int vpb, unsigned* err) {
+  const long long src = __ldg(pairs + 2 * (long long)blockIdx.x);
+  const long long dst = __ldg(pairs + 2 * (long long)blockIdx.x + 1);
+  if (src < 0 || src >= src_blocks || dst < 0 || dst >= dst_blocks) {
+    if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) atomicOr(err, kErrPair);
+    return;
+  }
+  const uint4* s = (blockIdx.z ? ptrs.src_v[blockIdx.y] : ptrs.src_k[blockIdx.y]) + src * vpb;
+  uint4* d = (blockIdx.z ? ptrs.dst_v[blockIdx.y] : ptrs.dst_k[blockIdx.y]) + dst * vpb;
   for (int i0 = threadIdx.x; i0 < vpb; i0 += 256 * VPT) {
     uint4 r[VPT];
 #pragma unroll
@@ -139,6 +178,48 @@ extern "C" pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches
     }
     dim3 grid((unsigned)num_pairs, (unsigned)nl, 2);
     copy_blocks_kernel<8><<<grid, 256, 0, stream>>>(ptrs, block_pairs, (long long)num_blocks, vpb, err);
+    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  }
+  return PA_OK;
+}
+
+extern "C" pa_status pa_swap_blocks(void* const* dst_k_caches, void* const* dst_v_caches,
+                                    const void* const* src_k_caches, const void* const* src_v_caches,
+                                    int num_layers, const int64_t* block_pairs, int num_pairs, int num_kv_heads,
+                                    int head_dim, int block_size, int64_t dst_num_blocks, int64_t src_num_blocks,
+                                    pa_dtype dtype, cudaStream_t stream) {
+  using namespace pa;
+  if (num_layers < 0 || num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+      dst_num_blocks <= 0 || src_num_blocks <= 0 || !valid_dtype(dtype))
+    return PA_ERR_INVALID_ARG;
+  if (num_layers == 0 || num_pairs == 0) return PA_OK;
+  if (!dst_k_caches || !dst_v_caches || !src_k_caches || !src_v_caches || !block_pairs ||
+      (reinterpret_cast<uintptr_t>(block_pairs) & 7u))
+    return PA_ERR_INVALID_ARG;
+  for (int l = 0; l < num_layers; ++l)
+    if (!dst_k_caches[l] || !dst_v_caches[l] || !src_k_caches[l] || !src_v_caches[l] ||
+        !aligned16(dst_k_caches[l]) || !aligned16(dst_v_caches[l]) || !aligned16(src_k_caches[l]) ||
+        !aligned16(src_v_caches[l]))
+      return PA_ERR_INVALID_ARG;
+  const long long block_bytes = (long long)num_kv_heads * block_size * head_dim * esize(dtype);
+  if (block_bytes % 16 || block_bytes / 16 > (1LL << 30) || num_pairs > 0x7fffffff / 2) return PA_ERR_UNSUPPORTED;
+  unsigned* err = nullptr;
+  int sms = 0;
+  pa_status st = device_state(&err, &sms);
+  if (st != PA_OK) return st;
+  const int vpb = (int)(block_bytes / 16);
+  for (int l0 = 0; l0 < num_layers; l0 += kMaxSwapLayers) {
+    const int nl = std::min(kMaxSwapLayers, num_layers - l0);
+    SwapPtrs ptrs;
+    for (int i = 0; i < kMaxSwapLayers; ++i) {
+      ptrs.src_k[i] = i < nl ? static_cast<const uint4*>(src_k_caches[l0 + i]) : nullptr;
+      ptrs.src_v[i] = i < nl ? static_cast<const uint4*>(src_v_caches[l0 + i]) : nullptr;
+      ptrs.dst_k[i] = i < nl ? static_cast<uint4*>(dst_k_caches[l0 + i]) : nullptr;
+      ptrs.dst_v[i] = i < nl ? static_cast<uint4*>(dst_v_caches[l0 + i]) : nullptr;
+    }
+    dim3 grid((unsigned)num_pairs, (unsigned)nl, 2);
+    swap_blocks_kernel<8><<<grid, 256, 0, stream>>>(ptrs, block_pairs, (long long)src_num_blocks,
+                                                    (long long)dst_num_blocks, vpb, err);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
   }
   return PA_OK;

@@ -42,7 +42,10 @@ namespace pa {
 constexpr int kMaxGroup = 8;          // query heads per kv head
 constexpr int kSortMaxSeqs = 2048;    // longest-first ordering up to this batch size
 constexpr int kSplitMaxSeqs = 2048;   // split mode keeps per-sequence offsets in shared memory
-constexpr int kLenBucketShift = 9;    // sort key: context length / 512
+#ifndef PA_LEN_BUCKET_SHIFT
+#define PA_LEN_BUCKET_SHIFT 9
+#endif
+constexpr int kLenBucketShift = PA_LEN_BUCKET_SHIFT;  // sort key: context length >> shift
 constexpr int kNumBuckets = 1024;     // longer contexts share the top bucket
 constexpr int kJobTokens = 16;        // tokens per TMA job
 
