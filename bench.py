@@ -52,8 +52,11 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
     ap.add_argument("--profile", action="store_true",
                     help="run only the step's kernels on a 64-sequence batch of the same shape (for ncu)")
+    ap.add_argument("--profile-fp8", action="store_true",
+                    help="the same 64-sequence case with an E4M3 cache (for ncu)")
     ap.add_argument("--workload", default="llama8b",
-                    choices=["llama8b", "tiny", "opt13b", "shared", "shared_cow", "long70b_b16", "long70b_b32"],
+                    choices=["llama8b", "tiny", "opt13b", "shared", "shared_cow", "long70b_b16", "long70b_b32",
+                             "llama8b_fp8", "long70b_b16_fp8"],
                     help="the other workload shapes give a device-timed line of their own (no e2e / CPU legs)")
     return ap.parse_args()
 
@@ -459,10 +462,16 @@ def run_workload(args):
                              for s, c in enumerate(wl.context_lens.tolist())], dtype=torch.int64, device=dev)
         wl.slot_mapping = last
         wl.new_key, wl.new_value = wl.new_key[:wl.S].contiguous(), wl.new_value[:wl.S].contiguous()
+    elif name == "llama8b_fp8":
+        wl = workloads.to_fp8(workloads.llama8b(device=dev))
     else:
-        B = 16 if name.endswith("16") else 32
+        B = 32 if "b32" in name else 16
         wl = workloads.long70b(device=dev, B=B)
+        if name.endswith("fp8"):
+            wl = workloads.to_fp8(wl)
         split, T = True, 512
+    fp8 = name.endswith("fp8")
+    ks, vs = wl.meta.get("k_scale", 1.0), wl.meta.get("v_scale", 1.0)
     out = torch.empty_like(wl.q)
     ws = None
     max_ctx = wl.max_context  # read once: it synchronises the device
@@ -475,6 +484,15 @@ def run_workload(args):
     pairs = wl.copy_pairs if wl.copy_pairs is not None and wl.copy_pairs.numel() else None
 
     def step():
+        if fp8:
+            pa.pa_reshape_and_cache_fp8(wl.new_key, wl.new_value, wl.k_cache, wl.v_cache, wl.slot_mapping, ks, vs)
+            if split:
+                pa.pa_decode_split_fp8(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens,
+                                       wl.scale, ks, vs, max_ctx, T, ws)
+            else:
+                pa.pa_decode_fp8(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale,
+                                 ks, vs)
+            return
         if pairs is not None:
             pa.pa_copy_blocks([wl.k_cache], [wl.v_cache], pairs)
         if wl.slot_mapping is not None:
@@ -501,11 +519,15 @@ def run_workload(args):
     torch.cuda.synchronize()
     ms = statistics.mean(x.elapsed_time(y) for x, y in times)
     e = wl.q.element_size()
+    ke = wl.k_cache.element_size()
     ctx = wl.context_lens.tolist()
-    dec = roofline.decode_bytes(ctx, wl.H, wl.G, wl.d, e)
+    dec = (roofline.decode_bytes(ctx, wl.H, wl.G, wl.d, ke) - 2 * wl.S * wl.H * wl.d * ke
+           + 2 * wl.S * wl.H * wl.d * e)  # K/V at the cache width, q and out at the query width
     extra = 0
     if wl.slot_mapping is not None:
-        extra += roofline.reshape_and_cache_bytes(wl.slot_mapping.numel(), wl.G, wl.d, e)
+        n = wl.slot_mapping.numel()
+        extra += (roofline.reshape_and_cache_bytes(n, wl.G, wl.d, e) if not fp8
+                  else 2 * n * wl.G * wl.d * (e + ke) + 8 * n)
     if pairs is not None:
         extra += roofline.copy_blocks_bytes(pairs.shape[0], 1, wl.B, wl.G, wl.d, e)
     unique = None
@@ -534,20 +556,28 @@ def run_profile_case(args):
     _build.ensure_built()
     dev = torch.device("cuda", 0)
     wl = workloads.llama8b(device=dev, S=64, num_blocks=16_000)
+    if args.profile_fp8:
+        wl = workloads.to_fp8(wl)
+        torch.cuda.empty_cache()
     out = torch.empty_like(wl.q)
+    ks, vs = wl.meta.get("k_scale", 1.0), wl.meta.get("v_scale", 1.0)
     for _ in range(args.warmup + args.steps):
-        pa.pa_reshape_and_cache(wl.new_key, wl.new_value, wl.k_cache, wl.v_cache, wl.slot_mapping)
-        pa.pa_decode(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale)
+        if args.profile_fp8:
+            pa.pa_reshape_and_cache_fp8(wl.new_key, wl.new_value, wl.k_cache, wl.v_cache, wl.slot_mapping, ks, vs)
+            pa.pa_decode_fp8(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale, ks, vs)
+        else:
+            pa.pa_reshape_and_cache(wl.new_key, wl.new_value, wl.k_cache, wl.v_cache, wl.slot_mapping)
+            pa.pa_decode(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale)
     torch.cuda.synchronize()
     from paged_kv_cache_04_gb300 import roofline
-    kv = roofline.decode_bytes(wl.context_lens.tolist(), wl.H, wl.G, wl.d, 2)
+    kv = roofline.decode_bytes(wl.context_lens.tolist(), wl.H, wl.G, wl.d, wl.k_cache.element_size())
     print(json.dumps({"profile_case": "llama8b S=64 pool 16000", "decode_bytes_per_launch": kv,
                       "source_sha256": kernel_source_sha(), "device_errors": pa.pa_get_error()}))
 
 
 def main():
     args = parse()
-    if args.profile:
+    if args.profile or args.profile_fp8:
         run_profile_case(args)
         return
     if args.workload != "llama8b":

@@ -29,7 +29,8 @@
  *     t % block_size. Query head h reads kv head h / (num_heads / num_kv_heads).
  *   - q, out, key, value and the caches must be 16-byte aligned.
  *   - Supported: head_dim 64 or 128; block_size 16 or 32; num_heads /
- *     num_kv_heads from 1 to 8; element types PA_F32, PA_F16, PA_BF16.
+ *     num_kv_heads from 1 to 8; element types PA_F32, PA_F16, PA_BF16, and
+ *     E4M3 caches through the *_fp8 calls (copy and swap move any type).
  */
 #ifndef PA_H
 #define PA_H
@@ -51,7 +52,11 @@ typedef enum {
   PA_ERR_CUDA = 4          /* a CUDA runtime call or launch failed */
 } pa_status;
 
-typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 } pa_dtype;
+/* Element types. PA_FP8_E4M3 is a cache-only type: one byte per element, an
+ * E4M3 code (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; no
+ * infinities; S.1111.111 is NaN; largest finite 448) read as code * scale with
+ * one fp32 scale per K or V tensor. */
+typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2, PA_FP8_E4M3 = 3 } pa_dtype;
 
 /* Bits of the device error word returned by pa_get_error(). */
 #define PA_DEVERR_BLOCK_ID 1u /* a block-table entry outside [0, num_blocks) was skipped */
@@ -201,6 +206,42 @@ pa_status pa_decode_split_static(void* out, const void* q, const void* k_cache, 
 pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers,
                          const int64_t* block_pairs, int num_pairs, int num_kv_heads, int head_dim,
                          int block_size, int64_t num_blocks, pa_dtype dtype, cudaStream_t stream);
+
+/*
+ * FP8 KV cache (E4M3 codes with one fp32 scale for K and one for V). Keeping
+ * the cache in 8 bits is one of the ways the pages list to make KV smaller
+ * (CS349E Lecture 7 notes, §10 and §11); it halves the bytes every decode step
+ * reads. Reading taken: element value = decode(code) * k_scale (or v_scale).
+ *
+ * pa_reshape_and_cache_fp8: as pa_reshape_and_cache, but key and value (of
+ * `in_dtype`: PA_F32, PA_F16 or PA_BF16) are quantised on the way in:
+ * code = E4M3(x / scale), the division in fp32 (correctly rounded), then round
+ * to nearest even on the E4M3 grid; finite values beyond +-448 saturate, NaN
+ * stays NaN. k_cache / v_cache hold codes, [num_blocks][num_kv_heads][block_size][head_dim].
+ *
+ * pa_decode_fp8 / pa_decode_split_fp8: as pa_decode / pa_decode_split over an
+ * E4M3 cache: out = softmax(scale * q . (k_scale * K)) (v_scale * V). q is of
+ * `q_dtype` (PA_F16 or PA_BF16) and is converted to fp16 inside the kernel
+ * (exact for |q| in [2^-14, 65504]); out is `q_dtype` or PA_F32. head_dim must
+ * be 128. The split variant uses the workspace layout of pa_decode_split.
+ */
+pa_status pa_reshape_and_cache_fp8(const void* key, const void* value, void* k_cache, void* v_cache,
+                                   const int64_t* slot_mapping, int num_tokens, int num_kv_heads, int head_dim,
+                                   int block_size, int64_t num_blocks, pa_dtype in_dtype, float k_scale,
+                                   float v_scale, cudaStream_t stream);
+
+pa_status pa_decode_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                        int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                        int64_t num_blocks, float scale, float k_scale, float v_scale, pa_dtype q_dtype,
+                        pa_dtype out_dtype, cudaStream_t stream);
+
+pa_status pa_decode_split_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                              int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                              int64_t num_blocks, float scale, float k_scale, float v_scale, pa_dtype q_dtype,
+                              pa_dtype out_dtype, int max_context_len, int partition_tokens, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * Move KV blocks between two pools in one launch: the GPU <-> CPU swap of

@@ -23,7 +23,7 @@ import os
 __all__ = [
     "PAError", "library", "library_path", "pa_reshape_and_cache", "pa_decode", "pa_decode_split",
     "pa_decode_split_workspace_bytes", "pa_decode_split_static", "pa_copy_blocks", "pa_swap_blocks",
-    "pa_get_error",
+    "pa_reshape_and_cache_fp8", "pa_decode_fp8", "pa_decode_split_fp8", "pa_get_error",
     "pa_version", "PA_STATIC_SCRATCH_BYTES",
     "PA_DEVERR_BLOCK_ID", "PA_DEVERR_SLOT", "PA_DEVERR_CONTEXT", "PA_DEVERR_PAIR", "PA_DEVERR_TIMEOUT",
 ]
@@ -32,7 +32,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_HERE, "libpa.so")
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_OUT_OF_RANGE, PA_ERR_CUDA = range(5)
-PA_F32, PA_F16, PA_BF16 = 0, 1, 2
+PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3 = 0, 1, 2, 3
 PA_DEVERR_BLOCK_ID, PA_DEVERR_SLOT, PA_DEVERR_CONTEXT, PA_DEVERR_PAIR, PA_DEVERR_TIMEOUT = 1, 2, 4, 8, 16
 PA_STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 
@@ -64,12 +64,16 @@ def library():
     lib.pa_decode_split_static.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I64, F, I, I, I, I, P]
     lib.pa_copy_blocks.argtypes = [P, P, I, P, I, I, I, I, I64, I, P]
     lib.pa_swap_blocks.argtypes = [P, P, P, P, I, P, I, I, I, I, I64, I64, I, P]
+    lib.pa_reshape_and_cache_fp8.argtypes = [P, P, P, P, P, I, I, I, I, I64, I, F, F, P]
+    lib.pa_decode_fp8.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I64, F, F, F, I, I, P]
+    lib.pa_decode_split_fp8.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I64, F, F, F, I, I, I, I, P, SZ, P]
     lib.pa_get_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), P]
     lib.pa_status_string.argtypes = [I]
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_version.argtypes = []
     for f in ("pa_reshape_and_cache", "pa_decode", "pa_decode_split", "pa_decode_split_static",
-              "pa_copy_blocks", "pa_swap_blocks", "pa_get_error", "pa_version"):
+              "pa_copy_blocks", "pa_swap_blocks", "pa_reshape_and_cache_fp8", "pa_decode_fp8",
+              "pa_decode_split_fp8", "pa_get_error", "pa_version"):
         getattr(lib, f).restype = I
     _lib = lib
     return lib
@@ -82,7 +86,8 @@ def _torch():
 
 def _dtype_code(t):
     torch = _torch()
-    codes = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16}
+    codes = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16, torch.uint8: PA_FP8_E4M3,
+             torch.float8_e4m3fn: PA_FP8_E4M3}
     if t.dtype not in codes:
         raise PAError("dtype", PA_ERR_UNSUPPORTED, str(t.dtype))
     return codes[t.dtype]
@@ -238,6 +243,67 @@ def pa_swap_blocks(dst_k_caches, dst_v_caches, src_k_caches, src_v_caches, block
     _check(f, library().pa_swap_blocks(arr(dk), arr(dv), arr(sk), arr(sv), L, _ptr(block_pairs),
                                        int(block_pairs.shape[0]), G, d, B, dshape[0], sshape[0], _dtype_code(dk[0]),
                                        _stream(stream)))
+
+
+def _is_code_tensor(t):
+    torch = _torch()
+    return t.dtype in (torch.uint8, torch.float8_e4m3fn)
+
+
+def pa_reshape_and_cache_fp8(key, value, k_cache, v_cache, slot_mapping, k_scale, v_scale, stream=None):
+    """Quantise each new token's K/V to E4M3 (x / scale, round to nearest even, saturating) into its slot.
+
+    ``k_cache`` / ``v_cache`` are uint8 (or float8_e4m3fn) CUDA tensors ``[num_blocks, G, B, d]``.
+    """
+    f = "pa_reshape_and_cache_fp8"
+    torch = _torch()
+    _dev(f, key, value, k_cache, v_cache, slot_mapping)
+    _need(slot_mapping.dtype == torch.int64, f, "slot_mapping must be int64")
+    _need(key.dtype == value.dtype and _is_code_tensor(k_cache) and _is_code_tensor(v_cache), f, "dtypes")
+    N, G, d = key.shape
+    nb, G2, B, d2 = k_cache.shape
+    _need(value.shape == key.shape and v_cache.shape == k_cache.shape and G2 == G and d2 == d, f, "shapes")
+    _need(slot_mapping.shape == (N,), f, "slot_mapping shape")
+    _check(f, library().pa_reshape_and_cache_fp8(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
+                                                 _ptr(slot_mapping), N, G, d, B, nb, _dtype_code(key),
+                                                 float(k_scale), float(v_scale), _stream(stream)))
+
+
+def _decode_args_fp8(f, out, q, k_cache, v_cache, block_tables, context_lens):
+    torch = _torch()
+    _dev(f, out, q, k_cache, v_cache, block_tables, context_lens)
+    _need(block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32, f,
+          "block_tables and context_lens must be int32")
+    _need(_is_code_tensor(k_cache) and _is_code_tensor(v_cache), f, "caches must hold E4M3 codes")
+    S, H, d = q.shape
+    nb, G, B, d2 = k_cache.shape
+    _need(v_cache.shape == k_cache.shape and d2 == d and out.shape == q.shape, f, "shapes")
+    _need(block_tables.dim() == 2 and block_tables.shape[0] == S and context_lens.shape == (S,), f,
+          "table shapes")
+    return S, H, G, d, B, nb, int(block_tables.shape[1])
+
+
+def pa_decode_fp8(out, q, k_cache, v_cache, block_tables, context_lens, scale, k_scale, v_scale, stream=None):
+    """Decode attention over an E4M3 cache: softmax(scale q . k_scale K) (v_scale V)."""
+    f = "pa_decode_fp8"
+    S, H, G, d, B, nb, maxb = _decode_args_fp8(f, out, q, k_cache, v_cache, block_tables, context_lens)
+    _check(f, library().pa_decode_fp8(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), maxb,
+                                      _ptr(context_lens), S, H, G, d, B, nb, float(scale), float(k_scale),
+                                      float(v_scale), _dtype_code(q), _dtype_code(out), _stream(stream)))
+
+
+def pa_decode_split_fp8(out, q, k_cache, v_cache, block_tables, context_lens, scale, k_scale, v_scale,
+                        max_context_len, partition_tokens, workspace, stream=None):
+    """Partitioned decode over an E4M3 cache (workspace as for ``pa_decode_split``)."""
+    f = "pa_decode_split_fp8"
+    S, H, G, d, B, nb, maxb = _decode_args_fp8(f, out, q, k_cache, v_cache, block_tables, context_lens)
+    _dev(f, workspace)
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(f, library().pa_decode_split_fp8(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                            maxb, _ptr(context_lens), S, H, G, d, B, nb, float(scale),
+                                            float(k_scale), float(v_scale), _dtype_code(q), _dtype_code(out),
+                                            int(max_context_len), int(partition_tokens), _ptr(workspace), nbytes,
+                                            _stream(stream)))
 
 
 def pa_get_error(stream=None) -> int:

@@ -28,7 +28,7 @@ DeviceState g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-int esize(pa_dtype dt) { return dt == PA_F32 ? 4 : 2; }
+int esize(pa_dtype dt) { return dt == PA_F32 ? 4 : (dt == PA_FP8_E4M3 ? 1 : 2); }
 bool valid_dtype(pa_dtype dt) { return dt == PA_F32 || dt == PA_F16 || dt == PA_BF16; }
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -55,9 +55,10 @@ pa_status make_pool_map(CUtensorMap* map, const void* base, pa_dtype dt, int D, 
   pa_status st = encoder(&enc);
   if (st != PA_OK) return st;
   const int e = esize(dt);
-  const CUtensorMapDataType t = dt == PA_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                : dt == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                               : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapDataType t = dt == PA_F32          ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                : dt == PA_F16        ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                : dt == PA_FP8_E4M3   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                                      : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)D * e};
   cuuint32_t box[2] = {(cuuint32_t)(128 / e), (cuuint32_t)kJobTokens};
@@ -80,6 +81,8 @@ struct DecodeArgs {
   long long num_blocks;
   float scale;
   pa_dtype dt, odt;
+  pa_dtype qdt = PA_F32;        // FP8 caches: the query type
+  float k_scale = 1.f, v_scale = 1.f;
 };
 
 pa_status check_decode(const DecodeArgs& a) {
@@ -98,27 +101,27 @@ pa_status check_decode(const DecodeArgs& a) {
   return PA_OK;
 }
 
-template <typename DT, typename OT, int D>
+template <typename DT, typename QT, typename OT, int D>
 pa_status dispatch_path(const CUtensorMap& km, const CUtensorMap& vm, const DecodeParams& p, int sms,
                         long long items, bool split, cudaStream_t st) {
-  // group >= 4 on 16-bit data: tensor cores; MHA: vector path with q in registers
-  if constexpr (sizeof(DT) == 2) {
+  // group >= 4 on 16-bit or FP8 data: tensor cores; MHA: vector path with q in registers
+  if constexpr (sizeof(DT) <= 2) {
     if (p.group >= 4)
-      return split ? launch_decode<DT, float, D, kPathMma, true>(km, vm, p, sms, items, st)
-                   : launch_decode<DT, OT, D, kPathMma, false>(km, vm, p, sms, items, st);
+      return split ? launch_decode<DT, QT, float, D, kPathMma, true>(km, vm, p, sms, items, st)
+                   : launch_decode<DT, QT, OT, D, kPathMma, false>(km, vm, p, sms, items, st);
   }
   if (p.group == 1)
-    return split ? launch_decode<DT, float, D, kPathVecMha, true>(km, vm, p, sms, items, st)
-                 : launch_decode<DT, OT, D, kPathVecMha, false>(km, vm, p, sms, items, st);
-  return split ? launch_decode<DT, float, D, kPathVec, true>(km, vm, p, sms, items, st)
-               : launch_decode<DT, OT, D, kPathVec, false>(km, vm, p, sms, items, st);
+    return split ? launch_decode<DT, QT, float, D, kPathVecMha, true>(km, vm, p, sms, items, st)
+                 : launch_decode<DT, QT, OT, D, kPathVecMha, false>(km, vm, p, sms, items, st);
+  return split ? launch_decode<DT, QT, float, D, kPathVec, true>(km, vm, p, sms, items, st)
+               : launch_decode<DT, QT, OT, D, kPathVec, false>(km, vm, p, sms, items, st);
 }
 
 template <typename DT, typename OT>
 pa_status dispatch_shape(const CUtensorMap& km, const CUtensorMap& vm, const DecodeParams& p, int D, int sms,
                          long long items, bool split, cudaStream_t st) {
-  if (D == 64) return dispatch_path<DT, OT, 64>(km, vm, p, sms, items, split, st);
-  if (D == 128) return dispatch_path<DT, OT, 128>(km, vm, p, sms, items, split, st);
+  if (D == 64) return dispatch_path<DT, DT, OT, 64>(km, vm, p, sms, items, split, st);
+  if (D == 128) return dispatch_path<DT, DT, OT, 128>(km, vm, p, sms, items, split, st);
   return PA_ERR_UNSUPPORTED;
 }
 
@@ -151,7 +154,8 @@ pa_status run_decode(const DecodeArgs& a, bool split, int partition, int max_par
   p.G = a.G;
   p.group = a.H / a.G;
   p.num_blocks = a.num_blocks;
-  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.scale_log2 = a.scale * a.k_scale * 1.4426950408889634f;
+  p.v_scale = a.v_scale;
   p.err = err;
   long long items = (long long)a.S * a.G;
   if (split) {
@@ -165,6 +169,16 @@ pa_status run_decode(const DecodeArgs& a, bool split, int partition, int max_par
     items *= max_partitions;
   }
   switch (a.dt) {
+    case PA_FP8_E4M3:
+      if (a.D != 128) return PA_ERR_UNSUPPORTED;
+      if (a.qdt == PA_BF16)
+        s = a.odt == PA_F32
+                ? dispatch_path<fp8e4m3, __nv_bfloat16, float, 128>(km, vm, p, sms, items, split, st)
+                : dispatch_path<fp8e4m3, __nv_bfloat16, __nv_bfloat16, 128>(km, vm, p, sms, items, split, st);
+      else
+        s = a.odt == PA_F32 ? dispatch_path<fp8e4m3, __half, float, 128>(km, vm, p, sms, items, split, st)
+                            : dispatch_path<fp8e4m3, __half, __half, 128>(km, vm, p, sms, items, split, st);
+      break;
     case PA_BF16:
       s = a.odt == PA_F32 ? dispatch_shape<__nv_bfloat16, float>(km, vm, p, a.D, sms, items, split, st)
                           : dispatch_shape<__nv_bfloat16, __nv_bfloat16>(km, vm, p, a.D, sms, items, split, st);
@@ -245,6 +259,66 @@ extern "C" pa_status pa_decode_split(void* out, const void* q, const void* k_cac
   if (s != PA_OK) return s;
   if (max_context_len < 0 || partition_tokens <= 0 || partition_tokens % block_size) return PA_ERR_INVALID_ARG;
   if (num_seqs == 0) return PA_OK;
+  if (num_seqs > kSplitMaxSeqs) return PA_ERR_UNSUPPORTED;
+  const size_t need =
+      pa_decode_split_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len, partition_tokens);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < need || need == 0) return PA_ERR_INVALID_ARG;
+  const long long P = std::max(1LL, ((long long)max_context_len + partition_tokens - 1) / partition_tokens);
+  if ((long long)num_seqs * num_kv_heads * P > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+  return run_decode(a, true, partition_tokens, (int)P, workspace, stream);
+}
+
+namespace {
+// FP8 entry points: the cache is E4M3 codes, q is bf16 or fp16, out is q's type or fp32.
+pa_status check_fp8(const pa::DecodeArgs& a) {
+  if (a.qdt != PA_F16 && a.qdt != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (a.odt != a.qdt && a.odt != PA_F32) return PA_ERR_UNSUPPORTED;
+  if (!std::isfinite(a.k_scale) || !std::isfinite(a.v_scale) || a.k_scale <= 0.f || a.v_scale <= 0.f)
+    return PA_ERR_INVALID_ARG;
+  if (a.D != 128) return PA_ERR_UNSUPPORTED;
+  return PA_OK;
+}
+}  // namespace
+
+extern "C" pa_status pa_decode_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                                   int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                                   int64_t num_blocks, float scale, float k_scale, float v_scale, pa_dtype q_dtype,
+                                   pa_dtype out_dtype, cudaStream_t stream) {
+  using namespace pa;
+  DecodeArgs a{out,      q,         k_cache,      v_cache,  block_tables, max_blocks_per_seq,
+               context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+               (long long)num_blocks, scale, q_dtype, out_dtype};
+  pa_status s = check_decode(a);  // shapes, pointers, alignment (q / out type as the 16-bit type)
+  if (s != PA_OK || num_seqs == 0) return s;
+  a.dt = PA_FP8_E4M3;
+  a.qdt = q_dtype;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  if ((s = check_fp8(a)) != PA_OK) return s;
+  return run_decode(a, false, 0, 0, nullptr, stream);
+}
+
+extern "C" pa_status pa_decode_split_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                         const int32_t* block_tables, int max_blocks_per_seq,
+                                         const int32_t* context_lens, int num_seqs, int num_heads,
+                                         int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                                         float scale, float k_scale, float v_scale, pa_dtype q_dtype,
+                                         pa_dtype out_dtype, int max_context_len, int partition_tokens,
+                                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  using namespace pa;
+  DecodeArgs a{out,      q,         k_cache,      v_cache,  block_tables, max_blocks_per_seq,
+               context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+               (long long)num_blocks, scale, q_dtype, out_dtype};
+  pa_status s = check_decode(a);
+  if (s != PA_OK) return s;
+  if (max_context_len < 0 || partition_tokens <= 0 || partition_tokens % block_size) return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PA_OK;
+  a.dt = PA_FP8_E4M3;
+  a.qdt = q_dtype;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  if ((s = check_fp8(a)) != PA_OK) return s;
   if (num_seqs > kSplitMaxSeqs) return PA_ERR_UNSUPPORTED;
   const size_t need =
       pa_decode_split_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len, partition_tokens);

@@ -112,8 +112,47 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-int esize(pa_dtype dt) { return dt == PA_F32 ? 4 : 2; }
-bool valid_dtype(pa_dtype dt) { return dt == PA_F32 || dt == PA_F16 || dt == PA_BF16; }
+int esize(pa_dtype dt) { return dt == PA_F32 ? 4 : (dt == PA_FP8_E4M3 ? 1 : 2); }
+bool valid_dtype(pa_dtype dt) { return dt == PA_F32 || dt == PA_F16 || dt == PA_BF16 || dt == PA_FP8_E4M3; }
+
+// FP8 cache write: one thread quantises and stores 16 consecutive elements of a
+// (token, K-or-V, kv head) row: code = E4M3(x / scale), fp32 division, round to
+// nearest even, saturating.
+template <typename IT>
+__global__ void __launch_bounds__(256)
+    reshape_and_cache_fp8_kernel(const IT* __restrict__ key, const IT* __restrict__ value, uint8_t* k_cache,
+                                 uint8_t* v_cache, const int64_t* __restrict__ slot_mapping, int num_tokens, int G,
+                                 int D, int BS, long long num_slots, float k_scale, float v_scale, unsigned* err) {
+  const int cpr = D / 16;  // 16-element chunks per row
+  const long long total = (long long)num_tokens * 2 * G * cpr;
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int c = (int)(idx % cpr);
+    long long rest = idx / cpr;
+    const int h = (int)(rest % G);
+    rest /= G;
+    const int which = (int)(rest & 1);
+    const long long t = rest >> 1;
+    const long long slot = __ldg(slot_mapping + t);
+    if (slot < 0) continue;
+    if (slot >= num_slots) {
+      if (c == 0 && h == 0 && which == 0) atomicOr(err, kErrSlot);
+      continue;
+    }
+    const IT* src = (which ? value : key) + (t * G + h) * D + c * 16;
+    const float sc = which ? v_scale : k_scale;
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float a0 = __fdiv_rn(to_f32(src[4 * i + 0]), sc), a1 = __fdiv_rn(to_f32(src[4 * i + 1]), sc);
+      const float a2 = __fdiv_rn(to_f32(src[4 * i + 2]), sc), a3 = __fdiv_rn(to_f32(src[4 * i + 3]), sc);
+      w[i] = f32x2_to_e4m3x2(a0, a1) | (f32x2_to_e4m3x2(a2, a3) << 16);
+    }
+    const long long blk = slot / BS, row = slot - blk * BS;
+    uint8_t* dst = (which ? v_cache : k_cache) + ((blk * G + h) * BS + row) * D + c * 16;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
@@ -223,4 +262,47 @@ extern "C" pa_status pa_swap_blocks(void* const* dst_k_caches, void* const* dst_
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
   }
   return PA_OK;
+}
+
+extern "C" pa_status pa_reshape_and_cache_fp8(const void* key, const void* value, void* k_cache, void* v_cache,
+                                              const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                                              int head_dim, int block_size, int64_t num_blocks, pa_dtype in_dtype,
+                                              float k_scale, float v_scale, cudaStream_t stream) {
+  using namespace pa;
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0 ||
+      !(in_dtype == PA_F32 || in_dtype == PA_F16 || in_dtype == PA_BF16) || !(k_scale > 0.f) ||
+      !(v_scale > 0.f) || k_scale == INFINITY || v_scale == INFINITY)
+    return PA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+  if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+    return PA_ERR_INVALID_ARG;
+  if (head_dim % 16) return PA_ERR_UNSUPPORTED;
+  unsigned* err = nullptr;
+  int sms = 0;
+  pa_status st = device_state(&err, &sms);
+  if (st != PA_OK) return st;
+  const long long total = (long long)num_tokens * 2 * num_kv_heads * (head_dim / 16);
+  const unsigned grid = (unsigned)std::min<long long>((total + 255) / 256, (long long)sms * 16);
+  uint8_t* kc = static_cast<uint8_t*>(k_cache);
+  uint8_t* vc = static_cast<uint8_t*>(v_cache);
+  const long long nslots = (long long)num_blocks * block_size;
+  switch (in_dtype) {
+    case PA_F32:
+      reshape_and_cache_fp8_kernel<float><<<grid, 256, 0, stream>>>(
+          static_cast<const float*>(key), static_cast<const float*>(value), kc, vc, slot_mapping, num_tokens,
+          num_kv_heads, head_dim, block_size, nslots, k_scale, v_scale, err);
+      break;
+    case PA_F16:
+      reshape_and_cache_fp8_kernel<__half><<<grid, 256, 0, stream>>>(
+          static_cast<const __half*>(key), static_cast<const __half*>(value), kc, vc, slot_mapping, num_tokens,
+          num_kv_heads, head_dim, block_size, nslots, k_scale, v_scale, err);
+      break;
+    default:
+      reshape_and_cache_fp8_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
+          static_cast<const __nv_bfloat16*>(key), static_cast<const __nv_bfloat16*>(value), kc, vc, slot_mapping,
+          num_tokens, num_kv_heads, head_dim, block_size, nslots, k_scale, v_scale, err);
+  }
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

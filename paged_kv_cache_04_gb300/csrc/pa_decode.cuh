@@ -70,6 +70,7 @@ struct DecodeParams {
   float* ws_o;                  // [S][H][P][D]
   float* ws_m;                  // [S][H][P]  (max score, base-2 units)
   float* ws_l;                  // [S][H][P]
+  float v_scale;                // FP8 caches: V scale applied to the output (1 otherwise)
   unsigned* err;
 };
 
@@ -80,8 +81,8 @@ struct SmemLayout {
 __host__ __device__ inline unsigned round_up(unsigned x, unsigned a) { return (x + a - 1) / a * a; }
 
 // Shared-memory map, computed identically on the host (launch size) and device.
-__host__ __device__ inline SmemLayout make_layout(int W, int R, int D, int esize, int group, int path, bool split,
-                                                  int S) {
+__host__ __device__ inline SmemLayout make_layout(int W, int R, int D, int esize, int qsize, int group, int path,
+                                                  bool split, int S) {
   SmemLayout L;
   L.stage_bytes = 2u * kJobTokens * D * esize;
   unsigned off = W * R * L.stage_bytes;
@@ -93,7 +94,7 @@ __host__ __device__ inline SmemLayout make_layout(int W, int R, int D, int esize
   if (!split) off += W * group * D * 4 + W * kMaxGroup * 2 * 4;
   L.q_off = off;
   if (path == kPathVec) off += W * group * D * 4;            // fp32 q rows per warp
-  if (path == kPathVecMha) off += round_up(W * 2 * D * esize, 16);  // double-buffered raw q row per warp
+  if (path == kPathVecMha) off += round_up(W * 2 * D * qsize, 16);  // double-buffered raw q row per warp
   L.sched_off = off;
   if (split)
     off += (S + 1) * 4;
@@ -178,23 +179,28 @@ struct Schedule {
   }
 };
 
-template <typename DT, typename OT, int D, int PATH, bool SPLIT>
+// DT: cache element type (float, __half, __nv_bfloat16 or fp8e4m3); QT: query
+// type (DT, or a 16-bit type over an FP8 cache); OT: output type.
+template <typename DT, typename QT, typename OT, int D, int PATH, bool SPLIT>
 __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         const DecodeParams p) {
   using Cfg = StageCfg<DT, D, PATH>;
   constexpr bool MMA = PATH == kPathMma;
+  constexpr bool F8 = std::is_same<DT, fp8e4m3>::value;
+  using MT = typename std::conditional<F8, __half, DT>::type;  // tensor-core operand type
+  static_assert(!F8 || D % 64 == 0, "FP8 caches need head_dim a multiple of 64");
   constexpr int W = Cfg::W, R = Cfg::R, E = Cfg::E, TILE = Cfg::TILE, JT = kJobTokens;
   constexpr int NCH = D * E / 16;     // 16-byte chunks per row
   constexpr int NREG = D * E / 128;   // 128-byte column regions (one TMA box each)
   constexpr int BOX_X = 128 / E;
   static_assert(NREG >= 1 && D * E % 128 == 0, "head_dim * element size must be a multiple of 128 bytes");
-  static_assert(!MMA || (sizeof(DT) == 2 && D % 16 == 0), "mma path needs 16-bit data");
+  static_assert(!MMA || ((sizeof(DT) == 2 || F8) && D % 16 == 0), "mma path needs 16-bit or FP8 data");
 
   extern __shared__ uint8_t smem_raw[];
   // TMA 128-byte swizzling needs 1024-byte aligned destinations: align the shared-window offset.
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const SmemLayout L = make_layout(W, R, D, E, p.group, PATH, SPLIT, p.S);
+  const SmemLayout L = make_layout(W, R, D, E, (int)sizeof(QT), p.group, PATH, SPLIT, p.S);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars_off);
   volatile uint8_t* stage_ok = smem + L.ok_off;                        // [W][R]
   float* mrg_o = reinterpret_cast<float*>(smem + L.merge_off);        // [W][group][D] (plain mode)
@@ -411,7 +417,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
         }
       }
       reinterpret_cast<OT*>(p.out)[((long long)x.s * p.H + hq0 + h) * D + i] =
-          from_f32<OT>(Lsum > 0.f ? O / Lsum : 0.f);
+          from_f32<OT>(Lsum > 0.f ? O * p.v_scale / Lsum : 0.f);
     }
     asm volatile("bar.sync 1, %0;" ::"n"(W * 32) : "memory");
   };
@@ -421,19 +427,38 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
     // ---------------- tensor-core path: group >= 4, 16-bit data ----------------
     const int g = lane >> 2, t4 = lane & 3;
     uint32_t qf[D / 16][2], qn[D / 16][2];
+    // FP8 caches permute head_dim inside each 64-wide slice so that a thread's
+    // K bytes for four k-steps are 16 contiguous bytes: k-step ks = 4 kb + j,
+    // MMA k-columns {2t, 2t+1, 2t+8, 2t+9} <-> d = 64 kb + 16 t + 4 j + {0,1,2,3};
+    // q takes the same permutation, so q . K is unchanged.
     auto load_q = [&](const Item& x, uint32_t (&dst)[D / 16][2]) {
-      const DT* qrow = reinterpret_cast<const DT*>(p.q) + ((long long)x.s * p.H + x.kv * p.group) * D;
+      const QT* qrow = reinterpret_cast<const QT*>(p.q) + ((long long)x.s * p.H + x.kv * p.group) * D;
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
         if (g < p.group) {
-          const DT* qr = qrow + (long long)g * D + ks * 16 + 2 * t4;
-          dst[ks][0] = __ldg(reinterpret_cast<const uint32_t*>(qr));
-          dst[ks][1] = __ldg(reinterpret_cast<const uint32_t*>(qr + 8));
+          if constexpr (F8) {
+            const QT* qr = qrow + (long long)g * D + 64 * (ks >> 2) + 16 * t4 + 4 * (ks & 3);
+            dst[ks][0] = Mma<__half>::pack(to_f32(qr[0]), to_f32(qr[1]));
+            dst[ks][1] = Mma<__half>::pack(to_f32(qr[2]), to_f32(qr[3]));
+          } else {
+            const QT* qr = qrow + (long long)g * D + ks * 16 + 2 * t4;
+            dst[ks][0] = __ldg(reinterpret_cast<const uint32_t*>(qr));
+            dst[ks][1] = __ldg(reinterpret_cast<const uint32_t*>(qr + 8));
+          }
         } else {
           dst[ks][0] = 0u;
           dst[ks][1] = 0u;
         }
       }
+    };
+    // FP8: MMA row r holds token tr(r) = (r & 7) / 2 + 4 (r & 1) + (r & 8), so the
+    // eight lanes of a quarter-warp read rows tr(2i), tr(2i+1) = i, i + 4, whose
+    // swizzled 16-byte chunks fall in different halves of the banks. K rows, V
+    // rows (hence P) and the masks all use the same order, so the sums are the
+    // same; 16-bit caches keep tr(r) = r (ldmatrix reads conflict-free already).
+    auto tr = [](int r) -> int {
+      if constexpr (F8) return ((r & 7) >> 1) + 4 * (r & 1) + (r & 8);
+      else return r;
     };
     bool have = sch.get(p, 0, warp, it);
     if (have) load_q(it, qn);
@@ -462,13 +487,31 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
           const int nv = min(JT, it.t1 - u * JT);
           // two independent accumulator chains over head_dim halve the MMA latency chain
           float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
+          const uint8_t* ktp = my_stages + stage * L.stage_bytes;
+          if constexpr (F8) {
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ks += 2) {
-            uint32_t a[4], b[4];
-            ldsm_x4(a, kt + sw128_offset(lane & 15, ks * 2 + (lane >> 4), JT));
-            ldsm_x4(b, kt + sw128_offset(lane & 15, ks * 2 + 2 + (lane >> 4), JT));
-            Mma<DT>::run(sc, a, qf[ks][0], qf[ks][1]);
-            Mma<DT>::run(sd, b, qf[ks + 1][0], qf[ks + 1][1]);
+            for (int kb = 0; kb < D / 64; ++kb) {
+              const uint4 r0 = *reinterpret_cast<const uint4*>(ktp + sw128_offset(tr(g), 4 * kb + t4, JT));
+              const uint4 r1 = *reinterpret_cast<const uint4*>(ktp + sw128_offset(tr(g + 8), 4 * kb + t4, JT));
+              const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w}, w1[4] = {r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                uint32_t a[4];
+                e4m3x4_to_f16x2x2(w0[j], a[0], a[2]);
+                e4m3x4_to_f16x2x2(w1[j], a[1], a[3]);
+                const int ks = 4 * kb + j;
+                Mma<MT>::run((j & 1) ? sd : sc, a, qf[ks][0], qf[ks][1]);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ks += 2) {
+              uint32_t a[4], b[4];
+              ldsm_x4(a, kt + sw128_offset(lane & 15, ks * 2 + (lane >> 4), JT));
+              ldsm_x4(b, kt + sw128_offset(lane & 15, ks * 2 + 2 + (lane >> 4), JT));
+              Mma<MT>::run(sc, a, qf[ks][0], qf[ks][1]);
+              Mma<MT>::run(sd, b, qf[ks + 1][0], qf[ks + 1][1]);
+            }
           }
 #pragma unroll
           for (int e = 0; e < 4; ++e) sc[e] += sd[e];
@@ -476,7 +519,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
           float mx0 = NEG_INF, mx1 = NEG_INF;
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int tok = g + ((e >> 1) << 3);
+            const int tok = tr(g + ((e >> 1) << 3));
             const float z = tok < nv ? sc[e] * p.scale_log2 : NEG_INF;
             sc[e] = z;
             if (e & 1) mx1 = fmaxf(mx1, z); else mx0 = fmaxf(mx0, z);
@@ -508,31 +551,63 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
           // weight, too coarse for a 2e-3 bound when a few tokens dominate, so P is
           // split into hi + lo 16-bit parts (P - hi - lo is below 2^-17 P) and each
           // part gets its own MMA into the same fp32 accumulator.
-          const uint32_t h01 = Mma<DT>::pack(sc[0], sc[1]);
-          const uint32_t h23 = Mma<DT>::pack(sc[2], sc[3]);
+          const uint32_t h01 = Mma<MT>::pack(sc[0], sc[1]);
+          const uint32_t h23 = Mma<MT>::pack(sc[2], sc[3]);
           float r0, r1, r2, r3;
-          unpack2(h01, (DT*)nullptr, r0, r1);
-          unpack2(h23, (DT*)nullptr, r2, r3);
+          unpack2(h01, (MT*)nullptr, r0, r1);
+          unpack2(h23, (MT*)nullptr, r2, r3);
           const uint32_t b0 = movmatrix_trans(h01);
           const uint32_t b1 = movmatrix_trans(h23);
-          const uint32_t e0 = movmatrix_trans(Mma<DT>::pack(sc[0] - r0, sc[1] - r1));
-          const uint32_t e1 = movmatrix_trans(Mma<DT>::pack(sc[2] - r2, sc[3] - r3));
+          const uint32_t e0 = movmatrix_trans(Mma<MT>::pack(sc[0] - r0, sc[1] - r1));
+          const uint32_t e1 = movmatrix_trans(Mma<MT>::pack(sc[2] - r2, sc[3] - r3));
           const int vtok = ((lane >> 4) << 3) + (lane & 7);
           // tokens held by this lane's A fragments: lo pair (a0, a1), hi pair (a2, a3);
           // rows past the context are zeroed so that 0 * (stale or NaN) cannot leak in
           const int tlo = 2 * t4;
-          const uint32_t mlo = (tlo < nv ? 0x0000ffffu : 0u) | (tlo + 1 < nv ? 0xffff0000u : 0u);
-          const uint32_t mhi = (tlo + 8 < nv ? 0x0000ffffu : 0u) | (tlo + 9 < nv ? 0xffff0000u : 0u);
+          const uint32_t mlo = (tr(tlo) < nv ? 0x0000ffffu : 0u) | (tr(tlo + 1) < nv ? 0xffff0000u : 0u);
+          const uint32_t mhi = (tr(tlo + 8) < nv ? 0x0000ffffu : 0u) | (tr(tlo + 9) < nv ? 0xffff0000u : 0u);
+          const bool full = nv == JT;  // every job but a sequence's last: no rows to mask
+          if constexpr (F8) {
+            // V^T fragments: this lane's 4 codes of rows g and g+8 -> fp16 pairs,
+            // each pair one row of an 8x8 tile; movmatrix transposes the tiles.
+            // head_dim rows of the result follow the permutation in drow().
+            const uint8_t* vtp = ktp + TILE;
 #pragma unroll
-          for (int mt = 0; mt < D / 16; ++mt) {
-            uint32_t a[4];
-            ldsm_x4_trans(a, vt + sw128_offset(vtok, mt * 2 + ((lane >> 3) & 1), JT));
-            a[0] &= mlo;
-            a[1] &= mlo;
-            a[2] &= mhi;
-            a[3] &= mhi;
-            Mma<DT>::run(o[mt], a, b0, b1);
-            Mma<DT>::run(o[mt], a, e0, e1);
+            for (int mb = 0; mb < D / 64; ++mb) {
+              const uint4 r0 = *reinterpret_cast<const uint4*>(vtp + sw128_offset(tr(g), 4 * mb + t4, JT));
+              const uint4 r1 = *reinterpret_cast<const uint4*>(vtp + sw128_offset(tr(g + 8), 4 * mb + t4, JT));
+              const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w}, w1[4] = {r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                uint32_t x0, x1, y0, y1;
+                e4m3x4_to_f16x2x2(w0[j], x0, x1);
+                e4m3x4_to_f16x2x2(w1[j], y0, y1);
+                uint32_t a[4] = {movmatrix_trans(x0), movmatrix_trans(x1), movmatrix_trans(y0), movmatrix_trans(y1)};
+                if (!full) {
+                  a[0] &= mlo;
+                  a[1] &= mlo;
+                  a[2] &= mhi;
+                  a[3] &= mhi;
+                }
+                const int mt = 4 * mb + j;
+                Mma<MT>::run(o[mt], a, b0, b1);
+                Mma<MT>::run(o[mt], a, e0, e1);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+              uint32_t a[4];
+              ldsm_x4_trans(a, vt + sw128_offset(vtok, mt * 2 + ((lane >> 3) & 1), JT));
+              if (!full) {
+                a[0] &= mlo;
+                a[1] &= mlo;
+                a[2] &= mhi;
+                a[3] &= mhi;
+              }
+              Mma<MT>::run(o[mt], a, b0, b1);
+              Mma<MT>::run(o[mt], a, e0, e1);
+            }
           }
         }
         job_done();
@@ -543,16 +618,25 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
         l1 += __shfl_xor_sync(0xffffffffu, l1, o2);
       }
       const int hA = 2 * t4, hB = hA + 1;
+      // head_dim index of accumulator row r (0..15) of m-tile mt
+      auto drow = [&](int mt, int r) -> int {
+        if constexpr (F8) {
+          const int rr = r & 7;
+          return 64 * (mt >> 2) + 16 * (rr >> 1) + 4 * (mt & 3) + ((r >> 3) << 1) + (rr & 1);
+        } else {
+          return mt * 16 + r;
+        }
+      };
       if (WARP_PARTS) {
         if (it.part >= 0) {
           const long long rowA = ((long long)it.s * p.H + it.kv * p.group + hA) * p.max_partitions + it.part;
           const long long rowB = rowA + p.max_partitions;
-          const float iA = l0 > 0.f ? 1.f / l0 : 0.f, iB = l1 > 0.f ? 1.f / l1 : 0.f;
+          const float iA = l0 > 0.f ? p.v_scale / l0 : 0.f, iB = l1 > 0.f ? p.v_scale / l1 : 0.f;
           if (hA < p.group) {
 #pragma unroll
             for (int mt = 0; mt < D / 16; ++mt) {
-              p.ws_o[rowA * D + mt * 16 + g] = o[mt][0] * iA;
-              p.ws_o[rowA * D + mt * 16 + g + 8] = o[mt][2] * iA;
+              p.ws_o[rowA * D + drow(mt, g)] = o[mt][0] * iA;
+              p.ws_o[rowA * D + drow(mt, g + 8)] = o[mt][2] * iA;
             }
             if (g == 0) {
               p.ws_m[rowA] = m0;
@@ -562,8 +646,8 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
           if (hB < p.group) {
 #pragma unroll
             for (int mt = 0; mt < D / 16; ++mt) {
-              p.ws_o[rowB * D + mt * 16 + g] = o[mt][1] * iB;
-              p.ws_o[rowB * D + mt * 16 + g + 8] = o[mt][3] * iB;
+              p.ws_o[rowB * D + drow(mt, g)] = o[mt][1] * iB;
+              p.ws_o[rowB * D + drow(mt, g + 8)] = o[mt][3] * iB;
             }
             if (g == 0) {
               p.ws_m[rowB] = m1;
@@ -576,15 +660,15 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
         if (hA < p.group) {
 #pragma unroll
           for (int mt = 0; mt < D / 16; ++mt) {
-            mo[hA * D + mt * 16 + g] = o[mt][0];
-            mo[hA * D + mt * 16 + g + 8] = o[mt][2];
+            mo[hA * D + drow(mt, g)] = o[mt][0];
+            mo[hA * D + drow(mt, g + 8)] = o[mt][2];
           }
         }
         if (hB < p.group) {
 #pragma unroll
           for (int mt = 0; mt < D / 16; ++mt) {
-            mo[hB * D + mt * 16 + g] = o[mt][1];
-            mo[hB * D + mt * 16 + g + 8] = o[mt][3];
+            mo[hB * D + drow(mt, g)] = o[mt][1];
+            mo[hB * D + drow(mt, g + 8)] = o[mt][3];
           }
         }
         if (g == 0) {
@@ -608,14 +692,15 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
     constexpr int EPC = 16 / E;              // elements per 16-byte chunk
     constexpr int EPL = D / 32;              // output elements per lane in P V
     constexpr int VB = EPL * E;              // V bytes per lane per row
-    constexpr int QCH = D * E / 16;          // 16-byte chunks of one q row
+    constexpr int QE = (int)sizeof(QT);
+    constexpr int QCH = D * QE / 16;         // 16-byte chunks of one q row
     float* qs = qs_all + warp * p.group * D;
-    uint8_t* qraw = qraw_all + warp * 2 * D * E;
+    uint8_t* qraw = qraw_all + warp * 2 * D * QE;
     const int t = lane % JT, part = lane / JT;
     float qreg[MHA ? CPL * EPC : 1];  // MHA: this lane's half of the q row
     auto fetch_q_raw = [&](const Item& x, int buf) {  // MHA: next q row -> shared memory, async
-      const uint8_t* src = reinterpret_cast<const uint8_t*>(p.q) + ((long long)x.s * p.H + x.kv) * D * E;
-      for (int c = lane; c < QCH; c += 32) cp_async16(qraw + buf * D * E + c * 16, src + c * 16);
+      const uint8_t* src = reinterpret_cast<const uint8_t*>(p.q) + ((long long)x.s * p.H + x.kv) * D * QE;
+      for (int c = lane; c < QCH; c += 32) cp_async16(qraw + buf * D * QE + c * 16, src + c * 16);
       cp_async_commit();
     };
     int qbuf = 0;
@@ -627,7 +712,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
       if constexpr (MHA) {
         cp_async_wait_all();
         __syncwarp();
-        const DT* qr = reinterpret_cast<const DT*>(qraw + qbuf * D * E);
+        const QT* qr = reinterpret_cast<const QT*>(qraw + qbuf * D * QE);
 #pragma unroll
         for (int c = 0; c < CPL; ++c)
 #pragma unroll
@@ -637,7 +722,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
         if (sch.get(p, k + 1, warp, nx)) fetch_q_raw(nx, qbuf ^ 1);
         qbuf ^= 1;
       } else {
-        const DT* qrow = reinterpret_cast<const DT*>(p.q) + ((long long)it.s * p.H + it.kv * p.group) * D;
+        const QT* qrow = reinterpret_cast<const QT*>(p.q) + ((long long)it.s * p.H + it.kv * p.group) * D;
         for (int i = lane; i < p.group * D; i += 32) qs[i] = to_f32(qrow[i]);
         __syncwarp();
       }
@@ -687,6 +772,17 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
                 z = fmaf(qv[1], __uint_as_float(raw.y), z);
                 z = fmaf(qv[2], __uint_as_float(raw.z), z);
                 z = fmaf(qv[3], __uint_as_float(raw.w), z);
+              } else if constexpr (E == 1) {
+                const uint32_t wd[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                for (int w4 = 0; w4 < 4; ++w4) {
+                  float f0, f1, f2, f3;
+                  e4m3x4_to_f32(wd[w4], f0, f1, f2, f3);
+                  z = fmaf(qv[4 * w4 + 0], f0, z);
+                  z = fmaf(qv[4 * w4 + 1], f1, z);
+                  z = fmaf(qv[4 * w4 + 2], f2, z);
+                  z = fmaf(qv[4 * w4 + 3], f3, z);
+                }
               } else {
                 float f0, f1, f2, f3, f4, f5, f6, f7;
                 unpack2(raw.x, (DT*)nullptr, f0, f1);
@@ -726,7 +822,16 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
               const float w = __shfl_sync(0xffffffffu, pt, tt);
               const int byte = lane * VB;
               const uint8_t* src = vt + sw128_offset(tt, byte >> 4, JT) + (byte & 15);
-              if constexpr (E == 4) {
+              if constexpr (E == 1) {
+                static_assert(VB == 4, "FP8 vector path reads 4 codes per lane");
+                const uint32_t raw = *reinterpret_cast<const uint32_t*>(src);
+                float f0, f1, f2, f3;
+                e4m3x4_to_f32(raw, f0, f1, f2, f3);
+                o[h][0] = fmaf(w, f0, o[h][0]);
+                o[h][1] = fmaf(w, f1, o[h][1]);
+                o[h][2] = fmaf(w, f2, o[h][2]);
+                o[h][3] = fmaf(w, f3, o[h][3]);
+              } else if constexpr (E == 4) {
                 if constexpr (VB == 16) {
                   const float4 v = *reinterpret_cast<const float4*>(src);
                   o[h][0] = fmaf(w, v.x, o[h][0]);
@@ -772,7 +877,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
         if (WARP_PARTS) {
           if (it.part >= 0) {
             const long long row = ((long long)it.s * p.H + it.kv * p.group + h) * p.max_partitions + it.part;
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float inv = l > 0.f ? p.v_scale / l : 0.f;
 #pragma unroll
             for (int e = 0; e < EPL; ++e) p.ws_o[row * D + lane * EPL + e] = o[h][e] * inv;
             if (lane == 0) {

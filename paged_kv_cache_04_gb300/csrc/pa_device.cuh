@@ -7,7 +7,10 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
+
+#include <type_traits>
 
 namespace pa {
 
@@ -179,6 +182,52 @@ struct Mma<__half> {
     return *reinterpret_cast<uint32_t*>(&v);
   }
 };
+
+// ---------------------------------------------------------------------------
+// FP8 (E4M3) cache codes
+// ---------------------------------------------------------------------------
+// Storage tag for a cache of E4M3 codes (one byte per element).
+struct fp8e4m3 {
+  uint8_t bits;
+};
+
+// Two E4M3 codes (low byte first) -> two fp16 values packed low-first. Every
+// E4M3 value is exact in fp16, so the conversion is exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+  uint32_t r;
+  const unsigned short c = static_cast<unsigned short>(two_codes & 0xffffu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(c));
+  return r;
+}
+
+// Four E4M3 codes (one 32-bit word, low byte first) -> two fp16 pairs:
+// lo = codes 0, 1 and hi = codes 2, 3 (each low-first); exact.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+// Four E4M3 codes (one 32-bit word, low byte first) -> four floats.
+__device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float& f0, float& f1, float& f2, float& f3) {
+  uint32_t lo, hi;
+  e4m3x4_to_f16x2x2(w, lo, hi);
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+  f0 = a.x;
+  f1 = a.y;
+  f2 = b.x;
+  f3 = b.y;
+}
+
+// Two floats -> two E4M3 codes (low byte first): round to nearest even,
+// finite values beyond +-448 saturate, NaN stays NaN.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
+}
 
 // ---------------------------------------------------------------------------
 // element conversions

@@ -14,9 +14,9 @@ struct DecodeParams;
 // of the error word and the SM count. Returns PA_ERR_CUDA if CUDA fails.
 pa_status device_state(unsigned** err, int* num_sms);
 
-// Launchers, one per (element type, output type, head_dim, path, split)
-// combination, instantiated in pa_decode_{f32,f16,bf16}.cu.
-template <typename DT, typename OT, int D, int PATH, bool SPLIT>
+// Launchers, one per (cache type, query type, output type, head_dim, path,
+// split) combination, instantiated in pa_decode_{f32,f16,bf16,fp8}.cu.
+template <typename DT, typename QT, typename OT, int D, int PATH, bool SPLIT>
 pa_status launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                         int num_sms, long long max_items, cudaStream_t stream);
 

@@ -283,6 +283,28 @@ def shared_prefix(device="cpu", prompts=64, samples=8, prefix=2048, tail_lo=0, t
     return wl
 
 
+def to_fp8(wl: Workload, k_scale=None, v_scale=None) -> Workload:
+    """The same batch with an E4M3 KV pool: codes of clamp(x / scale, +-448).
+
+    The scale defaults to max|x| / 448 over the pool (one fp32 per tensor). q
+    and the new tokens keep their type (the fp8 cache write quantises them).
+    """
+    def codes(t, sc):
+        out = torch.empty(t.shape, dtype=torch.uint8, device=t.device)
+        flat, of = t.view(t.shape[0], -1), out.view(t.shape[0], -1)
+        for r in range(0, t.shape[0], 4096):
+            x = (flat[r:r + 4096].float() / sc).clamp_(-448.0, 448.0)
+            of[r:r + 4096] = x.to(torch.float8_e4m3fn).view(torch.uint8)
+        return out
+    ks = float(k_scale if k_scale is not None else wl.k_cache.abs().max().float().item() / 448.0)
+    vs = float(v_scale if v_scale is not None else wl.v_cache.abs().max().float().item() / 448.0)
+    meta = dict(wl.meta)
+    meta.update(k_scale=ks, v_scale=vs, kv_dtype="fp8_e4m3")
+    return Workload(wl.name + "_fp8", wl.S, wl.H, wl.G, wl.d, wl.B, wl.dtype, wl.num_blocks, wl.scale,
+                    wl.context_lens, wl.block_tables, wl.q, codes(wl.k_cache, ks), codes(wl.v_cache, vs),
+                    wl.new_key, wl.new_value, wl.slot_mapping, wl.copy_pairs, wl.partition_tokens, meta)
+
+
 def by_name(name: str, device="cpu", **kw) -> Workload:
     table = {"tiny": tiny, "opt13b": opt13b, "llama8b": llama8b, "long70b": long70b,
              "shared": shared_prefix,
