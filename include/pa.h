@@ -49,7 +49,8 @@ typedef enum {
   PA_ERR_INVALID_ARG = 1, /* null / misaligned pointer, negative or inconsistent size */
   PA_ERR_UNSUPPORTED = 2, /* valid but outside what this build implements */
   PA_ERR_OUT_OF_RANGE = 3, /* (pa_get_error) a device-side value was out of range */
-  PA_ERR_CUDA = 4          /* a CUDA runtime call or launch failed */
+  PA_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+  PA_ERR_NO_BLOCKS = 5     /* (block manager) no free physical block is left */
 } pa_status;
 
 /* Element types. PA_FP8_E4M3 is a cache-only type: one byte per element, an
@@ -282,6 +283,54 @@ const char* pa_status_string(pa_status status);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 int pa_version(void);
+
+/*
+ * Host block manager (CPU only; no CUDA call). It produces the block tables,
+ * slot mappings and copy-on-write pairs the kernels above consume:
+ *   - a pool of num_blocks blocks of block_size tokens; a sequence gets a new
+ *     block only when its last one is full (CS349E Lecture 7 notes §4.1);
+ *   - fork shares blocks (reference counts); appending into a shared,
+ *     partially filled last block copies it first and returns the pair
+ *     (§5.1);
+ *   - with prefix_caching != 0, each full block is keyed by a chain hash of
+ *     (parent block's hash, its tokens), so only whole block-aligned prefixes
+ *     match (Month 2 · PagedAttention §6.3, §7.5); a new sequence reuses the
+ *     cached blocks of its longest matching prefix; a released block that holds
+ *     a cached full block stays reusable until it is evicted, least recently
+ *     released first, when no other free block is left (§7.2-§7.3; CS349E §8).
+ * Not thread-safe: one manager per thread (or external locking).
+ *
+ * pa_bm_create         NULL on bad sizes or allocation failure.
+ * pa_bm_add_sequence   prefill: blocks for tokens[0..num_tokens); *cached_tokens
+ *                      (may be NULL) receives how many leading tokens came from
+ *                      the prefix cache (a multiple of block_size). Unknown /
+ *                      duplicate ids: PA_ERR_INVALID_ARG; pool exhausted:
+ *                      PA_ERR_NO_BLOCKS (nothing is changed).
+ * pa_bm_fork           child shares every block of parent.
+ * pa_bm_append         reserve the slot of the sequence's next token (slot =
+ *                      block * block_size + row); *cow_src / *cow_dst receive the
+ *                      copy-on-write pair or -1.
+ * pa_bm_free           release the sequence's blocks (tail first).
+ * pa_bm_block_table    writes up to `capacity` block ids; returns the table
+ *                      length, or -1 for an unknown sequence.
+ * pa_bm_context_len    tokens of the sequence, or -1.
+ * pa_bm_num_free       blocks available (free + evictable).
+ * pa_bm_stats          out[6] = {prefix-cache block lookups, hits, evictions,
+ *                      copy-on-write copies, evictable blocks, cached blocks}.
+ */
+typedef struct pa_bm pa_bm;
+pa_bm* pa_bm_create(int64_t num_blocks, int block_size, int prefix_caching);
+void pa_bm_destroy(pa_bm* bm);
+pa_status pa_bm_add_sequence(pa_bm* bm, int64_t seq_id, const int32_t* tokens, int32_t num_tokens,
+                             int32_t* cached_tokens);
+pa_status pa_bm_fork(pa_bm* bm, int64_t parent_id, int64_t child_id);
+pa_status pa_bm_append(pa_bm* bm, int64_t seq_id, int32_t token, int64_t* slot, int64_t* cow_src,
+                       int64_t* cow_dst);
+pa_status pa_bm_free(pa_bm* bm, int64_t seq_id);
+int32_t pa_bm_block_table(const pa_bm* bm, int64_t seq_id, int32_t* out, int32_t capacity);
+int64_t pa_bm_context_len(const pa_bm* bm, int64_t seq_id);
+int64_t pa_bm_num_free(const pa_bm* bm);
+void pa_bm_stats(const pa_bm* bm, int64_t* out);
 
 #ifdef __cplusplus
 }

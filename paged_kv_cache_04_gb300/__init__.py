@@ -71,6 +71,24 @@ def library():
     lib.pa_status_string.argtypes = [I]
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_version.argtypes = []
+    lib.pa_bm_create.argtypes = [I64, I, I]
+    lib.pa_bm_create.restype = P
+    lib.pa_bm_destroy.argtypes = [P]
+    lib.pa_bm_destroy.restype = None
+    lib.pa_bm_add_sequence.argtypes = [P, I64, P, ctypes.c_int32, P]
+    lib.pa_bm_fork.argtypes = [P, I64, I64]
+    lib.pa_bm_append.argtypes = [P, I64, ctypes.c_int32, P, P, P]
+    lib.pa_bm_free.argtypes = [P, I64]
+    for f in ("pa_bm_add_sequence", "pa_bm_fork", "pa_bm_append", "pa_bm_free"):
+        getattr(lib, f).restype = I
+    lib.pa_bm_block_table.argtypes = [P, I64, P, ctypes.c_int32]
+    lib.pa_bm_block_table.restype = ctypes.c_int32
+    lib.pa_bm_context_len.argtypes = [P, I64]
+    lib.pa_bm_context_len.restype = I64
+    lib.pa_bm_num_free.argtypes = [P]
+    lib.pa_bm_num_free.restype = I64
+    lib.pa_bm_stats.argtypes = [P, P]
+    lib.pa_bm_stats.restype = None
     for f in ("pa_reshape_and_cache", "pa_decode", "pa_decode_split", "pa_decode_split_static",
               "pa_copy_blocks", "pa_swap_blocks", "pa_reshape_and_cache_fp8", "pa_decode_fp8",
               "pa_decode_split_fp8", "pa_get_error", "pa_version"):

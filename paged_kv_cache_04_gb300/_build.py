@@ -18,7 +18,7 @@ LIB = os.path.join(HERE, "libpa.so")
 OBJDIR = os.path.join(HERE, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["pa_api.cu", "pa_cache.cu", "pa_decode_bf16.cu", "pa_decode_f16.cu", "pa_decode_f32.cu",
-           "pa_decode_fp8.cu", "pa_static.cu"]
+           "pa_decode_fp8.cu", "pa_static.cu", "pa_block_manager.cpp"]
 
 
 def nvcc() -> str:
@@ -47,7 +47,7 @@ def build(verbose_ptxas: bool = False, jobs: int | None = None) -> str:
     flags = _flags(verbose_ptxas)
 
     def compile_one(src):
-        obj = os.path.join(OBJDIR, src.replace(".cu", ".o"))
+        obj = os.path.join(OBJDIR, src.rsplit(".", 1)[0] + ".o")
         cmd = [exe, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:

@@ -143,3 +143,75 @@ class BlockManager:
 
     def context_len(self, seq_id: int) -> int:
         return self.seqs[seq_id].num_tokens
+
+
+class NativeBlockManager:
+    """The library's C++ block manager (``pa_bm_*`` in ``include/pa.h``), with prefix caching.
+
+    Same operations as :class:`BlockManager` plus token-aware prefill that
+    reuses cached block-aligned prefixes (chain hash of parent hash and block
+    tokens) and LRU eviction of released cached blocks.
+    """
+
+    def __init__(self, num_blocks: int, block_size: int, prefix_caching: bool = True):
+        import ctypes
+        from . import library
+        self._ct = ctypes
+        self._lib = library()
+        self._h = self._lib.pa_bm_create(int(num_blocks), int(block_size), 1 if prefix_caching else 0)
+        if not self._h:
+            raise ValueError("bad block manager sizes")
+        self.num_blocks, self.block_size = num_blocks, block_size
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            self._lib.pa_bm_destroy(h)
+            self._h = None
+
+    def _check(self, st, what):
+        if st == 5:
+            raise OutOfBlocks(what)
+        if st != 0:
+            raise ValueError(f"{what}: status {st}")
+
+    def add_sequence(self, seq_id: int, tokens) -> int:
+        """Prefill ``tokens``; returns how many leading tokens came from the prefix cache."""
+        ct = self._ct
+        toks = (ct.c_int32 * len(tokens))(*[int(t) for t in tokens])
+        cached = ct.c_int32(0)
+        self._check(self._lib.pa_bm_add_sequence(self._h, int(seq_id), toks, len(tokens), ct.byref(cached)),
+                    "add_sequence")
+        return int(cached.value)
+
+    def fork(self, parent_id: int, child_id: int) -> None:
+        self._check(self._lib.pa_bm_fork(self._h, int(parent_id), int(child_id)), "fork")
+
+    def append_slot(self, seq_id: int, token: int = 0):
+        ct = self._ct
+        slot, src, dst = ct.c_int64(), ct.c_int64(), ct.c_int64()
+        self._check(self._lib.pa_bm_append(self._h, int(seq_id), int(token), ct.byref(slot), ct.byref(src),
+                                           ct.byref(dst)), "append")
+        return int(slot.value), (None if src.value < 0 else (int(src.value), int(dst.value)))
+
+    def free_sequence(self, seq_id: int) -> None:
+        self._check(self._lib.pa_bm_free(self._h, int(seq_id)), "free")
+
+    def block_table(self, seq_id: int) -> list:
+        n = self._lib.pa_bm_block_table(self._h, int(seq_id), None, 0)
+        if n < 0:
+            raise KeyError(seq_id)
+        buf = (self._ct.c_int32 * max(1, n))()
+        self._lib.pa_bm_block_table(self._h, int(seq_id), buf, n)
+        return list(buf[:n])
+
+    def context_len(self, seq_id: int) -> int:
+        return int(self._lib.pa_bm_context_len(self._h, int(seq_id)))
+
+    def num_free(self) -> int:
+        return int(self._lib.pa_bm_num_free(self._h))
+
+    def stats(self) -> dict:
+        out = (self._ct.c_int64 * 6)()
+        self._lib.pa_bm_stats(self._h, out)
+        return dict(zip(("queries", "hits", "evictions", "copies", "evictable", "cached"), list(out)))

@@ -350,6 +350,7 @@ extern "C" const char* pa_status_string(pa_status status) {
     case PA_ERR_UNSUPPORTED: return "unsupported configuration";
     case PA_ERR_OUT_OF_RANGE: return "device-side value out of range";
     case PA_ERR_CUDA: return "CUDA error";
+    case PA_ERR_NO_BLOCKS: return "no free block";
   }
   return "unknown status";
 }
