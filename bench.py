@@ -56,7 +56,7 @@ def parse():
                     help="the same 64-sequence case with an E4M3 cache (for ncu)")
     ap.add_argument("--workload", default="llama8b",
                     choices=["llama8b", "tiny", "opt13b", "shared", "shared_cow", "long70b_b16", "long70b_b32",
-                             "llama8b_fp8", "long70b_b16_fp8"],
+                             "llama8b_fp8", "long70b_b16_fp8", "shared_cascade", "shared_cow_cascade"],
                     help="the other workload shapes give a device-timed line of their own (no e2e / CPU legs)")
     return ap.parse_args()
 
@@ -452,7 +452,7 @@ def run_workload(args):
     elif name == "opt13b":
         wl = workloads.opt13b(device=dev)
     elif name.startswith("shared"):
-        wl = workloads.shared_prefix(device=dev, cow=name == "shared_cow")
+        wl = workloads.shared_prefix(device=dev, cow=name.startswith("shared_cow"))
         # set-up: the CoW copies and every appended token, once; a timed step then
         # repeats the copies and writes each sample's newest token before decoding
         if wl.copy_pairs.numel():
@@ -471,10 +471,20 @@ def run_workload(args):
             wl = workloads.to_fp8(wl)
         split, T = True, 512
     fp8 = name.endswith("fp8")
+    cascade = name.endswith("cascade")
     ks, vs = wl.meta.get("k_scale", 1.0), wl.meta.get("v_scale", 1.0)
+    if cascade:
+        gs = torch.tensor(wl.meta["group_starts"], dtype=torch.int32, device=dev)
+        pl = torch.tensor(wl.meta["prefix_lens"], dtype=torch.int32, device=dev)
+        gmax = max(b - a for a, b in zip(wl.meta["group_starts"][:-1], wl.meta["group_starts"][1:]))
+        pmax = max(wl.meta["prefix_lens"])
+        T = 512
     out = torch.empty_like(wl.q)
     ws = None
     max_ctx = wl.max_context  # read once: it synchronises the device
+    if cascade:
+        ws = torch.empty(pa.pa_decode_cascade_workspace_bytes(wl.S, wl.H, wl.d, pmax, max_ctx, T),
+                         dtype=torch.uint8, device=dev)
     if split:
         ws = torch.empty(pa.pa_decode_split_workspace_bytes(wl.S, wl.H, wl.d, max_ctx, T),
                          dtype=torch.uint8, device=dev)
@@ -497,7 +507,10 @@ def run_workload(args):
             pa.pa_copy_blocks([wl.k_cache], [wl.v_cache], pairs)
         if wl.slot_mapping is not None:
             pa.pa_reshape_and_cache(wl.new_key, wl.new_value, wl.k_cache, wl.v_cache, wl.slot_mapping)
-        if split:
+        if cascade:
+            pa.pa_decode_cascade(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale,
+                                 gs, pl, gmax, pmax, max_ctx, T, ws)
+        elif split:
             pa.pa_decode_split(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale,
                                max_ctx, T, ws)
         else:

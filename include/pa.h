@@ -190,6 +190,47 @@ pa_status pa_decode_split_static(void* out, const void* q, const void* k_cache, 
                                  cudaStream_t stream);
 
 /*
+ * Decode attention for batches whose sequences share prompt prefixes (parallel
+ * samples of one prompt, a common system prompt): sequences
+ * [group_starts[g], group_starts[g+1]) share their first prefix_lens[g] tokens
+ * through the same physical blocks (CS349E Lecture 7 notes §5.1 and §5.3).
+ * The result equals pa_decode's; attention over a context is the merge of
+ * attention over any split of it (CMU 15-779 Lecture 16 notes §3.3), so it is
+ * computed in three launches:
+ *   1. prefix pass: each (group, kv head, partition of the prefix) attends all
+ *      of the group's query rows at once, so a prefix block is read once per
+ *      group instead of once per member;
+ *   2. each sequence's own tokens [prefix, context) as one partial per
+ *      (sequence, head), scheduled like pa_decode (longest first);
+ *   3. the log-sum-exp reduce of both.
+ * Arguments as pa_decode_split, plus (device int32 arrays):
+ *   group_starts  [num_groups + 1], group_starts[0] = 0, non-decreasing,
+ *                 group_starts[num_groups] = num_seqs (every sequence in one group)
+ *   prefix_lens   [num_groups]; rounded down to whole blocks; must not exceed any
+ *                 member's context length (violations are clamped and recorded)
+ *   max_group_size     host int >= every group's size; max_group_size *
+ *                      (num_heads / num_kv_heads) <= 64
+ *   max_prefix_len     host int >= every prefix_lens[g]
+ *   max_context_len    host int >= every context length
+ * The tokens of a group's prefix are read through the block table of its
+ * first member. 16-bit caches only; num_seqs and num_groups at most 2048.
+ * Workspace: pa_decode_cascade_workspace_bytes(...) bytes, laid out as for
+ * pa_decode_split with P = ceil(max_prefix_len / T) + 1 slots: the prefix
+ * partitions, then one slot for each sequence's own tokens (max_context_len is
+ * accepted for symmetry with pa_decode_split and bounds nothing).
+ */
+size_t pa_decode_cascade_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_prefix_len,
+                                         int max_context_len, int partition_tokens);
+
+pa_status pa_decode_cascade(void* out, const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                            int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                            int64_t num_blocks, float scale, pa_dtype dtype, pa_dtype out_dtype,
+                            const int32_t* group_starts, const int32_t* prefix_lens, int num_groups,
+                            int max_group_size, int max_prefix_len, int max_context_len, int partition_tokens,
+                            void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Batched copy-on-write block copies (CS349E Lecture 7 notes §5.1 and §4.3: a
  * sample about to write into a shared block first gets its own copy; all copies
  * pending for a step go in one launch). For every pair p and every layer l:

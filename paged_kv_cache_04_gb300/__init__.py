@@ -23,7 +23,8 @@ import os
 __all__ = [
     "PAError", "library", "library_path", "pa_reshape_and_cache", "pa_decode", "pa_decode_split",
     "pa_decode_split_workspace_bytes", "pa_decode_split_static", "pa_copy_blocks", "pa_swap_blocks",
-    "pa_reshape_and_cache_fp8", "pa_decode_fp8", "pa_decode_split_fp8", "pa_get_error",
+    "pa_reshape_and_cache_fp8", "pa_decode_fp8", "pa_decode_split_fp8", "pa_decode_cascade",
+    "pa_decode_cascade_workspace_bytes", "pa_get_error",
     "pa_version", "PA_STATIC_SCRATCH_BYTES",
     "PA_DEVERR_BLOCK_ID", "PA_DEVERR_SLOT", "PA_DEVERR_CONTEXT", "PA_DEVERR_PAIR", "PA_DEVERR_TIMEOUT",
 ]
@@ -67,6 +68,10 @@ def library():
     lib.pa_reshape_and_cache_fp8.argtypes = [P, P, P, P, P, I, I, I, I, I64, I, F, F, P]
     lib.pa_decode_fp8.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I64, F, F, F, I, I, P]
     lib.pa_decode_split_fp8.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I64, F, F, F, I, I, I, I, P, SZ, P]
+    lib.pa_decode_cascade_workspace_bytes.argtypes = [I, I, I, I, I, I]
+    lib.pa_decode_cascade_workspace_bytes.restype = SZ
+    lib.pa_decode_cascade.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I64, F, I, I, P, P, I, I, I, I, I, P, SZ,
+                                      P]
     lib.pa_get_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), P]
     lib.pa_status_string.argtypes = [I]
     lib.pa_status_string.restype = ctypes.c_char_p
@@ -91,7 +96,7 @@ def library():
     lib.pa_bm_stats.restype = None
     for f in ("pa_reshape_and_cache", "pa_decode", "pa_decode_split", "pa_decode_split_static",
               "pa_copy_blocks", "pa_swap_blocks", "pa_reshape_and_cache_fp8", "pa_decode_fp8",
-              "pa_decode_split_fp8", "pa_get_error", "pa_version"):
+              "pa_decode_split_fp8", "pa_decode_cascade", "pa_get_error", "pa_version"):
         getattr(lib, f).restype = I
     _lib = lib
     return lib
@@ -213,6 +218,35 @@ def pa_decode_split_static(out, q, k_cache, v_cache, block_tables, context_lens,
                                                _ptr(block_tables), maxb, _ptr(context_lens), S, H, G, d, B,
                                                nb, float(scale), _dtype_code(q), _dtype_code(out),
                                                int(max_context_len), int(partition_tokens), _stream(stream)))
+
+
+def pa_decode_cascade_workspace_bytes(num_seqs, num_heads, head_dim, max_prefix_len, max_context_len,
+                                      partition_tokens):
+    return int(library().pa_decode_cascade_workspace_bytes(num_seqs, num_heads, head_dim, max_prefix_len,
+                                                           max_context_len, partition_tokens))
+
+
+def pa_decode_cascade(out, q, k_cache, v_cache, block_tables, context_lens, scale, group_starts, prefix_lens,
+                      max_group_size, max_prefix_len, max_context_len, partition_tokens, workspace, stream=None):
+    """Decode for batches whose sequences share prompt prefixes (same result as ``pa_decode``).
+
+    ``group_starts`` (int32 [G+1]) and ``prefix_lens`` (int32 [G]) are CUDA
+    tensors: sequences ``group_starts[g] .. group_starts[g+1]-1`` share their
+    first ``prefix_lens[g]`` tokens through the same physical blocks.
+    """
+    f = "pa_decode_cascade"
+    torch = _torch()
+    S, H, G, d, B, nb, maxb = _decode_args(f, out, q, k_cache, v_cache, block_tables, context_lens)
+    _dev(f, workspace, group_starts, prefix_lens)
+    _need(group_starts.dtype == torch.int32 and prefix_lens.dtype == torch.int32, f, "group arrays must be int32")
+    ng = int(prefix_lens.numel())
+    _need(group_starts.numel() == ng + 1, f, "group_starts must have num_groups + 1 entries")
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(f, library().pa_decode_cascade(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                          maxb, _ptr(context_lens), S, H, G, d, B, nb, float(scale), _dtype_code(q),
+                                          _dtype_code(out), _ptr(group_starts), _ptr(prefix_lens), ng,
+                                          int(max_group_size), int(max_prefix_len), int(max_context_len),
+                                          int(partition_tokens), _ptr(workspace), nbytes, _stream(stream)))
 
 
 def pa_copy_blocks(k_caches, v_caches, block_pairs, stream=None):

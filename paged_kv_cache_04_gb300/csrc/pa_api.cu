@@ -7,7 +7,7 @@
 #include <cstdint>
 #include <mutex>
 
-#include "pa_decode.cuh"
+#include "pa_cascade.cuh"
 #include "pa_internal.h"
 
 namespace pa {
@@ -101,27 +101,34 @@ pa_status check_decode(const DecodeArgs& a) {
   return PA_OK;
 }
 
+template <typename DT, typename QT, typename OT, int D, int PATH>
+pa_status dispatch_mode(const CUtensorMap& km, const CUtensorMap& vm, const DecodeParams& p, int sms,
+                        long long items, int mode, cudaStream_t st) {
+  if (mode == kModeSplit) return launch_decode<DT, QT, float, D, PATH, kModeSplit>(km, vm, p, sms, items, st);
+  if (mode == kModeSuffix) {
+    if constexpr (sizeof(DT) == 2)  // the shared-prefix decode serves 16-bit caches
+      return launch_decode<DT, QT, float, D, PATH, kModeSuffix>(km, vm, p, sms, items, st);
+    return PA_ERR_UNSUPPORTED;
+  }
+  return launch_decode<DT, QT, OT, D, PATH, kModePlain>(km, vm, p, sms, items, st);
+}
+
 template <typename DT, typename QT, typename OT, int D>
 pa_status dispatch_path(const CUtensorMap& km, const CUtensorMap& vm, const DecodeParams& p, int sms,
-                        long long items, bool split, cudaStream_t st) {
+                        long long items, int mode, cudaStream_t st) {
   // group >= 4 on 16-bit or FP8 data: tensor cores; MHA: vector path with q in registers
   if constexpr (sizeof(DT) <= 2) {
-    if (p.group >= 4)
-      return split ? launch_decode<DT, QT, float, D, kPathMma, true>(km, vm, p, sms, items, st)
-                   : launch_decode<DT, QT, OT, D, kPathMma, false>(km, vm, p, sms, items, st);
+    if (p.group >= 4) return dispatch_mode<DT, QT, OT, D, kPathMma>(km, vm, p, sms, items, mode, st);
   }
-  if (p.group == 1)
-    return split ? launch_decode<DT, QT, float, D, kPathVecMha, true>(km, vm, p, sms, items, st)
-                 : launch_decode<DT, QT, OT, D, kPathVecMha, false>(km, vm, p, sms, items, st);
-  return split ? launch_decode<DT, QT, float, D, kPathVec, true>(km, vm, p, sms, items, st)
-               : launch_decode<DT, QT, OT, D, kPathVec, false>(km, vm, p, sms, items, st);
+  if (p.group == 1) return dispatch_mode<DT, QT, OT, D, kPathVecMha>(km, vm, p, sms, items, mode, st);
+  return dispatch_mode<DT, QT, OT, D, kPathVec>(km, vm, p, sms, items, mode, st);
 }
 
 template <typename DT, typename OT>
 pa_status dispatch_shape(const CUtensorMap& km, const CUtensorMap& vm, const DecodeParams& p, int D, int sms,
-                         long long items, bool split, cudaStream_t st) {
-  if (D == 64) return dispatch_path<DT, DT, OT, 64>(km, vm, p, sms, items, split, st);
-  if (D == 128) return dispatch_path<DT, DT, OT, 128>(km, vm, p, sms, items, split, st);
+                         long long items, int mode, cudaStream_t st) {
+  if (D == 64) return dispatch_path<DT, DT, OT, 64>(km, vm, p, sms, items, mode, st);
+  if (D == 128) return dispatch_path<DT, DT, OT, 128>(km, vm, p, sms, items, mode, st);
   return PA_ERR_UNSUPPORTED;
 }
 
@@ -130,8 +137,17 @@ pa_status dispatch_reduce(const DecodeParams& p, int D, cudaStream_t st) {
   return D == 64 ? launch_lse_reduce<OT, 64>(p, st) : launch_lse_reduce<OT, 128>(p, st);
 }
 
+// Shared-prefix groups for pa_decode_cascade (all null / zero otherwise).
+struct CascadeArgs {
+  const int32_t* group_starts = nullptr;
+  const int32_t* prefix_lens = nullptr;
+  int num_groups = 0;
+  int prefix_slots = 0;  // workspace slots reserved for prefix partitions
+  int nt = 1;            // n-tiles of 8 query rows per consumer warp in the prefix pass
+};
+
 pa_status run_decode(const DecodeArgs& a, bool split, int partition, int max_partitions, void* ws,
-                     cudaStream_t st) {
+                     cudaStream_t st, const CascadeArgs& c = CascadeArgs()) {
   unsigned* err = nullptr;
   int sms = 0;
   pa_status s = device_state(&err, &sms);
@@ -166,29 +182,52 @@ pa_status run_decode(const DecodeArgs& a, bool split, int partition, int max_par
     p.ws_o = static_cast<float*>(ws);
     p.ws_m = reinterpret_cast<float*>(static_cast<char*>(ws) + align256(o_bytes));
     p.ws_l = reinterpret_cast<float*>(static_cast<char*>(ws) + align256(o_bytes) + align256(m_bytes));
-    items *= max_partitions;
+    if (!c.group_starts) items *= max_partitions;  // the suffix pass has one item per (sequence, kv head)
+  }
+  const int mode = !split ? kModePlain : (c.group_starts ? kModeSuffix : kModeSplit);
+  if (c.group_starts) {
+    p.group_starts = c.group_starts;
+    p.prefix_lens = c.prefix_lens;
+    p.num_groups = c.num_groups;
+    p.suffix_slot = c.prefix_slots;
+    p.suffix_single = 1;
+    if (c.prefix_slots > 0) {  // prefix pass: every group's query rows over its shared blocks
+      const long long pitems = (long long)c.num_groups * a.G * c.prefix_slots;
+      const bool bf = a.dt == PA_BF16;
+      if (a.D == 128)
+        s = c.nt == 1 ? (bf ? launch_cascade_prefix<__nv_bfloat16, 128, 1>(km, vm, p, sms, pitems, st)
+                            : launch_cascade_prefix<__half, 128, 1>(km, vm, p, sms, pitems, st))
+                      : (bf ? launch_cascade_prefix<__nv_bfloat16, 128, 2>(km, vm, p, sms, pitems, st)
+                            : launch_cascade_prefix<__half, 128, 2>(km, vm, p, sms, pitems, st));
+      else
+        s = c.nt == 1 ? (bf ? launch_cascade_prefix<__nv_bfloat16, 64, 1>(km, vm, p, sms, pitems, st)
+                            : launch_cascade_prefix<__half, 64, 1>(km, vm, p, sms, pitems, st))
+                      : (bf ? launch_cascade_prefix<__nv_bfloat16, 64, 2>(km, vm, p, sms, pitems, st)
+                            : launch_cascade_prefix<__half, 64, 2>(km, vm, p, sms, pitems, st));
+      if (s != PA_OK) return s;
+    }
   }
   switch (a.dt) {
     case PA_FP8_E4M3:
       if (a.D != 128) return PA_ERR_UNSUPPORTED;
       if (a.qdt == PA_BF16)
         s = a.odt == PA_F32
-                ? dispatch_path<fp8e4m3, __nv_bfloat16, float, 128>(km, vm, p, sms, items, split, st)
-                : dispatch_path<fp8e4m3, __nv_bfloat16, __nv_bfloat16, 128>(km, vm, p, sms, items, split, st);
+                ? dispatch_path<fp8e4m3, __nv_bfloat16, float, 128>(km, vm, p, sms, items, mode, st)
+                : dispatch_path<fp8e4m3, __nv_bfloat16, __nv_bfloat16, 128>(km, vm, p, sms, items, mode, st);
       else
-        s = a.odt == PA_F32 ? dispatch_path<fp8e4m3, __half, float, 128>(km, vm, p, sms, items, split, st)
-                            : dispatch_path<fp8e4m3, __half, __half, 128>(km, vm, p, sms, items, split, st);
+        s = a.odt == PA_F32 ? dispatch_path<fp8e4m3, __half, float, 128>(km, vm, p, sms, items, mode, st)
+                            : dispatch_path<fp8e4m3, __half, __half, 128>(km, vm, p, sms, items, mode, st);
       break;
     case PA_BF16:
-      s = a.odt == PA_F32 ? dispatch_shape<__nv_bfloat16, float>(km, vm, p, a.D, sms, items, split, st)
-                          : dispatch_shape<__nv_bfloat16, __nv_bfloat16>(km, vm, p, a.D, sms, items, split, st);
+      s = a.odt == PA_F32 ? dispatch_shape<__nv_bfloat16, float>(km, vm, p, a.D, sms, items, mode, st)
+                          : dispatch_shape<__nv_bfloat16, __nv_bfloat16>(km, vm, p, a.D, sms, items, mode, st);
       break;
     case PA_F16:
-      s = a.odt == PA_F32 ? dispatch_shape<__half, float>(km, vm, p, a.D, sms, items, split, st)
-                          : dispatch_shape<__half, __half>(km, vm, p, a.D, sms, items, split, st);
+      s = a.odt == PA_F32 ? dispatch_shape<__half, float>(km, vm, p, a.D, sms, items, mode, st)
+                          : dispatch_shape<__half, __half>(km, vm, p, a.D, sms, items, mode, st);
       break;
     default:
-      s = dispatch_shape<float, float>(km, vm, p, a.D, sms, items, split, st);
+      s = dispatch_shape<float, float>(km, vm, p, a.D, sms, items, mode, st);
   }
   if (s != PA_OK || !split) return s;
   switch (a.odt) {
@@ -326,6 +365,55 @@ extern "C" pa_status pa_decode_split_fp8(void* out, const void* q, const void* k
   const long long P = std::max(1LL, ((long long)max_context_len + partition_tokens - 1) / partition_tokens);
   if ((long long)num_seqs * num_kv_heads * P > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
   return run_decode(a, true, partition_tokens, (int)P, workspace, stream);
+}
+
+extern "C" size_t pa_decode_cascade_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_prefix_len,
+                                                    int max_context_len, int partition_tokens) {
+  if (num_seqs < 0 || num_heads <= 0 || head_dim <= 0 || max_prefix_len < 0 || max_context_len < 0 ||
+      partition_tokens <= 0)
+    return 0;
+  const long long P = ((long long)max_prefix_len + partition_tokens - 1) / partition_tokens + 1;
+  const size_t rows = (size_t)num_seqs * num_heads * P;
+  return pa::align256(rows * head_dim * 4) + 2 * pa::align256(rows * 4);
+}
+
+extern "C" pa_status pa_decode_cascade(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                       const int32_t* block_tables, int max_blocks_per_seq,
+                                       const int32_t* context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                                       int head_dim, int block_size, int64_t num_blocks, float scale,
+                                       pa_dtype dtype, pa_dtype out_dtype, const int32_t* group_starts,
+                                       const int32_t* prefix_lens, int num_groups, int max_group_size,
+                                       int max_prefix_len, int max_context_len, int partition_tokens,
+                                       void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  using namespace pa;
+  const DecodeArgs a{out,      q,         k_cache,      v_cache,  block_tables, max_blocks_per_seq,
+                     context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                     (long long)num_blocks, scale, dtype, out_dtype};
+  pa_status s = check_decode(a);
+  if (s != PA_OK) return s;
+  if (max_context_len < 0 || max_prefix_len < 0 || partition_tokens <= 0 || partition_tokens % block_size ||
+      num_groups <= 0 || max_group_size <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PA_OK;
+  if (!group_starts || !prefix_lens || (reinterpret_cast<uintptr_t>(group_starts) & 3u) ||
+      (reinterpret_cast<uintptr_t>(prefix_lens) & 3u))
+    return PA_ERR_INVALID_ARG;
+  if (dtype != PA_BF16 && dtype != PA_F16) return PA_ERR_UNSUPPORTED;
+  if (num_seqs > kSplitMaxSeqs || num_groups > kSplitMaxSeqs) return PA_ERR_UNSUPPORTED;
+  const long long rows_per_group = (long long)max_group_size * (num_heads / num_kv_heads);
+  if (rows_per_group > 2LL * 8 * kCascadeConsumers) return PA_ERR_UNSUPPORTED;
+  const size_t need = pa_decode_cascade_workspace_bytes(num_seqs, num_heads, head_dim, max_prefix_len,
+                                                        max_context_len, partition_tokens);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < need || need == 0) return PA_ERR_INVALID_ARG;
+  CascadeArgs c;
+  c.group_starts = group_starts;
+  c.prefix_lens = prefix_lens;
+  c.num_groups = num_groups;
+  c.prefix_slots = (max_prefix_len + partition_tokens - 1) / partition_tokens;
+  c.nt = rows_per_group > 8 * kCascadeConsumers ? 2 : 1;
+  const long long P = c.prefix_slots + 1;  // prefix partitions, then one slot for each sequence's own tokens
+  if ((long long)num_seqs * num_kv_heads * P > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+  return run_decode(a, true, partition_tokens, (int)P, workspace, stream, c);
 }
 
 extern "C" pa_status pa_get_error(uint32_t* error_bits, cudaStream_t stream) {

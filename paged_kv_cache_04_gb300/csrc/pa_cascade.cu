@@ -1,0 +1,59 @@
+// Launcher and instantiations of the shared-prefix (cascade) prefix pass.
+#include <mutex>
+
+#include "pa_cascade.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+template <typename DT, int D, int NT>
+pa_status launch_cascade_prefix(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
+                                int num_sms, long long max_items, cudaStream_t stream) {
+  auto kern = cascade_prefix_kernel<DT, D, NT>;
+  const CascadeLayout L = cascade_layout(D, (int)sizeof(DT), p.num_groups);
+  if (L.total > 227u * 1024u) return PA_ERR_UNSUPPORTED;
+  static std::mutex mu;
+  static unsigned set_bytes[64] = {0};
+  static unsigned occ_bytes[64] = {0};
+  static int occ_blocks[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
+  int per_sm = 1;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (set_bytes[dev] < L.total) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total) != cudaSuccess)
+        return PA_ERR_CUDA;
+      set_bytes[dev] = L.total;
+    }
+    if (occ_bytes[dev] != L.total) {
+      int n = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, (kCascadeConsumers + 1) * 32, L.total) !=
+          cudaSuccess)
+        return PA_ERR_CUDA;
+      occ_bytes[dev] = L.total;
+      occ_blocks[dev] = n;
+    }
+    per_sm = occ_blocks[dev];
+  }
+  if (per_sm < 1) return PA_ERR_UNSUPPORTED;
+  long long grid = (long long)num_sms * per_sm;
+  if (max_items < grid) grid = max_items;
+  if (grid <= 0) return PA_OK;
+  kern<<<(unsigned)grid, (kCascadeConsumers + 1) * 32, L.total, stream>>>(kmap, vmap, p);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+#define PA_INSTANTIATE_CASCADE(DT, D, NT)                                                                   \
+  template pa_status launch_cascade_prefix<DT, D, NT>(const CUtensorMap&, const CUtensorMap&, const DecodeParams&, \
+                                                      int, long long, cudaStream_t);
+PA_INSTANTIATE_CASCADE(__nv_bfloat16, 128, 1)
+PA_INSTANTIATE_CASCADE(__nv_bfloat16, 128, 2)
+PA_INSTANTIATE_CASCADE(__nv_bfloat16, 64, 1)
+PA_INSTANTIATE_CASCADE(__nv_bfloat16, 64, 2)
+PA_INSTANTIATE_CASCADE(__half, 128, 1)
+PA_INSTANTIATE_CASCADE(__half, 128, 2)
+PA_INSTANTIATE_CASCADE(__half, 64, 1)
+PA_INSTANTIATE_CASCADE(__half, 64, 2)
+
+}  // namespace pa

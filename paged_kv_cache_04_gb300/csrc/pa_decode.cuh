@@ -54,6 +54,12 @@ constexpr int kPathVec = 0;     // lanes split head_dim, FFMA; any group, q stag
 constexpr int kPathVecMha = 1;  // the same for group 1 (MHA), q held in registers
 constexpr int kPathMma = 2;     // group >= 4 on 16-bit data: mma.sync m16n8k16
 
+// What a launch writes.
+constexpr int kModePlain = 0;   // the attention output
+constexpr int kModeSplit = 1;   // per-partition partials; each warp owns whole partitions
+constexpr int kModeSuffix = 2;  // one partial per (sequence, head) over its own tokens after the
+                                // shared prefix (cascade decode), at workspace slot suffix_slot
+
 struct DecodeParams {
   void* out;                    // [S][H][D] out dtype (plain mode)
   const void* q;                // [S][H][D]
@@ -71,6 +77,15 @@ struct DecodeParams {
   float* ws_m;                  // [S][H][P]  (max score, base-2 units)
   float* ws_l;                  // [S][H][P]
   float v_scale;                // FP8 caches: V scale applied to the output (1 otherwise)
+  // Shared-prefix (cascade) decode: sequences [group_starts[g], group_starts[g+1])
+  // share their first prefix_lens[g] tokens (rounded down to whole blocks). The
+  // split pass then covers only each sequence's own tokens, writing its
+  // partitions from slot suffix_slot on; null group_starts: no shared prefixes.
+  const int32_t* group_starts;  // [num_groups + 1]
+  const int32_t* prefix_lens;   // [num_groups]
+  int num_groups;
+  int suffix_slot;
+  int suffix_single;            // 1: one suffix partial per row (kModeSuffix)
   unsigned* err;
 };
 
@@ -137,7 +152,34 @@ __device__ __forceinline__ int clamp_ctx(const DecodeParams& p, int s, bool spli
   return c;
 }
 
-template <bool SPLIT, int W>
+// Group of sequence s (largest g with group_starts[g] <= s).
+__device__ __forceinline__ int group_of(const DecodeParams& p, int s) {
+  int lo = 0, hi = p.num_groups - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(p.group_starts + mid) <= s) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Shared prefix length of group g in whole blocks.
+__device__ __forceinline__ int group_prefix(const DecodeParams& p, int g) {
+  const int pl = max(0, __ldg(p.prefix_lens + g));
+  return pl - (pl & (p.block_size - 1));
+}
+
+// First token of sequence s that is its own (after its group's shared prefix).
+__device__ __forceinline__ int seq_start(const DecodeParams& p, int s, int ctx) {
+  if (p.group_starts == nullptr) return 0;
+  const int st = group_prefix(p, group_of(p, s));
+  if (st > ctx) {
+    atomicOr(p.err, kErrContext);
+    return ctx;
+  }
+  return st;
+}
+
+template <int MODE, int W>
 struct Schedule {
   const uint16_t* order;  // plain mode: sequences longest-first (nullptr: batch order)
   const int* pstart;      // split mode: first item of each sequence, [S + 1]
@@ -151,7 +193,7 @@ struct Schedule {
     const int ii = (int)i;
     it.kv = ii % p.G;
     const int qi = ii / p.G;
-    if (SPLIT) {
+    if (MODE == kModeSplit) {
       int lo = 0, hi = p.S - 1;  // last s with pstart[s] <= qi
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -159,11 +201,12 @@ struct Schedule {
       }
       it.s = lo;
       const int c = clamp_ctx(p, lo, true);
-      const int nparts = (c + p.partition - 1) / p.partition;
+      const int st = seq_start(p, lo, c);
+      const int nparts = (c - st + p.partition - 1) / p.partition;
       const int part = (qi - pstart[lo]) * W + warp;
       if (part < nparts) {
-        it.part = part;
-        it.t0 = part * p.partition;
+        it.part = p.suffix_slot + part;  // workspace slot
+        it.t0 = st + part * p.partition;
         it.t1 = min(it.t0 + p.partition, c);
       } else {
         it.part = -1;
@@ -171,9 +214,9 @@ struct Schedule {
       }
     } else {
       it.s = order ? (int)order[qi] : qi;
-      it.part = 0;
-      it.t0 = 0;
       it.t1 = clamp_ctx(p, it.s, false);
+      it.t0 = MODE == kModeSuffix ? seq_start(p, it.s, it.t1) : 0;
+      it.part = MODE == kModeSuffix ? p.suffix_slot : 0;
     }
     return true;
   }
@@ -181,12 +224,14 @@ struct Schedule {
 
 // DT: cache element type (float, __half, __nv_bfloat16 or fp8e4m3); QT: query
 // type (DT, or a 16-bit type over an FP8 cache); OT: output type.
-template <typename DT, typename QT, typename OT, int D, int PATH, bool SPLIT>
+template <typename DT, typename QT, typename OT, int D, int PATH, int MODE>
 __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         const DecodeParams p) {
   using Cfg = StageCfg<DT, D, PATH>;
   constexpr bool MMA = PATH == kPathMma;
+  constexpr bool SPLIT = MODE == kModeSplit;
+  constexpr bool SUFFIX = MODE == kModeSuffix;
   constexpr bool F8 = std::is_same<DT, fp8e4m3>::value;
   using MT = typename std::conditional<F8, __half, DT>::type;  // tensor-core operand type
   static_assert(!F8 || D % 64 == 0, "FP8 caches need head_dim a multiple of 64");
@@ -223,7 +268,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
   }
 
   // ---- schedule tables (the stage buffers are free until the first copy) ------
-  Schedule<SPLIT, W> sch;
+  Schedule<MODE, W> sch;
   sch.order = nullptr;
   sch.pstart = nullptr;
   if (SPLIT) {
@@ -234,7 +279,8 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
       const int b = lane * per, e = min(p.S, b + per);
       auto items_of = [&](int s) {
         const int c = clamp_ctx(p, s, true);
-        return ((c + p.partition - 1) / p.partition + W - 1) / W;
+        const int st = seq_start(p, s, c);
+        return ((c - st + p.partition - 1) / p.partition + W - 1) / W;
       };
       int local = 0;
       for (int s = b; s < e; ++s) local += items_of(s);
@@ -263,7 +309,10 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
       for (int b = tid; b < kNumBuckets; b += nthreads) base[b] = 0;
       __syncthreads();
       auto bucket = [&](int s) {  // ascending bucket index = descending length
-        const int key = min(clamp_ctx(p, s, false) >> kLenBucketShift, kNumBuckets - 1);
+        // the suffix pass sorts by the sequence's own tokens, which are short: finer buckets
+        const int c = clamp_ctx(p, s, false);
+        const int key = SUFFIX ? min((c - seq_start(p, s, c)) >> 4, kNumBuckets - 1)
+                               : min(c >> kLenBucketShift, kNumBuckets - 1);
         return kNumBuckets - 1 - key;
       };
       for (int s = tid; s < p.S; s += nthreads) atomicAdd(&base[bucket(s)], 1);
@@ -416,8 +465,17 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
           O = fmaf(mrg_o[(w * p.group + h) * D + i], f, O);
         }
       }
-      reinterpret_cast<OT*>(p.out)[((long long)x.s * p.H + hq0 + h) * D + i] =
-          from_f32<OT>(Lsum > 0.f ? O * p.v_scale / Lsum : 0.f);
+      if (SUFFIX) {
+        const long long row = ((long long)x.s * p.H + hq0 + h) * p.max_partitions + x.part;
+        p.ws_o[row * D + i] = Lsum > 0.f ? O * p.v_scale / Lsum : 0.f;
+        if (i == 0) {
+          p.ws_m[row] = M;
+          p.ws_l[row] = Lsum;
+        }
+      } else {
+        reinterpret_cast<OT*>(p.out)[((long long)x.s * p.H + hq0 + h) * D + i] =
+            from_f32<OT>(Lsum > 0.f ? O * p.v_scale / Lsum : 0.f);
+      }
     }
     asm volatile("bar.sync 1, %0;" ::"n"(W * 32) : "memory");
   };
@@ -924,8 +982,15 @@ __global__ void __launch_bounds__(256) lse_reduce_kernel(const DecodeParams p) {
   const int s = row / p.H;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const float NEG_INF = -__int_as_float(0x7f800000);
-  const int c = clamp_ctx(p, s, true);
-  const int P = (c + p.partition - 1) / p.partition;
+  const int c = clamp_ctx(p, s, !p.suffix_single);  // one suffix slot bounds no context length
+  int Pp = 0, st = 0;
+  if (p.group_starts != nullptr) {
+    st = seq_start(p, s, c);
+    Pp = (st + p.partition - 1) / p.partition;
+  }
+  const int Ps = p.suffix_single ? 1 : (c - st + p.partition - 1) / p.partition;
+  const int P = Pp + Ps;  // merged slots: [0, Pp) and [suffix_slot, suffix_slot + Ps)
+  auto slot = [&](int q) { return q < Pp ? q : p.suffix_slot + (q - Pp); };
   const long long base = (long long)row * p.max_partitions;
   __shared__ float sh_w[CHUNK];
   __shared__ float sh_red[NT / 32];
@@ -933,7 +998,7 @@ __global__ void __launch_bounds__(256) lse_reduce_kernel(const DecodeParams p) {
 
   float mx = NEG_INF;
   for (int q = tid; q < P; q += NT) {
-    const float l = __ldg(p.ws_l + base + q), m = __ldg(p.ws_m + base + q);
+    const float l = __ldg(p.ws_l + base + slot(q)), m = __ldg(p.ws_m + base + slot(q));
     if (l > 0.f) mx = fmaxf(mx, m);
   }
 #pragma unroll
@@ -951,19 +1016,19 @@ __global__ void __launch_bounds__(256) lse_reduce_kernel(const DecodeParams p) {
   for (int q0 = 0; q0 < P; q0 += CHUNK) {
     const int n = min(CHUNK, P - q0);
     for (int q = tid; q < n; q += NT) {
-      const float l = __ldg(p.ws_l + base + q0 + q), m = __ldg(p.ws_m + base + q0 + q);
+      const float l = __ldg(p.ws_l + base + slot(q0 + q)), m = __ldg(p.ws_m + base + slot(q0 + q));
       const float w = l > 0.f ? l * exp2f(m - M) : 0.f;
       sh_w[q] = w;
       wsum += w;
     }
     __syncthreads();
-    const float4* src = reinterpret_cast<const float4*>(p.ws_o + (base + q0) * D) + v;
+    const float4* src = reinterpret_cast<const float4*>(p.ws_o + base * D) + v;
     for (int q = pg; q < n; q += PG * BATCH) {
       float4 x[BATCH];
 #pragma unroll
       for (int b = 0; b < BATCH; ++b) {
         const int qq = q + b * PG;
-        x[b] = qq < n ? __ldg(src + (long long)qq * VPR) : make_float4(0.f, 0.f, 0.f, 0.f);
+        x[b] = qq < n ? __ldg(src + (long long)slot(q0 + qq) * VPR) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int b = 0; b < BATCH; ++b) {
@@ -991,6 +1056,51 @@ __global__ void __launch_bounds__(256) lse_reduce_kernel(const DecodeParams p) {
     for (int g = 0; g < PG; ++g) O += reinterpret_cast<const float*>(&sh_acc[g][0])[i];
     reinterpret_cast<OT*>(p.out)[(long long)row * D + i] = from_f32<OT>(W > 0.f ? O / W : 0.f);
   }
+}
+
+// Pass 2 for rows with few partitions (at most 32 slots): one warp per row.
+template <typename OT, int D>
+__global__ void __launch_bounds__(256) lse_reduce_small_kernel(const DecodeParams p) {
+  constexpr int EPL = D / 32;
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= p.S * p.H) return;
+  const int s = row / p.H;
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  const int c = clamp_ctx(p, s, !p.suffix_single);  // one suffix slot bounds no context length
+  int Pp = 0, st = 0;
+  if (p.group_starts != nullptr) {
+    st = seq_start(p, s, c);
+    Pp = (st + p.partition - 1) / p.partition;
+  }
+  const int Ps = p.suffix_single ? 1 : (c - st + p.partition - 1) / p.partition;
+  const int P = min(Pp + Ps, 32);
+  const long long base = (long long)row * p.max_partitions;
+  // lane q holds slot q's (max, sum)
+  const int sl = lane < Pp ? lane : p.suffix_slot + (lane - Pp);
+  const float lq = lane < P ? __ldg(p.ws_l + base + sl) : 0.f;
+  const float mq = lane < P ? __ldg(p.ws_m + base + sl) : NEG_INF;
+  float M = lq > 0.f ? mq : NEG_INF;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float w = lq > 0.f ? lq * exp2f(mq - M) : 0.f;
+  float W = w;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
+  float acc[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+  for (int q = 0; q < P; ++q) {
+    const float wq = __shfl_sync(0xffffffffu, w, q);
+    const int slq = __shfl_sync(0xffffffffu, sl, q);
+    if (wq == 0.f) continue;
+    const float* oq = p.ws_o + (base + slq) * D + lane * EPL;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] = fmaf(wq, __ldg(oq + e), acc[e]);
+  }
+#pragma unroll
+  for (int e = 0; e < EPL; ++e)
+    reinterpret_cast<OT*>(p.out)[(long long)row * D + lane * EPL + e] = from_f32<OT>(W > 0.f ? acc[e] / W : 0.f);
 }
 
 }  // namespace pa

@@ -1,25 +1,31 @@
 // Decode-kernel instantiations for bf16 caches: the three compute paths, head_dim
-// 64/128, output in the cache type or fp32, plain and split mode.
+// 64/128, output in the cache type or fp32, plain, split and shared-prefix suffix mode.
 #include "pa_decode_launch.cuh"
 
 PA_INSTANTIATE_DECODE(__nv_bfloat16, __nv_bfloat16, __nv_bfloat16, 64, pa::kPathVec)
 PA_INSTANTIATE_DECODE(__nv_bfloat16, __nv_bfloat16, float, 64, pa::kPathVec)
 PA_INSTANTIATE_SPLIT(__nv_bfloat16, __nv_bfloat16, 64, pa::kPathVec)
+PA_INSTANTIATE_SUFFIX(__nv_bfloat16, __nv_bfloat16, 64, pa::kPathVec)
 PA_INSTANTIATE_DECODE(__nv_bfloat16, __nv_bfloat16, __nv_bfloat16, 64, pa::kPathVecMha)
 PA_INSTANTIATE_DECODE(__nv_bfloat16, __nv_bfloat16, float, 64, pa::kPathVecMha)
 PA_INSTANTIATE_SPLIT(__nv_bfloat16, __nv_bfloat16, 64, pa::kPathVecMha)
+PA_INSTANTIATE_SUFFIX(__nv_bfloat16, __nv_bfloat16, 64, pa::kPathVecMha)
 PA_INSTANTIATE_DECODE(__nv_bfloat16, __nv_bfloat16, __nv_bfloat16, 64, pa::kPathMma)
 PA_INSTANTIATE_DECODE(__nv_bfloat16, __nv_bfloat16, float, 64, pa::kPathMma)
 PA_INSTANTIATE_SPLIT(__nv_bfloat16, __nv_bfloat16, 64, pa::kPathMma)
+PA_INSTANTIATE_SUFFIX(__nv_bfloat16, __nv_bfloat16, 64, pa::kPathMma)
 PA_INSTANTIATE_DECODE(__nv_bfloat16, __nv_bfloat16, __nv_bfloat16, 128, pa::kPathVec)
 PA_INSTANTIATE_DECODE(__nv_bfloat16, __nv_bfloat16, float, 128, pa::kPathVec)
 PA_INSTANTIATE_SPLIT(__nv_bfloat16, __nv_bfloat16, 128, pa::kPathVec)
+PA_INSTANTIATE_SUFFIX(__nv_bfloat16, __nv_bfloat16, 128, pa::kPathVec)
 PA_INSTANTIATE_DECODE(__nv_bfloat16, __nv_bfloat16, __nv_bfloat16, 128, pa::kPathVecMha)
 PA_INSTANTIATE_DECODE(__nv_bfloat16, __nv_bfloat16, float, 128, pa::kPathVecMha)
 PA_INSTANTIATE_SPLIT(__nv_bfloat16, __nv_bfloat16, 128, pa::kPathVecMha)
+PA_INSTANTIATE_SUFFIX(__nv_bfloat16, __nv_bfloat16, 128, pa::kPathVecMha)
 PA_INSTANTIATE_DECODE(__nv_bfloat16, __nv_bfloat16, __nv_bfloat16, 128, pa::kPathMma)
 PA_INSTANTIATE_DECODE(__nv_bfloat16, __nv_bfloat16, float, 128, pa::kPathMma)
 PA_INSTANTIATE_SPLIT(__nv_bfloat16, __nv_bfloat16, 128, pa::kPathMma)
+PA_INSTANTIATE_SUFFIX(__nv_bfloat16, __nv_bfloat16, 128, pa::kPathMma)
 
 template pa_status pa::launch_lse_reduce<__nv_bfloat16, 64>(const pa::DecodeParams&, cudaStream_t);
 template pa_status pa::launch_lse_reduce<__nv_bfloat16, 128>(const pa::DecodeParams&, cudaStream_t);

@@ -8,12 +8,13 @@
 
 namespace pa {
 
-template <typename DT, typename QT, typename OT, int D, int PATH, bool SPLIT>
+template <typename DT, typename QT, typename OT, int D, int PATH, int MODE>
 pa_status launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                         int num_sms, long long max_items, cudaStream_t stream) {
   using Cfg = StageCfg<DT, D, PATH>;
-  auto kern = paged_decode_kernel<DT, QT, OT, D, PATH, SPLIT>;
-  const SmemLayout L = make_layout(Cfg::W, Cfg::R, D, Cfg::E, (int)sizeof(QT), p.group, PATH, SPLIT, p.S);
+  auto kern = paged_decode_kernel<DT, QT, OT, D, PATH, MODE>;
+  const SmemLayout L =
+      make_layout(Cfg::W, Cfg::R, D, Cfg::E, (int)sizeof(QT), p.group, PATH, MODE == kModeSplit, p.S);
   if (L.total > 227u * 1024u) return PA_ERR_UNSUPPORTED;
 
   // Opt in to the dynamic shared memory once per device, and remember the
@@ -53,7 +54,10 @@ template <typename OT, int D>
 pa_status launch_lse_reduce(const DecodeParams& p, cudaStream_t stream) {
   const long long rows = (long long)p.S * p.H;
   if (rows <= 0) return PA_OK;
-  lse_reduce_kernel<OT, D><<<(unsigned)rows, 256, 0, stream>>>(p);
+  if (p.max_partitions <= 32)
+    lse_reduce_small_kernel<OT, D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p);
+  else
+    lse_reduce_kernel<OT, D><<<(unsigned)rows, 256, 0, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -62,10 +66,11 @@ pa_status launch_lse_reduce(const DecodeParams& p, cudaStream_t stream) {
 // Explicit instantiations for one element type DT (the tensor-core path only
 // exists for 16-bit types).
 #define PA_INSTANTIATE_DECODE(DT, QT, OT, D, PATH)                                                        \
-  template pa_status pa::launch_decode<DT, QT, OT, D, PATH, false>(const CUtensorMap&, const CUtensorMap&, \
-                                                                   const pa::DecodeParams&, int, long long, \
-                                                                   cudaStream_t);
+  template pa_status pa::launch_decode<DT, QT, OT, D, PATH, pa::kModePlain>(                               \
+      const CUtensorMap&, const CUtensorMap&, const pa::DecodeParams&, int, long long, cudaStream_t);
 #define PA_INSTANTIATE_SPLIT(DT, QT, D, PATH)                                                               \
-  template pa_status pa::launch_decode<DT, QT, float, D, PATH, true>(const CUtensorMap&, const CUtensorMap&, \
-                                                                     const pa::DecodeParams&, int, long long, \
-                                                                     cudaStream_t);
+  template pa_status pa::launch_decode<DT, QT, float, D, PATH, pa::kModeSplit>(                            \
+      const CUtensorMap&, const CUtensorMap&, const pa::DecodeParams&, int, long long, cudaStream_t);
+#define PA_INSTANTIATE_SUFFIX(DT, QT, D, PATH)                                                              \
+  template pa_status pa::launch_decode<DT, QT, float, D, PATH, pa::kModeSuffix>(                           \
+      const CUtensorMap&, const CUtensorMap&, const pa::DecodeParams&, int, long long, cudaStream_t);

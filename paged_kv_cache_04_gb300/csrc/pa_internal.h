@@ -16,11 +16,16 @@ pa_status device_state(unsigned** err, int* num_sms);
 
 // Launchers, one per (cache type, query type, output type, head_dim, path,
 // split) combination, instantiated in pa_decode_{f32,f16,bf16,fp8}.cu.
-template <typename DT, typename QT, typename OT, int D, int PATH, bool SPLIT>
+template <typename DT, typename QT, typename OT, int D, int PATH, int MODE>
 pa_status launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                         int num_sms, long long max_items, cudaStream_t stream);
 
 template <typename OT, int D>
 pa_status launch_lse_reduce(const DecodeParams& p, cudaStream_t stream);
+
+// Prefix pass of the shared-prefix decode (pa_cascade.cu).
+template <typename DT, int D, int NT>
+pa_status launch_cascade_prefix(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
+                                int num_sms, long long max_items, cudaStream_t stream);
 
 }  // namespace pa

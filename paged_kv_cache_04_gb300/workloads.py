@@ -279,7 +279,10 @@ def shared_prefix(device="cpu", prompts=64, samples=8, prefix=2048, tail_lo=0, t
                   copy_pairs=torch.tensor(pairs, dtype=torch.int64, device=device).view(-1, 2),
                   meta={"prompts": prompts, "samples": samples, "prefix": prefix,
                         "prefix_extra": r, "cow_copies": len(pairs),
-                        "unique_tokens": sum(prefix + r[p] for p in range(prompts)) + N})
+                        "unique_tokens": sum(prefix + r[p] for p in range(prompts)) + N,
+                        # groups for the shared-prefix decode: one per prompt, its samples in order
+                        "group_starts": [p * samples for p in range(prompts + 1)],
+                        "prefix_lens": [prefix + r[p] for p in range(prompts)]})
     return wl
 
 
