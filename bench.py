@@ -56,8 +56,10 @@ def parse():
                     help="the same 64-sequence case with an E4M3 cache (for ncu)")
     ap.add_argument("--workload", default="llama8b",
                     choices=["llama8b", "tiny", "opt13b", "shared", "shared_cow", "long70b_b16", "long70b_b32",
-                             "llama8b_fp8", "long70b_b16_fp8", "shared_cascade", "shared_cow_cascade"],
-                    help="the other workload shapes give a device-timed line of their own (no e2e / CPU legs)")
+                             "llama8b_fp8", "long70b_b16_fp8", "shared_cascade", "shared_cow_cascade",
+                             "llama8b_nhd", "llama8b_fp8_nhd", "long70b_b16_nhd", "shared_cascade_nhd"],
+                    help="the other workload shapes give a device-timed line of their own (no e2e / CPU legs); "
+                         "a _nhd suffix stores the pools NHD")
     return ap.parse_args()
 
 
@@ -451,7 +453,8 @@ def run_workload(args):
     _build.ensure_built()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    name = args.workload
+    nhd = args.workload.endswith("_nhd")
+    name = args.workload[:-4] if nhd else args.workload
     split, T = False, None
     if name == "tiny":
         wl = workloads.tiny(device=dev)
@@ -468,14 +471,22 @@ def run_workload(args):
                              for s, c in enumerate(wl.context_lens.tolist())], dtype=torch.int64, device=dev)
         wl.slot_mapping = last
         wl.new_key, wl.new_value = wl.new_key[:wl.S].contiguous(), wl.new_value[:wl.S].contiguous()
+    elif name == "llama8b":  # the benchmark batch, device-timed here (its pool stored NHD)
+        wl = workloads.llama8b(device=dev)
     elif name == "llama8b_fp8":
         wl = workloads.to_fp8(workloads.llama8b(device=dev))
-    else:
+    elif name.startswith("long70b"):
         B = 32 if "b32" in name else 16
         wl = workloads.long70b(device=dev, B=B)
         if name.endswith("fp8"):
             wl = workloads.to_fp8(wl)
         split, T = True, 512
+    else:
+        raise ValueError(f"unknown workload {args.workload}")
+    if nhd:
+        wl = workloads.to_nhd(wl)
+        torch.cuda.synchronize()
+    lay = wl.layout
     fp8 = name.endswith("fp8")
     cascade = name.endswith("cascade")
     ks, vs = wl.meta.get("k_scale", 1.0), wl.meta.get("v_scale", 1.0)
@@ -501,26 +512,27 @@ def run_workload(args):
 
     def step():
         if fp8:
-            pa.pa_reshape_and_cache_fp8(wl.new_key, wl.new_value, wl.k_cache, wl.v_cache, wl.slot_mapping, ks, vs)
+            pa.pa_reshape_and_cache_fp8(wl.new_key, wl.new_value, wl.k_cache, wl.v_cache, wl.slot_mapping, ks, vs,
+                                        layout=lay)
             if split:
                 pa.pa_decode_split_fp8(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens,
-                                       wl.scale, ks, vs, max_ctx, T, ws)
+                                       wl.scale, ks, vs, max_ctx, T, ws, layout=lay)
             else:
                 pa.pa_decode_fp8(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale,
-                                 ks, vs)
+                                 ks, vs, layout=lay)
             return
         if pairs is not None:
             pa.pa_copy_blocks([wl.k_cache], [wl.v_cache], pairs)
         if wl.slot_mapping is not None:
-            pa.pa_reshape_and_cache(wl.new_key, wl.new_value, wl.k_cache, wl.v_cache, wl.slot_mapping)
+            pa.pa_reshape_and_cache(wl.new_key, wl.new_value, wl.k_cache, wl.v_cache, wl.slot_mapping, layout=lay)
         if cascade:
             pa.pa_decode_cascade(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale,
-                                 gs, pl, gmax, pmax, max_ctx, T, ws)
+                                 gs, pl, gmax, pmax, max_ctx, T, ws, layout=lay)
         elif split:
             pa.pa_decode_split(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale,
-                               max_ctx, T, ws)
+                               max_ctx, T, ws, layout=lay)
         else:
-            pa.pa_decode(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale)
+            pa.pa_decode(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale, layout=lay)
 
     for _ in range(args.warmup):
         step()
@@ -553,7 +565,7 @@ def run_workload(args):
     if name.startswith("shared"):
         unique = wl.meta["unique_tokens"] * roofline.kv_bytes_per_token(1, wl.G, wl.d, e) + 2 * wl.S * wl.H * wl.d * e
     peak, _ = measured_hbm_peak()
-    line = {"workload": name, "ms_per_step": round(ms, 5), "seqs_per_s": round(wl.S / (ms * 1e-3), 1),
+    line = {"workload": args.workload, "ms_per_step": round(ms, 5), "seqs_per_s": round(wl.S / (ms * 1e-3), 1),
             "kv_tokens_per_s": round(sum(ctx) / (ms * 1e-3), 1),
             "algorithmic_GBps": round((dec + extra) / (ms * 1e-3) / 1e9, 1),
             "frac_of_measured_peak": round((dec + extra) / (ms * 1e-3) / 1e9 / peak, 4),

@@ -23,10 +23,11 @@
  *     copy pairs) are checked by the kernels: an out-of-range value is skipped
  *     (never dereferenced) and recorded in a device error word that
  *     pa_get_error() reads. The kernels never trap.
- *   - Layouts are dense and row-major. The KV pool layout is HND:
- *     cache[num_blocks][num_kv_heads][block_size][head_dim]; token t of a
- *     sequence lives in physical block block_table[t / block_size], row
- *     t % block_size. Query head h reads kv head h / (num_heads / num_kv_heads).
+ *   - Layouts are dense and row-major. A KV pool is HND,
+ *     cache[num_blocks][num_kv_heads][block_size][head_dim], or NHD,
+ *     cache[num_blocks][block_size][num_kv_heads][head_dim] (pa_kv_layout);
+ *     token t of a sequence lives in physical block block_table[t / block_size],
+ *     row t % block_size. Query head h reads kv head h / (num_heads / num_kv_heads).
  *   - q, out, key, value and the caches must be 16-byte aligned.
  *   - Supported: head_dim 64 or 128; block_size 16 or 32; num_heads /
  *     num_kv_heads from 1 to 8; element types PA_F32, PA_F16, PA_BF16, and
@@ -59,6 +60,14 @@ typedef enum {
  * one fp32 scale per K or V tensor. */
 typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2, PA_FP8_E4M3 = 3 } pa_dtype;
 
+/* KV pool layouts, the two the pages name (Month 2 · PagedAttention, infra
+ * learning path, §5.2):
+ *   PA_LAYOUT_HND  cache[num_blocks][num_kv_heads][block_size][head_dim]
+ *   PA_LAYOUT_NHD  cache[num_blocks][block_size][num_kv_heads][head_dim]
+ * A whole block is contiguous in both, so pa_copy_blocks and pa_swap_blocks
+ * take no layout. An invalid value returns PA_ERR_INVALID_ARG. */
+typedef enum { PA_LAYOUT_HND = 0, PA_LAYOUT_NHD = 1 } pa_kv_layout;
+
 /* Bits of the device error word returned by pa_get_error(). */
 #define PA_DEVERR_BLOCK_ID 1u /* a block-table entry outside [0, num_blocks) was skipped */
 #define PA_DEVERR_SLOT 2u     /* a slot outside [-1, num_blocks * block_size) was skipped */
@@ -73,7 +82,7 @@ typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2, PA_FP8_E4M3 = 3 } pa_dtype;
  *
  *   key, value    [num_tokens][num_kv_heads][head_dim], element type `dtype`
  *   k_cache,
- *   v_cache       [num_blocks][num_kv_heads][block_size][head_dim], `dtype`
+ *   v_cache       pools of `dtype` in `layout` (HND or NHD, see pa_kv_layout)
  *   slot_mapping  int64 [num_tokens]; token t goes to block slot / block_size,
  *                 row slot % block_size; a negative slot means "skip" (padding)
  *
@@ -82,8 +91,8 @@ typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2, PA_FP8_E4M3 = 3 } pa_dtype;
  */
 pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
                                const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
-                               int head_dim, int block_size, int64_t num_blocks, pa_dtype dtype,
-                               cudaStream_t stream);
+                               int head_dim, int block_size, pa_kv_layout layout, int64_t num_blocks,
+                               pa_dtype dtype, cudaStream_t stream);
 
 /*
  * Decode attention over a paged KV cache: for every sequence s and query head h
@@ -92,7 +101,8 @@ pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache
  *   out[s][h] = sum_{t < context_lens[s]} softmax_t(scale * q[s][h] . K_s[t]) V_s[t]
  *
  * with K_s[t] = k_cache[block_tables[s][t / block_size]][h / group][t % block_size]
- * and group = num_heads / num_kv_heads.
+ * (HND; NHD swaps the last two indices before head_dim) and group =
+ * num_heads / num_kv_heads. Both layouts give bit-identical results.
  *
  *   out           [num_seqs][num_heads][head_dim], element type `out_dtype`
  *                 (`dtype` or PA_F32; accumulation is always fp32)
@@ -107,7 +117,7 @@ pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache
 pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
                     const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
                     int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
-                    int64_t num_blocks, float scale, pa_dtype dtype, pa_dtype out_dtype,
+                    pa_kv_layout layout, int64_t num_blocks, float scale, pa_dtype dtype, pa_dtype out_dtype,
                     cudaStream_t stream);
 
 /*
@@ -146,9 +156,9 @@ size_t pa_decode_split_workspace_bytes(int num_seqs, int num_heads, int head_dim
 pa_status pa_decode_split(void* out, const void* q, const void* k_cache, const void* v_cache,
                           const int32_t* block_tables, int max_blocks_per_seq,
                           const int32_t* context_lens, int num_seqs, int num_heads, int num_kv_heads,
-                          int head_dim, int block_size, int64_t num_blocks, float scale, pa_dtype dtype,
-                          pa_dtype out_dtype, int max_context_len, int partition_tokens, void* workspace,
-                          size_t workspace_bytes, cudaStream_t stream);
+                          int head_dim, int block_size, pa_kv_layout layout, int64_t num_blocks, float scale,
+                          pa_dtype dtype, pa_dtype out_dtype, int max_context_len, int partition_tokens,
+                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * Size of the scratch array built into the library for pa_decode_split_static:
@@ -185,9 +195,9 @@ pa_status pa_decode_split(void* out, const void* q, const void* k_cache, const v
 pa_status pa_decode_split_static(void* out, const void* q, const void* k_cache, const void* v_cache,
                                  const int32_t* block_tables, int max_blocks_per_seq,
                                  const int32_t* context_lens, int num_seqs, int num_heads, int num_kv_heads,
-                                 int head_dim, int block_size, int64_t num_blocks, float scale,
-                                 pa_dtype dtype, pa_dtype out_dtype, int max_context_len, int partition_tokens,
-                                 cudaStream_t stream);
+                                 int head_dim, int block_size, pa_kv_layout layout, int64_t num_blocks,
+                                 float scale, pa_dtype dtype, pa_dtype out_dtype, int max_context_len,
+                                 int partition_tokens, cudaStream_t stream);
 
 /*
  * Decode attention for batches whose sequences share prompt prefixes (parallel
@@ -225,8 +235,8 @@ size_t pa_decode_cascade_workspace_bytes(int num_seqs, int num_heads, int head_d
 pa_status pa_decode_cascade(void* out, const void* q, const void* k_cache, const void* v_cache,
                             const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
                             int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
-                            int64_t num_blocks, float scale, pa_dtype dtype, pa_dtype out_dtype,
-                            const int32_t* group_starts, const int32_t* prefix_lens, int num_groups,
+                            pa_kv_layout layout, int64_t num_blocks, float scale, pa_dtype dtype,
+                            pa_dtype out_dtype, const int32_t* group_starts, const int32_t* prefix_lens, int num_groups,
                             int max_group_size, int max_prefix_len, int max_context_len, int partition_tokens,
                             void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
@@ -239,6 +249,7 @@ pa_status pa_decode_cascade(void* out, const void* q, const void* k_cache, const
  *
  *   k_caches, v_caches  HOST arrays of num_layers device pointers, each a pool
  *                       [num_blocks][num_kv_heads][block_size][head_dim] of `dtype`
+ *                       (or NHD: the copy moves whole blocks, contiguous in both)
  *   block_pairs         int64 [num_pairs][2] (src, dst)
  *
  * The copy is bit-exact. Destinations must be distinct and no destination may
@@ -259,7 +270,7 @@ pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches, int num_l
  * `in_dtype`: PA_F32, PA_F16 or PA_BF16) are quantised on the way in:
  * code = E4M3(x / scale), the division in fp32 (correctly rounded), then round
  * to nearest even on the E4M3 grid; finite values beyond +-448 saturate, NaN
- * stays NaN. k_cache / v_cache hold codes, [num_blocks][num_kv_heads][block_size][head_dim].
+ * stays NaN. k_cache / v_cache hold codes in `layout`.
  *
  * pa_decode_fp8 / pa_decode_split_fp8: as pa_decode / pa_decode_split over an
  * E4M3 cache: out = softmax(scale * q . (k_scale * K)) (v_scale * V). q is of
@@ -269,20 +280,20 @@ pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches, int num_l
  */
 pa_status pa_reshape_and_cache_fp8(const void* key, const void* value, void* k_cache, void* v_cache,
                                    const int64_t* slot_mapping, int num_tokens, int num_kv_heads, int head_dim,
-                                   int block_size, int64_t num_blocks, pa_dtype in_dtype, float k_scale,
-                                   float v_scale, cudaStream_t stream);
+                                   int block_size, pa_kv_layout layout, int64_t num_blocks, pa_dtype in_dtype,
+                                   float k_scale, float v_scale, cudaStream_t stream);
 
 pa_status pa_decode_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
                         const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
                         int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
-                        int64_t num_blocks, float scale, float k_scale, float v_scale, pa_dtype q_dtype,
-                        pa_dtype out_dtype, cudaStream_t stream);
+                        pa_kv_layout layout, int64_t num_blocks, float scale, float k_scale, float v_scale,
+                        pa_dtype q_dtype, pa_dtype out_dtype, cudaStream_t stream);
 
 pa_status pa_decode_split_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
                               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
                               int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
-                              int64_t num_blocks, float scale, float k_scale, float v_scale, pa_dtype q_dtype,
-                              pa_dtype out_dtype, int max_context_len, int partition_tokens, void* workspace,
+                              pa_kv_layout layout, int64_t num_blocks, float scale, float k_scale, float v_scale,
+                              pa_dtype q_dtype, pa_dtype out_dtype, int max_context_len, int partition_tokens, void* workspace,
                               size_t workspace_bytes, cudaStream_t stream);
 
 /*

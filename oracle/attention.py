@@ -74,10 +74,23 @@ def _ptr(a):
     return a.ctypes.data_as(ctypes.c_void_p)
 
 
-def _common(q, k_cache, v_cache, block_tables, context_lens):
+def _hnd(a, layout):
+    """The pool as [num_blocks][G][B][d]. Month 2 · PagedAttention §5.2 names two
+    pool layouts: HND [blocks][heads][tokens][d] and NHD [blocks][tokens][heads][d];
+    NHD element [b][r][h] is HND element [b][h][r], so an NHD pool is its HND
+    form with axes 1 and 2 exchanged."""
+    if layout == "HND":
+        return a
+    if layout != "NHD":
+        raise ValueError(f"unknown layout {layout!r}")
+    return np.ascontiguousarray(a.transpose(0, 2, 1, 3))
+
+
+def _common(q, k_cache, v_cache, block_tables, context_lens, layout="HND"):
     qa, dq = _host(q, "q")
     ka, dk = _host(k_cache, "k_cache")
     va, dv = _host(v_cache, "v_cache")
+    ka, va = _hnd(ka, layout), _hnd(va, layout)
     if not (dq == dk == dv) or dq is None:
         raise TypeError("q, k_cache and v_cache must share one float dtype")
     bt = np.ascontiguousarray(_host(block_tables, "block_tables")[0], dtype=np.int32)
@@ -89,10 +102,10 @@ def _common(q, k_cache, v_cache, block_tables, context_lens):
     return qa, ka, va, dq, bt, cl, S, H, G, d, B, nb
 
 
-def decode(q, k_cache, v_cache, block_tables, context_lens, scale, num_threads=0, lib=None):
+def decode(q, k_cache, v_cache, block_tables, context_lens, scale, num_threads=0, lib=None, layout="HND"):
     """float64 ``out[S, H, d]`` = softmax(scale * q K^T) V over each sequence's paged context."""
     lib = lib or _load()
-    qa, ka, va, dt, bt, cl, S, H, G, d, B, nb = _common(q, k_cache, v_cache, block_tables, context_lens)
+    qa, ka, va, dt, bt, cl, S, H, G, d, B, nb = _common(q, k_cache, v_cache, block_tables, context_lens, layout)
     out = np.zeros((S, H, d), dtype=np.float64)
     rc = lib.pa_oracle_decode(_ptr(out), _ptr(qa), _ptr(ka), _ptr(va), dt, _ptr(bt), bt.shape[1],
                               _ptr(cl), S, H, G, d, B, nb, float(scale), int(num_threads))
@@ -102,10 +115,10 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale, num_threads=0
 
 
 def partitions(q, k_cache, v_cache, block_tables, context_lens, scale, T, P=None,
-               num_threads=0, lib=None):
+               num_threads=0, lib=None, layout="HND"):
     """Per-partition ``(o[S,H,P,d], m[S,H,P], l[S,H,P])`` for partitions of T tokens."""
     lib = lib or _load()
-    qa, ka, va, dt, bt, cl, S, H, G, d, B, nb = _common(q, k_cache, v_cache, block_tables, context_lens)
+    qa, ka, va, dt, bt, cl, S, H, G, d, B, nb = _common(q, k_cache, v_cache, block_tables, context_lens, layout)
     if P is None:
         P = max(1, -(-int(cl.max(initial=0)) // T))
     o = np.zeros((S, H, P, d), dtype=np.float64)

@@ -33,10 +33,11 @@ def _bits(x):
     return a
 
 
-def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping):
+def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, layout="HND"):
     """Return new (k_cache, v_cache) bit arrays after writing every new token.
 
-    key, value: [N, G, d]; caches: [num_blocks, G, B, d] (HND).
+    key, value: [N, G, d]; caches: [num_blocks, G, B, d] (HND) or
+    [num_blocks, B, G, d] (NHD; Month 2 · PagedAttention §5.2 names both).
     For token t with slot = slot_mapping[t] >= 0: block = slot // B, row = slot % B,
     and cache[block, h, row, :] = key[t, h, :] for every kv head h (CS349E
     Lecture 7 notes §4.1: a slot is a position inside a physical block; CMU
@@ -46,7 +47,13 @@ def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping):
     kb, vb = _bits(key), _bits(value)
     kc, vc = _bits(k_cache), _bits(v_cache)
     slots = np.asarray(_bits(slot_mapping), dtype=np.int64)
-    nb, G, B, d = kc.shape
+    if layout not in ("HND", "NHD"):
+        raise ValueError(f"unknown layout {layout!r}")
+    nhd = layout == "NHD"
+    if nhd:
+        nb, B, G, d = kc.shape
+    else:
+        nb, G, B, d = kc.shape
     N = kb.shape[0]
     if kb.shape != (N, G, d) or vb.shape != kb.shape or slots.shape != (N,) or vc.shape != kc.shape:
         raise ValueError("shape mismatch")
@@ -58,8 +65,12 @@ def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping):
         if block >= nb:
             raise IndexError(f"slot {slot} outside a pool of {nb} blocks of {B}")
         for h in range(G):
-            kc[block, h, row, :] = kb[t, h, :]
-            vc[block, h, row, :] = vb[t, h, :]
+            if nhd:
+                kc[block, row, h, :] = kb[t, h, :]
+                vc[block, row, h, :] = vb[t, h, :]
+            else:
+                kc[block, h, row, :] = kb[t, h, :]
+                vc[block, h, row, :] = vb[t, h, :]
     return kc, vc
 
 

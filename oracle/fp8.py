@@ -72,29 +72,38 @@ def quantize(x, scale):
     return e4m3_encode(q)
 
 
-def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, k_scale, v_scale):
+def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, k_scale, v_scale, layout="HND"):
     """New (k_cache, v_cache) code arrays after quantising and writing every new token.
 
     key, value: float arrays [N, G, d] (their exact values); caches: uint8 codes
-    [num_blocks, G, B, d]. Token t with slot >= 0 lands in block slot // B, row
-    slot % B, as in the unquantised cache write.
+    [num_blocks, G, B, d] (HND) or [num_blocks, B, G, d] (NHD). Token t with
+    slot >= 0 lands in block slot // B, row slot % B, as in the unquantised
+    cache write.
     """
     kq = quantize(_np(key), k_scale)
     vq = quantize(_np(value), v_scale)
     kc = np.array(_np(k_cache), dtype=np.uint8, copy=True)
     vc = np.array(_np(v_cache), dtype=np.uint8, copy=True)
     slots = np.asarray(_np(slot_mapping), dtype=np.int64)
-    B = kc.shape[2]
+    if layout not in ("HND", "NHD"):
+        raise ValueError(f"unknown layout {layout!r}")
+    nhd = layout == "NHD"
+    B = kc.shape[1] if nhd else kc.shape[2]
     for t, slot in enumerate(slots):
         if slot < 0:
             continue
         b, r = divmod(int(slot), B)
-        kc[b, :, r, :] = kq[t]
-        vc[b, :, r, :] = vq[t]
+        if nhd:
+            kc[b, r, :, :] = kq[t]
+            vc[b, r, :, :] = vq[t]
+        else:
+            kc[b, :, r, :] = kq[t]
+            vc[b, :, r, :] = vq[t]
     return kc, vc
 
 
-def decode(q, k_codes, v_codes, block_tables, context_lens, scale, k_scale, v_scale, num_threads=0):
+def decode(q, k_codes, v_codes, block_tables, context_lens, scale, k_scale, v_scale, num_threads=0,
+           layout="HND"):
     """float64 attention over an E4M3 cache with per-tensor scales.
 
     softmax(scale * q . (k_scale * K)) (v_scale * V): the scales are constants,
@@ -105,5 +114,5 @@ def decode(q, k_codes, v_codes, block_tables, context_lens, scale, k_scale, v_sc
     vf = e4m3_decode(_np(v_codes)).astype(np.float32)
     qf = _np(q).astype(np.float32)
     out = _decode(qf, kf, vf, block_tables, context_lens, float(scale) * float(k_scale),
-                  num_threads=num_threads)
+                  num_threads=num_threads, layout=layout)
     return out * float(v_scale)

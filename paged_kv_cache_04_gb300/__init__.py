@@ -8,7 +8,8 @@ fallback: if the library is missing or cannot load, every call raises.
 Tensors are ``torch`` CUDA tensors in the layouts the header documents:
 
 * ``q``, ``out``                 ``[num_seqs, num_heads, head_dim]``
-* ``k_cache``, ``v_cache``       ``[num_blocks, num_kv_heads, block_size, head_dim]``
+* ``k_cache``, ``v_cache``       ``[num_blocks, num_kv_heads, block_size, head_dim]`` (``layout="HND"``,
+  the default) or ``[num_blocks, block_size, num_kv_heads, head_dim]`` (``layout="NHD"``)
 * ``block_tables``               int32 ``[num_seqs, max_blocks_per_seq]``
 * ``context_lens``               int32 ``[num_seqs]``
 * ``key``, ``value``             ``[num_tokens, num_kv_heads, head_dim]``
@@ -25,7 +26,7 @@ __all__ = [
     "pa_decode_split_workspace_bytes", "pa_decode_split_static", "pa_copy_blocks", "pa_swap_blocks",
     "pa_reshape_and_cache_fp8", "pa_decode_fp8", "pa_decode_split_fp8", "pa_decode_cascade",
     "pa_decode_cascade_workspace_bytes", "pa_get_error",
-    "pa_version", "PA_STATIC_SCRATCH_BYTES",
+    "pa_version", "PA_STATIC_SCRATCH_BYTES", "PA_LAYOUT_HND", "PA_LAYOUT_NHD",
     "PA_DEVERR_BLOCK_ID", "PA_DEVERR_SLOT", "PA_DEVERR_CONTEXT", "PA_DEVERR_PAIR", "PA_DEVERR_TIMEOUT",
 ]
 
@@ -34,6 +35,7 @@ library_path = os.path.join(_HERE, "libpa.so")
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_OUT_OF_RANGE, PA_ERR_CUDA = range(5)
 PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3 = 0, 1, 2, 3
+PA_LAYOUT_HND, PA_LAYOUT_NHD = 0, 1
 PA_DEVERR_BLOCK_ID, PA_DEVERR_SLOT, PA_DEVERR_CONTEXT, PA_DEVERR_PAIR, PA_DEVERR_TIMEOUT = 1, 2, 4, 8, 16
 PA_STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 
@@ -57,21 +59,21 @@ def library():
         raise PAError("load", PA_ERR_CUDA, f"{library_path} not built")
     lib = ctypes.CDLL(library_path)
     P, I, I64, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
-    lib.pa_reshape_and_cache.argtypes = [P, P, P, P, P, I, I, I, I, I64, I, P]
-    lib.pa_decode.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I64, F, I, I, P]
+    lib.pa_reshape_and_cache.argtypes = [P, P, P, P, P, I, I, I, I, I, I64, I, P]
+    lib.pa_decode.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, I64, F, I, I, P]
     lib.pa_decode_split_workspace_bytes.argtypes = [I, I, I, I, I]
     lib.pa_decode_split_workspace_bytes.restype = SZ
-    lib.pa_decode_split.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I64, F, I, I, I, I, P, SZ, P]
-    lib.pa_decode_split_static.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I64, F, I, I, I, I, P]
+    lib.pa_decode_split.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, I64, F, I, I, I, I, P, SZ, P]
+    lib.pa_decode_split_static.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, I64, F, I, I, I, I, P]
     lib.pa_copy_blocks.argtypes = [P, P, I, P, I, I, I, I, I64, I, P]
     lib.pa_swap_blocks.argtypes = [P, P, P, P, I, P, I, I, I, I, I64, I64, I, P]
-    lib.pa_reshape_and_cache_fp8.argtypes = [P, P, P, P, P, I, I, I, I, I64, I, F, F, P]
-    lib.pa_decode_fp8.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I64, F, F, F, I, I, P]
-    lib.pa_decode_split_fp8.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I64, F, F, F, I, I, I, I, P, SZ, P]
+    lib.pa_reshape_and_cache_fp8.argtypes = [P, P, P, P, P, I, I, I, I, I, I64, I, F, F, P]
+    lib.pa_decode_fp8.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, I64, F, F, F, I, I, P]
+    lib.pa_decode_split_fp8.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, I64, F, F, F, I, I, I, I, P, SZ, P]
     lib.pa_decode_cascade_workspace_bytes.argtypes = [I, I, I, I, I, I]
     lib.pa_decode_cascade_workspace_bytes.restype = SZ
-    lib.pa_decode_cascade.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I64, F, I, I, P, P, I, I, I, I, I, P, SZ,
-                                      P]
+    lib.pa_decode_cascade.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, I64, F, I, I, P, P, I, I, I, I, I, P,
+                                      SZ, P]
     lib.pa_get_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), P]
     lib.pa_status_string.argtypes = [I]
     lib.pa_status_string.restype = ctypes.c_char_p
@@ -141,7 +143,15 @@ def _check(func, status):
         raise PAError(func, status)
 
 
-def pa_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, stream=None):
+def _pool(func, cache, layout):
+    """(layout code, num_blocks, num_kv_heads, block_size, head_dim) of a pool tensor."""
+    _need(layout in ("HND", "NHD"), func, "layout must be 'HND' or 'NHD'")
+    _need(cache.dim() == 4, func, "pools are 4-D")
+    nb, a, b, d = cache.shape
+    return (PA_LAYOUT_HND, nb, a, b, d) if layout == "HND" else (PA_LAYOUT_NHD, nb, b, a, d)
+
+
+def pa_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, stream=None, layout="HND"):
     """Write each new token's K/V into ``k_cache`` / ``v_cache`` at its slot (negative slot: skip)."""
     f = "pa_reshape_and_cache"
     torch = _torch()
@@ -149,34 +159,34 @@ def pa_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, stream=None
     _need(slot_mapping.dtype == torch.int64, f, "slot_mapping must be int64")
     _need(key.dtype == value.dtype == k_cache.dtype == v_cache.dtype, f, "dtype mismatch")
     N, G, d = key.shape
-    nb, G2, B, d2 = k_cache.shape
+    lc, nb, G2, B, d2 = _pool(f, k_cache, layout)
     _need(value.shape == key.shape and v_cache.shape == k_cache.shape and G2 == G and d2 == d, f, "shapes")
     _need(slot_mapping.shape == (N,), f, "slot_mapping shape")
     _check(f, library().pa_reshape_and_cache(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
-                                             _ptr(slot_mapping), N, G, d, B, nb, _dtype_code(key),
+                                             _ptr(slot_mapping), N, G, d, B, lc, nb, _dtype_code(key),
                                              _stream(stream)))
 
 
-def _decode_args(f, out, q, k_cache, v_cache, block_tables, context_lens):
+def _decode_args(f, out, q, k_cache, v_cache, block_tables, context_lens, layout):
     torch = _torch()
     _dev(f, out, q, k_cache, v_cache, block_tables, context_lens)
     _need(block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32, f,
           "block_tables and context_lens must be int32")
     _need(q.dtype == k_cache.dtype == v_cache.dtype, f, "q / cache dtype mismatch")
     S, H, d = q.shape
-    nb, G, B, d2 = k_cache.shape
+    lc, nb, G, B, d2 = _pool(f, k_cache, layout)
     _need(v_cache.shape == k_cache.shape and d2 == d and out.shape == q.shape, f, "shapes")
     _need(block_tables.dim() == 2 and block_tables.shape[0] == S and context_lens.shape == (S,), f,
           "table shapes")
-    return S, H, G, d, B, nb, int(block_tables.shape[1])
+    return S, H, G, d, B, lc, nb, int(block_tables.shape[1])
 
 
-def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, stream=None):
+def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, stream=None, layout="HND"):
     """``out[s, h] = softmax(scale * q[s, h] K_s^T) V_s`` over each sequence's paged context."""
     f = "pa_decode"
-    S, H, G, d, B, nb, maxb = _decode_args(f, out, q, k_cache, v_cache, block_tables, context_lens)
+    S, H, G, d, B, lc, nb, maxb = _decode_args(f, out, q, k_cache, v_cache, block_tables, context_lens, layout)
     _check(f, library().pa_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
-                                  maxb, _ptr(context_lens), S, H, G, d, B, nb, float(scale),
+                                  maxb, _ptr(context_lens), S, H, G, d, B, lc, nb, float(scale),
                                   _dtype_code(q), _dtype_code(out), _stream(stream)))
 
 
@@ -186,23 +196,23 @@ def pa_decode_split_workspace_bytes(num_seqs, num_heads, head_dim, max_context_l
 
 
 def pa_decode_split(out, q, k_cache, v_cache, block_tables, context_lens, scale, max_context_len,
-                    partition_tokens, workspace, stream=None):
+                    partition_tokens, workspace, stream=None, layout="HND"):
     """Partitioned decode (per-partition softmax, then a log-sum-exp reduce) into ``out``.
 
     ``workspace`` is a CUDA tensor of at least ``pa_decode_split_workspace_bytes(...)`` bytes.
     """
     f = "pa_decode_split"
-    S, H, G, d, B, nb, maxb = _decode_args(f, out, q, k_cache, v_cache, block_tables, context_lens)
+    S, H, G, d, B, lc, nb, maxb = _decode_args(f, out, q, k_cache, v_cache, block_tables, context_lens, layout)
     _dev(f, workspace)
     nbytes = workspace.numel() * workspace.element_size()
     _check(f, library().pa_decode_split(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
-                                        maxb, _ptr(context_lens), S, H, G, d, B, nb, float(scale),
+                                        maxb, _ptr(context_lens), S, H, G, d, B, lc, nb, float(scale),
                                         _dtype_code(q), _dtype_code(out), int(max_context_len),
                                         int(partition_tokens), _ptr(workspace), nbytes, _stream(stream)))
 
 
 def pa_decode_split_static(out, q, k_cache, v_cache, block_tables, context_lens, scale, max_context_len,
-                           partition_tokens, stream=None):
+                           partition_tokens, stream=None, layout="HND"):
     """``pa_decode_split`` for callers that cannot allocate: no workspace argument.
 
     The partition results go to a scratch array inside the library
@@ -213,10 +223,10 @@ def pa_decode_split_static(out, q, k_cache, v_cache, block_tables, context_lens,
     make it before any stream capture.
     """
     f = "pa_decode_split_static"
-    S, H, G, d, B, nb, maxb = _decode_args(f, out, q, k_cache, v_cache, block_tables, context_lens)
+    S, H, G, d, B, lc, nb, maxb = _decode_args(f, out, q, k_cache, v_cache, block_tables, context_lens, layout)
     _check(f, library().pa_decode_split_static(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                                _ptr(block_tables), maxb, _ptr(context_lens), S, H, G, d, B,
-                                               nb, float(scale), _dtype_code(q), _dtype_code(out),
+                                               lc, nb, float(scale), _dtype_code(q), _dtype_code(out),
                                                int(max_context_len), int(partition_tokens), _stream(stream)))
 
 
@@ -227,7 +237,8 @@ def pa_decode_cascade_workspace_bytes(num_seqs, num_heads, head_dim, max_prefix_
 
 
 def pa_decode_cascade(out, q, k_cache, v_cache, block_tables, context_lens, scale, group_starts, prefix_lens,
-                      max_group_size, max_prefix_len, max_context_len, partition_tokens, workspace, stream=None):
+                      max_group_size, max_prefix_len, max_context_len, partition_tokens, workspace, stream=None,
+                      layout="HND"):
     """Decode for batches whose sequences share prompt prefixes (same result as ``pa_decode``).
 
     ``group_starts`` (int32 [G+1]) and ``prefix_lens`` (int32 [G]) are CUDA
@@ -236,14 +247,14 @@ def pa_decode_cascade(out, q, k_cache, v_cache, block_tables, context_lens, scal
     """
     f = "pa_decode_cascade"
     torch = _torch()
-    S, H, G, d, B, nb, maxb = _decode_args(f, out, q, k_cache, v_cache, block_tables, context_lens)
+    S, H, G, d, B, lc, nb, maxb = _decode_args(f, out, q, k_cache, v_cache, block_tables, context_lens, layout)
     _dev(f, workspace, group_starts, prefix_lens)
     _need(group_starts.dtype == torch.int32 and prefix_lens.dtype == torch.int32, f, "group arrays must be int32")
     ng = int(prefix_lens.numel())
     _need(group_starts.numel() == ng + 1, f, "group_starts must have num_groups + 1 entries")
     nbytes = workspace.numel() * workspace.element_size()
     _check(f, library().pa_decode_cascade(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
-                                          maxb, _ptr(context_lens), S, H, G, d, B, nb, float(scale), _dtype_code(q),
+                                          maxb, _ptr(context_lens), S, H, G, d, B, lc, nb, float(scale), _dtype_code(q),
                                           _dtype_code(out), _ptr(group_starts), _ptr(prefix_lens), ng,
                                           int(max_group_size), int(max_prefix_len), int(max_context_len),
                                           int(partition_tokens), _ptr(workspace), nbytes, _stream(stream)))
@@ -302,10 +313,11 @@ def _is_code_tensor(t):
     return t.dtype in (torch.uint8, torch.float8_e4m3fn)
 
 
-def pa_reshape_and_cache_fp8(key, value, k_cache, v_cache, slot_mapping, k_scale, v_scale, stream=None):
+def pa_reshape_and_cache_fp8(key, value, k_cache, v_cache, slot_mapping, k_scale, v_scale, stream=None,
+                             layout="HND"):
     """Quantise each new token's K/V to E4M3 (x / scale, round to nearest even, saturating) into its slot.
 
-    ``k_cache`` / ``v_cache`` are uint8 (or float8_e4m3fn) CUDA tensors ``[num_blocks, G, B, d]``.
+    ``k_cache`` / ``v_cache`` are uint8 (or float8_e4m3fn) CUDA tensors in ``layout``.
     """
     f = "pa_reshape_and_cache_fp8"
     torch = _torch()
@@ -313,46 +325,47 @@ def pa_reshape_and_cache_fp8(key, value, k_cache, v_cache, slot_mapping, k_scale
     _need(slot_mapping.dtype == torch.int64, f, "slot_mapping must be int64")
     _need(key.dtype == value.dtype and _is_code_tensor(k_cache) and _is_code_tensor(v_cache), f, "dtypes")
     N, G, d = key.shape
-    nb, G2, B, d2 = k_cache.shape
+    lc, nb, G2, B, d2 = _pool(f, k_cache, layout)
     _need(value.shape == key.shape and v_cache.shape == k_cache.shape and G2 == G and d2 == d, f, "shapes")
     _need(slot_mapping.shape == (N,), f, "slot_mapping shape")
     _check(f, library().pa_reshape_and_cache_fp8(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
-                                                 _ptr(slot_mapping), N, G, d, B, nb, _dtype_code(key),
+                                                 _ptr(slot_mapping), N, G, d, B, lc, nb, _dtype_code(key),
                                                  float(k_scale), float(v_scale), _stream(stream)))
 
 
-def _decode_args_fp8(f, out, q, k_cache, v_cache, block_tables, context_lens):
+def _decode_args_fp8(f, out, q, k_cache, v_cache, block_tables, context_lens, layout):
     torch = _torch()
     _dev(f, out, q, k_cache, v_cache, block_tables, context_lens)
     _need(block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32, f,
           "block_tables and context_lens must be int32")
     _need(_is_code_tensor(k_cache) and _is_code_tensor(v_cache), f, "caches must hold E4M3 codes")
     S, H, d = q.shape
-    nb, G, B, d2 = k_cache.shape
+    lc, nb, G, B, d2 = _pool(f, k_cache, layout)
     _need(v_cache.shape == k_cache.shape and d2 == d and out.shape == q.shape, f, "shapes")
     _need(block_tables.dim() == 2 and block_tables.shape[0] == S and context_lens.shape == (S,), f,
           "table shapes")
-    return S, H, G, d, B, nb, int(block_tables.shape[1])
+    return S, H, G, d, B, lc, nb, int(block_tables.shape[1])
 
 
-def pa_decode_fp8(out, q, k_cache, v_cache, block_tables, context_lens, scale, k_scale, v_scale, stream=None):
+def pa_decode_fp8(out, q, k_cache, v_cache, block_tables, context_lens, scale, k_scale, v_scale, stream=None,
+                  layout="HND"):
     """Decode attention over an E4M3 cache: softmax(scale q . k_scale K) (v_scale V)."""
     f = "pa_decode_fp8"
-    S, H, G, d, B, nb, maxb = _decode_args_fp8(f, out, q, k_cache, v_cache, block_tables, context_lens)
+    S, H, G, d, B, lc, nb, maxb = _decode_args_fp8(f, out, q, k_cache, v_cache, block_tables, context_lens, layout)
     _check(f, library().pa_decode_fp8(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), maxb,
-                                      _ptr(context_lens), S, H, G, d, B, nb, float(scale), float(k_scale),
+                                      _ptr(context_lens), S, H, G, d, B, lc, nb, float(scale), float(k_scale),
                                       float(v_scale), _dtype_code(q), _dtype_code(out), _stream(stream)))
 
 
 def pa_decode_split_fp8(out, q, k_cache, v_cache, block_tables, context_lens, scale, k_scale, v_scale,
-                        max_context_len, partition_tokens, workspace, stream=None):
+                        max_context_len, partition_tokens, workspace, stream=None, layout="HND"):
     """Partitioned decode over an E4M3 cache (workspace as for ``pa_decode_split``)."""
     f = "pa_decode_split_fp8"
-    S, H, G, d, B, nb, maxb = _decode_args_fp8(f, out, q, k_cache, v_cache, block_tables, context_lens)
+    S, H, G, d, B, lc, nb, maxb = _decode_args_fp8(f, out, q, k_cache, v_cache, block_tables, context_lens, layout)
     _dev(f, workspace)
     nbytes = workspace.numel() * workspace.element_size()
     _check(f, library().pa_decode_split_fp8(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
-                                            maxb, _ptr(context_lens), S, H, G, d, B, nb, float(scale),
+                                            maxb, _ptr(context_lens), S, H, G, d, B, lc, nb, float(scale),
                                             float(k_scale), float(v_scale), _dtype_code(q), _dtype_code(out),
                                             int(max_context_len), int(partition_tokens), _ptr(workspace), nbytes,
                                             _stream(stream)))

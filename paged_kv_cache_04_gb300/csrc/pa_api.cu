@@ -47,10 +47,13 @@ pa_status encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
   return PA_OK;
 }
 
-// A 2-D view of a KV pool: rows = num_blocks * num_kv_heads * block_size, each
-// head_dim elements. One TMA box is 128 bytes of a row x 16 rows (one job),
-// staged with 128-byte swizzling.
-pa_status make_pool_map(CUtensorMap* map, const void* base, pa_dtype dt, int D, int BS, long long rows) {
+// The TMA view of a KV pool. One box is 128 bytes of head_dim x 16 tokens of
+// one (block, kv head) tile (one job), staged with 128-byte swizzling.
+//   HND [num_blocks][G][B][D]: 2-D, rows = num_blocks * G * B of D elements;
+//   NHD [num_blocks][B][G][D]: 3-D (D, G, num_blocks * B), so a box takes one
+//   kv head of 16 consecutive tokens (rows G * D elements apart).
+pa_status make_pool_map(CUtensorMap* map, const void* base, pa_dtype dt, int D, int G, int BS, long long num_blocks,
+                        pa_kv_layout layout) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
   pa_status st = encoder(&enc);
   if (st != PA_OK) return st;
@@ -59,12 +62,23 @@ pa_status make_pool_map(CUtensorMap* map, const void* base, pa_dtype dt, int D, 
                                 : dt == PA_F16        ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                 : dt == PA_FP8_E4M3   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)D * e};
-  cuuint32_t box[2] = {(cuuint32_t)(128 / e), (cuuint32_t)kJobTokens};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(map, t, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  const bool nhd = layout == PA_LAYOUT_NHD;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)(num_blocks * G * BS), 1};
+  cuuint64_t strides[2] = {(cuuint64_t)D * e, 0};
+  cuuint32_t box[3] = {(cuuint32_t)(128 / e), (cuuint32_t)kJobTokens, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  if (nhd) {
+    dims[1] = (cuuint64_t)G;
+    dims[2] = (cuuint64_t)(num_blocks * BS);
+    strides[1] = (cuuint64_t)G * D * e;
+    box[1] = 1;
+    box[2] = (cuuint32_t)kJobTokens;
+  }
+  // NHD rows of one kv head are G * D elements apart: promote only the 128 bytes a box reads, so a
+  // 128-byte row does not drag its neighbour head's row into L2.
+  CUresult r = enc(map, t, nhd ? 3 : 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   nhd ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
@@ -83,12 +97,14 @@ struct DecodeArgs {
   pa_dtype dt, odt;
   pa_dtype qdt = PA_F32;        // FP8 caches: the query type
   float k_scale = 1.f, v_scale = 1.f;
+  pa_kv_layout layout = PA_LAYOUT_HND;
 };
 
 pa_status check_decode(const DecodeArgs& a) {
   if (a.S < 0 || a.H <= 0 || a.G <= 0 || a.D <= 0 || a.BS <= 0 || a.num_blocks <= 0 || a.max_blocks <= 0)
     return PA_ERR_INVALID_ARG;
   if (a.H % a.G || !valid_dtype(a.dt) || !valid_dtype(a.odt) || !std::isfinite(a.scale)) return PA_ERR_INVALID_ARG;
+  if (a.layout != PA_LAYOUT_HND && a.layout != PA_LAYOUT_NHD) return PA_ERR_INVALID_ARG;
   if (a.S == 0) return PA_OK;
   if (!a.out || !a.q || !a.k_cache || !a.v_cache || !a.block_tables || !a.context_lens) return PA_ERR_INVALID_ARG;
   if (!aligned16(a.out) || !aligned16(a.q) || !aligned16(a.k_cache) || !aligned16(a.v_cache) ||
@@ -152,10 +168,9 @@ pa_status run_decode(const DecodeArgs& a, bool split, int partition, int max_par
   int sms = 0;
   pa_status s = device_state(&err, &sms);
   if (s != PA_OK) return s;
-  const long long rows = (long long)a.num_blocks * a.G * a.BS;
   CUtensorMap km, vm;
-  if ((s = make_pool_map(&km, a.k_cache, a.dt, a.D, a.BS, rows)) != PA_OK) return s;
-  if ((s = make_pool_map(&vm, a.v_cache, a.dt, a.D, a.BS, rows)) != PA_OK) return s;
+  if ((s = make_pool_map(&km, a.k_cache, a.dt, a.D, a.G, a.BS, a.num_blocks, a.layout)) != PA_OK) return s;
+  if ((s = make_pool_map(&vm, a.v_cache, a.dt, a.D, a.G, a.BS, a.num_blocks, a.layout)) != PA_OK) return s;
 
   DecodeParams p{};
   p.out = a.out;
@@ -172,6 +187,7 @@ pa_status run_decode(const DecodeArgs& a, bool split, int partition, int max_par
   p.num_blocks = a.num_blocks;
   p.scale_log2 = a.scale * a.k_scale * 1.4426950408889634f;
   p.v_scale = a.v_scale;
+  p.nhd = a.layout == PA_LAYOUT_NHD;
   p.err = err;
   long long items = (long long)a.S * a.G;
   if (split) {
@@ -263,13 +279,14 @@ pa_status device_state(unsigned** err, int* num_sms) {
 
 extern "C" pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
                                const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
-                               int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                               int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size, pa_kv_layout layout,
                                int64_t num_blocks, float scale, pa_dtype dtype, pa_dtype out_dtype,
                                cudaStream_t stream) {
   using namespace pa;
-  const DecodeArgs a{out,      q,         k_cache,      v_cache,  block_tables, max_blocks_per_seq,
+  DecodeArgs a{out,      q,         k_cache,      v_cache,  block_tables, max_blocks_per_seq,
                      context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
                      (long long)num_blocks, scale, dtype, out_dtype};
+  a.layout = layout;
   pa_status s = check_decode(a);
   if (s != PA_OK || num_seqs == 0) return s;
   return run_decode(a, false, 0, 0, nullptr, stream);
@@ -286,14 +303,15 @@ extern "C" size_t pa_decode_split_workspace_bytes(int num_seqs, int num_heads, i
 extern "C" pa_status pa_decode_split(void* out, const void* q, const void* k_cache, const void* v_cache,
                                      const int32_t* block_tables, int max_blocks_per_seq,
                                      const int32_t* context_lens, int num_seqs, int num_heads, int num_kv_heads,
-                                     int head_dim, int block_size, int64_t num_blocks, float scale,
+                                     int head_dim, int block_size, pa_kv_layout layout, int64_t num_blocks, float scale,
                                      pa_dtype dtype, pa_dtype out_dtype, int max_context_len,
                                      int partition_tokens, void* workspace, size_t workspace_bytes,
                                      cudaStream_t stream) {
   using namespace pa;
-  const DecodeArgs a{out,      q,         k_cache,      v_cache,  block_tables, max_blocks_per_seq,
+  DecodeArgs a{out,      q,         k_cache,      v_cache,  block_tables, max_blocks_per_seq,
                      context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
                      (long long)num_blocks, scale, dtype, out_dtype};
+  a.layout = layout;
   pa_status s = check_decode(a);
   if (s != PA_OK) return s;
   if (max_context_len < 0 || partition_tokens <= 0 || partition_tokens % block_size) return PA_ERR_INVALID_ARG;
@@ -321,13 +339,14 @@ pa_status check_fp8(const pa::DecodeArgs& a) {
 
 extern "C" pa_status pa_decode_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
                                    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
-                                   int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                                   int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size, pa_kv_layout layout,
                                    int64_t num_blocks, float scale, float k_scale, float v_scale, pa_dtype q_dtype,
                                    pa_dtype out_dtype, cudaStream_t stream) {
   using namespace pa;
   DecodeArgs a{out,      q,         k_cache,      v_cache,  block_tables, max_blocks_per_seq,
                context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
                (long long)num_blocks, scale, q_dtype, out_dtype};
+  a.layout = layout;
   pa_status s = check_decode(a);  // shapes, pointers, alignment (q / out type as the 16-bit type)
   if (s != PA_OK || num_seqs == 0) return s;
   a.dt = PA_FP8_E4M3;
@@ -341,7 +360,7 @@ extern "C" pa_status pa_decode_fp8(void* out, const void* q, const void* k_cache
 extern "C" pa_status pa_decode_split_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
                                          const int32_t* block_tables, int max_blocks_per_seq,
                                          const int32_t* context_lens, int num_seqs, int num_heads,
-                                         int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                                         int num_kv_heads, int head_dim, int block_size, pa_kv_layout layout, int64_t num_blocks,
                                          float scale, float k_scale, float v_scale, pa_dtype q_dtype,
                                          pa_dtype out_dtype, int max_context_len, int partition_tokens,
                                          void* workspace, size_t workspace_bytes, cudaStream_t stream) {
@@ -349,6 +368,7 @@ extern "C" pa_status pa_decode_split_fp8(void* out, const void* q, const void* k
   DecodeArgs a{out,      q,         k_cache,      v_cache,  block_tables, max_blocks_per_seq,
                context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
                (long long)num_blocks, scale, q_dtype, out_dtype};
+  a.layout = layout;
   pa_status s = check_decode(a);
   if (s != PA_OK) return s;
   if (max_context_len < 0 || partition_tokens <= 0 || partition_tokens % block_size) return PA_ERR_INVALID_ARG;
@@ -380,15 +400,16 @@ extern "C" size_t pa_decode_cascade_workspace_bytes(int num_seqs, int num_heads,
 extern "C" pa_status pa_decode_cascade(void* out, const void* q, const void* k_cache, const void* v_cache,
                                        const int32_t* block_tables, int max_blocks_per_seq,
                                        const int32_t* context_lens, int num_seqs, int num_heads, int num_kv_heads,
-                                       int head_dim, int block_size, int64_t num_blocks, float scale,
+                                       int head_dim, int block_size, pa_kv_layout layout, int64_t num_blocks, float scale,
                                        pa_dtype dtype, pa_dtype out_dtype, const int32_t* group_starts,
                                        const int32_t* prefix_lens, int num_groups, int max_group_size,
                                        int max_prefix_len, int max_context_len, int partition_tokens,
                                        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   using namespace pa;
-  const DecodeArgs a{out,      q,         k_cache,      v_cache,  block_tables, max_blocks_per_seq,
+  DecodeArgs a{out,      q,         k_cache,      v_cache,  block_tables, max_blocks_per_seq,
                      context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
                      (long long)num_blocks, scale, dtype, out_dtype};
+  a.layout = layout;
   pa_status s = check_decode(a);
   if (s != PA_OK) return s;
   if (max_context_len < 0 || max_prefix_len < 0 || partition_tokens <= 0 || partition_tokens % block_size ||

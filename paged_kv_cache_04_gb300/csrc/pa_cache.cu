@@ -12,11 +12,19 @@
 namespace pa {
 namespace {
 
+// Row of the pool that holds (slot, kv head h): HND [blocks][G][B] rows, NHD
+// [blocks][B][G] rows (where slot * G + h is the row).
+__device__ __forceinline__ long long pool_row(long long slot, int h, int G, int BS, int nhd) {
+  if (nhd) return slot * G + h;
+  const long long blk = slot / BS, row = slot - blk * BS;
+  return (blk * G + h) * BS + row;
+}
+
 // One thread per 16-byte vector of a (token, K-or-V, kv head) row.
 __global__ void __launch_bounds__(256)
     reshape_and_cache_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value, uint4* k_cache,
                              uint4* v_cache, const int64_t* __restrict__ slot_mapping, int num_tokens, int G,
-                             int vpr, int BS, long long num_slots, unsigned* err) {
+                             int vpr, int BS, int nhd, long long num_slots, unsigned* err) {
   const long long total = (long long)num_tokens * 2 * G * vpr;
   for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
        idx += (long long)gridDim.x * blockDim.x) {
@@ -32,10 +40,9 @@ __global__ void __launch_bounds__(256)
       if (v == 0 && h == 0 && which == 0) atomicOr(err, kErrSlot);
       continue;
     }
-    const long long blk = slot / BS, row = slot - blk * BS;
     const uint4* src = which ? value : key;
     uint4* dst = which ? v_cache : k_cache;
-    dst[((blk * G + h) * BS + row) * vpr + v] = __ldg(src + (t * G + h) * vpr + v);
+    dst[pool_row(slot, h, G, BS, nhd) * vpr + v] = __ldg(src + (t * G + h) * vpr + v);
   }
 }
 
@@ -122,7 +129,8 @@ template <typename IT>
 __global__ void __launch_bounds__(256)
     reshape_and_cache_fp8_kernel(const IT* __restrict__ key, const IT* __restrict__ value, uint8_t* k_cache,
                                  uint8_t* v_cache, const int64_t* __restrict__ slot_mapping, int num_tokens, int G,
-                                 int D, int BS, long long num_slots, float k_scale, float v_scale, unsigned* err) {
+                                 int D, int BS, int nhd, long long num_slots, float k_scale, float v_scale,
+                                 unsigned* err) {
   const int cpr = D / 16;  // 16-element chunks per row
   const long long total = (long long)num_tokens * 2 * G * cpr;
   for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
@@ -148,8 +156,7 @@ __global__ void __launch_bounds__(256)
       const float a2 = __fdiv_rn(to_f32(src[4 * i + 2]), sc), a3 = __fdiv_rn(to_f32(src[4 * i + 3]), sc);
       w[i] = f32x2_to_e4m3x2(a0, a1) | (f32x2_to_e4m3x2(a2, a3) << 16);
     }
-    const long long blk = slot / BS, row = slot - blk * BS;
-    uint8_t* dst = (which ? v_cache : k_cache) + ((blk * G + h) * BS + row) * D + c * 16;
+    uint8_t* dst = (which ? v_cache : k_cache) + pool_row(slot, h, G, BS, nhd) * D + c * 16;
     *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
@@ -160,11 +167,11 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 extern "C" pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
                                           const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
-                                          int head_dim, int block_size, int64_t num_blocks, pa_dtype dtype,
-                                          cudaStream_t stream) {
+                                          int head_dim, int block_size, pa_kv_layout layout, int64_t num_blocks,
+                                          pa_dtype dtype, cudaStream_t stream) {
   using namespace pa;
   if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0 ||
-      !valid_dtype(dtype))
+      !valid_dtype(dtype) || (layout != PA_LAYOUT_HND && layout != PA_LAYOUT_NHD))
     return PA_ERR_INVALID_ARG;
   if (num_tokens == 0) return PA_OK;
   if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
@@ -184,7 +191,7 @@ extern "C" pa_status pa_reshape_and_cache(const void* key, const void* value, vo
   reshape_and_cache_kernel<<<grid, 256, 0, stream>>>(
       static_cast<const uint4*>(key), static_cast<const uint4*>(value), static_cast<uint4*>(k_cache),
       static_cast<uint4*>(v_cache), slot_mapping, num_tokens, num_kv_heads, vpr, block_size,
-      (long long)num_blocks * block_size, err);
+      layout == PA_LAYOUT_NHD ? 1 : 0, (long long)num_blocks * block_size, err);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -266,9 +273,11 @@ extern "C" pa_status pa_swap_blocks(void* const* dst_k_caches, void* const* dst_
 
 extern "C" pa_status pa_reshape_and_cache_fp8(const void* key, const void* value, void* k_cache, void* v_cache,
                                               const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
-                                              int head_dim, int block_size, int64_t num_blocks, pa_dtype in_dtype,
-                                              float k_scale, float v_scale, cudaStream_t stream) {
+                                              int head_dim, int block_size, pa_kv_layout layout,
+                                              int64_t num_blocks, pa_dtype in_dtype, float k_scale, float v_scale,
+                                              cudaStream_t stream) {
   using namespace pa;
+  if (layout != PA_LAYOUT_HND && layout != PA_LAYOUT_NHD) return PA_ERR_INVALID_ARG;
   if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0 ||
       !(in_dtype == PA_F32 || in_dtype == PA_F16 || in_dtype == PA_BF16) || !(k_scale > 0.f) ||
       !(v_scale > 0.f) || k_scale == INFINITY || v_scale == INFINITY)
@@ -288,21 +297,22 @@ extern "C" pa_status pa_reshape_and_cache_fp8(const void* key, const void* value
   uint8_t* kc = static_cast<uint8_t*>(k_cache);
   uint8_t* vc = static_cast<uint8_t*>(v_cache);
   const long long nslots = (long long)num_blocks * block_size;
+  const int nhd = layout == PA_LAYOUT_NHD ? 1 : 0;
   switch (in_dtype) {
     case PA_F32:
       reshape_and_cache_fp8_kernel<float><<<grid, 256, 0, stream>>>(
           static_cast<const float*>(key), static_cast<const float*>(value), kc, vc, slot_mapping, num_tokens,
-          num_kv_heads, head_dim, block_size, nslots, k_scale, v_scale, err);
+          num_kv_heads, head_dim, block_size, nhd, nslots, k_scale, v_scale, err);
       break;
     case PA_F16:
       reshape_and_cache_fp8_kernel<__half><<<grid, 256, 0, stream>>>(
           static_cast<const __half*>(key), static_cast<const __half*>(value), kc, vc, slot_mapping, num_tokens,
-          num_kv_heads, head_dim, block_size, nslots, k_scale, v_scale, err);
+          num_kv_heads, head_dim, block_size, nhd, nslots, k_scale, v_scale, err);
       break;
     default:
       reshape_and_cache_fp8_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
           static_cast<const __nv_bfloat16*>(key), static_cast<const __nv_bfloat16*>(value), kc, vc, slot_mapping,
-          num_tokens, num_kv_heads, head_dim, block_size, nslots, k_scale, v_scale, err);
+          num_tokens, num_kv_heads, head_dim, block_size, nhd, nslots, k_scale, v_scale, err);
   }
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

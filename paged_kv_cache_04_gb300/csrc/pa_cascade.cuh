@@ -148,13 +148,13 @@ __global__ void __launch_bounds__((kCascadeConsumers + 1) * 32)
           }
           stage_ok[stage] = 1;
           uint8_t* kdst = smem + stage * L.stage_bytes;
-          const int row = (int)((phys * p.G + it.kv) << p.block_shift) + (tok - (blk << p.block_shift));
+          const int r0 = tok - (blk << p.block_shift);
           fence_proxy_async_smem();
           mbar_arrive_expect_tx(&full[stage], 2 * TILE);
 #pragma unroll
           for (int rg = 0; rg < NREG; ++rg) {
-            tma_load_2d(kdst + rg * JT * 128, &kmap, rg * BOX_X, row, &full[stage]);
-            tma_load_2d(kdst + TILE + rg * JT * 128, &vmap, rg * BOX_X, row, &full[stage]);
+            tma_load_tile(kdst + rg * JT * 128, &kmap, p, rg * BOX_X, phys, it.kv, r0, &full[stage]);
+            tma_load_tile(kdst + TILE + rg * JT * 128, &vmap, p, rg * BOX_X, phys, it.kv, r0, &full[stage]);
           }
         }
       }

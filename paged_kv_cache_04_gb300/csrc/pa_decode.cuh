@@ -86,8 +86,22 @@ struct DecodeParams {
   int num_groups;
   int suffix_slot;
   int suffix_single;            // 1: one suffix partial per row (kModeSuffix)
+  int nhd;                      // pool layout: 0 [blocks][G][B][d], 1 [blocks][B][G][d]
   unsigned* err;
 };
+
+// TMA copy of 16 rows (tokens r0 .. r0 + 15 of physical block phys, kv head kv)
+// and 128 bytes of head_dim starting at element x, into a 16 x 128-byte
+// swizzled stage. HND pools are a 2-D map over rows ((phys * G + kv) * B + r);
+// NHD pools a 3-D map (head_dim, kv head, phys * B + r). The box lands in shared
+// memory in the same order either way, so the consumers do not see the layout.
+__device__ __forceinline__ void tma_load_tile(void* dst, const CUtensorMap* map, const DecodeParams& p, int x,
+                                              long long phys, int kv, int r0, uint64_t* bar) {
+  if (p.nhd)
+    tma_load_3d(dst, map, x, kv, (int)(phys << p.block_shift) + r0, bar);
+  else
+    tma_load_2d(dst, map, x, (int)((phys * p.G + kv) << p.block_shift) + r0, bar);
+}
 
 struct SmemLayout {
   unsigned stage_bytes, bars_off, ok_off, merge_off, q_off, sched_off, misc_off, total;
@@ -403,13 +417,13 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
         my_ok[stage] = 1;
         uint8_t* kdst = my_stages + stage * L.stage_bytes;
         uint8_t* vdst = kdst + TILE;
-        const int row = (int)((phys * p.G + c.it.kv) << p.block_shift) + (tok - (blk << p.block_shift));
+        const int r0 = tok - (blk << p.block_shift);
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(bar, 2 * TILE);
 #pragma unroll
         for (int rg = 0; rg < NREG; ++rg) {
-          tma_load_2d(kdst + rg * JT * 128, &kmap, rg * BOX_X, row, bar);
-          tma_load_2d(vdst + rg * JT * 128, &vmap, rg * BOX_X, row, bar);
+          tma_load_tile(kdst + rg * JT * 128, &kmap, p, rg * BOX_X, phys, c.it.kv, r0, bar);
+          tma_load_tile(vdst + rg * JT * 128, &vmap, p, rg * BOX_X, phys, c.it.kv, r0, bar);
         }
       }
     }

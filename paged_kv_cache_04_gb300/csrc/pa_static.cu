@@ -40,13 +40,13 @@ pa_status scratch_address(void** out) {
 extern "C" pa_status pa_decode_split_static(void* out, const void* q, const void* k_cache, const void* v_cache,
                                             const int32_t* block_tables, int max_blocks_per_seq,
                                             const int32_t* context_lens, int num_seqs, int num_heads,
-                                            int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
-                                            float scale, pa_dtype dtype, pa_dtype out_dtype, int max_context_len,
+                                            int num_kv_heads, int head_dim, int block_size, pa_kv_layout layout,
+                                            int64_t num_blocks, float scale, pa_dtype dtype, pa_dtype out_dtype, int max_context_len,
                                             int partition_tokens, cudaStream_t stream) {
   if (num_seqs == 0)  // nothing to compute: the regular entry point checks the rest and returns
     return pa_decode_split(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
-                           num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, out_dtype,
-                           max_context_len, partition_tokens, nullptr, 0, stream);
+                           num_heads, num_kv_heads, head_dim, block_size, layout, num_blocks, scale, dtype,
+                           out_dtype, max_context_len, partition_tokens, nullptr, 0, stream);
   const size_t need =
       pa_decode_split_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len, partition_tokens);
   if (need == 0) return PA_ERR_INVALID_ARG;
@@ -57,6 +57,7 @@ extern "C" pa_status pa_decode_split_static(void* out, const void* q, const void
   // Nothing in the scratch has to start at zero: the first launch writes every
   // partition entry that the second launch reads.
   return pa_decode_split(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
-                         num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, out_dtype,
-                         max_context_len, partition_tokens, scratch, (size_t)PA_STATIC_SCRATCH_BYTES, stream);
+                         num_heads, num_kv_heads, head_dim, block_size, layout, num_blocks, scale, dtype,
+                         out_dtype, max_context_len, partition_tokens, scratch, (size_t)PA_STATIC_SCRATCH_BYTES,
+                         stream);
 }

@@ -60,14 +60,15 @@ class Workload:
     context_lens: torch.Tensor  # int32 [S], includes the new token
     block_tables: torch.Tensor  # int32 [S, max_blocks], -1 past the last used entry
     q: torch.Tensor             # [S, H, d]
-    k_cache: torch.Tensor       # [num_blocks, G, B, d]  (HND)
-    v_cache: torch.Tensor       # [num_blocks, G, B, d]
+    k_cache: torch.Tensor       # [num_blocks, G, B, d] (HND) or [num_blocks, B, G, d] (NHD)
+    v_cache: torch.Tensor       # same layout as k_cache
     new_key: Optional[torch.Tensor] = None     # [N, G, d]
     new_value: Optional[torch.Tensor] = None   # [N, G, d]
     slot_mapping: Optional[torch.Tensor] = None  # int64 [N]
     copy_pairs: Optional[torch.Tensor] = None    # int64 [P, 2] (src, dst)
     partition_tokens: Optional[int] = None
     meta: dict = field(default_factory=dict)
+    layout: str = "HND"         # pool layout of k_cache / v_cache
 
     @property
     def max_blocks(self) -> int:
@@ -84,7 +85,7 @@ class Workload:
                         self.num_blocks, self.scale, mv(self.context_lens), mv(self.block_tables),
                         mv(self.q), mv(self.k_cache), mv(self.v_cache), mv(self.new_key),
                         mv(self.new_value), mv(self.slot_mapping), mv(self.copy_pairs),
-                        self.partition_tokens, dict(self.meta))
+                        self.partition_tokens, dict(self.meta), self.layout)
 
 
 # ---------------------------------------------------------------------------
@@ -305,7 +306,25 @@ def to_fp8(wl: Workload, k_scale=None, v_scale=None) -> Workload:
     meta.update(k_scale=ks, v_scale=vs, kv_dtype="fp8_e4m3")
     return Workload(wl.name + "_fp8", wl.S, wl.H, wl.G, wl.d, wl.B, wl.dtype, wl.num_blocks, wl.scale,
                     wl.context_lens, wl.block_tables, wl.q, codes(wl.k_cache, ks), codes(wl.v_cache, vs),
-                    wl.new_key, wl.new_value, wl.slot_mapping, wl.copy_pairs, wl.partition_tokens, meta)
+                    wl.new_key, wl.new_value, wl.slot_mapping, wl.copy_pairs, wl.partition_tokens, meta,
+                    wl.layout)
+
+
+def to_nhd(wl: Workload) -> Workload:
+    """The same batch with its pools stored NHD, [num_blocks, B, G, d]: the same
+    values, each block's token and head axes exchanged."""
+    if wl.layout != "HND":
+        raise ValueError("to_nhd expects an HND workload")
+
+    def nhd(t):
+        out = torch.empty((t.shape[0], t.shape[2], t.shape[1], t.shape[3]), dtype=t.dtype, device=t.device)
+        for r in range(0, t.shape[0], 8192):
+            out[r:r + 8192].copy_(t[r:r + 8192].transpose(1, 2))
+        return out
+    return Workload(wl.name + "_nhd", wl.S, wl.H, wl.G, wl.d, wl.B, wl.dtype, wl.num_blocks, wl.scale,
+                    wl.context_lens, wl.block_tables, wl.q, nhd(wl.k_cache), nhd(wl.v_cache),
+                    wl.new_key, wl.new_value, wl.slot_mapping, wl.copy_pairs, wl.partition_tokens,
+                    dict(wl.meta), "NHD")
 
 
 def by_name(name: str, device="cpu", **kw) -> Workload:

@@ -39,7 +39,7 @@ def gpu_step(pa, wl, out_dtype=None, split=False, partition=None, workspace=None
         pa.pa_copy_blocks([wl.k_cache], [wl.v_cache], wl.copy_pairs, stream=stream)
     if wl.slot_mapping is not None:
         pa.pa_reshape_and_cache(wl.new_key, wl.new_value, wl.k_cache, wl.v_cache, wl.slot_mapping,
-                                stream=stream)
+                                stream=stream, layout=wl.layout)
     out = torch.empty(wl.q.shape, dtype=out_dtype or wl.dtype, device=wl.q.device)
     if split:
         T = partition or wl.partition_tokens or 512
@@ -48,10 +48,10 @@ def gpu_step(pa, wl, out_dtype=None, split=False, partition=None, workspace=None
             nbytes = pa.pa_decode_split_workspace_bytes(wl.S, wl.H, wl.d, mctx, T)
             workspace = torch.empty(nbytes, dtype=torch.uint8, device=wl.q.device)
         pa.pa_decode_split(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale,
-                           mctx, T, workspace, stream=stream)
+                           mctx, T, workspace, stream=stream, layout=wl.layout)
     else:
         pa.pa_decode(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale,
-                     stream=stream)
+                     stream=stream, layout=wl.layout)
     return out
 
 
@@ -100,7 +100,7 @@ class Pristine:
                     nslots.append(remap[sl // B] * B + sl % B)
             kt = torch.tensor(keep, dtype=torch.long)
             self.new = (wl.new_key.cpu()[kt], wl.new_value.cpu()[kt], torch.tensor(nslots, dtype=torch.int64))
-        self.B, self.scale, self.dtype = B, wl.scale, wl.dtype
+        self.B, self.scale, self.dtype, self.layout = B, wl.scale, wl.dtype, wl.layout
 
     def caches_after_writes(self):
         """Oracle: CoW copies, then new-token writes, on the host copies (bit patterns)."""
@@ -109,17 +109,18 @@ class Pristine:
             ks, vs = oracle.copy_blocks([k], [v], self.pairs)
             k, v = _from_bits(ks[0], self.dtype), _from_bits(vs[0], self.dtype)
         if self.new is not None:
-            kb, vb = oracle.reshape_and_cache(self.new[0], self.new[1], k, v, self.new[2])
+            kb, vb = oracle.reshape_and_cache(self.new[0], self.new[1], k, v, self.new[2], layout=self.layout)
             k, v = _from_bits(kb, self.dtype), _from_bits(vb, self.dtype)
         return k, v
 
     def decode(self, num_threads=0):
         k, v = self.caches_after_writes()
-        return oracle.decode(self.q, k, v, self.bt, self.ctx, self.scale, num_threads=num_threads)
+        return oracle.decode(self.q, k, v, self.bt, self.ctx, self.scale, num_threads=num_threads,
+                             layout=self.layout)
 
     def partitions(self, T):
         k, v = self.caches_after_writes()
-        return oracle.partitions(self.q, k, v, self.bt, self.ctx, self.scale, T)
+        return oracle.partitions(self.q, k, v, self.bt, self.ctx, self.scale, T, layout=self.layout)
 
 
 def _from_bits(bits, dtype):
@@ -143,7 +144,8 @@ def poison_free_slots(wl, value=float("nan")):
         live[bt[s, :n].long()] = True
         tail = c - (n - 1) * B
         live[int(bt[s, n - 1]), tail:] = False
-    mask = (~live).to(wl.k_cache.device).view(wl.num_blocks, 1, B, 1)
+    shape = (wl.num_blocks, 1, B, 1) if wl.layout == "HND" else (wl.num_blocks, B, 1, 1)
+    mask = (~live).to(wl.k_cache.device).view(*shape)
     wl.k_cache.masked_fill_(mask, value)
     wl.v_cache.masked_fill_(mask, value)
 

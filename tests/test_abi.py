@@ -56,29 +56,34 @@ def test_invalid_arguments_rejected_before_any_launch(lib_path):
     lib = pa.library()
     null = ctypes.c_void_p(0)
     # H % G != 0
-    assert lib.pa_decode(null, null, null, null, null, 1, null, 1, 6, 4, 128, 16, 10, 1.0, 2, 2, null) == 1
+    assert lib.pa_decode(null, null, null, null, null, 1, null, 1, 6, 4, 128, 16, 0, 10, 1.0, 2, 2, null) == 1
     # num_seqs == 0 is a no-op
-    assert lib.pa_decode(null, null, null, null, null, 1, null, 0, 8, 8, 128, 16, 10, 1.0, 2, 2, null) == 0
+    assert lib.pa_decode(null, null, null, null, null, 1, null, 0, 8, 8, 128, 16, 0, 10, 1.0, 2, 2, null) == 0
     # null pointers
-    assert lib.pa_decode(null, null, null, null, null, 1, null, 2, 8, 8, 128, 16, 10, 1.0, 2, 2, null) == 1
+    assert lib.pa_decode(null, null, null, null, null, 1, null, 2, 8, 8, 128, 16, 0, 10, 1.0, 2, 2, null) == 1
     # misaligned pointers are rejected before the shape checks launch anything
     odd = ctypes.c_void_p(0x1008)
-    assert lib.pa_decode(odd, odd, odd, odd, odd, 1, odd, 2, 8, 8, 128, 16, 10, 1.0, 2, 2, null) == 1
+    assert lib.pa_decode(odd, odd, odd, odd, odd, 1, odd, 2, 8, 8, 128, 16, 0, 10, 1.0, 2, 2, null) == 1
     # unsupported head_dim / block size / group
     al = ctypes.c_void_p(0x10000)
-    assert lib.pa_decode(al, al, al, al, al, 1, al, 2, 8, 8, 96, 16, 10, 1.0, 2, 2, null) == 2
-    assert lib.pa_decode(al, al, al, al, al, 1, al, 2, 8, 8, 128, 8, 10, 1.0, 2, 2, null) == 2
-    assert lib.pa_decode(al, al, al, al, al, 1, al, 2, 32, 2, 128, 16, 10, 1.0, 2, 2, null) == 2
+    assert lib.pa_decode(al, al, al, al, al, 1, al, 2, 8, 8, 96, 16, 0, 10, 1.0, 2, 2, null) == 2
+    assert lib.pa_decode(al, al, al, al, al, 1, al, 2, 8, 8, 128, 8, 0, 10, 1.0, 2, 2, null) == 2
+    assert lib.pa_decode(al, al, al, al, al, 1, al, 2, 32, 2, 128, 16, 0, 10, 1.0, 2, 2, null) == 2
     # out dtype must be the cache dtype or fp32
-    assert lib.pa_decode(al, al, al, al, al, 1, al, 2, 8, 8, 128, 16, 10, 1.0, 2, 1, null) == 2
+    assert lib.pa_decode(al, al, al, al, al, 1, al, 2, 8, 8, 128, 16, 0, 10, 1.0, 2, 1, null) == 2
     # split: partition not a multiple of the block size; workspace too small
-    assert lib.pa_decode_split(al, al, al, al, al, 1, al, 2, 8, 8, 128, 16, 10, 1.0, 2, 2, 100, 24, al, 1 << 20,
+    assert lib.pa_decode_split(al, al, al, al, al, 1, al, 2, 8, 8, 128, 16, 0, 10, 1.0, 2, 2, 100, 24, al, 1 << 20,
                                null) == 1
-    assert lib.pa_decode_split(al, al, al, al, al, 1, al, 2, 8, 8, 128, 16, 10, 1.0, 2, 2, 100, 32, al, 16,
+    assert lib.pa_decode_split(al, al, al, al, al, 1, al, 2, 8, 8, 128, 16, 0, 10, 1.0, 2, 2, 100, 32, al, 16,
                                null) == 1
     # reshape_and_cache: zero tokens is a no-op; misaligned slot mapping rejected
-    assert lib.pa_reshape_and_cache(null, null, null, null, null, 0, 8, 128, 16, 10, 2, null) == 0
-    assert lib.pa_reshape_and_cache(al, al, al, al, ctypes.c_void_p(0x10004), 4, 8, 128, 16, 10, 2, null) == 1
+    assert lib.pa_reshape_and_cache(null, null, null, null, null, 0, 8, 128, 16, 0, 10, 2, null) == 0
+    assert lib.pa_reshape_and_cache(al, al, al, al, ctypes.c_void_p(0x10004), 4, 8, 128, 16, 0, 10, 2, null) == 1
+    # a pool layout other than HND (0) and NHD (1) is rejected, even with nothing to do
+    assert lib.pa_decode(null, null, null, null, null, 1, null, 0, 8, 8, 128, 16, 2, 10, 1.0, 2, 2, null) == 1
+    assert lib.pa_reshape_and_cache(null, null, null, null, null, 0, 8, 128, 16, 7, 10, 2, null) == 1
+    assert lib.pa_reshape_and_cache_fp8(null, null, null, null, null, 0, 8, 128, 16, -1, 10, 2, 1.0, 1.0,
+                                        null) == 1
     # copy_blocks: no pairs is a no-op
     arr = (ctypes.c_void_p * 1)(0x10000)
     assert lib.pa_copy_blocks(arr, arr, 1, al, 0, 8, 128, 16, 10, 2, null) == 0

@@ -30,14 +30,18 @@ ORACLE_SRC = os.path.join(os.path.dirname(oracle.__file__), "pa_oracle.c")
 # ---------------------------------------------------------------------------
 # helpers (test-side): scatter a contiguous K/V into a shuffled block pool
 # ---------------------------------------------------------------------------
-def paged_from_contiguous(Ks, Vs, B, rng, extra_blocks=3, fill=np.nan):
-    """Ks, Vs: lists of float32 arrays [ctx, G, d]. Returns (k_cache, v_cache, block_tables)."""
+def paged_from_contiguous(Ks, Vs, B, rng, extra_blocks=3, fill=np.nan, layout="HND"):
+    """Ks, Vs: lists of float32 arrays [ctx, G, d]. Returns (k_cache, v_cache, block_tables).
+
+    layout "HND" gives pools [nb, G, B, d]; "NHD" gives [nb, B, G, d].
+    """
     G, d = Ks[0].shape[1], Ks[0].shape[2]
     nblk = [-(-K.shape[0] // B) for K in Ks]
     nb = sum(nblk) + extra_blocks
     perm = rng.permutation(nb)
-    k_cache = np.full((nb, G, B, d), fill, dtype=np.float32)
-    v_cache = np.full((nb, G, B, d), fill, dtype=np.float32)
+    shape = (nb, G, B, d) if layout == "HND" else (nb, B, G, d)
+    k_cache = np.full(shape, fill, dtype=np.float32)
+    v_cache = np.full(shape, fill, dtype=np.float32)
     width = max(1, max(nblk))
     bt = np.full((len(Ks), width), -1, dtype=np.int32)
     nxt = 0
@@ -50,8 +54,9 @@ def paged_from_contiguous(Ks, Vs, B, rng, extra_blocks=3, fill=np.nan):
                 t = j * B + r
                 if t < K.shape[0]:
                     for h in range(G):
-                        k_cache[phys, h, r, :] = K[t, h, :]
-                        v_cache[phys, h, r, :] = V[t, h, :]
+                        idx = (phys, h, r) if layout == "HND" else (phys, r, h)
+                        k_cache[idx] = K[t, h, :]
+                        v_cache[idx] = V[t, h, :]
     return k_cache, v_cache, bt
 
 
@@ -91,6 +96,24 @@ def pin_paged_equals_contiguous(lib):
                 ref = sdpa_reference(q[s], Ks[s], Vs[s], scale)
                 err = np.abs(out[s] - ref).max()
                 assert err <= 1e-12, f"paged != contiguous (H={H} G={G} B={B} s={s}): {err}"
+
+
+def pin_nhd_paged_equals_contiguous(lib):
+    """NHD pools (Month 2 · PagedAttention §5.2) give the contiguous result too,
+    for the plain and the partitioned oracle; G != B and G == B both occur."""
+    rng = np.random.default_rng(19)
+    ctxs = [1, 4, 9, 33, 70]
+    for H, G, B in ((8, 2, 4), (4, 4, 4), (8, 8, 16)):
+        q, Ks, Vs = random_case(rng, ctxs, H, G, 16)
+        kc, vc, bt = paged_from_contiguous(Ks, Vs, B, rng, layout="NHD")
+        cl = np.array(ctxs, np.int32)
+        out = oatt.decode(q, kc, vc, bt, cl, 0.41, lib=lib, layout="NHD")
+        o, m, l = oatt.partitions(q, kc, vc, bt, cl, 0.41, 2 * B, lib=lib, layout="NHD")
+        merged = oatt.merge(o, m, l, lib=lib)
+        for s in range(len(ctxs)):
+            ref = sdpa_reference(q[s], Ks[s], Vs[s], 0.41)
+            assert np.abs(out[s] - ref).max() <= 1e-12, f"NHD paged != contiguous (G={G} B={B} s={s})"
+            assert np.abs(merged[s] - ref).max() <= 1e-12, f"NHD partitions != contiguous (G={G} B={B})"
 
 
 def pin_one_token_is_v(lib):
@@ -211,7 +234,7 @@ def pin_empty_context_is_zero(lib):
     assert np.array_equal(out[0], np.zeros_like(out[0]))
 
 
-PINS = [pin_paged_equals_contiguous, pin_one_token_is_v, pin_equal_scores_give_mean,
+PINS = [pin_paged_equals_contiguous, pin_nhd_paged_equals_contiguous, pin_one_token_is_v, pin_equal_scores_give_mean,
         pin_weights_sum_to_one, pin_brute_force_tiny, pin_decoders, pin_16bit_paths_match_upcast,
         pin_partitions_merge_to_decode, pin_empty_context_is_zero]
 
@@ -270,6 +293,37 @@ def test_unmutated_battery_passes(tmp_path):
     shutil.copy(ORACLE_SRC, p)
     lib = oatt.load_variant(str(p), str(tmp_path / "copy.so"))
     assert _run_battery(lib) == []
+
+
+def test_dropped_nhd_transpose_is_caught(monkeypatch):
+    """Planted mistake in the oracle's layout handling: reading an NHD pool as if
+    it were HND must fail the NHD pin."""
+    monkeypatch.setattr(oatt, "_hnd", lambda a, layout: a)
+    with pytest.raises((AssertionError, ValueError)):
+        pin_nhd_paged_equals_contiguous(oatt._load())
+
+
+def test_nhd_cache_write_places_rows():
+    """NHD cache write: token t lands at [slot // B, slot % B, h, :]; the HND
+    write of the same tokens holds the same rows with axes 1 and 2 exchanged."""
+    from oracle import cache_ops
+    rng = np.random.default_rng(20)
+    N, G, B, d, nb = 7, 3, 4, 8, 5
+    key = rng.standard_normal((N, G, d)).astype(np.float32)
+    val = rng.standard_normal((N, G, d)).astype(np.float32)
+    slots = np.array([0, 5, 19, -1, 7, 12, 3], np.int64)
+    zh = np.zeros((nb, G, B, d), np.float32)
+    zn = np.zeros((nb, B, G, d), np.float32)
+    kh, vh = cache_ops.reshape_and_cache(key, val, zh, zh, slots)
+    kn, vn = cache_ops.reshape_and_cache(key, val, zn, zn, slots, layout="NHD")
+    for t, sl in enumerate(slots):
+        if sl < 0:
+            continue
+        b, r = divmod(int(sl), B)
+        assert np.array_equal(kn[b, r].view(np.float32), key[t])
+        assert np.array_equal(vn[b, r].view(np.float32), val[t])
+    assert np.array_equal(kn, kh.transpose(0, 2, 1, 3)) and np.array_equal(vn, vh.transpose(0, 2, 1, 3))
+    assert np.count_nonzero(kn.view(np.float32)) == 6 * G * d
 
 
 def test_oracle_rejects_out_of_range_block():
