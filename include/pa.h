@@ -211,7 +211,7 @@ pa_status pa_decode_split_static(void* out, const void* q, const void* k_cache, 
  *      of the group's query rows at once, so a prefix block is read once per
  *      group instead of once per member;
  *   2. each sequence's own tokens [prefix, context) as one partial per
- *      (sequence, head), scheduled like pa_decode (longest first);
+ *      (sequence, head), one warp per (sequence, kv head), longest first;
  *   3. the log-sum-exp reduce of both.
  * Arguments as pa_decode_split, plus (device int32 arrays):
  *   group_starts  [num_groups + 1], group_starts[0] = 0, non-decreasing,

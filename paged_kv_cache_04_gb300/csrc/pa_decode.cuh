@@ -199,10 +199,13 @@ struct Schedule {
   const int* pstart;      // split mode: first item of each sequence, [S + 1]
   int num_items;
 
-  // k-th item of this CTA (serpentine deal over the grid), as seen by `warp`.
+  // k-th item of this CTA (serpentine deal over the grid), as seen by `warp`. The
+  // suffix pass deals items to warps (each warp attends one sequence's short tail
+  // alone and writes its partial), the other modes to whole CTAs.
   __device__ __forceinline__ bool get(const DecodeParams& p, int k, int warp, Item& it) const {
     const int pos = (k & 1) ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x;
-    const long long i = (long long)k * gridDim.x + pos;
+    const long long i = MODE == kModeSuffix ? ((long long)k * gridDim.x + pos) * W + warp
+                                            : (long long)k * gridDim.x + pos;
     if (i >= num_items) return false;
     const int ii = (int)i;
     it.kv = ii % p.G;
@@ -247,6 +250,8 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
   constexpr bool SPLIT = MODE == kModeSplit;
   constexpr bool SUFFIX = MODE == kModeSuffix;
   constexpr bool F8 = std::is_same<DT, fp8e4m3>::value;
+  constexpr bool PAIR = F8 && !SPLIT;  // tensor-core path: two jobs per softmax step
+  static_assert(!PAIR || StageCfg<DT, D, PATH>::R >= 2, "two jobs per step need two stages");
   using MT = typename std::conditional<F8, __half, DT>::type;  // tensor-core operand type
   static_assert(!F8 || D % 64 == 0, "FP8 caches need head_dim a multiple of 64");
   constexpr int W = Cfg::W, R = Cfg::R, E = Cfg::E, TILE = Cfg::TILE, JT = kJobTokens;
@@ -372,7 +377,8 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
   uint8_t* my_stages = smem + warp * R * L.stage_bytes;
   uint64_t* my_bars = bars + warp * R;
   volatile uint8_t* my_ok = stage_ok + warp * R;
-  constexpr bool WARP_PARTS = SPLIT;  // split mode: each warp owns whole partitions
+  // split mode: each warp owns whole partitions; suffix mode: each warp owns items
+  constexpr bool WARP_PARTS = SPLIT || SUFFIX;
   const int job_step = WARP_PARTS ? 1 : W;
 
   struct Cursor {
@@ -443,9 +449,11 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
   // ---- consume -----------------------------------------------------------------
   int n_done = 0;
   const float NEG_INF = -__int_as_float(0x7f800000);
-  auto next_job = [&](int& stage_out) -> bool {  // wait for this warp's next job
-    stage_out = n_done % R;
-    bool ok = mbar_wait_bounded(&my_bars[stage_out], (n_done / R) & 1, abort_flag, p.err, kWaitLimitNs);
+  // wait for this warp's next job (ahead = 1: the one after it, still unreleased)
+  auto next_job = [&](int& stage_out, int ahead) -> bool {
+    const int n = n_done + ahead;
+    stage_out = n % R;
+    bool ok = mbar_wait_bounded(&my_bars[stage_out], (n / R) & 1, abort_flag, p.err, kWaitLimitNs);
     ok = __all_sync(0xffffffffu, ok);
     return ok && my_ok[stage_out];
   };
@@ -479,17 +487,8 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
           O = fmaf(mrg_o[(w * p.group + h) * D + i], f, O);
         }
       }
-      if (SUFFIX) {
-        const long long row = ((long long)x.s * p.H + hq0 + h) * p.max_partitions + x.part;
-        p.ws_o[row * D + i] = Lsum > 0.f ? O * p.v_scale / Lsum : 0.f;
-        if (i == 0) {
-          p.ws_m[row] = M;
-          p.ws_l[row] = Lsum;
-        }
-      } else {
-        reinterpret_cast<OT*>(p.out)[((long long)x.s * p.H + hq0 + h) * D + i] =
-            from_f32<OT>(Lsum > 0.f ? O * p.v_scale / Lsum : 0.f);
-      }
+      reinterpret_cast<OT*>(p.out)[((long long)x.s * p.H + hq0 + h) * D + i] =
+          from_f32<OT>(Lsum > 0.f ? O * p.v_scale / Lsum : 0.f);
     }
     asm volatile("bar.sync 1, %0;" ::"n"(W * 32) : "memory");
   };
@@ -550,67 +549,150 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
       for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
       float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
       const int ub = it.t0 / JT + (WARP_PARTS ? 0 : warp), ue = (it.t1 + JT - 1) / JT;
-#pragma unroll 1
-      for (int u = ub; u < ue; u += job_step) {
-        int stage;
-        if (next_job(stage)) {
-          const uint32_t kt = smem_u32(my_stages + stage * L.stage_bytes);
-          const uint32_t vt = kt + TILE;
-          const int nv = min(JT, it.t1 - u * JT);
-          // two independent accumulator chains over head_dim halve the MMA latency chain
-          float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
-          const uint8_t* ktp = my_stages + stage * L.stage_bytes;
-          if constexpr (F8) {
+      // Scores of one job: z[e] = scale_log2 * q . k for token tr(g + 8 (e >> 1)),
+      // head 2 t4 + (e & 1); NEG_INF past the context.
+      auto job_scores = [&](const uint8_t* ktp, int nv, float (&z)[4]) {
+        const uint32_t kt = smem_u32(ktp);
+        // two independent accumulator chains over head_dim halve the MMA latency chain
+        float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
+        if constexpr (F8) {
 #pragma unroll
-            for (int kb = 0; kb < D / 64; ++kb) {
-              const uint4 r0 = *reinterpret_cast<const uint4*>(ktp + sw128_offset(tr(g), 4 * kb + t4, JT));
-              const uint4 r1 = *reinterpret_cast<const uint4*>(ktp + sw128_offset(tr(g + 8), 4 * kb + t4, JT));
-              const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w}, w1[4] = {r1.x, r1.y, r1.z, r1.w};
+          for (int kb = 0; kb < D / 64; ++kb) {
+            const uint4 r0 = *reinterpret_cast<const uint4*>(ktp + sw128_offset(tr(g), 4 * kb + t4, JT));
+            const uint4 r1 = *reinterpret_cast<const uint4*>(ktp + sw128_offset(tr(g + 8), 4 * kb + t4, JT));
+            const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w}, w1[4] = {r1.x, r1.y, r1.z, r1.w};
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                uint32_t a[4];
-                e4m3x4_to_f16x2x2(w0[j], a[0], a[2]);
-                e4m3x4_to_f16x2x2(w1[j], a[1], a[3]);
-                const int ks = 4 * kb + j;
-                Mma<MT>::run((j & 1) ? sd : sc, a, qf[ks][0], qf[ks][1]);
-              }
-            }
-          } else {
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ks += 2) {
-              uint32_t a[4], b[4];
-              ldsm_x4(a, kt + sw128_offset(lane & 15, ks * 2 + (lane >> 4), JT));
-              ldsm_x4(b, kt + sw128_offset(lane & 15, ks * 2 + 2 + (lane >> 4), JT));
-              Mma<MT>::run(sc, a, qf[ks][0], qf[ks][1]);
-              Mma<MT>::run(sd, b, qf[ks + 1][0], qf[ks + 1][1]);
+            for (int j = 0; j < 4; ++j) {
+              uint32_t a[4];
+              e4m3x4_to_f16x2x2(w0[j], a[0], a[2]);
+              e4m3x4_to_f16x2x2(w1[j], a[1], a[3]);
+              const int ks = 4 * kb + j;
+              Mma<MT>::run((j & 1) ? sd : sc, a, qf[ks][0], qf[ks][1]);
             }
           }
+        } else {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) sc[e] += sd[e];
-          // sc[e]: token g + 8*(e>>1), head 2*t4 + (e&1)
-          float mx0 = NEG_INF, mx1 = NEG_INF;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int tok = tr(g + ((e >> 1) << 3));
-            const float z = tok < nv ? sc[e] * p.scale_log2 : NEG_INF;
-            sc[e] = z;
-            if (e & 1) mx1 = fmaxf(mx1, z); else mx0 = fmaxf(mx0, z);
+          for (int ks = 0; ks < D / 16; ks += 2) {
+            uint32_t a[4], b[4];
+            ldsm_x4(a, kt + sw128_offset(lane & 15, ks * 2 + (lane >> 4), JT));
+            ldsm_x4(b, kt + sw128_offset(lane & 15, ks * 2 + 2 + (lane >> 4), JT));
+            Mma<MT>::run(sc, a, qf[ks][0], qf[ks][1]);
+            Mma<MT>::run(sd, b, qf[ks + 1][0], qf[ks + 1][1]);
           }
+        }
 #pragma unroll
-          for (int o2 = 4; o2 < 32; o2 <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o2));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o2));
+        for (int e = 0; e < 4; ++e) {
+          const int tok = tr(g + ((e >> 1) << 3));
+          z[e] = tok < nv ? (sc[e] + sd[e]) * p.scale_log2 : NEG_INF;
+        }
+      };
+      // P V of one job into o. P (this job's weights w, same order as z) enters as a
+      // 16-bit operand (both operands of one MMA share a type). Rounding P to bf16
+      // alone costs up to 2^-9 relative per weight, too coarse for a 2e-3 bound when
+      // a few tokens dominate, so P is split into hi + lo 16-bit parts (P - hi - lo
+      // is below 2^-17 P) and each part gets its own MMA into the same accumulator.
+      auto job_pv = [&](const uint8_t* ktp, int nv, const float (&w)[4]) {
+        const uint32_t h01 = Mma<MT>::pack(w[0], w[1]);
+        const uint32_t h23 = Mma<MT>::pack(w[2], w[3]);
+        float r0, r1, r2, r3;
+        unpack2(h01, (MT*)nullptr, r0, r1);
+        unpack2(h23, (MT*)nullptr, r2, r3);
+        const uint32_t b0 = movmatrix_trans(h01);
+        const uint32_t b1 = movmatrix_trans(h23);
+        const uint32_t e0 = movmatrix_trans(Mma<MT>::pack(w[0] - r0, w[1] - r1));
+        const uint32_t e1 = movmatrix_trans(Mma<MT>::pack(w[2] - r2, w[3] - r3));
+        // tokens held by this lane's A fragments: lo pair (a0, a1), hi pair (a2, a3);
+        // rows past the context are zeroed so that 0 * (stale or NaN) cannot leak in
+        const int tlo = 2 * t4;
+        const uint32_t mlo = (tr(tlo) < nv ? 0x0000ffffu : 0u) | (tr(tlo + 1) < nv ? 0xffff0000u : 0u);
+        const uint32_t mhi = (tr(tlo + 8) < nv ? 0x0000ffffu : 0u) | (tr(tlo + 9) < nv ? 0xffff0000u : 0u);
+        const bool full = nv == JT;  // every job but a sequence's last: no rows to mask
+        if constexpr (F8) {
+          // V^T fragments straight from the codes. The A fragment of m-tile mt
+          // pairs, per register, two tokens at one head_dim index: k = 2 t4, 2 t4 + 1
+          // (a0, a1) or 2 t4 + 8, 2 t4 + 9 (a2, a3), i.e. token rows t4 + 4j
+          // (j = 0..3) in the tr() order. The lane reads 16 bytes (chunk vchunk(g))
+          // of each of those four rows, interleaves two rows' bytes with one byte
+          // permute and converts the pairs: accumulator row r of m-tile mt is head_dim
+          // 16 vchunk(r & 7) + 2 mt + (r >> 3) (see drow()). vchunk puts lanes g and
+          // g + 1 in opposite halves of the row, so a quarter-warp reads 8 bank groups.
+          static_assert(!F8 || D == 128, "the FP8 V fragments cover 128 head_dim bytes");
+          const uint8_t* vtp = ktp + TILE;
+          const int vch = ((g & 1) << 2) | (g >> 1);
+          uint4 rv[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            rv[j] = *reinterpret_cast<const uint4*>(vtp + sw128_offset(t4 + 4 * j, vch, JT));
+          auto word = [](const uint4& v, int i) -> uint32_t {
+            return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+          };
+#pragma unroll
+          for (int mt = 0; mt < D / 16; ++mt) {
+            // bytes 2 mt, 2 mt + 1 of two rows, interleaved row by row
+            const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+            uint32_t a[4];
+            e4m3x4_to_f16x2x2(__byte_perm(word(rv[0], mt >> 1), word(rv[1], mt >> 1), sel), a[0], a[1]);
+            e4m3x4_to_f16x2x2(__byte_perm(word(rv[2], mt >> 1), word(rv[3], mt >> 1), sel), a[2], a[3]);
+            if (!full) {
+              a[0] &= mlo;
+              a[1] &= mlo;
+              a[2] &= mhi;
+              a[3] &= mhi;
+            }
+            Mma<MT>::run(o[mt], a, b0, b1);
+            Mma<MT>::run(o[mt], a, e0, e1);
           }
-          const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-          const float c0 = exp2f(m0 - mn0), c1 = exp2f(m1 - mn1);
-          m0 = mn0;
-          m1 = mn1;
-          sc[0] = exp2f(sc[0] - mn0);
-          sc[1] = exp2f(sc[1] - mn1);
-          sc[2] = exp2f(sc[2] - mn0);
-          sc[3] = exp2f(sc[3] - mn1);
-          l0 = l0 * c0 + sc[0] + sc[2];
-          l1 = l1 * c1 + sc[1] + sc[3];
+        } else {
+          const uint32_t vt = smem_u32(ktp) + TILE;
+          const int vtok = ((lane >> 4) << 3) + (lane & 7);
+#pragma unroll
+          for (int mt = 0; mt < D / 16; ++mt) {
+            uint32_t a[4];
+            ldsm_x4_trans(a, vt + sw128_offset(vtok, mt * 2 + ((lane >> 3) & 1), JT));
+            if (!full) {
+              a[0] &= mlo;
+              a[1] &= mlo;
+              a[2] &= mhi;
+              a[3] &= mhi;
+            }
+            Mma<MT>::run(o[mt], a, b0, b1);
+            Mma<MT>::run(o[mt], a, e0, e1);
+          }
+        }
+      };
+      // Online-softmax step over N jobs' scores: update the running max (m0, m1)
+      // and sums (l0, l1), rescale o if a max grew, turn z into weights in place.
+      auto softmax_step = [&](float (*z)[4], int N) {
+        float mx0 = NEG_INF, mx1 = NEG_INF;
+#pragma unroll
+        for (int n = 0; n < N; ++n) {
+          mx0 = fmaxf(mx0, fmaxf(z[n][0], z[n][2]));
+          mx1 = fmaxf(mx1, fmaxf(z[n][1], z[n][3]));
+        }
+#pragma unroll
+        for (int o2 = 4; o2 < 32; o2 <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o2));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o2));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        // the accumulators need rescaling only when some head's running max grew
+        // (otherwise the factor is exactly 1); after the first jobs it seldom does
+        const bool grew = __any_sync(0xffffffffu, (mn0 != m0) | (mn1 != m1));
+        const float c0 = exp2f(m0 - mn0), c1 = exp2f(m1 - mn1);
+        m0 = mn0;
+        m1 = mn1;
+        l0 *= c0;
+        l1 *= c1;
+#pragma unroll
+        for (int n = 0; n < N; ++n) {
+          z[n][0] = exp2f(z[n][0] - mn0);
+          z[n][1] = exp2f(z[n][1] - mn1);
+          z[n][2] = exp2f(z[n][2] - mn0);
+          z[n][3] = exp2f(z[n][3] - mn1);
+          l0 += z[n][0] + z[n][2];
+          l1 += z[n][1] + z[n][3];
+        }
+        if (grew) {
 #pragma unroll
           for (int mt = 0; mt < D / 16; ++mt) {
             o[mt][0] *= c0;
@@ -618,71 +700,47 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
             o[mt][1] *= c1;
             o[mt][3] *= c1;
           }
-          // P enters the P V product as a 16-bit operand (both operands of one MMA
-          // share a type). Rounding P to bf16 alone costs up to 2^-9 relative per
-          // weight, too coarse for a 2e-3 bound when a few tokens dominate, so P is
-          // split into hi + lo 16-bit parts (P - hi - lo is below 2^-17 P) and each
-          // part gets its own MMA into the same fp32 accumulator.
-          const uint32_t h01 = Mma<MT>::pack(sc[0], sc[1]);
-          const uint32_t h23 = Mma<MT>::pack(sc[2], sc[3]);
-          float r0, r1, r2, r3;
-          unpack2(h01, (MT*)nullptr, r0, r1);
-          unpack2(h23, (MT*)nullptr, r2, r3);
-          const uint32_t b0 = movmatrix_trans(h01);
-          const uint32_t b1 = movmatrix_trans(h23);
-          const uint32_t e0 = movmatrix_trans(Mma<MT>::pack(sc[0] - r0, sc[1] - r1));
-          const uint32_t e1 = movmatrix_trans(Mma<MT>::pack(sc[2] - r2, sc[3] - r3));
-          const int vtok = ((lane >> 4) << 3) + (lane & 7);
-          // tokens held by this lane's A fragments: lo pair (a0, a1), hi pair (a2, a3);
-          // rows past the context are zeroed so that 0 * (stale or NaN) cannot leak in
-          const int tlo = 2 * t4;
-          const uint32_t mlo = (tr(tlo) < nv ? 0x0000ffffu : 0u) | (tr(tlo + 1) < nv ? 0xffff0000u : 0u);
-          const uint32_t mhi = (tr(tlo + 8) < nv ? 0x0000ffffu : 0u) | (tr(tlo + 9) < nv ? 0xffff0000u : 0u);
-          const bool full = nv == JT;  // every job but a sequence's last: no rows to mask
-          if constexpr (F8) {
-            // V^T fragments: this lane's 4 codes of rows g and g+8 -> fp16 pairs,
-            // each pair one row of an 8x8 tile; movmatrix transposes the tiles.
-            // head_dim rows of the result follow the permutation in drow().
-            const uint8_t* vtp = ktp + TILE;
-#pragma unroll
-            for (int mb = 0; mb < D / 64; ++mb) {
-              const uint4 r0 = *reinterpret_cast<const uint4*>(vtp + sw128_offset(tr(g), 4 * mb + t4, JT));
-              const uint4 r1 = *reinterpret_cast<const uint4*>(vtp + sw128_offset(tr(g + 8), 4 * mb + t4, JT));
-              const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w}, w1[4] = {r1.x, r1.y, r1.z, r1.w};
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                uint32_t x0, x1, y0, y1;
-                e4m3x4_to_f16x2x2(w0[j], x0, x1);
-                e4m3x4_to_f16x2x2(w1[j], y0, y1);
-                uint32_t a[4] = {movmatrix_trans(x0), movmatrix_trans(x1), movmatrix_trans(y0), movmatrix_trans(y1)};
-                if (!full) {
-                  a[0] &= mlo;
-                  a[1] &= mlo;
-                  a[2] &= mhi;
-                  a[3] &= mhi;
-                }
-                const int mt = 4 * mb + j;
-                Mma<MT>::run(o[mt], a, b0, b1);
-                Mma<MT>::run(o[mt], a, e0, e1);
-              }
-            }
-          } else {
-#pragma unroll
-            for (int mt = 0; mt < D / 16; ++mt) {
-              uint32_t a[4];
-              ldsm_x4_trans(a, vt + sw128_offset(vtok, mt * 2 + ((lane >> 3) & 1), JT));
-              if (!full) {
-                a[0] &= mlo;
-                a[1] &= mlo;
-                a[2] &= mhi;
-                a[3] &= mhi;
-              }
-              Mma<MT>::run(o[mt], a, b0, b1);
-              Mma<MT>::run(o[mt], a, e0, e1);
-            }
-          }
         }
-        job_done();
+      };
+      if constexpr (PAIR) {
+        // two jobs per step: one softmax update per 32 tokens, and two independent
+        // score chains in flight (the FP8 path is bound by instruction latency)
+#pragma unroll 1
+        for (int u = ub; u < ue; u += 2 * job_step) {
+          const bool two = u + job_step < ue;
+          int sa = 0, sb = 0;
+          const bool oka = next_job(sa, 0);
+          const bool okb = two && next_job(sb, 1);
+          const uint8_t* ka = my_stages + sa * L.stage_bytes;
+          const uint8_t* kb = my_stages + sb * L.stage_bytes;
+          const int nva = min(JT, it.t1 - u * JT), nvb = min(JT, it.t1 - (u + job_step) * JT);
+          float z[2][4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) z[0][e] = z[1][e] = NEG_INF;
+          if (oka) job_scores(ka, nva, z[0]);
+          if (okb) job_scores(kb, nvb, z[1]);
+          if (oka || okb) {
+            softmax_step(z, 2);
+            if (oka) job_pv(ka, nva, z[0]);
+            if (okb) job_pv(kb, nvb, z[1]);
+          }
+          job_done();
+          if (two) job_done();
+        }
+      } else {
+#pragma unroll 1
+        for (int u = ub; u < ue; u += job_step) {
+          int stage;
+          if (next_job(stage, 0)) {
+            const uint8_t* ktp = my_stages + stage * L.stage_bytes;
+            const int nv = min(JT, it.t1 - u * JT);
+            float z[1][4];
+            job_scores(ktp, nv, z[0]);
+            softmax_step(z, 1);
+            job_pv(ktp, nv, z[0]);
+          }
+          job_done();
+        }
       }
 #pragma unroll
       for (int o2 = 4; o2 < 32; o2 <<= 1) {
@@ -694,7 +752,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
       auto drow = [&](int mt, int r) -> int {
         if constexpr (F8) {
           const int rr = r & 7;
-          return 64 * (mt >> 2) + 16 * (rr >> 1) + 4 * (mt & 3) + ((r >> 3) << 1) + (rr & 1);
+          return 16 * (((rr & 1) << 2) | (rr >> 1)) + 2 * mt + (r >> 3);
         } else {
           return mt * 16 + r;
         }
@@ -811,7 +869,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
 #pragma unroll 1
       for (int u = ub; u < ue; u += job_step) {
         int stage;
-        if (next_job(stage)) {
+        if (next_job(stage, 0)) {
           const uint8_t* kt = my_stages + stage * L.stage_bytes;
           const uint8_t* vt = kt + TILE;
           const int nv = min(JT, it.t1 - u * JT);

@@ -44,7 +44,9 @@ pa_status launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const 
   }
   if (per_sm < 1) return PA_ERR_UNSUPPORTED;
   long long grid = (long long)num_sms * per_sm;
-  if (max_items < grid) grid = max_items;
+  // the suffix pass deals items to warps, the other modes to CTAs
+  const long long ctas = MODE == kModeSuffix ? (max_items + Cfg::W - 1) / Cfg::W : max_items;
+  if (ctas < grid) grid = ctas;
   if (grid <= 0) return PA_OK;
   kern<<<(unsigned)grid, Cfg::W * 32, L.total, stream>>>(kmap, vmap, p);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
