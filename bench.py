@@ -57,7 +57,8 @@ def parse():
     ap.add_argument("--workload", default="llama8b",
                     choices=["llama8b", "tiny", "opt13b", "shared", "shared_cow", "long70b_b16", "long70b_b32",
                              "llama8b_fp8", "long70b_b16_fp8", "shared_cascade", "shared_cow_cascade",
-                             "llama8b_nhd", "llama8b_fp8_nhd", "long70b_b16_nhd", "shared_cascade_nhd"],
+                             "llama8b_nhd", "llama8b_fp8_nhd", "long70b_b16_nhd", "shared_cascade_nhd",
+                             "copy_blocks", "swap_out", "swap_in", "reshape", "reshape_prefill"],
                     help="the other workload shapes give a device-timed line of their own (no e2e / CPU legs); "
                          "a _nhd suffix stores the pools NHD")
     return ap.parse_args()
@@ -445,6 +446,159 @@ def run_reference(args, rank, world, local):
     }
 
 
+def decode_oracle_baseline(wl, seconds, fp8=False):
+    """The oracle's decode (float64, all host cores) on the first sequences of a workload,
+    grown until one call takes about ``seconds``: GB/s of the same algorithmic bytes."""
+    import torch
+    import oracle
+    from oracle import fp8 as ofp8
+    from paged_kv_cache_04_gb300 import roofline
+    threads = len(os.sched_getaffinity(0))
+    B = wl.B
+    bt_all, ctx_all = wl.block_tables.cpu(), wl.context_lens.cpu()
+    n = 1
+    while True:
+        seqs = list(range(n))
+        blocks = sorted({int(b) for s in seqs for b in bt_all[s, :-(-int(ctx_all[s]) // B)].tolist()})
+        remap = {b: i for i, b in enumerate(blocks)}
+        idx = torch.tensor(blocks if blocks else [0], dtype=torch.long, device=wl.k_cache.device)
+        k, v = wl.k_cache.index_select(0, idx).cpu(), wl.v_cache.index_select(0, idx).cpu()
+        bt = torch.full((n, bt_all.shape[1]), -1, dtype=torch.int32)
+        for i, s in enumerate(seqs):
+            m = -(-int(ctx_all[s]) // B)
+            bt[i, :m] = torch.tensor([remap[int(b)] for b in bt_all[s, :m].tolist()], dtype=torch.int32)
+        q, ctx = wl.q.cpu()[seqs], ctx_all[seqs].clone()
+        t = time.perf_counter()
+        if fp8:
+            ofp8.decode(q, k.numpy(), v.numpy(), bt, ctx, wl.scale, wl.meta["k_scale"], wl.meta["v_scale"],
+                        num_threads=threads, layout=wl.layout)
+        else:
+            oracle.decode(q, k, v, bt, ctx, wl.scale, num_threads=threads, layout=wl.layout)
+        dt = time.perf_counter() - t
+        if dt >= seconds or n >= wl.S:
+            break
+        n = min(wl.S, max(n + 1, int(n * min(8.0, 1.2 * seconds / max(dt, 1e-3)))))
+    ke = wl.k_cache.element_size()
+    byt = (roofline.decode_bytes(ctx.tolist(), wl.H, wl.G, wl.d, ke) - 2 * n * wl.H * wl.d * ke
+           + 2 * n * wl.H * wl.d * wl.q.element_size())
+    return {"value": round(byt / dt / 1e9, 4), "unit": "GB/s", "cores": min(threads, oracle.max_threads()),
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": f"decode of the first {n} of {wl.S} sequences, float64 oracle, OpenMP over (sequence, head)"}
+
+
+def time_steps(step, steps, warmup, flush):
+    """Mean CUDA-event time (ms) of ``step`` after warm-up, reading ``flush`` (larger than L2) between steps."""
+    import torch
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    torch.cuda._sleep(int(2e6 * (2 + steps)))
+    times = []
+    for _ in range(steps):
+        flush.sum()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        times.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.mean(x.elapsed_time(y) for x, y in times)
+
+
+def run_cache_workload(args, name):
+    """The cache kernels on their own: CoW block copies, swap to and from pinned host
+    memory, and the cache write at decode and at prefill size."""
+    import numpy as np
+    import torch
+    import paged_kv_cache_04_gb300 as pa
+    import oracle
+    from paged_kv_cache_04_gb300 import roofline, workloads
+    dev = torch.device("cuda", 0)
+    G, B, d, dt = 8, 16, 128, torch.bfloat16
+    L = 32  # layers moved per call (the pages' copies and swaps run over every layer)
+    flush = torch.ones(128 * 1024 * 1024, dtype=torch.int32, device=dev)
+    peak, _ = measured_hbm_peak()
+    g = torch.Generator().manual_seed(0)
+    line = {"workload": name}
+    cpu = None
+    if name == "copy_blocks":
+        wl = workloads.shared_prefix(device="cpu", cow=True)   # its 448 copy-on-write pairs and pool size
+        pairs = wl.copy_pairs.to(dev)
+        nb = wl.num_blocks
+        kp = [torch.empty((nb, G, B, d), dtype=dt, device=dev) for _ in range(L)]
+        vp = [torch.empty((nb, G, B, d), dtype=dt, device=dev) for _ in range(L)]
+        ms = time_steps(lambda: pa.pa_copy_blocks(kp, vp, pairs), args.steps, args.warmup, flush)
+        byt = roofline.copy_blocks_bytes(pairs.shape[0], L, B, G, d, 2)
+        # the 7 samples of a prompt all copy its one partial block: reads repeat through L2
+        nsrc = len(set(wl.copy_pairs[:, 0].tolist()))
+        uniq = (nsrc + pairs.shape[0]) * L * roofline.kv_block_bytes(B, G, d, 2)
+        line.update(desc=f"{pairs.shape[0]} CoW pairs ({nsrc} distinct sources) x {L} layers, bf16 blocks of "
+                         f"16 x 8 heads x 128", bound="hbm",
+                    unique_GBps=round(uniq / (ms * 1e-3) / 1e9, 1),
+                    unique_frac_of_measured_peak=round(uniq / (ms * 1e-3) / 1e9 / peak, 4))
+        P = int(pairs.shape[0])  # the oracle copies the same number of pairs within a compact pool
+        kc = np.random.default_rng(0).integers(0, 1 << 16, (2 * P, G, B, d), dtype=np.uint16)
+        cp = torch.stack([torch.arange(P), torch.arange(P, 2 * P)], 1)
+        t = time.perf_counter()
+        oracle.copy_blocks([kc], [kc.copy()], cp)
+        cdt = time.perf_counter() - t
+        cpu = {"value": round(roofline.copy_blocks_bytes(pairs.shape[0], 1, B, G, d, 2) / cdt / 1e9, 4),
+               "unit": "GB/s", "cores": 1, "kind": "oracle", "seconds": round(cdt, 3),
+               "sample": f"{pairs.shape[0]} pairs x 1 layer, numpy element copies"}
+    elif name in ("swap_out", "swap_in"):
+        nd, nh, P = 4096, 1024, 512
+        dk = [torch.empty((nd, G, B, d), dtype=dt, device=dev) for _ in range(L)]
+        dv = [torch.empty((nd, G, B, d), dtype=dt, device=dev) for _ in range(L)]
+        hk = [torch.empty((nh, G, B, d), dtype=dt).pin_memory() for _ in range(L)]
+        hv = [torch.empty((nh, G, B, d), dtype=dt).pin_memory() for _ in range(L)]
+        src = torch.randperm(nd, generator=g)[:P]
+        dst = torch.randperm(nh, generator=g)[:P]
+        if name == "swap_out":
+            pairs = torch.stack([src, dst], 1).to(dev)
+            step = lambda: pa.pa_swap_blocks(hk, hv, dk, dv, pairs)  # noqa: E731
+        else:
+            pairs = torch.stack([dst, src], 1).to(dev)
+            step = lambda: pa.pa_swap_blocks(dk, dv, hk, hv, pairs)  # noqa: E731
+        ms = time_steps(step, args.steps, args.warmup, flush)
+        byt = P * L * roofline.kv_block_bytes(B, G, d, 2)  # bytes moved across the host link
+        # the same byte count as one contiguous copy over the same link, timed here
+        dbuf = torch.empty(byt // 2, dtype=dt, device=dev)
+        hbuf = torch.empty(byt // 2, dtype=dt).pin_memory()
+        ref = (lambda: hbuf.copy_(dbuf, non_blocking=True)) if name == "swap_out" else \
+            (lambda: dbuf.copy_(hbuf, non_blocking=True))
+        ref_ms = time_steps(ref, args.steps, args.warmup, flush)
+        line.update(desc=f"{P} blocks x {L} layers (K and V) {'device -> pinned host' if name == 'swap_out' else 'pinned host -> device'}, one launch",
+                    bound="host link", contiguous_copy_GBps=round(byt / (ref_ms * 1e-3) / 1e9, 1),
+                    frac_of_contiguous_copy=round(ref_ms / ms, 4))
+    else:  # reshape (the benchmark step's 256 new tokens) or reshape_prefill (32 prompts x 1024 tokens)
+        N = 256 if name == "reshape" else 32 * 1024
+        nb = 100_000
+        kc = torch.empty((nb, G, B, d), dtype=dt, device=dev)
+        vc = torch.empty((nb, G, B, d), dtype=dt, device=dev)
+        key = torch.randn((N, G, d), generator=g).to(dt).to(dev)
+        val = torch.randn((N, G, d), generator=g).to(dt).to(dev)
+        slots = torch.randperm(nb * B, generator=g)[:N].to(dev)
+        ms = time_steps(lambda: pa.pa_reshape_and_cache(key, val, kc, vc, slots), args.steps, args.warmup, flush)
+        byt = roofline.reshape_and_cache_bytes(N, G, d, 2)
+        line.update(desc=f"{N} new tokens x 8 kv heads x 128 (bf16) into a 100k-block pool, random slots",
+                    bound="hbm" if N > 1024 else "launch latency",
+                    frac_of_measured_peak=round(byt / (ms * 1e-3) / 1e9 / peak, 4))
+        n = min(N, 256)
+        kh = np.zeros((64, G, B, d), np.uint16)
+        t = time.perf_counter()
+        oracle.reshape_and_cache(key[:n].cpu(), val[:n].cpu(), kh, kh.copy(), torch.arange(n, dtype=torch.int64))
+        cdt = time.perf_counter() - t
+        cpu = {"value": round(roofline.reshape_and_cache_bytes(n, G, d, 2) / cdt / 1e9, 4), "unit": "GB/s",
+               "cores": 1, "kind": "oracle", "seconds": round(cdt, 3),
+               "sample": f"{n} tokens, numpy element copies"}
+    line.update(ms_per_step=round(ms, 5), algorithmic_GBps=round(byt / (ms * 1e-3) / 1e9, 1), bytes_per_step=byt,
+                l2="512 MiB buffer read between timed steps", device_errors=pa.pa_get_error())
+    if cpu is not None and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+
+
 def run_workload(args):
     """Device-timed step of one of the other workload shapes (single GPU)."""
     import torch
@@ -453,6 +607,8 @@ def run_workload(args):
     _build.ensure_built()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
+    if args.workload in ("copy_blocks", "swap_out", "swap_in", "reshape", "reshape_prefill"):
+        return run_cache_workload(args, args.workload)
     nhd = args.workload.endswith("_nhd")
     name = args.workload[:-4] if nhd else args.workload
     split, T = False, None
@@ -571,6 +727,8 @@ def run_workload(args):
             "frac_of_measured_peak": round((dec + extra) / (ms * 1e-3) / 1e9 / peak, 4),
             "bytes_per_step": dec + extra, "l2": "512 MiB buffer read between timed steps",
             "device_errors": pa.pa_get_error()}
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = decode_oracle_baseline(wl, min(args.cpu_seconds, 5.0), fp8=fp8)
     if unique is not None:
         line["unique_GBps"] = round((unique + extra) / (ms * 1e-3) / 1e9, 1)
         line["unique_frac_of_measured_peak"] = round((unique + extra) / (ms * 1e-3) / 1e9 / peak, 4)

@@ -20,29 +20,37 @@ __device__ __forceinline__ long long pool_row(long long slot, int h, int G, int 
   return (blk * G + h) * BS + row;
 }
 
-// One thread per 16-byte vector of a (token, K-or-V, kv head) row.
+// One thread per VPT consecutive 16-byte vectors of a (token, K-or-V, kv head)
+// row; its VPT loads (which do not depend on the slot) are all in flight before
+// the stores.
+template <int VPT>
 __global__ void __launch_bounds__(256)
     reshape_and_cache_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value, uint4* k_cache,
                              uint4* v_cache, const int64_t* __restrict__ slot_mapping, int num_tokens, int G,
                              int vpr, int BS, int nhd, long long num_slots, unsigned* err) {
-  const long long total = (long long)num_tokens * 2 * G * vpr;
+  const int gpr = vpr / VPT;  // vector groups per row
+  const long long total = (long long)num_tokens * 2 * G * gpr;
   for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
        idx += (long long)gridDim.x * blockDim.x) {
-    const int v = (int)(idx % vpr);
-    long long rest = idx / vpr;
+    const int v0 = (int)(idx % gpr) * VPT;
+    long long rest = idx / gpr;
     const int h = (int)(rest % G);
     rest /= G;
     const int which = (int)(rest & 1);
     const long long t = rest >> 1;
     const long long slot = __ldg(slot_mapping + t);
+    const uint4* src = (which ? value : key) + (t * G + h) * vpr + v0;
+    uint4 r[VPT];
+#pragma unroll
+    for (int u = 0; u < VPT; ++u) r[u] = __ldg(src + u);
     if (slot < 0) continue;
     if (slot >= num_slots) {
-      if (v == 0 && h == 0 && which == 0) atomicOr(err, kErrSlot);
+      if (v0 == 0 && h == 0 && which == 0) atomicOr(err, kErrSlot);
       continue;
     }
-    const uint4* src = which ? value : key;
-    uint4* dst = which ? v_cache : k_cache;
-    dst[pool_row(slot, h, G, BS, nhd) * vpr + v] = __ldg(src + (t * G + h) * vpr + v);
+    uint4* dst = (which ? v_cache : k_cache) + pool_row(slot, h, G, BS, nhd) * vpr + v0;
+#pragma unroll
+    for (int u = 0; u < VPT; ++u) dst[u] = r[u];
   }
 }
 
@@ -185,13 +193,15 @@ extern "C" pa_status pa_reshape_and_cache(const void* key, const void* value, vo
   pa_status st = device_state(&err, &sms);
   if (st != PA_OK) return st;
   const int vpr = row_bytes / 16;
-  const long long total = (long long)num_tokens * 2 * num_kv_heads * vpr;
+  const int vpt = vpr % 4 == 0 ? 4 : (vpr % 2 == 0 ? 2 : 1);
+  const long long total = (long long)num_tokens * 2 * num_kv_heads * (vpr / vpt);
   const long long want = (total + 255) / 256;
   const unsigned grid = (unsigned)std::min<long long>(want, (long long)sms * 16);
-  reshape_and_cache_kernel<<<grid, 256, 0, stream>>>(
-      static_cast<const uint4*>(key), static_cast<const uint4*>(value), static_cast<uint4*>(k_cache),
-      static_cast<uint4*>(v_cache), slot_mapping, num_tokens, num_kv_heads, vpr, block_size,
-      layout == PA_LAYOUT_NHD ? 1 : 0, (long long)num_blocks * block_size, err);
+  auto kern = vpt == 4 ? reshape_and_cache_kernel<4> : (vpt == 2 ? reshape_and_cache_kernel<2> : reshape_and_cache_kernel<1>);
+  kern<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(key), static_cast<const uint4*>(value),
+                                 static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slot_mapping, num_tokens,
+                                 num_kv_heads, vpr, block_size, layout == PA_LAYOUT_NHD ? 1 : 0,
+                                 (long long)num_blocks * block_size, err);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
