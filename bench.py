@@ -54,6 +54,9 @@ def parse():
                     help="run only the step's kernels on a 64-sequence batch of the same shape (for ncu)")
     ap.add_argument("--profile-fp8", action="store_true",
                     help="the same 64-sequence case with an E4M3 cache (for ncu)")
+    ap.add_argument("--profile-case", choices=["split", "cascade", "mha"], default=None,
+                    help="a small case of another path for ncu: split (2 seqs, 48K-64K tokens, 64 q / 8 kv), "
+                         "cascade (32 prompts x 8 samples), mha (the OPT-13B batch)")
     ap.add_argument("--workload", default="llama8b",
                     choices=["llama8b", "tiny", "opt13b", "shared", "shared_cow", "long70b_b16", "long70b_b32",
                              "llama8b_fp8", "long70b_b16_fp8", "shared_cascade", "shared_cow_cascade",
@@ -764,10 +767,58 @@ def run_profile_case(args):
                       "source_sha256": kernel_source_sha(), "device_errors": pa.pa_get_error()}))
 
 
+def run_other_profile_case(args):
+    """Small cases (K/V still larger than L2) of the split, shared-prefix and MHA paths, for ncu."""
+    import torch
+    import paged_kv_cache_04_gb300 as pa
+    from paged_kv_cache_04_gb300 import _build, roofline, workloads
+    _build.ensure_built()
+    dev = torch.device("cuda", 0)
+    name = args.profile_case
+    if name == "split":
+        wl = workloads.long70b(device=dev, S=2, lo=48_000, hi=64_000)
+    elif name == "cascade":
+        wl = workloads.shared_prefix(device=dev, prompts=32)
+    else:
+        wl = workloads.opt13b(device=dev)
+    out = torch.empty_like(wl.q)
+    mctx, T = wl.max_context, 512
+    if name == "cascade":
+        pa.pa_reshape_and_cache(wl.new_key, wl.new_value, wl.k_cache, wl.v_cache, wl.slot_mapping)
+        gs = torch.tensor(wl.meta["group_starts"], dtype=torch.int32, device=dev)
+        pl = torch.tensor(wl.meta["prefix_lens"], dtype=torch.int32, device=dev)
+        pmax = max(wl.meta["prefix_lens"])
+        ws = torch.empty(pa.pa_decode_cascade_workspace_bytes(wl.S, wl.H, wl.d, pmax, mctx, T), dtype=torch.uint8,
+                         device=dev)
+    elif name == "split":
+        ws = torch.empty(pa.pa_decode_split_workspace_bytes(wl.S, wl.H, wl.d, mctx, T), dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup + args.steps):
+        if name == "cascade":
+            pa.pa_decode_cascade(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale,
+                                 gs, pl, 8, pmax, mctx, T, ws)
+        elif name == "split":
+            pa.pa_reshape_and_cache(wl.new_key, wl.new_value, wl.k_cache, wl.v_cache, wl.slot_mapping)
+            pa.pa_decode_split(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale,
+                               mctx, T, ws)
+        else:
+            pa.pa_reshape_and_cache(wl.new_key, wl.new_value, wl.k_cache, wl.v_cache, wl.slot_mapping)
+            pa.pa_decode(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale)
+    torch.cuda.synchronize()
+    kv = roofline.decode_bytes(wl.context_lens.tolist(), wl.H, wl.G, wl.d, wl.k_cache.element_size())
+    info = {"profile_case": name, "seqs": wl.S, "tokens": int(wl.context_lens.sum().item()),
+            "decode_bytes_per_launch": kv, "device_errors": pa.pa_get_error()}
+    if name == "cascade":
+        info["unique_kv_tokens"] = wl.meta["unique_tokens"]
+    print(json.dumps(info))
+
+
 def main():
     args = parse()
     if args.profile or args.profile_fp8:
         run_profile_case(args)
+        return
+    if args.profile_case:
+        run_other_profile_case(args)
         return
     if args.workload != "llama8b":
         run_workload(args)
