@@ -52,8 +52,10 @@ pa_status encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
 //   HND [num_blocks][G][B][D]: 2-D, rows = num_blocks * G * B of D elements;
 //   NHD [num_blocks][B][G][D]: 3-D (D, G, num_blocks * B), so a box takes one
 //   kv head of 16 consecutive tokens (rows G * D elements apart).
+//   swizzle: 128-byte swizzled stages (read by ldmatrix / by columns), or plain
+//   row-major stages (V of the vector paths, whose lanes read one row at a time).
 pa_status make_pool_map(CUtensorMap* map, const void* base, pa_dtype dt, int D, int G, int BS, long long num_blocks,
-                        pa_kv_layout layout) {
+                        pa_kv_layout layout, bool swizzle = true) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
   pa_status st = encoder(&enc);
   if (st != PA_OK) return st;
@@ -77,7 +79,7 @@ pa_status make_pool_map(CUtensorMap* map, const void* base, pa_dtype dt, int D, 
   // NHD rows of one kv head are G * D elements apart: promote only the 128 bytes a box reads, so a
   // 128-byte row does not drag its neighbour head's row into L2.
   CUresult r = enc(map, t, nhd ? 3 : 2, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                    nhd ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
@@ -168,9 +170,12 @@ pa_status run_decode(const DecodeArgs& a, bool split, int partition, int max_par
   int sms = 0;
   pa_status s = device_state(&err, &sms);
   if (s != PA_OK) return s;
+  // tensor-core path (16-bit or FP8 data, group >= 4) or vector path: see dispatch_path
+  const bool mma_path = esize(a.dt) <= 2 && a.H / a.G >= 4;
   CUtensorMap km, vm;
   if ((s = make_pool_map(&km, a.k_cache, a.dt, a.D, a.G, a.BS, a.num_blocks, a.layout)) != PA_OK) return s;
-  if ((s = make_pool_map(&vm, a.v_cache, a.dt, a.D, a.G, a.BS, a.num_blocks, a.layout)) != PA_OK) return s;
+  if ((s = make_pool_map(&vm, a.v_cache, a.dt, a.D, a.G, a.BS, a.num_blocks, a.layout, mma_path)) != PA_OK)
+    return s;
 
   DecodeParams p{};
   p.out = a.out;
@@ -209,17 +214,21 @@ pa_status run_decode(const DecodeArgs& a, bool split, int partition, int max_par
     p.suffix_single = 1;
     if (c.prefix_slots > 0) {  // prefix pass: every group's query rows over its shared blocks
       const long long pitems = (long long)c.num_groups * a.G * c.prefix_slots;
+      CUtensorMap vsw = vm;  // the prefix pass reads V with ldmatrix: swizzled stages
+      if (!mma_path &&
+          (s = make_pool_map(&vsw, a.v_cache, a.dt, a.D, a.G, a.BS, a.num_blocks, a.layout)) != PA_OK)
+        return s;
       const bool bf = a.dt == PA_BF16;
       if (a.D == 128)
-        s = c.nt == 1 ? (bf ? launch_cascade_prefix<__nv_bfloat16, 128, 1>(km, vm, p, sms, pitems, st)
-                            : launch_cascade_prefix<__half, 128, 1>(km, vm, p, sms, pitems, st))
-                      : (bf ? launch_cascade_prefix<__nv_bfloat16, 128, 2>(km, vm, p, sms, pitems, st)
-                            : launch_cascade_prefix<__half, 128, 2>(km, vm, p, sms, pitems, st));
+        s = c.nt == 1 ? (bf ? launch_cascade_prefix<__nv_bfloat16, 128, 1>(km, vsw, p, sms, pitems, st)
+                            : launch_cascade_prefix<__half, 128, 1>(km, vsw, p, sms, pitems, st))
+                      : (bf ? launch_cascade_prefix<__nv_bfloat16, 128, 2>(km, vsw, p, sms, pitems, st)
+                            : launch_cascade_prefix<__half, 128, 2>(km, vsw, p, sms, pitems, st));
       else
-        s = c.nt == 1 ? (bf ? launch_cascade_prefix<__nv_bfloat16, 64, 1>(km, vm, p, sms, pitems, st)
-                            : launch_cascade_prefix<__half, 64, 1>(km, vm, p, sms, pitems, st))
-                      : (bf ? launch_cascade_prefix<__nv_bfloat16, 64, 2>(km, vm, p, sms, pitems, st)
-                            : launch_cascade_prefix<__half, 64, 2>(km, vm, p, sms, pitems, st));
+        s = c.nt == 1 ? (bf ? launch_cascade_prefix<__nv_bfloat16, 64, 1>(km, vsw, p, sms, pitems, st)
+                            : launch_cascade_prefix<__half, 64, 1>(km, vsw, p, sms, pitems, st))
+                      : (bf ? launch_cascade_prefix<__nv_bfloat16, 64, 2>(km, vsw, p, sms, pitems, st)
+                            : launch_cascade_prefix<__half, 64, 2>(km, vsw, p, sms, pitems, st));
       if (s != PA_OK) return s;
     }
   }

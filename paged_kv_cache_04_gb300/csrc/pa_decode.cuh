@@ -111,7 +111,7 @@ __device__ __forceinline__ void tma_load_tile(void* dst, const CUtensorMap* map,
 }
 
 struct SmemLayout {
-  unsigned stage_bytes, bars_off, ok_off, merge_off, q_off, sched_off, misc_off, total;
+  unsigned stage_bytes, bars_off, ok_off, merge_off, q_off, wts_off, sched_off, misc_off, total;
 };
 
 __host__ __device__ inline unsigned round_up(unsigned x, unsigned a) { return (x + a - 1) / a * a; }
@@ -131,6 +131,8 @@ __host__ __device__ inline SmemLayout make_layout(int W, int R, int D, int esize
   L.q_off = off;
   if (path == kPathVec) off += W * group * D * 4;            // fp32 q rows per warp
   if (path == kPathVecMha) off += round_up(W * 2 * D * qsize, 16);  // double-buffered raw q row per warp
+  L.wts_off = off;
+  if (path != kPathMma) off += W * kJobTokens * 4;             // vector paths: one job's weights per warp
   L.sched_off = off;
   if (split)
     off += (S + 1) * 4;
@@ -149,7 +151,9 @@ struct StageCfg {
   static constexpr int TILE = kJobTokens * D * E;  // one K (or V) job tile
   static constexpr int kStage = 2 * TILE;
   static constexpr int W = 4;
-  static constexpr int R = kStage <= 4096 ? 4 : 3;
+  // The MHA path is bound by instruction latency with 2 CTAs per SM: two 8 KiB
+  // stages per warp let 3 CTAs fit (50% more warps, the same bytes in flight).
+  static constexpr int R = kStage <= 4096 ? 4 : (PATH == kPathVecMha ? 2 : 3);
 };
 
 struct Item {
@@ -278,6 +282,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
   float* mrg_ml = mrg_o + W * p.group * D;                             // [W][kMaxGroup][2]
   float* qs_all = reinterpret_cast<float*>(smem + L.q_off);            // [W][group][D] (vector path)
   uint8_t* qraw_all = smem + L.q_off;                                  // [W][2][D] raw (MHA path)
+  float* wts_all = reinterpret_cast<float*>(smem + L.wts_off);         // [W][JT] (vector paths)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc_off);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -958,11 +963,16 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
             lr[h] = lr[h] * corr + (part == 0 ? pt : 0.f);
 #pragma unroll
             for (int e = 0; e < EPL; ++e) o[h][e] *= corr;
-#pragma unroll 4
-            for (int tt = 0; tt < nv; ++tt) {
-              const float w = __shfl_sync(0xffffffffu, pt, tt);
-              const int byte = lane * VB;
-              const uint8_t* src = vt + sw128_offset(tt, byte >> 4, JT) + (byte & 15);
+            // P V: the job's 16 weights go through shared memory (4 broadcast loads
+            // instead of 16 shuffles); V tiles of the vector paths are staged without
+            // swizzling, so token tt of this lane's columns is at a fixed offset.
+            float* wb = wts_all + warp * JT;
+            if (lane < JT) wb[lane] = pt;
+            __syncwarp();
+            const int byte = lane * VB;
+            const uint8_t* vsrc = vt + (byte >> 7) * JT * 128 + (byte & 127);
+            auto pv_token = [&](int tt, float w) {
+              const uint8_t* src = vsrc + tt * 128;
               if constexpr (E == 1) {
                 static_assert(VB == 4, "FP8 vector path reads 4 codes per lane");
                 const uint32_t raw = *reinterpret_cast<const uint32_t*>(src);
@@ -1002,7 +1012,24 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
                   o[h][1] = fmaf(w, f1, o[h][1]);
                 }
               }
+            };
+            if (nv == JT) {  // every job but a sequence's last: fully unrolled
+              float wv[JT];
+#pragma unroll
+              for (int i = 0; i < JT; i += 4) {
+                const float4 w4 = *reinterpret_cast<const float4*>(wb + i);
+                wv[i] = w4.x;
+                wv[i + 1] = w4.y;
+                wv[i + 2] = w4.z;
+                wv[i + 3] = w4.w;
+              }
+#pragma unroll
+              for (int tt = 0; tt < JT; ++tt) pv_token(tt, wv[tt]);
+            } else {
+#pragma unroll 4
+              for (int tt = 0; tt < nv; ++tt) pv_token(tt, wb[tt]);
             }
+            __syncwarp();  // the weights are read before the next head or job rewrites them
           }
         }
         job_done();
