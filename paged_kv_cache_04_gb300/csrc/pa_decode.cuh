@@ -1078,19 +1078,21 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
 
 // Pass 2 of split mode: merge the partitions of one (sequence, head) row with
 // log-sum-exp weights, M = max_p m_p, w_p = l_p * 2^(m_p - M),
-// out = sum_p w_p o_p / sum_p w_p. One CTA per row; the row's partials are read
-// with every load of a thread issued before any is used, so the kernel costs a
-// few memory round trips rather than one per partition.
+// out = sum_p w_p o_p / sum_p w_p. One CTA per row: thread (v, pg) owns float4
+// column v of the partitions p = pg (mod PG) and merges them online as their
+// loads arrive (a running max, rescaling its sum and accumulator when the max
+// grows), BATCH partitions' loads in flight at a time; the PG partial merges of
+// each column are then combined through shared memory. No pass is spent finding
+// the row's maximum first.
 template <typename OT, int D>
 __global__ void __launch_bounds__(256) lse_reduce_kernel(const DecodeParams p) {
   constexpr int NT = 256;
   constexpr int VPR = D / 4;        // float4 vectors per partial row
   constexpr int PG = NT / VPR;      // partition groups (8 for D = 128, 16 for D = 64)
-  constexpr int BATCH = 8;          // loads in flight per thread
-  constexpr int CHUNK = 2048;       // partitions whose weights sit in shared memory at a time
+  constexpr int BATCH = 8;          // partitions in flight per thread
   const int row = blockIdx.x;       // s * H + h
   const int s = row / p.H;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x;
   const float NEG_INF = -__int_as_float(0x7f800000);
   const int c = clamp_ctx(p, s, !p.suffix_single);  // one suffix slot bounds no context length
   int Pp = 0, st = 0;
@@ -1102,69 +1104,70 @@ __global__ void __launch_bounds__(256) lse_reduce_kernel(const DecodeParams p) {
   const int P = Pp + Ps;  // merged slots: [0, Pp) and [suffix_slot, suffix_slot + Ps)
   auto slot = [&](int q) { return q < Pp ? q : p.suffix_slot + (q - Pp); };
   const long long base = (long long)row * p.max_partitions;
-  __shared__ float sh_w[CHUNK];
-  __shared__ float sh_red[NT / 32];
-  __shared__ float4 sh_acc[PG][VPR];
-
-  float mx = NEG_INF;
-  for (int q = tid; q < P; q += NT) {
-    const float l = __ldg(p.ws_l + base + slot(q)), m = __ldg(p.ws_m + base + slot(q));
-    if (l > 0.f) mx = fmaxf(mx, m);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if (lane == 0) sh_red[warp] = mx;
-  __syncthreads();
-  float M = sh_red[0];
-#pragma unroll
-  for (int w = 1; w < NT / 32; ++w) M = fmaxf(M, sh_red[w]);
-  __syncthreads();
-
   const int v = tid % VPR, pg = tid / VPR;
+  const float4* src = reinterpret_cast<const float4*>(p.ws_o + base * D) + v;
+
+  float M = NEG_INF, W = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float wsum = 0.f;
-  for (int q0 = 0; q0 < P; q0 += CHUNK) {
-    const int n = min(CHUNK, P - q0);
-    for (int q = tid; q < n; q += NT) {
-      const float l = __ldg(p.ws_l + base + slot(q0 + q)), m = __ldg(p.ws_m + base + slot(q0 + q));
-      const float w = l > 0.f ? l * exp2f(m - M) : 0.f;
-      sh_w[q] = w;
-      wsum += w;
-    }
-    __syncthreads();
-    const float4* src = reinterpret_cast<const float4*>(p.ws_o + base * D) + v;
-    for (int q = pg; q < n; q += PG * BATCH) {
-      float4 x[BATCH];
+  for (int q0 = pg; q0 < P; q0 += PG * BATCH) {
+    float4 x[BATCH];
+    float mq[BATCH], lq[BATCH];
 #pragma unroll
-      for (int b = 0; b < BATCH; ++b) {
-        const int qq = q + b * PG;
-        x[b] = qq < n ? __ldg(src + (long long)slot(q0 + qq) * VPR) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int b = 0; b < BATCH; ++b) {
-        const int qq = q + b * PG;
-        const float w = qq < n ? sh_w[qq] : 0.f;
-        acc.x = fmaf(w, x[b].x, acc.x);
-        acc.y = fmaf(w, x[b].y, acc.y);
-        acc.z = fmaf(w, x[b].z, acc.z);
-        acc.w = fmaf(w, x[b].w, acc.w);
+    for (int b = 0; b < BATCH; ++b) {
+      const int q = q0 + b * PG;
+      if (q < P) {
+        const int sl = slot(q);
+        x[b] = __ldg(src + (long long)sl * VPR);
+        mq[b] = __ldg(p.ws_m + base + sl);
+        lq[b] = __ldg(p.ws_l + base + sl);
+      } else {
+        lq[b] = 0.f;
       }
     }
-    __syncthreads();
+#pragma unroll
+    for (int b = 0; b < BATCH; ++b) {
+      if (!(lq[b] > 0.f)) continue;  // empty partition
+      const float Mn = fmaxf(M, mq[b]);
+      const float r = exp2f(M - Mn), w = lq[b] * exp2f(mq[b] - Mn);
+      acc.x = fmaf(w, x[b].x, acc.x * r);
+      acc.y = fmaf(w, x[b].y, acc.y * r);
+      acc.z = fmaf(w, x[b].z, acc.z * r);
+      acc.w = fmaf(w, x[b].w, acc.w * r);
+      W = fmaf(W, r, w);
+      M = Mn;
+    }
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
-  if (lane == 0) sh_red[warp] = wsum;
+  __shared__ float sh_m[PG][VPR], sh_w[PG][VPR];
+  __shared__ float4 sh_acc[PG][VPR];
+  sh_m[pg][v] = M;
+  sh_w[pg][v] = W;
   sh_acc[pg][v] = acc;
   __syncthreads();
-  float W = 0.f;
+  if (pg == 0) {
+    float Mt = NEG_INF;
 #pragma unroll
-  for (int w = 0; w < NT / 32; ++w) W += sh_red[w];
-  for (int i = tid; i < D; i += NT) {
-    float O = 0.f;
+    for (int gi = 0; gi < PG; ++gi)
+      if (sh_w[gi][v] > 0.f) Mt = fmaxf(Mt, sh_m[gi][v]);
+    float Wt = 0.f;
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int g = 0; g < PG; ++g) O += reinterpret_cast<const float*>(&sh_acc[g][0])[i];
-    reinterpret_cast<OT*>(p.out)[(long long)row * D + i] = from_f32<OT>(W > 0.f ? O / W : 0.f);
+    for (int gi = 0; gi < PG; ++gi) {
+      const float wg = sh_w[gi][v];
+      if (!(wg > 0.f)) continue;
+      const float r = exp2f(sh_m[gi][v] - Mt);
+      const float4 a = sh_acc[gi][v];
+      O.x = fmaf(r, a.x, O.x);
+      O.y = fmaf(r, a.y, O.y);
+      O.z = fmaf(r, a.z, O.z);
+      O.w = fmaf(r, a.w, O.w);
+      Wt = fmaf(r, wg, Wt);
+    }
+    const float inv = Wt > 0.f ? 1.f / Wt : 0.f;
+    OT* out = reinterpret_cast<OT*>(p.out) + (long long)row * D + 4 * v;
+    out[0] = from_f32<OT>(O.x * inv);
+    out[1] = from_f32<OT>(O.y * inv);
+    out[2] = from_f32<OT>(O.z * inv);
+    out[3] = from_f32<OT>(O.w * inv);
   }
 }
 
