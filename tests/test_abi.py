@@ -79,6 +79,8 @@ def test_invalid_arguments_rejected_before_any_launch(lib_path):
     # reshape_and_cache: zero tokens is a no-op; misaligned slot mapping rejected
     assert lib.pa_reshape_and_cache(null, null, null, null, null, 0, 8, 128, 16, 0, 10, 2, null) == 0
     assert lib.pa_reshape_and_cache(al, al, al, al, ctypes.c_void_p(0x10004), 4, 8, 128, 16, 0, 10, 2, null) == 1
+    # pools whose rows (num_blocks x kv heads x block size) overflow the 32-bit TMA row coordinate
+    assert lib.pa_decode(al, al, al, al, al, 1, al, 2, 8, 8, 128, 16, 0, 1 << 28, 1.0, 2, 2, null) == 2
     # a pool layout other than HND (0) and NHD (1) is rejected, even with nothing to do
     assert lib.pa_decode(null, null, null, null, null, 1, null, 0, 8, 8, 128, 16, 2, 10, 1.0, 2, 2, null) == 1
     assert lib.pa_reshape_and_cache(null, null, null, null, null, 0, 8, 128, 16, 7, 10, 2, null) == 1

@@ -306,13 +306,47 @@ def test_non_default_stream(pa, cuda_device):
     assert torch.equal(out, ref)
 
 
-def test_large_batch_natural_order(pa, cuda_device):
-    """Batches above the in-kernel sort limit run in batch order; results are unchanged."""
-    ctx = [int(x) for x in torch.randint(1, 200, (1500,), generator=torch.Generator().manual_seed(3))]
+@pytest.mark.parametrize("S", [2048, 2500])
+def test_large_batches(pa, cuda_device, S):
+    """2048 sequences (the largest batch the kernel orders longest first) and 2500
+    (above it: batch order); results must not depend on the order."""
+    ctx = [int(x) for x in torch.randint(1, 200, (S,), generator=torch.Generator().manual_seed(3))]
     nb = sum(-(-c // 16) for c in ctx) + 10
-    wl = workloads.batch_with_new_tokens("big", 1500, 8, 2, 64, 16, torch.bfloat16, ctx, nb, cuda_device,
+    for Hh, G in ((8, 2), (32, 8)):  # vector path and tensor-core path
+        wl = workloads.batch_with_new_tokens("big", S, Hh, G, 64, 16, torch.bfloat16, ctx, nb, cuda_device,
+                                             new_token=False)
+        seqs = H.sample_seqs(wl, 40)
+        ref = H.Pristine(wl, seqs).decode()
+        out = H.gpu_step(pa, wl, out_dtype=torch.float32)
+        H.check_close(out[seqs], ref, torch.float32, f"S={S} H={Hh} G={G}")
+    _no_device_errors(pa)
+
+
+def test_all_contexts_empty(pa, cuda_device):
+    """A batch in which no sequence has a token yet: every output row is zero, plain and split."""
+    wl = workloads.batch_with_new_tokens("empty", 6, 32, 8, 128, 16, torch.bfloat16, [0] * 6, 8, cuda_device,
                                          new_token=False)
-    seqs = H.sample_seqs(wl, 40)
-    ref = H.Pristine(wl, seqs).decode()
+    for split in (False, True):
+        out = H.gpu_step(pa, wl, out_dtype=torch.float32, split=split, partition=64)
+        assert torch.equal(out, torch.zeros_like(out))
+    _no_device_errors(pa)
+
+
+def test_one_long_sequence_plain(pa, cuda_device):
+    """A single 64K-token sequence through the single-pass kernel (8 work items for
+    the whole GPU): long items, a last block of one token."""
+    ctx = [65537]
+    nb = -(-ctx[0] // 16) + 5
+    wl = workloads.batch_with_new_tokens("long1", 1, 32, 8, 128, 16, torch.bfloat16, ctx, nb, cuda_device)
+    ref = H.Pristine(wl).decode()
     out = H.gpu_step(pa, wl, out_dtype=torch.float32)
-    H.check_close(out[seqs], ref, torch.float32, "S=1500")
+    H.check_close(out, ref, torch.float32, "one 64K sequence")
+    _no_device_errors(pa)
+
+
+def test_split_rejects_batches_above_its_limit(pa, cuda_device):
+    S = 2049
+    wl = workloads.batch_with_new_tokens("wide", S, 8, 8, 64, 16, torch.bfloat16, [3] * S, S + 2, cuda_device,
+                                         new_token=False)
+    with pytest.raises(pa.PAError):
+        H.gpu_step(pa, wl, split=True, partition=64)
