@@ -28,6 +28,7 @@ __global__ void __launch_bounds__(256)
     reshape_and_cache_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value, uint4* k_cache,
                              uint4* v_cache, const int64_t* __restrict__ slot_mapping, int num_tokens, int G,
                              int vpr, int BS, int nhd, long long num_slots, unsigned* err) {
+  pdl_begin();
   const int gpr = vpr / VPT;  // vector groups per row
   const long long total = (long long)num_tokens * 2 * G * gpr;
   for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
@@ -65,6 +66,7 @@ template <int VPT>
 __global__ void __launch_bounds__(256)
     copy_blocks_kernel(const LayerPtrs ptrs, const int64_t* __restrict__ pairs, long long num_blocks,
                        int vpb, unsigned* err) {
+  pdl_begin();
   const long long src = __ldg(pairs + 2 * (long long)blockIdx.x);
   const long long dst = __ldg(pairs + 2 * (long long)blockIdx.x + 1);
   if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
@@ -104,6 +106,7 @@ template <int VPT>
 __global__ void __launch_bounds__(256)
     swap_blocks_kernel(const SwapPtrs ptrs, const int64_t* __restrict__ pairs, long long src_blocks,
                        long long dst_blocks, int vpb, unsigned* err) {
+  pdl_begin();
   const long long src = __ldg(pairs + 2 * (long long)blockIdx.x);
   const long long dst = __ldg(pairs + 2 * (long long)blockIdx.x + 1);
   if (src < 0 || src >= src_blocks || dst < 0 || dst >= dst_blocks) {
@@ -139,6 +142,7 @@ __global__ void __launch_bounds__(256)
                                  uint8_t* v_cache, const int64_t* __restrict__ slot_mapping, int num_tokens, int G,
                                  int D, int BS, int nhd, long long num_slots, float k_scale, float v_scale,
                                  unsigned* err) {
+  pdl_begin();
   const int cpr = D / 16;  // 16-element chunks per row
   const long long total = (long long)num_tokens * 2 * G * cpr;
   for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
@@ -198,11 +202,12 @@ extern "C" pa_status pa_reshape_and_cache(const void* key, const void* value, vo
   const long long want = (total + 255) / 256;
   const unsigned grid = (unsigned)std::min<long long>(want, (long long)sms * 16);
   auto kern = vpt == 4 ? reshape_and_cache_kernel<4> : (vpt == 2 ? reshape_and_cache_kernel<2> : reshape_and_cache_kernel<1>);
-  kern<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(key), static_cast<const uint4*>(value),
-                                 static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slot_mapping, num_tokens,
-                                 num_kv_heads, vpr, block_size, layout == PA_LAYOUT_NHD ? 1 : 0,
-                                 (long long)num_blocks * block_size, err);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  const cudaError_t e =
+      launch_pdl(kern, dim3(grid), dim3(256), 0, stream, static_cast<const uint4*>(key),
+                 static_cast<const uint4*>(value), static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+                 slot_mapping, num_tokens, num_kv_heads, vpr, block_size, layout == PA_LAYOUT_NHD ? 1 : 0,
+                 (long long)num_blocks * block_size, err);
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 extern "C" pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers,
@@ -233,8 +238,9 @@ extern "C" pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches
       ptrs.v[i] = i < nl ? static_cast<uint4*>(v_caches[l0 + i]) : nullptr;
     }
     dim3 grid((unsigned)num_pairs, (unsigned)nl, 2);
-    copy_blocks_kernel<8><<<grid, 256, 0, stream>>>(ptrs, block_pairs, (long long)num_blocks, vpb, err);
-    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    if (launch_pdl(copy_blocks_kernel<8>, grid, dim3(256), 0, stream, ptrs, block_pairs, (long long)num_blocks, vpb,
+                   err) != cudaSuccess)
+      return PA_ERR_CUDA;
   }
   return PA_OK;
 }
@@ -274,9 +280,9 @@ extern "C" pa_status pa_swap_blocks(void* const* dst_k_caches, void* const* dst_
       ptrs.dst_v[i] = i < nl ? static_cast<uint4*>(dst_v_caches[l0 + i]) : nullptr;
     }
     dim3 grid((unsigned)num_pairs, (unsigned)nl, 2);
-    swap_blocks_kernel<8><<<grid, 256, 0, stream>>>(ptrs, block_pairs, (long long)src_num_blocks,
-                                                    (long long)dst_num_blocks, vpb, err);
-    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    if (launch_pdl(swap_blocks_kernel<8>, grid, dim3(256), 0, stream, ptrs, block_pairs, (long long)src_num_blocks,
+                   (long long)dst_num_blocks, vpb, err) != cudaSuccess)
+      return PA_ERR_CUDA;
   }
   return PA_OK;
 }
@@ -308,21 +314,23 @@ extern "C" pa_status pa_reshape_and_cache_fp8(const void* key, const void* value
   uint8_t* vc = static_cast<uint8_t*>(v_cache);
   const long long nslots = (long long)num_blocks * block_size;
   const int nhd = layout == PA_LAYOUT_NHD ? 1 : 0;
+  cudaError_t e;
   switch (in_dtype) {
     case PA_F32:
-      reshape_and_cache_fp8_kernel<float><<<grid, 256, 0, stream>>>(
-          static_cast<const float*>(key), static_cast<const float*>(value), kc, vc, slot_mapping, num_tokens,
-          num_kv_heads, head_dim, block_size, nhd, nslots, k_scale, v_scale, err);
+      e = launch_pdl(reshape_and_cache_fp8_kernel<float>, dim3(grid), dim3(256), 0, stream,
+                     static_cast<const float*>(key), static_cast<const float*>(value), kc, vc, slot_mapping,
+                     num_tokens, num_kv_heads, head_dim, block_size, nhd, nslots, k_scale, v_scale, err);
       break;
     case PA_F16:
-      reshape_and_cache_fp8_kernel<__half><<<grid, 256, 0, stream>>>(
-          static_cast<const __half*>(key), static_cast<const __half*>(value), kc, vc, slot_mapping, num_tokens,
-          num_kv_heads, head_dim, block_size, nhd, nslots, k_scale, v_scale, err);
+      e = launch_pdl(reshape_and_cache_fp8_kernel<__half>, dim3(grid), dim3(256), 0, stream,
+                     static_cast<const __half*>(key), static_cast<const __half*>(value), kc, vc, slot_mapping,
+                     num_tokens, num_kv_heads, head_dim, block_size, nhd, nslots, k_scale, v_scale, err);
       break;
     default:
-      reshape_and_cache_fp8_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
-          static_cast<const __nv_bfloat16*>(key), static_cast<const __nv_bfloat16*>(value), kc, vc, slot_mapping,
-          num_tokens, num_kv_heads, head_dim, block_size, nhd, nslots, k_scale, v_scale, err);
+      e = launch_pdl(reshape_and_cache_fp8_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, stream,
+                     static_cast<const __nv_bfloat16*>(key), static_cast<const __nv_bfloat16*>(value), kc, vc,
+                     slot_mapping, num_tokens, num_kv_heads, head_dim, block_size, nhd, nslots, k_scale, v_scale,
+                     err);
   }
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

@@ -40,8 +40,10 @@ pa_status launch_cascade_prefix(const CUtensorMap& kmap, const CUtensorMap& vmap
   long long grid = (long long)num_sms * per_sm;
   if (max_items < grid) grid = max_items;
   if (grid <= 0) return PA_OK;
-  kern<<<(unsigned)grid, (kCascadeConsumers + 1) * 32, L.total, stream>>>(kmap, vmap, p);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  return launch_pdl(kern, dim3((unsigned)grid), dim3((kCascadeConsumers + 1) * 32), L.total, stream, kmap, vmap, p) ==
+                 cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
 }
 
 #define PA_INSTANTIATE_CASCADE(DT, D, NT)                                                                   \

@@ -55,6 +55,7 @@ template <typename DT, int D, int NT>
 __global__ void __launch_bounds__((kCascadeConsumers + 1) * 32)
     cascade_prefix_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                           const DecodeParams p) {
+  pdl_begin();
   constexpr int WC = kCascadeConsumers, R = kCascadeStages, JT = kJobTokens, E = (int)sizeof(DT);
   constexpr int TILE = JT * D * E;
   constexpr int NREG = D * E / 128;

@@ -256,6 +256,7 @@ template <typename DT, typename QT, typename OT, int D, int PATH, int MODE>
 __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         const DecodeParams p) {
+  pdl_begin();
   using Cfg = StageCfg<DT, D, PATH>;
   constexpr bool MMA = PATH == kPathMma;
   constexpr bool SPLIT = MODE == kModeSplit;
@@ -1086,6 +1087,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
 // the row's maximum first.
 template <typename OT, int D>
 __global__ void __launch_bounds__(256) lse_reduce_kernel(const DecodeParams p) {
+  pdl_begin();
   constexpr int NT = 256;
   constexpr int VPR = D / 4;        // float4 vectors per partial row
   constexpr int PG = NT / VPR;      // partition groups (8 for D = 128, 16 for D = 64)
@@ -1174,6 +1176,7 @@ __global__ void __launch_bounds__(256) lse_reduce_kernel(const DecodeParams p) {
 // Pass 2 for rows with few partitions (at most 32 slots): one warp per row.
 template <typename OT, int D>
 __global__ void __launch_bounds__(256) lse_reduce_small_kernel(const DecodeParams p) {
+  pdl_begin();
   constexpr int EPL = D / 32;
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;

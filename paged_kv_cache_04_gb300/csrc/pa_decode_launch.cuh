@@ -48,19 +48,20 @@ pa_status launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const 
   const long long ctas = MODE == kModeSuffix ? (max_items + Cfg::W - 1) / Cfg::W : max_items;
   if (ctas < grid) grid = ctas;
   if (grid <= 0) return PA_OK;
-  kern<<<(unsigned)grid, Cfg::W * 32, L.total, stream>>>(kmap, vmap, p);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(Cfg::W * 32), L.total, stream, kmap, vmap, p) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
 }
 
 template <typename OT, int D>
 pa_status launch_lse_reduce(const DecodeParams& p, cudaStream_t stream) {
   const long long rows = (long long)p.S * p.H;
   if (rows <= 0) return PA_OK;
-  if (p.max_partitions <= 32)
-    lse_reduce_small_kernel<OT, D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p);
-  else
-    lse_reduce_kernel<OT, D><<<(unsigned)rows, 256, 0, stream>>>(p);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  const cudaError_t e =
+      p.max_partitions <= 32
+          ? launch_pdl(lse_reduce_small_kernel<OT, D>, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, stream, p)
+          : launch_pdl(lse_reduce_kernel<OT, D>, dim3((unsigned)rows), dim3(256), 0, stream, p);
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 }  // namespace pa
