@@ -167,11 +167,16 @@ DECODE_KERNEL_SOURCES = ("pa_api.cu", "pa_decode.cuh", "pa_decode_bf16.cu", "pa_
 
 
 def kernel_source_sha():
+    """Hash of the decode kernel's sources with comments and whitespace removed
+    (a comment edit does not change the kernel the counters were taken on)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_04_gb300", "csrc")
     for name in DECODE_KERNEL_SOURCES:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(name.encode() + " ".join(text.split()).encode())
     return h.hexdigest()
 
 

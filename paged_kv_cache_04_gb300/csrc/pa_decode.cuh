@@ -6,33 +6,45 @@
 // §5.4; CS349E Lecture 7 notes, §4.2): for sequence s, query head h and kv head
 // kv = h / (H / G),
 //     out[s][h] = sum_t softmax_t(scale * q[s][h] . K[s][t]) V[s][t],  t < ctx[s],
-// where K[s][t] = k_cache[block_tables[s][t / B]][kv][t % B] (HND pool layout).
-// Blockwise evaluation with an online softmax merge gives the same result as a
-// contiguous cache (CMU 15-779 Lecture 16 notes, §3.3).
+// where K[s][t] = k_cache[block_tables[s][t / B]][kv][t % B] (HND pool layout;
+// NHD swaps the last two indices before head_dim). Blockwise evaluation with an
+// online softmax merge gives the same result as a contiguous cache (CMU 15-779
+// Lecture 16 notes, §3.3).
 //
 // Design (one launch, persistent CTAs):
 //   * the unit of data movement is a 16-token job: one (K, V) pair of TMA
 //     boxes of 16 rows x head_dim, taken from one physical block (a 32-token
 //     block is two jobs). Each warp owns R job stages in shared memory, filled
-//     by TMA tensor copies with 128-byte swizzling that complete on the
-//     stage's mbarrier, so a warp always has R - 1 jobs in flight while it
-//     computes one;
+//     by TMA tensor copies (2-D over HND rows, 3-D for NHD; the box lands the
+//     same way) that complete on the stage's mbarrier; the warp's lane 0 issues
+//     the copy of the job R ahead each time it finishes one, so a warp always
+//     has R - 1 jobs in flight while it computes one (a single producer warp
+//     feeding all four rings measured 45% slower: its serial block-table and
+//     context-length loads at item boundaries stall every ring at once);
 //   * plain mode: a work item is (sequence, kv head); items are dealt to CTAs
-//     in a serpentine order, longest contexts first (512-token length buckets,
-//     ties in batch order), and an item's jobs go round-robin to the CTA's W
-//     warps, whose partial (max, sum, output) triples are merged through shared
-//     memory at the end of the item;
+//     in a serpentine order, longest contexts first (ties in batch order), and
+//     an item's jobs go round-robin to the CTA's W warps, whose partial (max,
+//     sum, output) triples are merged through shared memory at the end of the
+//     item;
 //   * split mode: an item is (sequence, kv head, W consecutive partitions) and
 //     warp w handles partition w of it alone, writing its normalised partial
 //     output and (max, sum) to the caller's workspace -- no merge or barrier
 //     inside the CTA (a shared-partition variant with a per-partition merge
 //     measured 40% slower on 32K-128K contexts); a second kernel merges
 //     partitions with log-sum-exp weights;
+//   * suffix mode (shared-prefix decode): items (sequence, kv head) over each
+//     sequence's own tokens are dealt to single warps, which write one partial
+//     each into the slot after the prefix partitions;
 //   * a KV job is read once for all H / G query heads of its kv head: with a
-//     group of >= 4 heads on 16-bit data the step is a small dense contraction
-//     and runs on mma.sync m16n8k16 (tokens x heads for q K^T, d x heads for
-//     P V); otherwise (MHA, fp32) lanes split head_dim and use FFMA;
-//   * the softmax is online, in fp32, base 2, with warp shuffles for the maxima.
+//     group of >= 4 heads on 16-bit or E4M3 data the step is a small dense
+//     contraction and runs on mma.sync m16n8k16 (tokens x heads for q K^T, d x
+//     heads for P V; E4M3 codes are converted to fp16 on the way into the
+//     fragments); otherwise (MHA, group < 4, fp32) lanes split head_dim and use
+//     FFMA, with V staged unswizzled so a token row sits at fixed offsets;
+//   * the softmax is online, in fp32, base 2, with warp shuffles for the maxima;
+//     the output accumulators are rescaled only when a running max grew;
+//   * every kernel waits for the grid before it (programmatic dependent launch)
+//     before touching global memory.
 #pragma once
 
 #include "pa_device.cuh"

@@ -229,15 +229,6 @@ struct fp8e4m3 {
   uint8_t bits;
 };
 
-// Two E4M3 codes (low byte first) -> two fp16 values packed low-first. Every
-// E4M3 value is exact in fp16, so the conversion is exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-  uint32_t r;
-  const unsigned short c = static_cast<unsigned short>(two_codes & 0xffffu);
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(c));
-  return r;
-}
-
 // Four E4M3 codes (one 32-bit word, low byte first) -> two fp16 pairs:
 // lo = codes 0, 1 and hi = codes 2, 3 (each low-first); exact.
 __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
