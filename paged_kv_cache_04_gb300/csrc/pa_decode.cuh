@@ -166,6 +166,11 @@ struct StageCfg {
   // The MHA path is bound by instruction latency with 2 CTAs per SM: two 8 KiB
   // stages per warp let 3 CTAs fit (50% more warps, the same bytes in flight).
   static constexpr int R = kStage <= 4096 ? 4 : (PATH == kPathVecMha ? 2 : 3);
+  // Minimum CTAs per SM for the register allocator (0: unspecified). The E4M3
+  // tensor-core kernels fit 3 CTAs per SM by shared memory; saying so gives them
+  // the registers of that occupancy (left alone, the compiler settles for 128
+  // registers and spills in split mode).
+  static constexpr int MINB = E == 1 && PATH == kPathMma ? 3 : 0;
 };
 
 struct Item {
@@ -265,7 +270,7 @@ struct Schedule {
 // DT: cache element type (float, __half, __nv_bfloat16 or fp8e4m3); QT: query
 // type (DT, or a 16-bit type over an FP8 cache); OT: output type.
 template <typename DT, typename QT, typename OT, int D, int PATH, int MODE>
-__global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
+__global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D, PATH>::MINB)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         const DecodeParams p) {
   pdl_begin();
@@ -274,7 +279,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32)
   constexpr bool SPLIT = MODE == kModeSplit;
   constexpr bool SUFFIX = MODE == kModeSuffix;
   constexpr bool F8 = std::is_same<DT, fp8e4m3>::value;
-  constexpr bool PAIR = F8 && !SPLIT;  // tensor-core path: two jobs per softmax step
+  constexpr bool PAIR = F8;  // tensor-core path: two jobs per softmax step
   static_assert(!PAIR || StageCfg<DT, D, PATH>::R >= 2, "two jobs per step need two stages");
   using MT = typename std::conditional<F8, __half, DT>::type;  // tensor-core operand type
   static_assert(!F8 || D % 64 == 0, "FP8 caches need head_dim a multiple of 64");
