@@ -186,3 +186,37 @@ def test_matches_python_manager_without_caching(seed):
         assert py.num_free() == nat.num_free()
         for s in live:
             assert py.context_len(s) == nat.context_len(s)
+
+
+def test_chain_hash_demo():
+    """The pages' block-size-4 demo: a shared system prompt and start give three
+    equal block hashes and a different fourth; one changed system-prompt token
+    changes that block's hash and every later one."""
+    e = GOLD["chain_hash_demo"]
+    B, n = e["block_size"], e["shared_blocks"]
+    system, start = [11, 12, 13, 14, 15, 16], [21, 22, 23, 24, 25, 26]
+    a = system + start + [31, 32, 33, 34]   # 16 tokens: four full blocks
+    b = system + start + [41, 42, 43, 44]   # differs only in the fourth block
+    bm = NativeBlockManager(64, B)
+    assert bm.add_sequence(0, a) == 0
+    assert bm.add_sequence(1, b) == n * B
+    assert bm.block_table(1)[:n] == bm.block_table(0)[:n]
+    assert bm.block_table(1)[n] != bm.block_table(0)[n]
+    c = list(b)
+    c[5] = 99                               # a system-prompt token in the second block
+    assert bm.add_sequence(2, c) == 1 * B   # only the first block still matches
+    d = list(b)
+    d[0] = 99                               # ... in the first block: nothing matches
+    assert bm.add_sequence(3, d) == 0
+
+
+def test_block_aligned_prefix_only():
+    """Prompts that first differ at token 17 share exactly the first 16-token block."""
+    e = GOLD["block_aligned_prefix"]
+    B = e["block_size"]
+    k = e["first_differing_token"] - 1       # 0-based index of the first different token
+    a = list(range(100, 140))
+    b = a[:k] + [999] + a[k + 1:]
+    bm = NativeBlockManager(64, B)
+    bm.add_sequence(0, a)
+    assert bm.add_sequence(1, b) == e["shared_tokens"]
