@@ -277,15 +277,35 @@ def run_ours(args, rank, world, local):
     h2d = sum(v.numel() * v.element_size() for k, v in host[0][0].items() if k != "out")
     d2h = host[0][0]["out"].numel() * host[0][0]["out"].element_size()
 
+    # As a serving loop would: step i's inputs go up on an upload stream while step
+    # i - 1 computes, and its output comes back on a download stream; events keep
+    # each double-buffered input / output pair from being reused too early.
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    computed = [torch.cuda.Event() for _ in range(2)]
+    fetched = [torch.cuda.Event() for _ in range(2)]
+    for j in range(2):  # every buffer starts free
+        computed[j].record(stream)
+        fetched[j].record(stream)
+
     def e2e_step(i):
-        wl = batches[i % 2]
-        h, d = host[i % 2]
-        for k in d:
-            d[k].copy_(h[k], non_blocking=True)
+        j = i % 2
+        wl = batches[j]
+        h, d = host[j]
+        with torch.cuda.stream(up):
+            up.wait_event(computed[j])  # step i - 2 has finished reading these device inputs
+            for k in d:
+                d[k].copy_(h[k], non_blocking=True)
+            in_ready[j].record(up)
+        stream.wait_event(in_ready[j])
+        stream.wait_event(fetched[j])  # step i - 2's output has left this buffer
         pa.pa_reshape_and_cache(d["new_key"], d["new_value"], wl.k_cache, wl.v_cache, d["slot_mapping"])
-        pa.pa_decode(outs[i % 2], d["q"], wl.k_cache, wl.v_cache, d["block_tables"], d["context_lens"],
-                     wl.scale)
-        h["out"].copy_(outs[i % 2], non_blocking=True)
+        pa.pa_decode(outs[j], d["q"], wl.k_cache, wl.v_cache, d["block_tables"], d["context_lens"], wl.scale)
+        computed[j].record(stream)
+        with torch.cuda.stream(down):
+            down.wait_event(computed[j])
+            h["out"].copy_(outs[j], non_blocking=True)
+            fetched[j].record(down)
 
     for i in range(3):
         e2e_step(i)
@@ -295,13 +315,18 @@ def run_ours(args, rank, world, local):
     barrier(world)
     torch.cuda.synchronize()
     e0.record(stream)
+    up.wait_event(e0)
     for i in range(K2):
         e2e_step(i)
+    stream.wait_event(fetched[(K2 - 1) % 2])  # the last output is on the host
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     clk = clocks.stop()
+    for j in range(2):  # the overlapped copies delivered each batch's output
+        if not torch.equal(host[j][0]["out"], outs[j].cpu()):
+            raise RuntimeError("end-to-end output on the host differs from the device output")
     err = pa.pa_get_error()
     if err:
         raise RuntimeError(f"device error word set: {err}")
