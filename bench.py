@@ -59,7 +59,7 @@ def parse():
                          "cascade (32 prompts x 8 samples), mha (the OPT-13B batch)")
     ap.add_argument("--workload", default="llama8b",
                     choices=["llama8b", "tiny", "opt13b", "shared", "shared_cow", "long70b_b16", "long70b_b32",
-                             "llama8b_fp8", "long70b_b16_fp8", "shared_cascade", "shared_cow_cascade",
+                             "llama8b_fp8", "long70b_b16_fp8", "shared_cascade", "shared_cow_cascade", "gemma_d256",
                              "llama8b_nhd", "llama8b_fp8_nhd", "long70b_b16_nhd", "shared_cascade_nhd",
                              "copy_blocks", "swap_out", "swap_in", "reshape", "reshape_prefill"],
                     help="the other workload shapes give a device-timed line of their own (no e2e / CPU legs); "
@@ -664,6 +664,8 @@ def run_workload(args):
         wl = workloads.llama8b(device=dev)
     elif name == "llama8b_fp8":
         wl = workloads.to_fp8(workloads.llama8b(device=dev))
+    elif name == "gemma_d256":
+        wl = workloads.gemma_d256(device=dev)
     elif name.startswith("long70b"):
         B = 32 if "b32" in name else 16
         wl = workloads.long70b(device=dev, B=B)

@@ -29,9 +29,11 @@
  *     token t of a sequence lives in physical block block_table[t / block_size],
  *     row t % block_size. Query head h reads kv head h / (num_heads / num_kv_heads).
  *   - q, out, key, value and the caches must be 16-byte aligned.
- *   - Supported: head_dim 64 or 128; block_size 16 or 32; num_heads /
+ *   - Supported: head_dim 64, 128 or 256; block_size 16 or 32; num_heads /
  *     num_kv_heads from 1 to 8; element types PA_F32, PA_F16, PA_BF16, and
  *     E4M3 caches through the *_fp8 calls (copy and swap move any type).
+ *     The E4M3 decode calls take head_dim 128 and pa_decode_cascade head_dim
+ *     64 or 128; other values return PA_ERR_UNSUPPORTED.
  */
 #ifndef PA_H
 #define PA_H

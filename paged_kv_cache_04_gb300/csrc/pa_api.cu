@@ -112,7 +112,8 @@ pa_status check_decode(const DecodeArgs& a) {
   if (!aligned16(a.out) || !aligned16(a.q) || !aligned16(a.k_cache) || !aligned16(a.v_cache) ||
       (reinterpret_cast<uintptr_t>(a.block_tables) & 3u) || (reinterpret_cast<uintptr_t>(a.context_lens) & 3u))
     return PA_ERR_INVALID_ARG;
-  if ((a.D != 64 && a.D != 128) || (a.BS != 16 && a.BS != 32) || a.H / a.G > kMaxGroup) return PA_ERR_UNSUPPORTED;
+  if ((a.D != 64 && a.D != 128 && a.D != 256) || (a.BS != 16 && a.BS != 32) || a.H / a.G > kMaxGroup)
+    return PA_ERR_UNSUPPORTED;
   if (a.odt != a.dt && a.odt != PA_F32) return PA_ERR_UNSUPPORTED;
   // TMA row coordinates are 32-bit
   if ((long long)a.num_blocks * a.G * a.BS > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
@@ -124,7 +125,7 @@ pa_status dispatch_mode(const CUtensorMap& km, const CUtensorMap& vm, const Deco
                         long long items, int mode, cudaStream_t st) {
   if (mode == kModeSplit) return launch_decode<DT, QT, float, D, PATH, kModeSplit>(km, vm, p, sms, items, st);
   if (mode == kModeSuffix) {
-    if constexpr (sizeof(DT) == 2)  // the shared-prefix decode serves 16-bit caches
+    if constexpr (sizeof(DT) == 2 && D <= 128)  // the shared-prefix decode: 16-bit caches, head_dim <= 128
       return launch_decode<DT, QT, float, D, PATH, kModeSuffix>(km, vm, p, sms, items, st);
     return PA_ERR_UNSUPPORTED;
   }
@@ -138,7 +139,10 @@ pa_status dispatch_path(const CUtensorMap& km, const CUtensorMap& vm, const Deco
   if constexpr (sizeof(DT) <= 2) {
     if (p.group >= 4) return dispatch_mode<DT, QT, OT, D, kPathMma>(km, vm, p, sms, items, mode, st);
   }
-  if (p.group == 1) return dispatch_mode<DT, QT, OT, D, kPathVecMha>(km, vm, p, sms, items, mode, st);
+  // (head_dim 256: q stays in shared memory; a lane's half of a 256-wide row in registers would spill)
+  if constexpr (D <= 128) {
+    if (p.group == 1) return dispatch_mode<DT, QT, OT, D, kPathVecMha>(km, vm, p, sms, items, mode, st);
+  }
   return dispatch_mode<DT, QT, OT, D, kPathVec>(km, vm, p, sms, items, mode, st);
 }
 
@@ -147,12 +151,14 @@ pa_status dispatch_shape(const CUtensorMap& km, const CUtensorMap& vm, const Dec
                          long long items, int mode, cudaStream_t st) {
   if (D == 64) return dispatch_path<DT, DT, OT, 64>(km, vm, p, sms, items, mode, st);
   if (D == 128) return dispatch_path<DT, DT, OT, 128>(km, vm, p, sms, items, mode, st);
+  if (D == 256) return dispatch_path<DT, DT, OT, 256>(km, vm, p, sms, items, mode, st);
   return PA_ERR_UNSUPPORTED;
 }
 
 template <typename OT>
 pa_status dispatch_reduce(const DecodeParams& p, int D, cudaStream_t st) {
-  return D == 64 ? launch_lse_reduce<OT, 64>(p, st) : launch_lse_reduce<OT, 128>(p, st);
+  if (D == 64) return launch_lse_reduce<OT, 64>(p, st);
+  return D == 128 ? launch_lse_reduce<OT, 128>(p, st) : launch_lse_reduce<OT, 256>(p, st);
 }
 
 // Shared-prefix groups for pa_decode_cascade (all null / zero otherwise).
@@ -429,6 +435,7 @@ extern "C" pa_status pa_decode_cascade(void* out, const void* q, const void* k_c
       (reinterpret_cast<uintptr_t>(prefix_lens) & 3u))
     return PA_ERR_INVALID_ARG;
   if (dtype != PA_BF16 && dtype != PA_F16) return PA_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;  // the prefix pass: head_dim <= 128
   if (num_seqs > kSplitMaxSeqs || num_groups > kSplitMaxSeqs) return PA_ERR_UNSUPPORTED;
   const long long rows_per_group = (long long)max_group_size * (num_heads / num_kv_heads);
   if (rows_per_group > 2LL * 8 * kCascadeConsumers) return PA_ERR_UNSUPPORTED;

@@ -165,12 +165,14 @@ struct StageCfg {
   static constexpr int W = 4;
   // The MHA path is bound by instruction latency with 2 CTAs per SM: two 8 KiB
   // stages per warp let 3 CTAs fit (50% more warps, the same bytes in flight).
-  static constexpr int R = kStage <= 4096 ? 4 : (PATH == kPathVecMha ? 2 : 3);
+  // head_dim 256 makes a job 16 KiB (16-bit) or 32 KiB (fp32): one stage per
+  // warp, so that two CTAs (eight warps) share an SM instead of one.
+  static constexpr int R = D > 128 ? 1 : (kStage <= 4096 ? 4 : (PATH == kPathVecMha ? 2 : 3));
   // Minimum CTAs per SM for the register allocator (0: unspecified). The E4M3
   // tensor-core kernels fit 3 CTAs per SM by shared memory; saying so gives them
   // the registers of that occupancy (left alone, the compiler settles for 128
-  // registers and spills in split mode).
-  static constexpr int MINB = E == 1 && PATH == kPathMma ? 3 : 0;
+  // registers and spills in split mode). head_dim 256 runs two CTAs per SM.
+  static constexpr int MINB = E == 1 && PATH == kPathMma ? 3 : (D > 128 ? 2 : 0);
 };
 
 struct Item {
@@ -1001,7 +1003,18 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
                 o[h][2] = fmaf(w, f2, o[h][2]);
                 o[h][3] = fmaf(w, f3, o[h][3]);
               } else if constexpr (E == 4) {
-                if constexpr (VB == 16) {
+                if constexpr (VB == 32) {
+                  const float4 v0 = *reinterpret_cast<const float4*>(src);
+                  const float4 v1 = *reinterpret_cast<const float4*>(src + 16);
+                  o[h][0] = fmaf(w, v0.x, o[h][0]);
+                  o[h][1] = fmaf(w, v0.y, o[h][1]);
+                  o[h][2] = fmaf(w, v0.z, o[h][2]);
+                  o[h][3] = fmaf(w, v0.w, o[h][3]);
+                  o[h][4] = fmaf(w, v1.x, o[h][4]);
+                  o[h][5] = fmaf(w, v1.y, o[h][5]);
+                  o[h][6] = fmaf(w, v1.z, o[h][6]);
+                  o[h][7] = fmaf(w, v1.w, o[h][7]);
+                } else if constexpr (VB == 16) {
                   const float4 v = *reinterpret_cast<const float4*>(src);
                   o[h][0] = fmaf(w, v.x, o[h][0]);
                   o[h][1] = fmaf(w, v.y, o[h][1]);
@@ -1013,7 +1026,17 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
                   o[h][1] = fmaf(w, v.y, o[h][1]);
                 }
               } else {
-                if constexpr (VB == 8) {
+                if constexpr (VB == 16) {
+                  const uint4 raw = *reinterpret_cast<const uint4*>(src);
+                  const uint32_t wd[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) {
+                    float f0, f1;
+                    unpack2(wd[i], (DT*)nullptr, f0, f1);
+                    o[h][2 * i] = fmaf(w, f0, o[h][2 * i]);
+                    o[h][2 * i + 1] = fmaf(w, f1, o[h][2 * i + 1]);
+                  }
+                } else if constexpr (VB == 8) {
                   const uint2 raw = *reinterpret_cast<const uint2*>(src);
                   float f0, f1, f2, f3;
                   unpack2(raw.x, (DT*)nullptr, f0, f1);

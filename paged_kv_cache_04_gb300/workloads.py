@@ -220,6 +220,15 @@ def llama8b(device="cpu", S=256, num_blocks=100_000, new_token=True, rotate=0) -
                                  device, new_token=new_token, rotate=rotate)
 
 
+def gemma_d256(device="cpu", S=256, num_blocks=50_000, new_token=True) -> Workload:
+    """head_dim 256 with a group of 2 (16 q / 8 kv heads, the Gemma-2-9B layer
+    shape), bf16, block 16: the Llama-3.1-8B batch's lengths (U[512, 4096]) and a
+    shuffled pool of the same byte size (a block holds 2x the bytes)."""
+    ctx = uniform_lengths(S, 512, 4096, _gen(SEED_CTX)).tolist()
+    return batch_with_new_tokens("gemma_d256", S, 16, 8, 256, 16, torch.bfloat16, ctx, num_blocks,
+                                 device, new_token=new_token)
+
+
 def long70b(device="cpu", S=8, B=16, lo=32768, hi=131072, partition_tokens=512,
             new_token=True) -> Workload:
     ctx = uniform_lengths(S, lo, hi, _gen(SEED_CTX)).tolist()
@@ -328,7 +337,7 @@ def to_nhd(wl: Workload) -> Workload:
 
 
 def by_name(name: str, device="cpu", **kw) -> Workload:
-    table = {"tiny": tiny, "opt13b": opt13b, "llama8b": llama8b, "long70b": long70b,
+    table = {"tiny": tiny, "opt13b": opt13b, "llama8b": llama8b, "long70b": long70b, "gemma_d256": gemma_d256,
              "shared": shared_prefix,
              "shared_cow": lambda device="cpu", **k: shared_prefix(device, cow=True, **k)}
     return table[name](device=device, **kw)

@@ -69,6 +69,11 @@ def test_invalid_arguments_rejected_before_any_launch(lib_path):
     assert lib.pa_decode(al, al, al, al, al, 1, al, 2, 8, 8, 96, 16, 0, 10, 1.0, 2, 2, null) == 2
     assert lib.pa_decode(al, al, al, al, al, 1, al, 2, 8, 8, 128, 8, 0, 10, 1.0, 2, 2, null) == 2
     assert lib.pa_decode(al, al, al, al, al, 1, al, 2, 32, 2, 128, 16, 0, 10, 1.0, 2, 2, null) == 2
+    assert lib.pa_decode(al, al, al, al, al, 1, al, 2, 8, 8, 512, 16, 0, 10, 1.0, 2, 2, null) == 2
+    # head_dim 256 is served by pa_decode / pa_decode_split, not by the E4M3 calls or the cascade
+    assert lib.pa_decode_fp8(al, al, al, al, al, 1, al, 2, 8, 8, 256, 16, 0, 10, 1.0, 1.0, 1.0, 2, 2, null) == 2
+    assert lib.pa_decode_cascade(al, al, al, al, al, 4, al, 2, 8, 8, 256, 16, 0, 10, 1.0, 2, 2, al, al, 1, 2, 32,
+                                 64, 32, al, 1 << 30, null) == 2
     # out dtype must be the cache dtype or fp32
     assert lib.pa_decode(al, al, al, al, al, 1, al, 2, 8, 8, 128, 16, 0, 10, 1.0, 2, 1, null) == 2
     # split: partition not a multiple of the block size; workspace too small

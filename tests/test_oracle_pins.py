@@ -116,6 +116,24 @@ def pin_nhd_paged_equals_contiguous(lib):
             assert np.abs(merged[s] - ref).max() <= 1e-12, f"NHD partitions != contiguous (G={G} B={B})"
 
 
+def pin_head_dim_256(lib):
+    """head_dim 256 (HND and NHD, plain and partitioned) gives the contiguous SDPA
+    result: nothing in the oracle depends on the width of a head."""
+    rng = np.random.default_rng(23)
+    ctxs = [1, 17, 50]
+    for layout in ("HND", "NHD"):
+        for H, G, B in ((4, 2, 16), (2, 2, 32)):
+            q, Ks, Vs = random_case(rng, ctxs, H, G, 256)
+            kc, vc, bt = paged_from_contiguous(Ks, Vs, B, rng, layout=layout)
+            cl = np.array(ctxs, np.int32)
+            out = oatt.decode(q, kc, vc, bt, cl, 0.0625, lib=lib, layout=layout)
+            merged = oatt.merge(*oatt.partitions(q, kc, vc, bt, cl, 0.0625, B, lib=lib, layout=layout), lib=lib)
+            for s in range(len(ctxs)):
+                ref = sdpa_reference(q[s], Ks[s], Vs[s], 0.0625)
+                assert np.abs(out[s] - ref).max() <= 1e-12, f"d=256 {layout} paged != contiguous"
+                assert np.abs(merged[s] - ref).max() <= 1e-12, f"d=256 {layout} partitions != contiguous"
+
+
 def pin_one_token_is_v(lib):
     rng = np.random.default_rng(12)
     q, Ks, Vs = random_case(rng, [1, 1, 1], 4, 2, 16)
@@ -234,8 +252,8 @@ def pin_empty_context_is_zero(lib):
     assert np.array_equal(out[0], np.zeros_like(out[0]))
 
 
-PINS = [pin_paged_equals_contiguous, pin_nhd_paged_equals_contiguous, pin_one_token_is_v, pin_equal_scores_give_mean,
-        pin_weights_sum_to_one, pin_brute_force_tiny, pin_decoders, pin_16bit_paths_match_upcast,
+PINS = [pin_paged_equals_contiguous, pin_nhd_paged_equals_contiguous, pin_head_dim_256, pin_one_token_is_v,
+        pin_equal_scores_give_mean, pin_weights_sum_to_one, pin_brute_force_tiny, pin_decoders, pin_16bit_paths_match_upcast,
         pin_partitions_merge_to_decode, pin_empty_context_is_zero]
 
 
