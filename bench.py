@@ -54,12 +54,13 @@ def parse():
                     help="run only the step's kernels on a 64-sequence batch of the same shape (for ncu)")
     ap.add_argument("--profile-fp8", action="store_true",
                     help="the same 64-sequence case with an E4M3 cache (for ncu)")
-    ap.add_argument("--profile-case", choices=["split", "cascade", "mha"], default=None,
+    ap.add_argument("--profile-case", choices=["split", "cascade", "cascade_x16", "mha"], default=None,
                     help="a small case of another path for ncu: split (2 seqs, 48K-64K tokens, 64 q / 8 kv), "
                          "cascade (32 prompts x 8 samples), mha (the OPT-13B batch)")
     ap.add_argument("--workload", default="llama8b",
                     choices=["llama8b", "tiny", "opt13b", "shared", "shared_cow", "long70b_b16", "long70b_b32",
                              "llama8b_fp8", "long70b_b16_fp8", "shared_cascade", "shared_cow_cascade", "gemma_d256",
+                             "shared_x16", "shared_x16_cascade",
                              "llama8b_nhd", "llama8b_fp8_nhd", "long70b_b16_nhd", "shared_cascade_nhd",
                              "copy_blocks", "swap_out", "swap_in", "reshape", "reshape_prefill"],
                     help="the other workload shapes give a device-timed line of their own (no e2e / CPU legs); "
@@ -650,7 +651,9 @@ def run_workload(args):
     elif name == "opt13b":
         wl = workloads.opt13b(device=dev)
     elif name.startswith("shared"):
-        wl = workloads.shared_prefix(device=dev, cow=name.startswith("shared_cow"))
+        # _x16: 32 prompts x 16 samples (64 query rows per group), else 64 x 8 (32 rows)
+        wl = workloads.shared_prefix(device=dev, cow=name.startswith("shared_cow"),
+                                     **({"prompts": 32, "samples": 16} if "_x16" in name else {}))
         # set-up: the CoW copies and every appended token, once; a timed step then
         # repeats the copies and writes each sample's newest token before decoding
         if wl.copy_pairs.numel():
@@ -811,11 +814,13 @@ def run_other_profile_case(args):
         wl = workloads.long70b(device=dev, S=2, lo=48_000, hi=64_000)
     elif name == "cascade":
         wl = workloads.shared_prefix(device=dev, prompts=32)
+    elif name == "cascade_x16":  # 64 query rows per group: the tcgen05 prefix pass
+        wl = workloads.shared_prefix(device=dev, prompts=16, samples=16)
     else:
         wl = workloads.opt13b(device=dev)
     out = torch.empty_like(wl.q)
     mctx, T = wl.max_context, 512
-    if name == "cascade":
+    if name.startswith("cascade"):
         pa.pa_reshape_and_cache(wl.new_key, wl.new_value, wl.k_cache, wl.v_cache, wl.slot_mapping)
         gs = torch.tensor(wl.meta["group_starts"], dtype=torch.int32, device=dev)
         pl = torch.tensor(wl.meta["prefix_lens"], dtype=torch.int32, device=dev)
@@ -825,9 +830,9 @@ def run_other_profile_case(args):
     elif name == "split":
         ws = torch.empty(pa.pa_decode_split_workspace_bytes(wl.S, wl.H, wl.d, mctx, T), dtype=torch.uint8, device=dev)
     for _ in range(args.warmup + args.steps):
-        if name == "cascade":
+        if name.startswith("cascade"):
             pa.pa_decode_cascade(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale,
-                                 gs, pl, 8, pmax, mctx, T, ws)
+                                 gs, pl, wl.meta["samples"], pmax, mctx, T, ws)
         elif name == "split":
             pa.pa_reshape_and_cache(wl.new_key, wl.new_value, wl.k_cache, wl.v_cache, wl.slot_mapping)
             pa.pa_decode_split(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale,
@@ -839,7 +844,7 @@ def run_other_profile_case(args):
     kv = roofline.decode_bytes(wl.context_lens.tolist(), wl.H, wl.G, wl.d, wl.k_cache.element_size())
     info = {"profile_case": name, "seqs": wl.S, "tokens": int(wl.context_lens.sum().item()),
             "decode_bytes_per_launch": kv, "device_errors": pa.pa_get_error()}
-    if name == "cascade":
+    if name.startswith("cascade"):
         info["unique_kv_tokens"] = wl.meta["unique_tokens"]
     print(json.dumps(info))
 

@@ -218,23 +218,31 @@ pa_status run_decode(const DecodeArgs& a, bool split, int partition, int max_par
     p.num_groups = c.num_groups;
     p.suffix_slot = c.prefix_slots;
     p.suffix_single = 1;
+    const long long lim_ws = (long long)c.prefix_slots * partition, lim_bt = (long long)a.max_blocks * a.BS;
+    p.prefix_limit = (int)(lim_ws < lim_bt ? lim_ws : lim_bt);
     if (c.prefix_slots > 0) {  // prefix pass: every group's query rows over its shared blocks
       const long long pitems = (long long)c.num_groups * a.G * c.prefix_slots;
       CUtensorMap vsw = vm;  // the prefix pass reads V with ldmatrix: swizzled stages
       if (!mma_path &&
           (s = make_pool_map(&vsw, a.v_cache, a.dt, a.D, a.G, a.BS, a.num_blocks, a.layout)) != PA_OK)
         return s;
+      // A group of more than 32 query rows fills the M = 64 tile of the tcgen05
+      // pass; up to 32 rows, the mma.sync pass (four warps of 8 rows) wastes no lane.
       const bool bf = a.dt == PA_BF16;
-      if (a.D == 128)
-        s = c.nt == 1 ? (bf ? launch_cascade_prefix<__nv_bfloat16, 128, 1>(km, vsw, p, sms, pitems, st)
-                            : launch_cascade_prefix<__half, 128, 1>(km, vsw, p, sms, pitems, st))
-                      : (bf ? launch_cascade_prefix<__nv_bfloat16, 128, 2>(km, vsw, p, sms, pitems, st)
-                            : launch_cascade_prefix<__half, 128, 2>(km, vsw, p, sms, pitems, st));
-      else
-        s = c.nt == 1 ? (bf ? launch_cascade_prefix<__nv_bfloat16, 64, 1>(km, vsw, p, sms, pitems, st)
-                            : launch_cascade_prefix<__half, 64, 1>(km, vsw, p, sms, pitems, st))
-                      : (bf ? launch_cascade_prefix<__nv_bfloat16, 64, 2>(km, vsw, p, sms, pitems, st)
-                            : launch_cascade_prefix<__half, 64, 2>(km, vsw, p, sms, pitems, st));
+      if (c.nt == 2) {
+        if (a.D == 128)
+          s = bf ? launch_cascade_prefix_tc<__nv_bfloat16, 128>(km, vsw, p, sms, pitems, st)
+                 : launch_cascade_prefix_tc<__half, 128>(km, vsw, p, sms, pitems, st);
+        else
+          s = bf ? launch_cascade_prefix_tc<__nv_bfloat16, 64>(km, vsw, p, sms, pitems, st)
+                 : launch_cascade_prefix_tc<__half, 64>(km, vsw, p, sms, pitems, st);
+      } else if (a.D == 128) {
+        s = bf ? launch_cascade_prefix<__nv_bfloat16, 128, 1>(km, vsw, p, sms, pitems, st)
+               : launch_cascade_prefix<__half, 128, 1>(km, vsw, p, sms, pitems, st);
+      } else {
+        s = bf ? launch_cascade_prefix<__nv_bfloat16, 64, 1>(km, vsw, p, sms, pitems, st)
+               : launch_cascade_prefix<__half, 64, 1>(km, vsw, p, sms, pitems, st);
+      }
       if (s != PA_OK) return s;
     }
   }
@@ -447,7 +455,7 @@ extern "C" pa_status pa_decode_cascade(void* out, const void* q, const void* k_c
   c.prefix_lens = prefix_lens;
   c.num_groups = num_groups;
   c.prefix_slots = (max_prefix_len + partition_tokens - 1) / partition_tokens;
-  c.nt = rows_per_group > 8 * kCascadeConsumers ? 2 : 1;
+  c.nt = rows_per_group > 8 * kCascadeConsumers ? 2 : 1;  // 2: the tcgen05 prefix pass
   const long long P = c.prefix_slots + 1;  // prefix partitions, then one slot for each sequence's own tokens
   if ((long long)num_seqs * num_kv_heads * P > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
   return run_decode(a, true, partition_tokens, (int)P, workspace, stream, c);

@@ -89,7 +89,10 @@ __global__ void __launch_bounds__((kCascadeConsumers + 1) * 32)
     const int b = lane * per, e = min(p.num_groups, b + per);
     auto parts = [&](int g) { return (group_prefix(p, g) + p.partition - 1) / p.partition; };
     int local = 0;
-    for (int g = b; g < e; ++g) local += parts(g);
+    for (int g = b; g < e; ++g) {
+      if (blockIdx.x == 0) check_group_prefix(p, g);
+      local += parts(g);
+    }
     int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {

@@ -1,0 +1,569 @@
+// Shared-prefix (cascade) decode, prefix pass on the fifth-generation tensor
+// cores (tcgen05, accumulators in tensor memory).
+//
+// What is computed is the same as for the other prefix pass: every query row of
+// a group (member x query head of one kv head) attends the group's shared
+// prefix, partition by partition, and writes the partition's normalised
+// partial output with its (max, sum) (CS349E Lecture 7 notes §5.1 and §5.3 for
+// the shared blocks; CMU 15-779 Lecture 16 notes §3.3 for the merge). Here the
+// group's rows form the M = 64 side of real matrix products:
+//   S = Q K^T   M = 64 rows (padded), N = 32 tokens, K = head_dim
+//   O += P V    M = 64 rows, N = head_dim, K = 32 tokens
+// Warp roles (192 threads):
+//   warps 0-3  softmax: thread t < 16 of warp w owns query row 16 w + t, which
+//              an M = 64 accumulator keeps in tensor-memory lane 32 w + t; it
+//              reads its row of S, keeps the running (max, sum), writes its row
+//              of P (16-bit hi + lo parts) to shared memory and, at the end of
+//              an item, reads its row of O;
+//   warp 4     TMA producer: two 16-token jobs per stage (K and V, 128-byte
+//              swizzle), a ring of three stages;
+//   warp 5     owns the tensor memory (allocation, release); its lane 0 issues
+//              every MMA and commits them to mbarriers.
+// S is double-buffered in tensor memory and P in shared memory, so the scores
+// of a tile are computed, and the P V of the one before runs, while the
+// softmax warps work on a tile. The accumulator O is rescaled
+// lazily: a row's reference max moves only when a score exceeds it by more
+// than kTcRescale (log2 units); weights then stay below 2^kTcRescale and the
+// result is the same softmax (numerator and denominator share the reference).
+// Every wait is time-bounded; on a timeout all roles stop, the copies and
+// MMAs in flight are waited for, and the tensor memory is released.
+#pragma once
+
+#include "pa_decode.cuh"
+
+namespace pa {
+
+constexpr int kTcRows = 64;        // M: query rows of one group (members x heads), padded
+constexpr int kTcTokens = 32;      // N of S, K of P V: tokens per stage (two TMA jobs)
+constexpr int kTcStages = 3;
+constexpr int kTcThreads = 192;
+constexpr float kTcRescale = 8.f;
+
+struct TcLayout {
+  unsigned q_bytes, stage_off, stage_bytes, p_off, bar_off, misc_off, sched_off, total;
+};
+
+// Offsets from the 1024-byte aligned base: two Q tiles, the stages (K then V,
+// each [head_dim / 64 regions][32 tokens][128 B]), two P buffers ([64 rows]
+// [128 B]: a row's 32 hi weights, then its 32 lo weights), mbarriers, the
+// tensor-memory base, the abort flag, per-stage job flags and the group scan.
+__host__ __device__ inline TcLayout tc_layout(int D, int num_groups) {
+  TcLayout L;
+  L.q_bytes = kTcRows * D * 2;
+  L.stage_off = 2 * L.q_bytes;
+  L.stage_bytes = 2u * kTcTokens * D * 2;
+  L.p_off = L.stage_off + kTcStages * L.stage_bytes;
+  L.bar_off = L.p_off + 2 * kTcRows * 128;
+  L.misc_off = L.bar_off + (2 * kTcStages + 12) * 8;
+  L.sched_off = round_up(L.misc_off + 16, 16);
+  L.total = round_up(L.sched_off + (num_groups + 1) * 4, 16) + 1024;
+  return L;
+}
+
+// ---- tcgen05 ------------------------------------------------------------------
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor, 128-byte swizzle: start address, leading and
+// stride byte offsets (>> 4 each), descriptor version 1, layout type 2.
+//   K-major tile ([rows][64-element regions]): stride offset = 1024 (one group
+//   of 8 rows), leading offset unused;
+//   MN-major tile (rows along K): leading offset = the stride between
+//   64-element regions along MN, stride offset = 1024 (8 rows along K).
+__device__ __forceinline__ uint64_t tc_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of kind::f16 with an fp32 accumulator: operand format
+// (0 fp16, 1 bf16) for A and B, B MN-major or K-major, N >> 3, M >> 4.
+template <typename DT>
+__host__ __device__ constexpr uint32_t tc_idesc(int M, int N, bool b_mn_major) {
+  return (1u << 4) | ((std::is_same<DT, __nv_bfloat16>::value ? 1u : 0u) << 7) |
+         ((std::is_same<DT, __nv_bfloat16>::value ? 1u : 0u) << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every MMA this thread issued before has completed.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// 32 consecutive 32-bit columns of this thread's lane (warp-collective).
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// A box of fill values (zeros) for a job that does not exist: every row of the
+// box lies before the start of the pool.
+__device__ __forceinline__ void tma_load_zero_tile(void* dst, const CUtensorMap* map, const DecodeParams& p, int x,
+                                                   uint64_t* bar) {
+  if (p.nhd)
+    tma_load_3d(dst, map, x, 0, -kJobTokens, bar);
+  else
+    tma_load_2d(dst, map, x, -kJobTokens, bar);
+}
+
+template <typename DT, int D>
+__global__ void __launch_bounds__(kTcThreads, 2)
+    cascade_prefix_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                             const DecodeParams p) {
+  pdl_begin();
+  static_assert(sizeof(DT) == 2 && (D == 64 || D == 128), "tensor-core prefix pass: 16-bit caches, head_dim 64/128");
+  constexpr int R = kTcStages, NT = kTcTokens, JT = kJobTokens, M = kTcRows;
+  constexpr int NREG = D / 64;            // 128-byte regions of a row
+  constexpr int TILE = NT * D * 2;        // K (or V) bytes of one stage
+  constexpr int REG_BYTES = NT * 128;     // one region of a stage's K (or V): [32 tokens][128 B]
+  constexpr int KSTEPS = D / 16;
+  constexpr uint32_t TCOLS = D + 2 * NT <= 128 ? 128u : 256u;  // O (D columns) + two S buffers
+  constexpr uint32_t O_COL = 0, S_COL = D;
+  constexpr uint32_t ID_S = tc_idesc<DT>(M, NT, false);
+  constexpr uint32_t ID_PV = tc_idesc<DT>(M, D, true);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const TcLayout L = tc_layout(D, p.num_groups);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
+  uint64_t* full = bars;              // [R] TMA -> MMA
+  uint64_t* empty = bars + R;         // [R] MMA (P V done) -> TMA
+  uint64_t* s_full = bars + 2 * R;    // [2] S written -> softmax
+  uint64_t* s_free = s_full + 2;      // [2] S read -> MMA
+  uint64_t* q_full = s_full + 4;      // [2] Q tile written -> MMA
+  uint64_t* p_full = s_full + 6;      // [2] P buffer written -> MMA
+  uint64_t* pv_done = s_full + 8;     // [2] P V of that buffer done -> softmax (buffer free; O current)
+  uint64_t* o_free = s_full + 10;     // O read at the end of an item -> MMA
+  uint64_t* fin = s_full + 11;        // every MMA done (teardown)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc_off);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc_off + 4);
+  // [R] bit j: job j of the stage comes from a block in the pool. Written before
+  // the producer's arrive on full[stage] and read after a wait on it.
+  volatile uint8_t* job_ok = smem + L.misc_off + 8;
+  int* pstart = reinterpret_cast<int*>(smem + L.sched_off);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < R; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&s_free[b], 4);
+      mbar_init(&q_full[b], 4);
+      mbar_init(&p_full[b], 4);
+      mbar_init(&pv_done[b], 1);
+    }
+    mbar_init(o_free, 4);
+    mbar_init(fin, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (threadIdx.x == 32) {
+    prefetch_tensormap(&kmap);
+    prefetch_tensormap(&vmap);
+  }
+  if (warp == 5) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(TCOLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (warp == 0) {  // exclusive scan over groups of their prefix partitions
+    const int per = (p.num_groups + 31) / 32;
+    const int b = lane * per, e = min(p.num_groups, b + per);
+    auto parts = [&](int g) { return (group_prefix(p, g) + p.partition - 1) / p.partition; };
+    int local = 0;
+    for (int g = b; g < e; ++g) {
+      if (blockIdx.x == 0) check_group_prefix(p, g);
+      local += parts(g);
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+    for (int g = b; g < e; ++g) {
+      pstart[g] = run;
+      run += parts(g);
+    }
+    if (lane == 31) pstart[p.num_groups] = incl;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const int num_items = pstart[p.num_groups] * p.G;
+
+  struct PItem {
+    int g, kv, part, s0, members, t0, t1;
+  };
+  auto get = [&](int k, PItem& it) -> bool {  // k-th item of this CTA (serpentine deal)
+    const int pos = (k & 1) ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x;
+    const long long i = (long long)k * gridDim.x + pos;
+    if (i >= num_items) return false;
+    it.kv = (int)(i % p.G);
+    const int qi = (int)(i / p.G);
+    int lo = 0, hi = p.num_groups - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pstart[mid] <= qi) lo = mid; else hi = mid - 1;
+    }
+    it.g = lo;
+    it.part = qi - pstart[lo];
+    it.s0 = __ldg(p.group_starts + lo);
+    it.members = __ldg(p.group_starts + lo + 1) - it.s0;
+    it.t0 = it.part * p.partition;
+    it.t1 = min(it.t0 + p.partition, group_prefix(p, lo));
+    return true;
+  };
+  auto num_tiles = [&](const PItem& it) { return ((it.t1 - it.t0 + JT - 1) / JT + 1) / 2; };
+  const uint32_t q_base = smem_u32(smem);
+  const uint32_t st_base = smem_u32(smem + L.stage_off);
+  const uint32_t p_base = smem_u32(smem + L.p_off);
+
+  if (warp == 4) {
+    // ------------------------------- producer -------------------------------
+    // The warp reads the block ids of 32 jobs at a time (one per lane) and lane 0
+    // takes them by shuffle, so no table load waits between two tiles' copies.
+    int n = 0;
+    PItem it;
+    for (int k = 0; get(k, it); ++k) {
+      if (__shfl_sync(0xffffffffu, (int)*abort_flag, 0)) break;
+      const int32_t* table = p.block_tables + (long long)it.s0 * p.max_blocks;
+      const int u0 = it.t0 / JT, ue = (it.t1 + JT - 1) / JT;  // the item's jobs
+      const int nt = num_tiles(it);
+      int wbase = u0;
+      long long wphys = u0 + lane < ue ? (long long)__ldg(table + (((u0 + lane) * JT) >> p.block_shift)) : -1;
+      bool stop = false;
+      for (int i = 0; i < nt; ++i, ++n) {
+        const int ua = u0 + 2 * i;
+        if (ua + 1 >= wbase + 32) {  // the window moves to this tile
+          wbase = ua;
+          wphys = ua + lane < ue ? (long long)__ldg(table + (((ua + lane) * JT) >> p.block_shift)) : -1;
+        }
+        long long ph[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          ph[j] = __shfl_sync(0xffffffffu, wphys, ua + j - wbase);
+          if (ua + j >= ue) ph[j] = -2;  // no such job in this item
+        }
+        int ok = 1;
+        if (lane == 0) {
+          const int stage = n % R;
+          ok = mbar_wait_bounded(&empty[stage], ((n / R) & 1) ^ 1, abort_flag, p.err, kWaitLimitNs);
+          if (ok) {
+            uint8_t* kdst = smem + L.stage_off + stage * L.stage_bytes;
+            uint8_t* vdst = kdst + TILE;
+            job_ok[stage] = (uint8_t)((ph[0] >= 0 && ph[0] < p.num_blocks ? 1 : 0) |
+                                      (ph[1] >= 0 && ph[1] < p.num_blocks ? 2 : 0));
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&full[stage], 2 * TILE);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              long long phys = ph[j];
+              if (phys != -2 && (phys < 0 || phys >= p.num_blocks)) atomicOr(p.err, kErrBlockId);
+              if (phys >= p.num_blocks) phys = -1;
+              const int tok = (ua + j) * JT;
+              const int r0 = tok - ((tok >> p.block_shift) << p.block_shift);
+#pragma unroll
+              for (int rg = 0; rg < NREG; ++rg) {
+                uint8_t* kd = kdst + rg * REG_BYTES + j * JT * 128;
+                uint8_t* vd = vdst + rg * REG_BYTES + j * JT * 128;
+                if (phys >= 0) {
+                  tma_load_tile(kd, &kmap, p, rg * 64, phys, it.kv, r0, &full[stage]);
+                  tma_load_tile(vd, &vmap, p, rg * 64, phys, it.kv, r0, &full[stage]);
+                } else {  // absent or out-of-pool job: zeros (the softmax masks its tokens)
+                  tma_load_zero_tile(kd, &kmap, p, rg * 64, &full[stage]);
+                  tma_load_zero_tile(vd, &vmap, p, rg * 64, &full[stage]);
+                }
+              }
+            }
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+          stop = true;
+          break;
+        }
+      }
+      if (stop) break;
+    }
+    // let the last copies land before the block can exit
+    if (lane == 0) {
+      const int first = n - R > 0 ? n - R : 0;
+      for (int m = first; m < n; ++m) mbar_wait_bounded(&full[m % R], (m / R) & 1, nullptr, p.err, kDrainLimitNs);
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------ MMA issuer -------------------------------
+    if (lane == 0) {
+      int n = 0;
+      bool issued = false;
+      PItem it;
+      // P V of tile m (the item's `first` tile overwrites O)
+      auto pv = [&](int m, bool first, int k) -> bool {
+        if (!mbar_wait_bounded(&p_full[m & 1], (m >> 1) & 1, abort_flag, p.err, kWaitLimitNs)) return false;
+        if (first && k > 0 && !mbar_wait_bounded(o_free, (k - 1) & 1, abort_flag, p.err, kWaitLimitNs))
+          return false;
+        tc_fence_after();
+        const uint32_t vst = st_base + (m % R) * L.stage_bytes + TILE;
+        const uint32_t pbuf = p_base + (m & 1) * (M * 128);
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {  // hi weights (K columns 0-31), then lo (32-63)
+#pragma unroll
+          for (int ks = 0; ks < NT / 16; ++ks) {
+            const uint64_t a = tc_desc(pbuf + (part * (NT / 16) + ks) * 32, 16, 1024);
+            const uint64_t b = tc_desc(vst + ks * 2048, REG_BYTES, 1024);
+            tc_mma(tbase + O_COL, a, b, ID_PV, !(first && part == 0 && ks == 0));
+          }
+        }
+        tc_commit(&pv_done[m & 1]);
+        tc_commit(&empty[m % R]);
+        issued = true;
+        return true;
+      };
+      for (int k = 0; get(k, it); ++k) {
+        if (!mbar_wait_bounded(&q_full[k & 1], (k >> 1) & 1, abort_flag, p.err, kWaitLimitNs)) break;
+        const int nt = num_tiles(it);
+        const uint32_t qa = q_base + (k & 1) * L.q_bytes;
+        bool stop = false;
+        for (int i = 0; i < nt; ++i, ++n) {
+          const int stage = n % R, b = n & 1;
+          if (!mbar_wait_bounded(&full[stage], (n / R) & 1, abort_flag, p.err, kWaitLimitNs) ||
+              !mbar_wait_bounded(&s_free[b], ((n >> 1) & 1) ^ 1, abort_flag, p.err, kWaitLimitNs)) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t kst = st_base + stage * L.stage_bytes;
+#pragma unroll
+          for (int ks = 0; ks < KSTEPS; ++ks) {
+            const uint64_t a = tc_desc(qa + (ks >> 2) * (M * 128) + (ks & 3) * 32, 16, 1024);
+            const uint64_t bd = tc_desc(kst + (ks >> 2) * REG_BYTES + (ks & 3) * 32, 16, 1024);
+            tc_mma(tbase + S_COL + b * NT, a, bd, ID_S, ks > 0);
+          }
+          tc_commit(&s_full[b]);
+          issued = true;
+          if (i > 0 && !pv(n - 1, i == 1, k)) {
+            stop = true;
+            break;
+          }
+        }
+        if (stop || !pv(n - 1, nt == 1, k)) break;
+      }
+      if (issued) {  // every MMA issued has completed before the tensor memory is released
+        tc_commit(fin);
+        mbar_wait_bounded(fin, 0, nullptr, p.err, kDrainLimitNs);
+      }
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------- softmax --------------------------------
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    const int row = 16 * warp + lane;    // row of the M = 64 tiles (lanes >= 16 hold none)
+    const bool has_row = lane < 16;
+    const uint32_t lane_addr = tbase + ((uint32_t)(32 * warp) << 16);
+    // Q of an item into its buffer: row r = member r / group, head r % group, by
+    // cp.async (padding rows are zero); 128 threads, 16-byte chunks, 128-byte
+    // swizzle. finish_q waits for the copies and hands the tile to the MMA.
+    auto issue_q = [&](const PItem& x, int buf) {
+      uint8_t* q = smem + buf * L.q_bytes;
+      const int rows = x.members * p.group;
+      constexpr int CPR = D / 8;  // 16-byte chunks per row
+      for (int c = threadIdx.x; c < M * CPR; c += 128) {
+        const int r = c / CPR, ch = c % CPR;
+        uint8_t* dst = q + (ch >> 3) * (M * 128) + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+        if (r < rows)
+          cp_async16(dst, reinterpret_cast<const DT*>(p.q) +
+                              ((long long)(x.s0 + r / p.group) * p.H + x.kv * p.group + r % p.group) * D + ch * 8);
+        else
+          *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      cp_async_commit();
+    };
+    auto finish_q = [&](int buf) {
+      cp_async_wait_all();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_full[buf]);
+    };
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+      const bool ok = mbar_wait_bounded(bar, parity, abort_flag, p.err, kWaitLimitNs);
+      return __all_sync(0xffffffffu, ok);
+    };
+    int n = 0;
+    PItem it, nx;
+    bool have = get(0, it);
+    if (have) {
+      issue_q(it, 0);
+      finish_q(0);
+    }
+    for (int k = 0; have; ++k) {
+      const bool have_next = get(k + 1, nx);
+      if (have_next) issue_q(nx, (k + 1) & 1);  // that buffer's last reader (item k - 1) has finished
+      const int rows = it.members * p.group;
+      const int nt = num_tiles(it);
+      float m_ref = NEG_INF, l = 0.f;
+      bool stop = false;
+      for (int i = 0; i < nt; ++i, ++n) {
+        const int b = n & 1;
+        if (!wait_all(&s_full[b], (n >> 1) & 1) || !wait_all(&full[n % R], (n / R) & 1)) {
+          stop = true;
+          break;
+        }
+        // the tile's jobs with a block in the pool (the producer zero-filled the
+        // others); full[stage] completed before S was computed and cannot move on
+        // before this tile's P V has read the stage
+        const unsigned ok = job_ok[n % R];
+        tc_fence_after();
+        uint32_t s[32];
+        tc_ld32(lane_addr + S_COL + b * NT, s);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[b]);
+        // scores of this tile's real tokens, in base-2 units
+        const int nv = min(NT, it.t1 - (it.t0 + 2 * i * JT));
+        float z[32], t16[16];
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+          const bool real = t < nv && ((ok >> (t / JT)) & 1u);
+          z[t] = real ? __uint_as_float(s[t]) * p.scale_log2 : NEG_INF;
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) t16[e] = fmaxf(z[e], z[e + 16]);  // the row max as a tree
+#pragma unroll
+        for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+          for (int e = 0; e < w; ++e) t16[e] = fmaxf(t16[e], t16[e + w]);
+        const float mx = t16[0];
+        const bool move = mx > m_ref + kTcRescale || (m_ref == NEG_INF && mx > NEG_INF);
+        const float m_new = move ? mx : m_ref;
+        const float c = move ? exp2f(m_ref - m_new) : 1.f;
+        const float msub = m_new == NEG_INF ? 0.f : m_new;
+        l *= c;
+        m_ref = m_new;
+        // this row's weights as hi + lo 16-bit parts
+        uint32_t hw[16], lw[16];
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: short dependency chains
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float w0 = exp2f(z[2 * e] - msub), w1 = exp2f(z[2 * e + 1] - msub);
+          ls[e & 3] += w0 + w1;
+          hw[e] = Mma<DT>::pack(w0, w1);
+          float r0, r1;
+          unpack2(hw[e], (DT*)nullptr, r0, r1);
+          lw[e] = Mma<DT>::pack(w0 - r0, w1 - r1);
+        }
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        // P buffer n & 1 is free once the P V of tile n - 2 has completed; O may be
+        // rescaled once the P V of tile n - 1 has
+        const int pb = n & 1;
+        if (n >= 2 && !wait_all(&pv_done[pb], ((n >> 1) & 1) ^ 1)) {
+          stop = true;
+          break;
+        }
+        if (i > 0 && __any_sync(0xffffffffu, has_row && move)) {
+          if (!wait_all(&pv_done[pb ^ 1], ((n - 1) >> 1) & 1)) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          const float cr = has_row ? c : 1.f;
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tc_ld32(lane_addr + O_COL + c0, o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * cr);
+            tc_st32(lane_addr + O_COL + c0, o);
+          }
+        }
+        if (has_row) {  // chunks 0-3: hi weights of tokens 8 ch .. 8 ch + 7; chunks 4-7: lo
+          uint8_t* pr = smem + L.p_off + pb * (M * 128) + row * 128;
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            *reinterpret_cast<uint4*>(pr + ((ch ^ (row & 7)) << 4)) =
+                make_uint4(hw[4 * ch], hw[4 * ch + 1], hw[4 * ch + 2], hw[4 * ch + 3]);
+            *reinterpret_cast<uint4*>(pr + (((ch + 4) ^ (row & 7)) << 4)) =
+                make_uint4(lw[4 * ch], lw[4 * ch + 1], lw[4 * ch + 2], lw[4 * ch + 3]);
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[pb]);
+      }
+      if (stop) break;
+      if (have_next) finish_q((k + 1) & 1);
+      // the item's last P V, then this thread's row of O: normalised partial, max, sum
+      if (!wait_all(&pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1)) break;
+      tc_fence_after();
+      const bool write = has_row && row < rows;
+      const long long wrow = ((long long)(it.s0 + row / p.group) * p.H + it.kv * p.group + row % p.group) *
+                                 p.max_partitions + it.part;
+      const float inv = l > 0.f ? p.v_scale / l : 0.f;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t o[32];
+        tc_ld32(lane_addr + O_COL + c0, o);
+        if (write) {
+          float4* dst = reinterpret_cast<float4*>(p.ws_o + wrow * D + c0);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            dst[e] = make_float4(__uint_as_float(o[4 * e]) * inv, __uint_as_float(o[4 * e + 1]) * inv,
+                                 __uint_as_float(o[4 * e + 2]) * inv, __uint_as_float(o[4 * e + 3]) * inv);
+        }
+      }
+      if (write) {
+        p.ws_m[wrow] = m_ref;
+        p.ws_l[wrow] = l;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_free);
+      have = have_next;
+      it = nx;
+    }
+    cp_async_wait_all();  // no copy into shared memory outlives the block
+  }
+
+  // ---- teardown: every role has stopped; release the tensor memory ----------------
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(TCOLS) : "memory");
+}
+
+}  // namespace pa

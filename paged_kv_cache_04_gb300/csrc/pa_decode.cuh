@@ -105,6 +105,7 @@ struct DecodeParams {
   int num_groups;
   int suffix_slot;
   int suffix_single;            // 1: one suffix partial per row (kModeSuffix)
+  int prefix_limit;             // longest usable shared prefix: suffix_slot x partition, table width
   int nhd;                      // pool layout: 0 [blocks][G][B][d], 1 [blocks][B][G][d]
   unsigned* err;
 };
@@ -206,10 +207,16 @@ __device__ __forceinline__ int group_of(const DecodeParams& p, int s) {
   return lo;
 }
 
-// Shared prefix length of group g in whole blocks.
+// Shared prefix length of group g in whole blocks, clamped to what the
+// workspace's prefix slots and the block table can hold (prefix_limit; the
+// prefix passes record a longer value, see check_group_prefix).
 __device__ __forceinline__ int group_prefix(const DecodeParams& p, int g) {
-  const int pl = max(0, __ldg(p.prefix_lens + g));
+  const int pl = min(max(0, __ldg(p.prefix_lens + g)), p.prefix_limit);
   return pl - (pl & (p.block_size - 1));
+}
+
+__device__ __forceinline__ void check_group_prefix(const DecodeParams& p, int g) {
+  if (__ldg(p.prefix_lens + g) > p.prefix_limit) atomicOr(p.err, kErrContext);
 }
 
 // First token of sequence s that is its own (after its group's shared prefix).

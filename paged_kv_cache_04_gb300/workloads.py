@@ -239,7 +239,7 @@ def long70b(device="cpu", S=8, B=16, lo=32768, hi=131072, partition_tokens=512,
 
 
 def shared_prefix(device="cpu", prompts=64, samples=8, prefix=2048, tail_lo=0, tail_hi=512,
-                  cow=False, num_blocks=None) -> Workload:
+                  cow=False, num_blocks=None, H=32, G=8, d=128, B=16, dtype=torch.bfloat16) -> Workload:
     """Parallel sampling: ``prompts`` prompts forked into ``samples`` samples each.
 
     The prompt blocks are ref-counted and shared by all samples of the prompt.
@@ -247,9 +247,8 @@ def shared_prefix(device="cpu", prompts=64, samples=8, prefix=2048, tail_lo=0, t
     appends go through the block manager, which emits the copy-on-write pairs.
     The step is: copy_blocks(pairs), reshape_and_cache(all appended tokens),
     decode.  Before the step the pool holds the prompt tokens (and garbage
-    elsewhere).
+    elsewhere). The default head shape is the Llama-3.1-8B layer's.
     """
-    B, G, H, d = 16, 8, 32, 128
     gctx = _gen(SEED_CTX)
     r = (uniform_lengths(prompts, 1, B - 1, gctx) if cow
          else torch.zeros(prompts, dtype=torch.int64)).tolist()
@@ -276,15 +275,15 @@ def shared_prefix(device="cpu", prompts=64, samples=8, prefix=2048, tail_lo=0, t
     ctx_t, bt = _tables(bm, seq_ids, B)
     g = _gen(SEED_DATA, device)
     kshape = (nb, G, B, d)
-    k_cache = randn_big(kshape, torch.bfloat16, g, device)
-    v_cache = randn_big(kshape, torch.bfloat16, g, device)
+    k_cache = randn_big(kshape, dtype, g, device)
+    v_cache = randn_big(kshape, dtype, g, device)
     S = len(seq_ids)
-    q = randn((S, H, d), torch.bfloat16, g, device)
+    q = randn((S, H, d), dtype, g, device)
     N = len(slots)
-    wl = Workload("shared_cow" if cow else "shared", S, H, G, d, B, torch.bfloat16, nb,
+    wl = Workload("shared_cow" if cow else "shared", S, H, G, d, B, dtype, nb,
                   1.0 / math.sqrt(d), ctx_t.to(device), bt.to(device), q, k_cache, v_cache,
-                  new_key=randn((N, G, d), torch.bfloat16, g, device),
-                  new_value=randn((N, G, d), torch.bfloat16, g, device),
+                  new_key=randn((N, G, d), dtype, g, device),
+                  new_value=randn((N, G, d), dtype, g, device),
                   slot_mapping=torch.tensor(slots, dtype=torch.int64, device=device),
                   copy_pairs=torch.tensor(pairs, dtype=torch.int64, device=device).view(-1, 2),
                   meta={"prompts": prompts, "samples": samples, "prefix": prefix,
