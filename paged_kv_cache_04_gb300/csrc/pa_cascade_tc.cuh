@@ -124,6 +124,43 @@ __device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32])
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Bounded wait whose polls suspend the thread for up to `hint_ns` while the
+// phase is incomplete, so a waiting role leaves the issue slots to the others;
+// otherwise as mbar_wait_bounded.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                unsigned* err, unsigned long long limit_ns) {
+  constexpr uint32_t hint_ns = 2000;
+  auto poll = [&]() {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+  };
+  if (poll()) return true;
+  const unsigned long long t0 = globaltimer();
+  for (;;) {
+    if (poll()) return true;
+    if (abort_flag != nullptr && *abort_flag) return false;
+    if (globaltimer() - t0 > limit_ns) {
+      if (abort_flag != nullptr) *abort_flag = 1;
+      atomicOr(err, kErrTimeout);
+      return false;
+    }
+  }
+}
+
+// 2^x on the special-function unit (inputs below -126 give 0).
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // A box of fill values (zeros) for a job that does not exist: every row of the
 // box lies before the start of the pool.
 __device__ __forceinline__ void tma_load_zero_tile(void* dst, const CUtensorMap* map, const DecodeParams& p, int x,
@@ -279,38 +316,35 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           ph[j] = __shfl_sync(0xffffffffu, wphys, ua + j - wbase);
           if (ua + j >= ue) ph[j] = -2;  // no such job in this item
         }
+        // lane 0 waits for the stage and announces its bytes; lanes 0 .. 4 NREG - 1
+        // then issue one box each (job j, K or V, region rg): a single thread
+        // issuing all of a tile's boxes in turn measured slower than the copy itself
+        const int stage = n % R;
         int ok = 1;
         if (lane == 0) {
-          const int stage = n % R;
-          ok = mbar_wait_bounded(&empty[stage], ((n / R) & 1) ^ 1, abort_flag, p.err, kWaitLimitNs);
+          ok = mbar_wait_sleep(&empty[stage], ((n / R) & 1) ^ 1, abort_flag, p.err, kWaitLimitNs);
           if (ok) {
-            uint8_t* kdst = smem + L.stage_off + stage * L.stage_bytes;
-            uint8_t* vdst = kdst + TILE;
             job_ok[stage] = (uint8_t)((ph[0] >= 0 && ph[0] < p.num_blocks ? 1 : 0) |
                                       (ph[1] >= 0 && ph[1] < p.num_blocks ? 2 : 0));
-            fence_proxy_async_smem();
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+              if (ph[j] != -2 && (ph[j] < 0 || ph[j] >= p.num_blocks)) atomicOr(p.err, kErrBlockId);
             mbar_arrive_expect_tx(&full[stage], 2 * TILE);
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              long long phys = ph[j];
-              if (phys != -2 && (phys < 0 || phys >= p.num_blocks)) atomicOr(p.err, kErrBlockId);
-              if (phys >= p.num_blocks) phys = -1;
-              const int tok = (ua + j) * JT;
-              const int r0 = tok - ((tok >> p.block_shift) << p.block_shift);
-#pragma unroll
-              for (int rg = 0; rg < NREG; ++rg) {
-                uint8_t* kd = kdst + rg * REG_BYTES + j * JT * 128;
-                uint8_t* vd = vdst + rg * REG_BYTES + j * JT * 128;
-                if (phys >= 0) {
-                  tma_load_tile(kd, &kmap, p, rg * 64, phys, it.kv, r0, &full[stage]);
-                  tma_load_tile(vd, &vmap, p, rg * 64, phys, it.kv, r0, &full[stage]);
-                } else {  // absent or out-of-pool job: zeros (the softmax masks its tokens)
-                  tma_load_zero_tile(kd, &kmap, p, rg * 64, &full[stage]);
-                  tma_load_zero_tile(vd, &vmap, p, rg * 64, &full[stage]);
-                }
-              }
-            }
           }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (ok && lane < 4 * NREG) {
+          const int j = lane / (2 * NREG), is_v = (lane / NREG) & 1, rg = lane % NREG;
+          long long phys = ph[j];
+          if (phys >= p.num_blocks) phys = -1;
+          const int tok = (ua + j) * JT;
+          const int r0 = tok - ((tok >> p.block_shift) << p.block_shift);
+          uint8_t* dst = smem + L.stage_off + stage * L.stage_bytes + is_v * TILE + rg * REG_BYTES + j * JT * 128;
+          const CUtensorMap* map = is_v ? &vmap : &kmap;
+          if (phys >= 0)
+            tma_load_tile(dst, map, p, rg * 64, phys, it.kv, r0, &full[stage]);
+          else  // absent or out-of-pool job: zeros (the softmax masks its tokens)
+            tma_load_zero_tile(dst, map, p, rg * 64, &full[stage]);
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) {
           stop = true;
@@ -333,8 +367,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       PItem it;
       // P V of tile m (the item's `first` tile overwrites O)
       auto pv = [&](int m, bool first, int k) -> bool {
-        if (!mbar_wait_bounded(&p_full[m & 1], (m >> 1) & 1, abort_flag, p.err, kWaitLimitNs)) return false;
-        if (first && k > 0 && !mbar_wait_bounded(o_free, (k - 1) & 1, abort_flag, p.err, kWaitLimitNs))
+        if (!mbar_wait_sleep(&p_full[m & 1], (m >> 1) & 1, abort_flag, p.err, kWaitLimitNs)) return false;
+        if (first && k > 0 && !mbar_wait_sleep(o_free, (k - 1) & 1, abort_flag, p.err, kWaitLimitNs))
           return false;
         tc_fence_after();
         const uint32_t vst = st_base + (m % R) * L.stage_bytes + TILE;
@@ -354,14 +388,24 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         return true;
       };
       for (int k = 0; get(k, it); ++k) {
-        if (!mbar_wait_bounded(&q_full[k & 1], (k >> 1) & 1, abort_flag, p.err, kWaitLimitNs)) break;
+        if (!mbar_wait_sleep(&q_full[k & 1], (k >> 1) & 1, abort_flag, p.err, kWaitLimitNs)) break;
         const int nt = num_tiles(it);
         const uint32_t qa = q_base + (k & 1) * L.q_bytes;
         bool stop = false;
         for (int i = 0; i < nt; ++i, ++n) {
           const int stage = n % R, b = n & 1;
-          if (!mbar_wait_bounded(&full[stage], (n / R) & 1, abort_flag, p.err, kWaitLimitNs) ||
-              !mbar_wait_bounded(&s_free[b], ((n >> 1) & 1) ^ 1, abort_flag, p.err, kWaitLimitNs)) {
+          // the last tile's P V first when its P is already there: the sooner it
+          // runs, the sooner its stage is refilled
+          bool pv_pending = i > 0;
+          if (pv_pending && mbar_try_wait(&p_full[(n - 1) & 1], ((n - 1) >> 1) & 1)) {
+            if (!pv(n - 1, i == 1, k)) {
+              stop = true;
+              break;
+            }
+            pv_pending = false;
+          }
+          if (!mbar_wait_sleep(&full[stage], (n / R) & 1, abort_flag, p.err, kWaitLimitNs) ||
+              !mbar_wait_sleep(&s_free[b], ((n >> 1) & 1) ^ 1, abort_flag, p.err, kWaitLimitNs)) {
             stop = true;
             break;
           }
@@ -375,7 +419,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           }
           tc_commit(&s_full[b]);
           issued = true;
-          if (i > 0 && !pv(n - 1, i == 1, k)) {
+          if (pv_pending && !pv(n - 1, i == 1, k)) {
             stop = true;
             break;
           }
@@ -455,10 +499,15 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         // scores of this tile's real tokens, in base-2 units
         const int nv = min(NT, it.t1 - (it.t0 + 2 * i * JT));
         float z[32], t16[16];
+        if (nv == NT && ok == 3u) {  // every tile but an item's ragged or faulty last one
 #pragma unroll
-        for (int t = 0; t < 32; ++t) {
-          const bool real = t < nv && ((ok >> (t / JT)) & 1u);
-          z[t] = real ? __uint_as_float(s[t]) * p.scale_log2 : NEG_INF;
+          for (int t = 0; t < 32; ++t) z[t] = __uint_as_float(s[t]) * p.scale_log2;
+        } else {
+#pragma unroll
+          for (int t = 0; t < 32; ++t) {
+            const bool real = t < nv && ((ok >> (t / JT)) & 1u);
+            z[t] = real ? __uint_as_float(s[t]) * p.scale_log2 : NEG_INF;
+          }
         }
 #pragma unroll
         for (int e = 0; e < 16; ++e) t16[e] = fmaxf(z[e], z[e + 16]);  // the row max as a tree
@@ -478,7 +527,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         float ls[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: short dependency chains
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float w0 = exp2f(z[2 * e] - msub), w1 = exp2f(z[2 * e + 1] - msub);
+          const float w0 = ex2_ftz(z[2 * e] - msub), w1 = ex2_ftz(z[2 * e + 1] - msub);
           ls[e & 3] += w0 + w1;
           hw[e] = Mma<DT>::pack(w0, w1);
           float r0, r1;
