@@ -16,12 +16,15 @@
 //              of P (16-bit hi + lo parts) to shared memory and, at the end of
 //              an item, reads its row of O;
 //   warp 4     TMA producer: two 16-token jobs per stage (K and V, 128-byte
-//              swizzle), a ring of three stages;
+//              swizzle), a ring of five stages;
 //   warp 5     owns the tensor memory (allocation, release); its lane 0 issues
 //              every MMA and commits them to mbarriers.
-// S is double-buffered in tensor memory and P in shared memory, so the scores
-// of a tile are computed, and the P V of the one before runs, while the
-// softmax warps work on a tile. The accumulator O is rescaled
+// S is double-buffered in tensor memory, so the scores of a tile are computed
+// while the softmax warps work on the one before; the softmax computes a
+// tile's weights before it waits for the last P V to release the P buffer.
+// (Shared memory goes to stages: with a per-stage life of several thousand
+// cycles, five stages measured faster than four with a second P buffer, or
+// three with a second Q tile.) The accumulator O is rescaled
 // lazily: a row's reference max moves only when a score exceeds it by more
 // than kTcRescale (log2 units); weights then stay below 2^kTcRescale and the
 // result is the same softmax (numerator and denominator share the reference).
@@ -35,7 +38,7 @@ namespace pa {
 
 constexpr int kTcRows = 64;        // M: query rows of one group (members x heads), padded
 constexpr int kTcTokens = 32;      // N of S, K of P V: tokens per stage (two TMA jobs)
-constexpr int kTcStages = 3;
+constexpr int kTcStages = 5;
 constexpr int kTcThreads = 192;
 constexpr float kTcRescale = 8.f;
 
@@ -43,17 +46,17 @@ struct TcLayout {
   unsigned q_bytes, stage_off, stage_bytes, p_off, bar_off, misc_off, sched_off, total;
 };
 
-// Offsets from the 1024-byte aligned base: two Q tiles, the stages (K then V,
-// each [head_dim / 64 regions][32 tokens][128 B]), two P buffers ([64 rows]
+// Offsets from the 1024-byte aligned base: the Q tile, the stages (K then V,
+// each [head_dim / 64 regions][32 tokens][128 B]), the P buffer ([64 rows]
 // [128 B]: a row's 32 hi weights, then its 32 lo weights), mbarriers, the
 // tensor-memory base, the abort flag, per-stage job flags and the group scan.
 __host__ __device__ inline TcLayout tc_layout(int D, int num_groups) {
   TcLayout L;
   L.q_bytes = kTcRows * D * 2;
-  L.stage_off = 2 * L.q_bytes;
+  L.stage_off = L.q_bytes;
   L.stage_bytes = 2u * kTcTokens * D * 2;
   L.p_off = L.stage_off + kTcStages * L.stage_bytes;
-  L.bar_off = L.p_off + 2 * kTcRows * 128;
+  L.bar_off = L.p_off + kTcRows * 128;
   L.misc_off = L.bar_off + (2 * kTcStages + 12) * 8;
   L.sched_off = round_up(L.misc_off + 16, 16);
   L.total = round_up(L.sched_off + (num_groups + 1) * 4, 16) + 1024;
@@ -195,9 +198,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   uint64_t* empty = bars + R;         // [R] MMA (P V done) -> TMA
   uint64_t* s_full = bars + 2 * R;    // [2] S written -> softmax
   uint64_t* s_free = s_full + 2;      // [2] S read -> MMA
-  uint64_t* q_full = s_full + 4;      // [2] Q tile written -> MMA
-  uint64_t* p_full = s_full + 6;      // [2] P buffer written -> MMA
-  uint64_t* pv_done = s_full + 8;     // [2] P V of that buffer done -> softmax (buffer free; O current)
+  uint64_t* q_full = s_full + 4;      // [0]: the item's Q tile written -> MMA
+  uint64_t* p_full = s_full + 6;      // [0]: P written -> MMA
+  uint64_t* pv_done = s_full + 8;     // [0]: P V done -> softmax (P free, O current)
   uint64_t* o_free = s_full + 10;     // O read at the end of an item -> MMA
   uint64_t* fin = s_full + 11;        // every MMA done (teardown)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc_off);
@@ -367,12 +370,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       PItem it;
       // P V of tile m (the item's `first` tile overwrites O)
       auto pv = [&](int m, bool first, int k) -> bool {
-        if (!mbar_wait_sleep(&p_full[m & 1], (m >> 1) & 1, abort_flag, p.err, kWaitLimitNs)) return false;
+        if (!mbar_wait_sleep(&p_full[0], m & 1, abort_flag, p.err, kWaitLimitNs)) return false;
         if (first && k > 0 && !mbar_wait_sleep(o_free, (k - 1) & 1, abort_flag, p.err, kWaitLimitNs))
           return false;
         tc_fence_after();
         const uint32_t vst = st_base + (m % R) * L.stage_bytes + TILE;
-        const uint32_t pbuf = p_base + (m & 1) * (M * 128);
+        const uint32_t pbuf = p_base;
 #pragma unroll
         for (int part = 0; part < 2; ++part) {  // hi weights (K columns 0-31), then lo (32-63)
 #pragma unroll
@@ -382,22 +385,22 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             tc_mma(tbase + O_COL, a, b, ID_PV, !(first && part == 0 && ks == 0));
           }
         }
-        tc_commit(&pv_done[m & 1]);
+        tc_commit(&pv_done[0]);
         tc_commit(&empty[m % R]);
         issued = true;
         return true;
       };
       for (int k = 0; get(k, it); ++k) {
-        if (!mbar_wait_sleep(&q_full[k & 1], (k >> 1) & 1, abort_flag, p.err, kWaitLimitNs)) break;
+        if (!mbar_wait_sleep(&q_full[0], k & 1, abort_flag, p.err, kWaitLimitNs)) break;
         const int nt = num_tiles(it);
-        const uint32_t qa = q_base + (k & 1) * L.q_bytes;
+        const uint32_t qa = q_base;
         bool stop = false;
         for (int i = 0; i < nt; ++i, ++n) {
           const int stage = n % R, b = n & 1;
           // the last tile's P V first when its P is already there: the sooner it
           // runs, the sooner its stage is refilled
           bool pv_pending = i > 0;
-          if (pv_pending && mbar_try_wait(&p_full[(n - 1) & 1], ((n - 1) >> 1) & 1)) {
+          if (pv_pending && mbar_try_wait(&p_full[0], (n - 1) & 1)) {
             if (!pv(n - 1, i == 1, k)) {
               stop = true;
               break;
@@ -438,7 +441,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     const int row = 16 * warp + lane;    // row of the M = 64 tiles (lanes >= 16 hold none)
     const bool has_row = lane < 16;
     const uint32_t lane_addr = tbase + ((uint32_t)(32 * warp) << 16);
-    // Q of an item into its buffer: row r = member r / group, head r % group, by
+    // Q of an item into the Q tile: row r = member r / group, head r % group, by
     // cp.async (padding rows are zero); 128 threads, 16-byte chunks, 128-byte
     // swizzle. finish_q waits for the copies and hands the tile to the MMA.
     auto issue_q = [&](const PItem& x, int buf) {
@@ -475,7 +478,6 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     }
     for (int k = 0; have; ++k) {
       const bool have_next = get(k + 1, nx);
-      if (have_next) issue_q(nx, (k + 1) & 1);  // that buffer's last reader (item k - 1) has finished
       const int rows = it.members * p.group;
       const int nt = num_tiles(it);
       float m_ref = NEG_INF, l = 0.f;
@@ -535,18 +537,13 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           lw[e] = Mma<DT>::pack(w0 - r0, w1 - r1);
         }
         l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-        // P buffer n & 1 is free once the P V of tile n - 2 has completed; O may be
-        // rescaled once the P V of tile n - 1 has
-        const int pb = n & 1;
-        if (n >= 2 && !wait_all(&pv_done[pb], ((n >> 1) & 1) ^ 1)) {
+        // P (and O, for a rescale) are free once the P V of tile n - 1 has completed
+        const int pb = 0;
+        if (n >= 1 && !wait_all(&pv_done[0], (n - 1) & 1)) {
           stop = true;
           break;
         }
         if (i > 0 && __any_sync(0xffffffffu, has_row && move)) {
-          if (!wait_all(&pv_done[pb ^ 1], ((n - 1) >> 1) & 1)) {
-            stop = true;
-            break;
-          }
           tc_fence_after();
           const float cr = has_row ? c : 1.f;
 #pragma unroll 1
@@ -574,10 +571,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         if (lane == 0) mbar_arrive(&p_full[pb]);
       }
       if (stop) break;
-      if (have_next) finish_q((k + 1) & 1);
       // the item's last P V, then this thread's row of O: normalised partial, max, sum
-      if (!wait_all(&pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1)) break;
+      if (!wait_all(&pv_done[0], (n - 1) & 1)) break;
       tc_fence_after();
+      if (have_next) issue_q(nx, 0);  // every score MMA of this item has read Q
       const bool write = has_row && row < rows;
       const long long wrow = ((long long)(it.s0 + row / p.group) * p.H + it.kv * p.group + row % p.group) *
                                  p.max_partitions + it.part;
@@ -601,6 +598,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(o_free);
+      if (have_next) finish_q(0);
       have = have_next;
       it = nx;
     }
