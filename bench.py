@@ -60,7 +60,7 @@ def parse():
     ap.add_argument("--workload", default="llama8b",
                     choices=["llama8b", "tiny", "opt13b", "shared", "shared_cow", "long70b_b16", "long70b_b32",
                              "llama8b_fp8", "long70b_b16_fp8", "shared_cascade", "shared_cow_cascade", "gemma_d256",
-                             "shared_x16", "shared_x16_cascade",
+                             "shared_x16", "shared_x16_cascade", "shared_x32", "shared_x32_cascade",
                              "llama8b_nhd", "llama8b_fp8_nhd", "long70b_b16_nhd", "shared_cascade_nhd",
                              "copy_blocks", "swap_out", "swap_in", "reshape", "reshape_prefill"],
                     help="the other workload shapes give a device-timed line of their own (no e2e / CPU legs); "
@@ -651,9 +651,11 @@ def run_workload(args):
     elif name == "opt13b":
         wl = workloads.opt13b(device=dev)
     elif name.startswith("shared"):
-        # _x16: 32 prompts x 16 samples (64 query rows per group), else 64 x 8 (32 rows)
-        wl = workloads.shared_prefix(device=dev, cow=name.startswith("shared_cow"),
-                                     **({"prompts": 32, "samples": 16} if "_x16" in name else {}))
+        # _x16: 32 prompts x 16 samples (64 query rows per group), _x32: 16 x 32 (128
+        # rows), else 64 x 8 (32 rows); 512 sequences each
+        shape = {"prompts": 32, "samples": 16} if "_x16" in name else (
+            {"prompts": 16, "samples": 32} if "_x32" in name else {})
+        wl = workloads.shared_prefix(device=dev, cow=name.startswith("shared_cow"), **shape)
         # set-up: the CoW copies and every appended token, once; a timed step then
         # repeats the copies and writes each sample's newest token before decoding
         if wl.copy_pairs.numel():

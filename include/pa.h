@@ -212,7 +212,7 @@ pa_status pa_decode_split_static(void* out, const void* q, const void* k_cache, 
  *   1. prefix pass: each (group, kv head, partition of the prefix) attends all
  *      of the group's query rows at once, so a prefix block is read once per
  *      group instead of once per member (groups of more than 32 query rows run
- *      it on tcgen05 tensor cores, M = 64 rows per tile);
+ *      it on tcgen05 tensor cores, M = 64 or 128 rows per tile);
  *   2. each sequence's own tokens [prefix, context) as one partial per
  *      (sequence, head), one warp per (sequence, kv head), longest first;
  *   3. the log-sum-exp reduce of both.
@@ -222,7 +222,7 @@ pa_status pa_decode_split_static(void* out, const void* q, const void* k_cache, 
  *   prefix_lens   [num_groups]; rounded down to whole blocks; must not exceed any
  *                 member's context length (violations are clamped and recorded)
  *   max_group_size     host int >= every group's size; max_group_size *
- *                      (num_heads / num_kv_heads) <= 64
+ *                      (num_heads / num_kv_heads) <= 128
  *   max_prefix_len     host int >= every prefix_lens[g] (a longer prefix_lens[g],
  *                      or one past the block table's width, is clamped to
  *                      what the workspace and table hold and recorded as

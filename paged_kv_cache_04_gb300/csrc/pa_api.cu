@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "pa_cascade.cuh"
+#include "pa_cascade_tc.cuh"
 #include "pa_internal.h"
 
 namespace pa {
@@ -167,7 +168,7 @@ struct CascadeArgs {
   const int32_t* prefix_lens = nullptr;
   int num_groups = 0;
   int prefix_slots = 0;  // workspace slots reserved for prefix partitions
-  int nt = 1;            // n-tiles of 8 query rows per consumer warp in the prefix pass
+  int rows = 0;          // query rows per group (members x query heads), at most 128
 };
 
 pa_status run_decode(const DecodeArgs& a, bool split, int partition, int max_partitions, void* ws,
@@ -226,16 +227,24 @@ pa_status run_decode(const DecodeArgs& a, bool split, int partition, int max_par
       if (!mma_path &&
           (s = make_pool_map(&vsw, a.v_cache, a.dt, a.D, a.G, a.BS, a.num_blocks, a.layout)) != PA_OK)
         return s;
-      // A group of more than 32 query rows fills the M = 64 tile of the tcgen05
-      // pass; up to 32 rows, the mma.sync pass (four warps of 8 rows) wastes no lane.
+      // Groups of 33-64 query rows fill the M = 64 tile of the tcgen05 pass and
+      // groups of 65-128 its M = 128 tile; up to 32 rows, the mma.sync pass (four
+      // warps of 8 rows) wastes no lane.
       const bool bf = a.dt == PA_BF16;
-      if (c.nt == 2) {
+      if (c.rows > 64) {
         if (a.D == 128)
-          s = bf ? launch_cascade_prefix_tc<__nv_bfloat16, 128>(km, vsw, p, sms, pitems, st)
-                 : launch_cascade_prefix_tc<__half, 128>(km, vsw, p, sms, pitems, st);
+          s = bf ? launch_cascade_prefix_tc<__nv_bfloat16, 128, 128>(km, vsw, p, sms, pitems, st)
+                 : launch_cascade_prefix_tc<__half, 128, 128>(km, vsw, p, sms, pitems, st);
         else
-          s = bf ? launch_cascade_prefix_tc<__nv_bfloat16, 64>(km, vsw, p, sms, pitems, st)
-                 : launch_cascade_prefix_tc<__half, 64>(km, vsw, p, sms, pitems, st);
+          s = bf ? launch_cascade_prefix_tc<__nv_bfloat16, 64, 128>(km, vsw, p, sms, pitems, st)
+                 : launch_cascade_prefix_tc<__half, 64, 128>(km, vsw, p, sms, pitems, st);
+      } else if (c.rows > 8 * kCascadeConsumers) {
+        if (a.D == 128)
+          s = bf ? launch_cascade_prefix_tc<__nv_bfloat16, 128, 64>(km, vsw, p, sms, pitems, st)
+                 : launch_cascade_prefix_tc<__half, 128, 64>(km, vsw, p, sms, pitems, st);
+        else
+          s = bf ? launch_cascade_prefix_tc<__nv_bfloat16, 64, 64>(km, vsw, p, sms, pitems, st)
+                 : launch_cascade_prefix_tc<__half, 64, 64>(km, vsw, p, sms, pitems, st);
       } else if (a.D == 128) {
         s = bf ? launch_cascade_prefix<__nv_bfloat16, 128, 1>(km, vsw, p, sms, pitems, st)
                : launch_cascade_prefix<__half, 128, 1>(km, vsw, p, sms, pitems, st);
@@ -446,7 +455,7 @@ extern "C" pa_status pa_decode_cascade(void* out, const void* q, const void* k_c
   if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;  // the prefix pass: head_dim <= 128
   if (num_seqs > kSplitMaxSeqs || num_groups > kSplitMaxSeqs) return PA_ERR_UNSUPPORTED;
   const long long rows_per_group = (long long)max_group_size * (num_heads / num_kv_heads);
-  if (rows_per_group > 2LL * 8 * kCascadeConsumers) return PA_ERR_UNSUPPORTED;
+  if (rows_per_group > kTcMaxRows) return PA_ERR_UNSUPPORTED;
   const size_t need = pa_decode_cascade_workspace_bytes(num_seqs, num_heads, head_dim, max_prefix_len,
                                                         max_context_len, partition_tokens);
   if (!workspace || !aligned16(workspace) || workspace_bytes < need || need == 0) return PA_ERR_INVALID_ARG;
@@ -455,7 +464,7 @@ extern "C" pa_status pa_decode_cascade(void* out, const void* q, const void* k_c
   c.prefix_lens = prefix_lens;
   c.num_groups = num_groups;
   c.prefix_slots = (max_prefix_len + partition_tokens - 1) / partition_tokens;
-  c.nt = rows_per_group > 8 * kCascadeConsumers ? 2 : 1;  // 2: the tcgen05 prefix pass
+  c.rows = (int)rows_per_group;
   const long long P = c.prefix_slots + 1;  // prefix partitions, then one slot for each sequence's own tokens
   if ((long long)num_seqs * num_kv_heads * P > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
   return run_decode(a, true, partition_tokens, (int)P, workspace, stream, c);

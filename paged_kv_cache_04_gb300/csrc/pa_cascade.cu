@@ -50,11 +50,11 @@ pa_status launch_cascade_prefix(const CUtensorMap& kmap, const CUtensorMap& vmap
              : PA_ERR_CUDA;
 }
 
-template <typename DT, int D>
+template <typename DT, int D, int MR>
 pa_status launch_cascade_prefix_tc(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                                    int num_sms, long long max_items, cudaStream_t stream) {
-  auto kern = cascade_prefix_tc_kernel<DT, D>;
-  const TcLayout L = tc_layout(D, p.num_groups);
+  auto kern = cascade_prefix_tc_kernel<DT, D, MR>;
+  const TcLayout L = tc_layout(D, p.num_groups, MR);
   if (L.total > 227u * 1024u) return PA_ERR_UNSUPPORTED;
   static std::mutex mu;
   static unsigned set_bytes[64] = {0};
@@ -93,14 +93,17 @@ pa_status launch_cascade_prefix_tc(const CUtensorMap& kmap, const CUtensorMap& v
              : PA_ERR_CUDA;
 }
 
-template pa_status launch_cascade_prefix_tc<__nv_bfloat16, 128>(const CUtensorMap&, const CUtensorMap&,
-                                                                 const DecodeParams&, int, long long, cudaStream_t);
-template pa_status launch_cascade_prefix_tc<__nv_bfloat16, 64>(const CUtensorMap&, const CUtensorMap&,
-                                                                const DecodeParams&, int, long long, cudaStream_t);
-template pa_status launch_cascade_prefix_tc<__half, 128>(const CUtensorMap&, const CUtensorMap&, const DecodeParams&,
-                                                          int, long long, cudaStream_t);
-template pa_status launch_cascade_prefix_tc<__half, 64>(const CUtensorMap&, const CUtensorMap&, const DecodeParams&,
-                                                         int, long long, cudaStream_t);
+#define PA_INSTANTIATE_CASCADE_TC(DT, D, MR)                                                                \
+  template pa_status launch_cascade_prefix_tc<DT, D, MR>(const CUtensorMap&, const CUtensorMap&,               \
+                                                         const DecodeParams&, int, long long, cudaStream_t);
+PA_INSTANTIATE_CASCADE_TC(__nv_bfloat16, 128, 64)
+PA_INSTANTIATE_CASCADE_TC(__nv_bfloat16, 128, 128)
+PA_INSTANTIATE_CASCADE_TC(__nv_bfloat16, 64, 64)
+PA_INSTANTIATE_CASCADE_TC(__nv_bfloat16, 64, 128)
+PA_INSTANTIATE_CASCADE_TC(__half, 128, 64)
+PA_INSTANTIATE_CASCADE_TC(__half, 128, 128)
+PA_INSTANTIATE_CASCADE_TC(__half, 64, 64)
+PA_INSTANTIATE_CASCADE_TC(__half, 64, 128)
 
 #define PA_INSTANTIATE_CASCADE(DT, D, NT)                                                                   \
   template pa_status launch_cascade_prefix<DT, D, NT>(const CUtensorMap&, const CUtensorMap&, const DecodeParams&, \

@@ -6,17 +6,18 @@
 // prefix, partition by partition, and writes the partition's normalised
 // partial output with its (max, sum) (CS349E Lecture 7 notes §5.1 and §5.3 for
 // the shared blocks; CMU 15-779 Lecture 16 notes §3.3 for the merge). Here the
-// group's rows form the M = 64 side of real matrix products:
-//   S = Q K^T   M = 64 rows (padded), N = 32 tokens, K = head_dim
-//   O += P V    M = 64 rows, N = head_dim, K = 32 tokens
+// group's rows form the M side (64 or 128, padded) of real matrix products:
+//   S = Q K^T   M rows, N = 32 tokens, K = head_dim
+//   O += P V    M rows, N = head_dim, K = 32 tokens
 // Warp roles (192 threads):
-//   warps 0-3  softmax: thread t < 16 of warp w owns query row 16 w + t, which
-//              an M = 64 accumulator keeps in tensor-memory lane 32 w + t; it
+//   warps 0-3  softmax: each thread owns one query row (M = 64: thread t < 16 of
+//              warp w owns row 16 w + t, kept in tensor-memory lane 32 w + t;
+//              M = 128: thread t of warp w owns row 32 w + t, in that lane); it
 //              reads its row of S, keeps the running (max, sum), writes its row
 //              of P (16-bit hi + lo parts) to shared memory and, at the end of
 //              an item, reads its row of O;
 //   warp 4     TMA producer: two 16-token jobs per stage (K and V, 128-byte
-//              swizzle), a ring of five stages;
+//              swizzle), a ring of five stages (three for M = 128);
 //   warp 5     owns the tensor memory (allocation, release); its lane 0 issues
 //              every MMA and commits them to mbarriers.
 // S is double-buffered in tensor memory, so the scores of a tile are computed
@@ -36,9 +37,11 @@
 
 namespace pa {
 
-constexpr int kTcRows = 64;        // M: query rows of one group (members x heads), padded
+constexpr int kTcMaxRows = 128;    // query rows of one group (members x heads) the pass takes
 constexpr int kTcTokens = 32;      // N of S, K of P V: tokens per stage (two TMA jobs)
-constexpr int kTcStages = 5;
+// M of the tiles is 64 (groups of 33-64 query rows) or 128 (65-128); the
+// larger Q tile of M = 128 leaves room for three stages instead of five.
+__host__ __device__ constexpr int tc_stages(int MR) { return MR == 64 ? 5 : 3; }
 constexpr int kTcThreads = 192;
 constexpr float kTcRescale = 8.f;
 
@@ -50,14 +53,14 @@ struct TcLayout {
 // each [head_dim / 64 regions][32 tokens][128 B]), the P buffer ([64 rows]
 // [128 B]: a row's 32 hi weights, then its 32 lo weights), mbarriers, the
 // tensor-memory base, the abort flag, per-stage job flags and the group scan.
-__host__ __device__ inline TcLayout tc_layout(int D, int num_groups) {
+__host__ __device__ inline TcLayout tc_layout(int D, int num_groups, int MR) {
   TcLayout L;
-  L.q_bytes = kTcRows * D * 2;
+  L.q_bytes = MR * D * 2;
   L.stage_off = L.q_bytes;
   L.stage_bytes = 2u * kTcTokens * D * 2;
-  L.p_off = L.stage_off + kTcStages * L.stage_bytes;
-  L.bar_off = L.p_off + kTcRows * 128;
-  L.misc_off = L.bar_off + (2 * kTcStages + 12) * 8;
+  L.p_off = L.stage_off + tc_stages(MR) * L.stage_bytes;
+  L.bar_off = L.p_off + MR * 128;
+  L.misc_off = L.bar_off + (2 * tc_stages(MR) + 12) * 8;
   L.sched_off = round_up(L.misc_off + 16, 16);
   L.total = round_up(L.sched_off + (num_groups + 1) * 4, 16) + 1024;
   return L;
@@ -174,13 +177,14 @@ __device__ __forceinline__ void tma_load_zero_tile(void* dst, const CUtensorMap*
     tma_load_2d(dst, map, x, -kJobTokens, bar);
 }
 
-template <typename DT, int D>
+template <typename DT, int D, int MR>
 __global__ void __launch_bounds__(kTcThreads, 2)
     cascade_prefix_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                              const DecodeParams p) {
   pdl_begin();
   static_assert(sizeof(DT) == 2 && (D == 64 || D == 128), "tensor-core prefix pass: 16-bit caches, head_dim 64/128");
-  constexpr int R = kTcStages, NT = kTcTokens, JT = kJobTokens, M = kTcRows;
+  static_assert(MR == 64 || MR == 128, "tiles of 64 or 128 query rows");
+  constexpr int R = tc_stages(MR), NT = kTcTokens, JT = kJobTokens, M = MR;
   constexpr int NREG = D / 64;            // 128-byte regions of a row
   constexpr int TILE = NT * D * 2;        // K (or V) bytes of one stage
   constexpr int REG_BYTES = NT * 128;     // one region of a stage's K (or V): [32 tokens][128 B]
@@ -192,7 +196,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const TcLayout L = tc_layout(D, p.num_groups);
+  const TcLayout L = tc_layout(D, p.num_groups, MR);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
   uint64_t* full = bars;              // [R] TMA -> MMA
   uint64_t* empty = bars + R;         // [R] MMA (P V done) -> TMA
@@ -338,7 +342,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (ok && lane < 4 * NREG) {
           const int j = lane / (2 * NREG), is_v = (lane / NREG) & 1, rg = lane % NREG;
-          long long phys = ph[j];
+          long long phys = j ? ph[1] : ph[0];  // (a select: no local-memory array)
           if (phys >= p.num_blocks) phys = -1;
           const int tok = (ua + j) * JT;
           const int r0 = tok - ((tok >> p.block_shift) << p.block_shift);
@@ -438,8 +442,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   } else {
     // -------------------------------- softmax --------------------------------
     const float NEG_INF = -__int_as_float(0x7f800000);
-    const int row = 16 * warp + lane;    // row of the M = 64 tiles (lanes >= 16 hold none)
-    const bool has_row = lane < 16;
+    // the row this thread owns: an M = 64 accumulator keeps row 16 w + t in lane
+    // 32 w + t (lanes t >= 16 hold none), an M = 128 one keeps row 32 w + t in lane 32 w + t
+    const int row = MR == 64 ? 16 * warp + lane : 32 * warp + lane;
+    const bool has_row = MR == 128 || lane < 16;
     const uint32_t lane_addr = tbase + ((uint32_t)(32 * warp) << 16);
     // Q of an item into the Q tile: row r = member r / group, head r % group, by
     // cp.async (padding rows are zero); 128 threads, 16-byte chunks, 128-byte

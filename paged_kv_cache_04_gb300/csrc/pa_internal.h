@@ -29,7 +29,7 @@ pa_status launch_cascade_prefix(const CUtensorMap& kmap, const CUtensorMap& vmap
                                 int num_sms, long long max_items, cudaStream_t stream);
 
 // The same pass on tcgen05 tensor cores (pa_cascade.cu).
-template <typename DT, int D>
+template <typename DT, int D, int MR>
 pa_status launch_cascade_prefix_tc(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                                    int num_sms, long long max_items, cudaStream_t stream);
 

@@ -76,6 +76,6 @@ def test_cascade_degenerate_groupings(pa, cuda_device):
 
 
 def test_cascade_rejects_wide_groups(pa, cuda_device):
-    wl = workloads.shared_prefix(device=cuda_device, prompts=1, samples=32, prefix=64, tail_hi=8)
+    wl = workloads.shared_prefix(device=cuda_device, prompts=1, samples=33, prefix=64, tail_hi=8)
     with pytest.raises(pa.PAError):
-        _cascade(pa, wl, wl.meta["group_starts"], wl.meta["prefix_lens"])  # 32 x 4 rows > 64
+        _cascade(pa, wl, wl.meta["group_starts"], wl.meta["prefix_lens"])  # 33 x 4 rows > 128

@@ -1,7 +1,8 @@
-"""The tcgen05 prefix pass of pa_decode_cascade (groups of 33-64 query rows).
+"""The tcgen05 prefix pass of pa_decode_cascade (groups of 33-128 query rows).
 
-Groups of 16 samples x 4 query heads (or 8 x 8) fill the M = 64 tile, so the
-shared-prefix decode runs its prefix pass on the fifth-generation tensor cores.
+Groups of 16 samples x 4 query heads (or 8 x 8) fill the M = 64 tile, groups of
+32 x 4 (or 16 x 8) the M = 128 tile, so the shared-prefix decode runs its
+prefix pass on the fifth-generation tensor cores.
 Each case is checked against the oracle (which sees the pool before any kernel
 ran) and against plain pa_decode of the same batch: long prefixes (many tiles
 and several items per CTA), a last partition of one 16-token job, both block
@@ -51,6 +52,11 @@ CASES = [
     (12, 32, 8, 128, 16, torch.bfloat16, 777, "HND", True),    # 48 rows: a partly filled tile
     (16, 32, 8, 64, 16, torch.bfloat16, 1300, "HND", False),   # head_dim 64
     (16, 16, 4, 64, 32, torch.float16, 1500, "NHD", False),
+    # M = 128 tiles
+    (32, 32, 8, 128, 16, torch.bfloat16, 1040, "HND", True),   # 128 rows
+    (16, 64, 8, 128, 32, torch.float16, 1300, "NHD", False),   # 16 samples x group 8
+    (20, 32, 8, 128, 16, torch.bfloat16, 700, "HND", False),   # 80 rows: a partly filled tile
+    (32, 32, 8, 64, 16, torch.float16, 900, "NHD", True),      # head_dim 64
 ]
 
 
@@ -73,10 +79,11 @@ def test_tc_prefix_matches_oracle(pa, cuda_device, case):
     assert pa.pa_get_error() == 0
 
 
-def test_tc_prefix_rescales(pa, cuda_device):
+@pytest.mark.parametrize("samples", [16, 32], ids=["m64", "m128"])
+def test_tc_prefix_rescales(pa, cuda_device, samples):
     """q scaled by 40: scores spread over tens of log2 units, so a row's reference
     max moves many times within an item (and the accumulator is rescaled)."""
-    wl = workloads.shared_prefix(device=cuda_device, prompts=2, samples=16, prefix=2000, tail_hi=50)
+    wl = workloads.shared_prefix(device=cuda_device, prompts=2, samples=samples, prefix=2000, tail_hi=50)
     wl.q.mul_(40.0)
     ref = H.Pristine(wl).decode()
     _writes(pa, wl)

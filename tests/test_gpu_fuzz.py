@@ -85,12 +85,13 @@ def test_fuzz(pa, cuda_device, i):
 
 def _cascade_case(i):
     r = random.Random(5000 + i)
-    return dict(prompts=r.randint(1, 6), samples=r.choice([1, 2, 3, 8, 16]), prefix=r.choice([0, 5, 16, 100, 700]),
+    return dict(prompts=r.randint(1, 6), samples=r.choice([1, 2, 3, 8, 16, 24, 32]),
+                prefix=r.choice([0, 5, 16, 100, 700]),
                 tail_hi=r.choice([1, 40, 300]), cow=r.random() < 0.5, T=16 * r.choice([1, 4, 32]),
                 layout=r.choice(["HND", "NHD"]))
 
 
-@pytest.mark.parametrize("i", range(16))
+@pytest.mark.parametrize("i", range(20))
 def test_fuzz_cascade(pa, cuda_device, i):
     c = _cascade_case(i)
     wl = workloads.shared_prefix(device=cuda_device, prompts=c["prompts"], samples=c["samples"], prefix=c["prefix"],
