@@ -200,6 +200,8 @@ pa_status run_decode(const DecodeArgs& a, bool split, int partition, int max_par
   p.scale_log2 = a.scale * a.k_scale * 1.4426950408889634f;
   p.v_scale = a.v_scale;
   p.nhd = a.layout == PA_LAYOUT_NHD;
+  p.k_cache = a.k_cache;
+  p.v_cache = a.v_cache;
   p.err = err;
   long long items = (long long)a.S * a.G;
   if (split) {

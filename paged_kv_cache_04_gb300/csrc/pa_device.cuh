@@ -94,6 +94,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// A hint: fetch `bytes` (a multiple of 16, 16-byte aligned) at `src` into L2.
+__device__ __forceinline__ void l2_prefetch(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // TMA: tiled 2-D tensor load into shared memory, completion on an mbarrier
 // ---------------------------------------------------------------------------
