@@ -366,7 +366,11 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
       // stable counting sort of the sequences by length bucket, longest first
       constexpr bool FINE_ORDER = !MMA || F8 || SUFFIX;
       uint16_t* order = reinterpret_cast<uint16_t*>(smem + L.sched_off);
-      int* base = reinterpret_cast<int*>(smem);  // kNumBuckets counters, in stage memory
+      // kNumBuckets counters, then each sequence's bucket, in stage memory (at least
+      // 32 KiB, free until the first copy): a bucket is computed once, by the whole
+      // CTA (in suffix mode it takes a search over the groups)
+      int* base = reinterpret_cast<int*>(smem);
+      uint16_t* keys = reinterpret_cast<uint16_t*>(smem + kNumBuckets * 4);
       for (int b = tid; b < kNumBuckets; b += nthreads) base[b] = 0;
       __syncthreads();
       auto bucket = [&](int s) {  // ascending bucket index = descending length
@@ -379,7 +383,11 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
                                    : min(c >> 9, kNumBuckets - 1);
         return kNumBuckets - 1 - key;
       };
-      for (int s = tid; s < p.S; s += nthreads) atomicAdd(&base[bucket(s)], 1);
+      for (int s = tid; s < p.S; s += nthreads) {
+        const int b = bucket(s);
+        keys[s] = (uint16_t)b;
+        atomicAdd(&base[b], 1);
+      }
       __syncthreads();
       if (warp == 0) {
         constexpr int PER = kNumBuckets / 32;
@@ -403,7 +411,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
         const unsigned lt = (1u << lane) - 1u;
         for (int c0 = 0; c0 < p.S; c0 += 32) {
           const int s = c0 + lane;
-          const int key = s < p.S ? bucket(s) : -1 - lane;  // padding lanes: keys of their own
+          const int key = s < p.S ? (int)keys[s] : -1 - lane;  // padding lanes: keys of their own
           const unsigned peers = __match_any_sync(0xffffffffu, key);
           if (s < p.S) order[base[key] + __popc(peers & lt)] = (uint16_t)s;
           __syncwarp();
