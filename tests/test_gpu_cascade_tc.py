@@ -57,6 +57,11 @@ CASES = [
     (16, 64, 8, 128, 32, torch.float16, 1300, "NHD", False),   # 16 samples x group 8
     (20, 32, 8, 128, 16, torch.bfloat16, 700, "HND", False),   # 80 rows: a partly filled tile
     (32, 32, 8, 64, 16, torch.float16, 900, "NHD", True),      # head_dim 64
+    # MHA and group 2: the vector-path suffix passes, and row counts that are not multiples of 16
+    (8, 8, 8, 128, 16, torch.float16, 600, "HND", True),       # MHA, 8 rows (mma.sync prefix pass)
+    (40, 8, 8, 128, 16, torch.bfloat16, 700, "HND", False),    # MHA, 40 rows (M = 64)
+    (100, 8, 8, 128, 32, torch.float16, 500, "NHD", True),     # MHA, 100 rows (M = 128)
+    (20, 16, 8, 128, 16, torch.bfloat16, 800, "HND", False),   # group 2, 40 rows
 ]
 
 
