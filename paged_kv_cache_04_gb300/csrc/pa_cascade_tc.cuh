@@ -50,7 +50,7 @@ struct TcLayout {
 };
 
 // Offsets from the 1024-byte aligned base: the Q tile, the stages (K then V,
-// each [head_dim / 64 regions][32 tokens][128 B]), the P buffer ([64 rows]
+// each [head_dim / 64 regions][32 tokens][128 B]), the P buffer ([M rows]
 // [128 B]: a row's 32 hi weights, then its 32 lo weights), mbarriers, the
 // tensor-memory base, the abort flag, per-stage job flags and the group scan.
 __host__ __device__ inline TcLayout tc_layout(int D, int num_groups, int MR) {
@@ -202,9 +202,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   uint64_t* empty = bars + R;         // [R] MMA (P V done) -> TMA
   uint64_t* s_full = bars + 2 * R;    // [2] S written -> softmax
   uint64_t* s_free = s_full + 2;      // [2] S read -> MMA
-  uint64_t* q_full = s_full + 4;      // [0]: the item's Q tile written -> MMA
-  uint64_t* p_full = s_full + 6;      // [0]: P written -> MMA
-  uint64_t* pv_done = s_full + 8;     // [0]: P V done -> softmax (P free, O current)
+  uint64_t* q_full = s_full + 4;      // [0]: the item's Q tile written -> MMA ([1] unused)
+  uint64_t* p_full = s_full + 6;      // [0]: P written -> MMA ([1] unused)
+  uint64_t* pv_done = s_full + 8;     // [0]: P V done -> softmax (P free, O current; [1] unused)
   uint64_t* o_free = s_full + 10;     // O read at the end of an item -> MMA
   uint64_t* fin = s_full + 11;        // every MMA done (teardown)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc_off);
