@@ -42,7 +42,9 @@
 //     fragments); otherwise (MHA, group < 4, fp32) lanes split head_dim and use
 //     FFMA, with V staged unswizzled so a token row sits at fixed offsets;
 //   * the softmax is online, in fp32, base 2, with warp shuffles for the maxima;
-//     the output accumulators are rescaled only when a running max grew;
+//     the output accumulators are rescaled only when a running max grew; in
+//     plain mode the running max may also lag the true one by up to kLazyTau
+//     (see below);
 //   * every kernel waits for the grid before it (programmatic dependent launch)
 //     before touching global memory.
 #pragma once
@@ -52,6 +54,14 @@
 namespace pa {
 
 constexpr int kMaxGroup = 8;          // query heads per kv head
+// Plain mode keeps a stale running max m while no new score exceeds it by more
+// than kLazyTau (base 2): weights exp2(z - m) then stay below 2^kLazyTau, which
+// fp32 sums and the hi + lo 16-bit split of P carry without loss, and the job
+// skips the max shuffles and the accumulator rescale. The result is the same
+// softmax (numerator and denominator share the stale reference); only the
+// rounding differs. Split and suffix passes keep the exact per-partition max
+// (a lagging max there measured slower on 32K-128K-token split decode).
+constexpr float kLazyTau = 8.f;
 constexpr int kSortMaxSeqs = 2048;    // longest-first ordering up to this batch size
 constexpr int kSplitMaxSeqs = 2048;   // split mode keeps per-sequence offsets in shared memory
 // Sort key of a length: about 8 log2(len) (the exponent and the top three
@@ -289,6 +299,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
   constexpr bool MMA = PATH == kPathMma;
   constexpr bool SPLIT = MODE == kModeSplit;
   constexpr bool SUFFIX = MODE == kModeSuffix;
+  constexpr bool LAZY = MODE == kModePlain;  // stale running max, see kLazyTau
   constexpr bool F8 = std::is_same<DT, fp8e4m3>::value;
   constexpr bool PAIR = F8;  // tensor-core path: two jobs per softmax step
   static_assert(!PAIR || StageCfg<DT, D, PATH>::R >= 2, "two jobs per step need two stages");
@@ -765,6 +776,23 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
       // Online-softmax step over N jobs' scores: update the running max (m0, m1)
       // and sums (l0, l1), rescale o if a max grew, turn z into weights in place.
       auto softmax_step = [&](float (*z)[4], int N) {
+        bool up = false;  // some head's new score passes its running max by > kLazyTau
+#pragma unroll
+        for (int n = 0; n < N; ++n)
+          up |= (fmaxf(z[n][0], z[n][2]) > m0 + kLazyTau) | (fmaxf(z[n][1], z[n][3]) > m1 + kLazyTau);
+        if (LAZY && !__any_sync(0xffffffffu, up)) {
+          // the first job of an item always takes the exact branch (m0 = m1 = -inf)
+#pragma unroll
+          for (int n = 0; n < N; ++n) {
+            z[n][0] = exp2f(z[n][0] - m0);
+            z[n][1] = exp2f(z[n][1] - m1);
+            z[n][2] = exp2f(z[n][2] - m0);
+            z[n][3] = exp2f(z[n][3] - m1);
+            l0 += z[n][0] + z[n][2];
+            l1 += z[n][1] + z[n][3];
+          }
+          return;
+        }
         float mx0 = NEG_INF, mx1 = NEG_INF;
 #pragma unroll
         for (int n = 0; n < N; ++n) {
@@ -1039,16 +1067,22 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
             float z = zc[0];
             if (LPT == 2) z += __shfl_xor_sync(0xffffffffu, z, 16);
             z = t < nv ? z * p.scale_log2 : NEG_INF;
-            float mx = z;
+            float pt;
+            if (!LAZY || __any_sync(0xffffffffu, z > mr[h] + kLazyTau)) {
+              float mx = z;
 #pragma unroll
-            for (int o2 = 1; o2 < 16; o2 <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
-            const float mn = fmaxf(mr[h], mx);
-            const float corr = exp2f(mr[h] - mn);
-            mr[h] = mn;
-            const float pt = exp2f(z - mn);
-            lr[h] = lr[h] * corr + (part == 0 ? pt : 0.f);
+              for (int o2 = 1; o2 < 16; o2 <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+              const float mn = fmaxf(mr[h], mx);
+              const float corr = exp2f(mr[h] - mn);
+              mr[h] = mn;
+              pt = exp2f(z - mn);
+              lr[h] = lr[h] * corr + (part == 0 ? pt : 0.f);
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) o[h][e] *= corr;
+              for (int e = 0; e < EPL; ++e) o[h][e] *= corr;
+            } else {  // stale max within kLazyTau of every score: no rescale
+              pt = exp2f(z - mr[h]);
+              lr[h] += part == 0 ? pt : 0.f;
+            }
             // P V: the job's 16 weights go through shared memory (4 broadcast loads
             // instead of 16 shuffles); V tiles of the vector paths are staged without
             // swizzling, so token tt of this lane's columns is at a fixed offset.
