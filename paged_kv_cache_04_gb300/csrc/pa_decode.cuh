@@ -16,9 +16,11 @@
 //     boxes of 16 rows x head_dim, taken from one physical block (a 32-token
 //     block is two jobs). Each warp owns R job stages in shared memory, filled
 //     by TMA tensor copies (2-D over HND rows, 3-D for NHD; the box lands the
-//     same way) that complete on the stage's mbarrier; the warp's lane 0 issues
-//     the copy of the job R ahead each time it finishes one, so a warp always
-//     has R - 1 jobs in flight while it computes one (a single producer warp
+//     same way) that complete on the stage's K and V mbarriers; the warp's lane
+//     0 issues the copy of the job R ahead each time it finishes one, so a warp
+//     always has R - 1 jobs in flight while it computes one (plain-mode tensor
+//     cores issue the K half as soon as q K^T has read the old one; a single
+//     producer warp
 //     feeding all four rings measured 45% slower: its serial block-table and
 //     context-length loads at item boundaries stall every ring at once);
 //   * plain mode: a work item is (sequence, kv head); items are dealt to CTAs
@@ -148,7 +150,7 @@ __host__ __device__ inline SmemLayout make_layout(int W, int R, int D, int esize
   L.stage_bytes = 2u * kJobTokens * D * esize;
   unsigned off = W * R * L.stage_bytes;
   L.bars_off = off;
-  off += W * R * 8;
+  off += W * R * 16;  // per stage: K barrier, V barrier
   L.ok_off = off;
   off = round_up(off + W * R, 16);
   L.merge_off = off;
@@ -302,6 +304,17 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
   constexpr bool LAZY = MODE == kModePlain;  // stale running max, see kLazyTau
   constexpr bool F8 = std::is_same<DT, fp8e4m3>::value;
   constexpr bool PAIR = F8;  // tensor-core path: two jobs per softmax step
+  // Plain-mode tensor-core step on 16-bit data: a stage's K tile is refilled
+  // right after q K^T, its V tile after P V (two barriers per stage). Measured
+  // +2.7% on the Llama batch; the same split in split mode, in the suffix pass
+  // and on the MHA vector path was 2-4% slower, so those refill whole stages.
+  constexpr bool KV_SPLIT = PATH == kPathMma && !F8 && MODE == kModePlain;
+  // The 16-bit tensor-core paths land K and V on separate barriers in every
+  // mode (split decode measured +2% with it); E4M3 (two jobs per step) and the
+  // vector paths keep one barrier for both (two measured 1.5-2.5% slower on
+  // E4M3 and 1.4% on the one-stage head_dim-256 vector path).
+  constexpr bool TWO_BARS = MMA && !F8;
+  static_assert(!KV_SPLIT || TWO_BARS, "a split refill needs a barrier per half");
   static_assert(!PAIR || StageCfg<DT, D, PATH>::R >= 2, "two jobs per step need two stages");
   using MT = typename std::conditional<F8, __half, DT>::type;  // tensor-core operand type
   static_assert(!F8 || D % 64 == 0, "FP8 caches need head_dim a multiple of 64");
@@ -329,7 +342,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
   const int tid = threadIdx.x, nthreads = W * 32;
 
   if (tid == 0) {
-    for (int i = 0; i < W * R; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < 2 * W * R; ++i) mbar_init(&bars[i], 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -465,7 +478,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
 
   // ---- per-warp issue cursor over this warp's jobs ---------------------------
   uint8_t* my_stages = smem + warp * R * L.stage_bytes;
-  uint64_t* my_bars = bars + warp * R;
+  uint64_t* my_bars = bars + warp * 2 * R;  // [0, R): K tiles, [R, 2R): V tiles
   volatile uint8_t* my_ok = stage_ok + warp * R;
   // split mode: each warp owns whole partitions; suffix mode: each warp owns items
   constexpr bool WARP_PARTS = SPLIT || SUFFIX;
@@ -512,30 +525,43 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
     cursor_settle(ic);
   }
 
-  auto issue = [&](const Cursor& c, int n) {
+  // part: kPartK (the K tile and the stage's ok flag), kPartV, or both
+  constexpr int kPartK = 1, kPartV = 2;
+  auto issue = [&](const Cursor& c, int n, int part) {
     if (lane == 0) {
       const int stage = n % R;
-      uint64_t* bar = &my_bars[stage];
+      uint64_t* kbar = &my_bars[stage];
+      uint64_t* vbar = TWO_BARS ? &my_bars[R + stage] : kbar;
       const int tok = c.u * JT;
       const int blk = tok >> p.block_shift;
       const long long phys = c.phys;
       if (phys < 0 || phys >= p.num_blocks) {
-        atomicOr(p.err, kErrBlockId);
-        my_ok[stage] = 0;
-        mbar_arrive(bar);  // completes the phase with no data; the consumer skips the job
+        // complete the phases with no data; the consumer skips the job
+        if (part & kPartK) {
+          atomicOr(p.err, kErrBlockId);
+          my_ok[stage] = 0;
+          mbar_arrive(kbar);
+        }
+        if (TWO_BARS && (part & kPartV)) mbar_arrive(vbar);
       } else {
-        my_ok[stage] = 1;
         uint8_t* kdst = my_stages + stage * L.stage_bytes;
         uint8_t* vdst = kdst + TILE;
         const int r0 = tok - (blk << p.block_shift);
+        if (part & kPartK) my_ok[stage] = 1;
         fence_proxy_async_smem();
-        mbar_arrive_expect_tx(bar, 2 * TILE);
+        if (part & kPartK) {
+          mbar_arrive_expect_tx(kbar, TWO_BARS ? TILE : 2 * TILE);
 #pragma unroll
-        for (int rg = 0; rg < NREG; ++rg) {
-          tma_load_tile(kdst + rg * JT * 128, &kmap, p, rg * BOX_X, phys, c.it.kv, r0, bar);
-          tma_load_tile(vdst + rg * JT * 128, &vmap, p, rg * BOX_X, phys, c.it.kv, r0, bar);
+          for (int rg = 0; rg < NREG; ++rg)
+            tma_load_tile(kdst + rg * JT * 128, &kmap, p, rg * BOX_X, phys, c.it.kv, r0, kbar);
         }
-        if constexpr (PREFETCH) {
+        if (part & kPartV) {
+          if (TWO_BARS) mbar_arrive_expect_tx(vbar, TILE);
+#pragma unroll
+          for (int rg = 0; rg < NREG; ++rg)
+            tma_load_tile(vdst + rg * JT * 128, &vmap, p, rg * BOX_X, phys, c.it.kv, r0, vbar);
+        }
+        if (PREFETCH && (part & kPartV)) {
           if (c.pf >= 0 && c.pf < p.num_blocks) {  // [pf][kv][rows of job u + PF_AHEAD]: 16 x D contiguous
             const int tokf = (c.u + PF_AHEAD) * JT;
             const size_t off =
@@ -554,7 +580,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
   int n_issue = 0;
 #pragma unroll 1
   for (int r = 0; r < R && ic.valid; ++r) {
-    issue(ic, n_issue++);
+    issue(ic, n_issue++, kPartK | kPartV);
     ic.u += job_step;
     cursor_settle(ic);
   }
@@ -567,14 +593,45 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
     const int n = n_done + ahead;
     stage_out = n % R;
     bool ok = mbar_wait_bounded(&my_bars[stage_out], (n / R) & 1, abort_flag, p.err, kWaitLimitNs);
+    if (TWO_BARS && !KV_SPLIT && ok)
+      ok = mbar_wait_bounded(&my_bars[R + stage_out], (n / R) & 1, abort_flag, p.err, kWaitLimitNs);
     ok = __all_sync(0xffffffffu, ok);
     return ok && my_ok[stage_out];
+  };
+  // KV_SPLIT: the current job's V tile, waited for only before P V
+  auto wait_v = [&]() -> bool {
+    if constexpr (!KV_SPLIT) return true;  // next_job waited for the whole stage
+    const int n = n_done;
+    const bool ok = mbar_wait_bounded(&my_bars[R + n % R], (n / R) & 1, abort_flag, p.err, kWaitLimitNs);
+    return __all_sync(0xffffffffu, ok);
+  };
+  // KV_SPLIT: the current job's K tile is read; refill it with the K of the job R
+  // ahead now, and its V after P V (job_done). After an abort no new half goes
+  // out; a K half already out without its V is drained on its own at the end.
+  auto aborted = [&]() -> bool { return __shfl_sync(0xffffffffu, *abort_flag, 0) != 0; };
+  bool v_pending = false, k_orphan = false;
+  auto k_done = [&]() {
+    if constexpr (!KV_SPLIT) return;  // the stage is refilled whole by job_done
+    __syncwarp();
+    v_pending = ic.valid && !aborted();
+    if (v_pending) issue(ic, n_issue, kPartK);
   };
   auto job_done = [&]() {  // release the stage and refill it with the job R ahead
     __syncwarp();
     ++n_done;
-    if (ic.valid && !*abort_flag) {
-      issue(ic, n_issue++);
+    if constexpr (KV_SPLIT) {
+      if (v_pending) {
+        v_pending = false;
+        if (aborted()) {
+          k_orphan = true;  // job n_issue: K in flight, V never issued
+        } else {
+          issue(ic, n_issue++, kPartV);
+          ic.u += job_step;
+          cursor_settle(ic);
+        }
+      }
+    } else if (ic.valid && !*abort_flag) {
+      issue(ic, n_issue++, kPartK | kPartV);
       ic.u += job_step;
       cursor_settle(ic);
     }
@@ -866,8 +923,11 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
             const int nv = min(JT, it.t1 - u * JT);
             float z[1][4];
             job_scores(ktp, nv, z[0]);
+            k_done();
             softmax_step(z, 1);
-            job_pv(ktp, nv, z[0]);
+            if (wait_v()) job_pv(ktp, nv, z[0]);
+          } else {
+            k_done();
           }
           job_done();
         }
@@ -1211,8 +1271,11 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
   // ---- let every copy this warp started land before the block exits ------------
   if (lane == 0) {
     const int first = n_issue - R > 0 ? n_issue - R : 0;
-    for (int n = first; n < n_issue; ++n)
+    for (int n = first; n < n_issue; ++n) {
       mbar_wait_bounded(&my_bars[n % R], (n / R) & 1, nullptr, p.err, kDrainLimitNs);
+      if (TWO_BARS) mbar_wait_bounded(&my_bars[R + n % R], (n / R) & 1, nullptr, p.err, kDrainLimitNs);
+    }
+    if (k_orphan) mbar_wait_bounded(&my_bars[n_issue % R], (n_issue / R) & 1, nullptr, p.err, kDrainLimitNs);
   }
   __syncwarp();
 }
