@@ -336,6 +336,24 @@ pa_status pa_swap_blocks(void* const* dst_k_caches, void* const* dst_v_caches,
  */
 pa_status pa_get_error(uint32_t* error_bits, cudaStream_t stream);
 
+/*
+ * Diagnostic of the bounded waits that every kernel uses on its mbarriers
+ * (each gives up after a time limit instead of spinning forever).
+ *
+ * Launches one CTA of two warps on `stream`. Warp 0 waits on an mbarrier that
+ * nothing completes and gives up after limit_ns (host value, nanoseconds); it
+ * raises the CTA's abort flag and ORs PA_DEVERR_TIMEOUT into the error word.
+ * Warp 1 waits on a second such barrier with a limit 50 times longer and must
+ * leave as soon as it sees the abort flag, as the decode kernels' warps do
+ * once one of them has given up. The call therefore takes about limit_ns of
+ * device time, not 50 times that, and leaves the CUDA context usable. Read the
+ * result with pa_get_error().
+ *
+ * limit_ns must lie in [1000, 100000000] (1 us to 100 ms); otherwise
+ * PA_ERR_INVALID_ARG, with no CUDA call. Asynchronous; allocates nothing.
+ */
+pa_status pa_check_wait_limit(uint64_t limit_ns, cudaStream_t stream);
+
 /* A static, human-readable name for a status. */
 const char* pa_status_string(pa_status status);
 

@@ -25,7 +25,7 @@ __all__ = [
     "PAError", "library", "library_path", "pa_reshape_and_cache", "pa_decode", "pa_decode_split",
     "pa_decode_split_workspace_bytes", "pa_decode_split_static", "pa_copy_blocks", "pa_swap_blocks",
     "pa_reshape_and_cache_fp8", "pa_decode_fp8", "pa_decode_split_fp8", "pa_decode_cascade",
-    "pa_decode_cascade_workspace_bytes", "pa_get_error",
+    "pa_decode_cascade_workspace_bytes", "pa_get_error", "pa_check_wait_limit",
     "pa_version", "PA_STATIC_SCRATCH_BYTES", "PA_LAYOUT_HND", "PA_LAYOUT_NHD",
     "PA_DEVERR_BLOCK_ID", "PA_DEVERR_SLOT", "PA_DEVERR_CONTEXT", "PA_DEVERR_PAIR", "PA_DEVERR_TIMEOUT",
 ]
@@ -75,6 +75,7 @@ def library():
     lib.pa_decode_cascade.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, I64, F, I, I, P, P, I, I, I, I, I, P,
                                       SZ, P]
     lib.pa_get_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), P]
+    lib.pa_check_wait_limit.argtypes = [ctypes.c_uint64, P]
     lib.pa_status_string.argtypes = [I]
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_version.argtypes = []
@@ -98,7 +99,7 @@ def library():
     lib.pa_bm_stats.restype = None
     for f in ("pa_reshape_and_cache", "pa_decode", "pa_decode_split", "pa_decode_split_static",
               "pa_copy_blocks", "pa_swap_blocks", "pa_reshape_and_cache_fp8", "pa_decode_fp8",
-              "pa_decode_split_fp8", "pa_decode_cascade", "pa_get_error", "pa_version"):
+              "pa_decode_split_fp8", "pa_decode_cascade", "pa_get_error", "pa_check_wait_limit", "pa_version"):
         getattr(lib, f).restype = I
     _lib = lib
     return lib
@@ -378,6 +379,13 @@ def pa_get_error(stream=None) -> int:
     if st not in (PA_OK, PA_ERR_OUT_OF_RANGE):
         raise PAError("pa_get_error", st)
     return int(bits.value)
+
+
+def pa_check_wait_limit(limit_ns, stream=None):
+    """Diagnostic: one warp's mbarrier wait runs out after ``limit_ns`` and a second
+    warp, whose limit is 50 times longer, follows it out through the abort flag;
+    ``PA_DEVERR_TIMEOUT`` is then set in the error word (read it with ``pa_get_error``)."""
+    _check("pa_check_wait_limit", library().pa_check_wait_limit(int(limit_ns), _stream(stream)))
 
 
 def pa_version() -> int:

@@ -95,6 +95,10 @@ def test_invalid_arguments_rejected_before_any_launch(lib_path):
     arr = (ctypes.c_void_p * 1)(0x10000)
     assert lib.pa_copy_blocks(arr, arr, 1, al, 0, 8, 128, 16, 10, 2, null) == 0
     assert lib.pa_copy_blocks(arr, arr, 1, null, 3, 8, 128, 16, 10, 2, null) == 1
+    # the bounded-wait diagnostic takes limits of 1 us to 100 ms only
+    assert lib.pa_check_wait_limit(0, null) == 1
+    assert lib.pa_check_wait_limit(999, null) == 1
+    assert lib.pa_check_wait_limit(100_000_001, null) == 1
 
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
