@@ -45,7 +45,8 @@
 //     FFMA, with V staged unswizzled so a token row sits at fixed offsets;
 //   * the softmax is online, in fp32, base 2, with warp shuffles for the maxima;
 //     the output accumulators are rescaled only when a running max grew; in
-//     plain mode the running max may also lag the true one by up to kLazyTau
+//     plain mode (and E4M3 split mode) the running max may also lag the true
+//     one by up to kLazyTau
 //     (see below);
 //   * every kernel waits for the grid before it (programmatic dependent launch)
 //     before touching global memory.
@@ -61,8 +62,10 @@ constexpr int kMaxGroup = 8;          // query heads per kv head
 // fp32 sums and the hi + lo 16-bit split of P carry without loss, and the job
 // skips the max shuffles and the accumulator rescale. The result is the same
 // softmax (numerator and denominator share the stale reference); only the
-// rounding differs. Split and suffix passes keep the exact per-partition max
-// (a lagging max there measured slower on 32K-128K-token split decode).
+// rounding differs. Plain mode uses it, and so does E4M3 split decode; 16-bit
+// split decode and the suffix pass keep the exact per-partition max (a lagging
+// max measured slower there). A split partial's (m, l) then describe the same
+// log-sum-exp, m + log2 l, whichever reference m is.
 constexpr float kLazyTau = 8.f;
 constexpr int kSortMaxSeqs = 2048;    // longest-first ordering up to this batch size
 constexpr int kSplitMaxSeqs = 2048;   // split mode keeps per-sequence offsets in shared memory
@@ -301,9 +304,11 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
   constexpr bool MMA = PATH == kPathMma;
   constexpr bool SPLIT = MODE == kModeSplit;
   constexpr bool SUFFIX = MODE == kModeSuffix;
-  constexpr bool LAZY = MODE == kModePlain;  // stale running max, see kLazyTau
   constexpr bool F8 = std::is_same<DT, fp8e4m3>::value;
   constexpr bool PAIR = F8;  // tensor-core path: two jobs per softmax step
+  // stale running max (see kLazyTau): plain mode, and E4M3 split mode (+2.8%
+  // there; 16-bit split decode measured 6% slower with it)
+  constexpr bool LAZY = MODE == kModePlain || (F8 && MODE == kModeSplit);
   // Plain-mode tensor-core step on 16-bit data: a stage's K tile is refilled
   // right after q K^T, its V tile after P V (two barriers per stage). Measured
   // +2.7% on the Llama batch; the same split in split mode, in the suffix pass
