@@ -22,6 +22,7 @@ RESERVED_PER_CTA = 1024
 PROGRAM = r"""
 #include <cstdio>
 #include "pa_decode.cuh"
+#include "pa_cascade_tc.cuh"
 using namespace pa;
 template <typename DT, typename QT, int D, int PATH>
 void row(const char* name, int group, int split, int S) {
@@ -39,6 +40,11 @@ int main() {
         row<__half, __half, 128, kPathVecMha>("mha_d128", 1, sp, S);
         row<__nv_bfloat16, __nv_bfloat16, 256, kPathVec>("vec_d256", 2, sp, S);
       }
+  // the tcgen05 prefix pass of shared-prefix decode: (groups) in the group slot
+  for (int D : {64, 128})
+    for (int MR : {64, 128})
+      for (int g : {32, 512, 2048})
+        printf("tc_d%d_m%d %d 0 0 %u\n", D, MR, g, tc_layout(D, g, MR).total);
 }
 """
 
@@ -79,18 +85,23 @@ HOLDS = [
     (("mha_d128", 1, 1, 256), 3),
     (("mma16_d256", 4, 0, 2048), 2),  # head_dim 256: one stage per warp, two CTAs
     (("vec_d256", 2, 0, 2048), 2),
+    (("tc_d128_m64", 512, 0, 0), 2),   # tcgen05 prefix pass, 33-64 rows per group
+    (("tc_d128_m128", 2048, 0, 0), 2),  # 65-128 rows per group
+    (("tc_d64_m64", 2048, 0, 0), 2),    # (tensor memory caps this kernel at two CTAs per SM)
 ]
 
 # Known cliffs, kept as strict expected failures so that a fix shows up here:
 # the fp32 merge area (warps x group x head_dim x 4 bytes) doubles at group 8;
 # the sort order (2 bytes per sequence) pushes E4M3 plain decode over the
 # three-CTA budget above about 750 sequences; the split schedule (4 bytes per
-# sequence) does the same to MHA split decode above about 1,900.
+# sequence) does the same to MHA split decode above about 1,900; the tcgen05
+# prefix pass's group scan costs its M = 64 form a CTA above about 2,000 groups.
 GAPS = [
     (("mma16_d128", 8, 0, 256), 2),
     (("fp8_d128", 8, 0, 256), 3),
     (("fp8_d128", 4, 0, 2048), 3),
     (("mha_d128", 1, 1, 2048), 3),
+    (("tc_d128_m64", 2048, 0, 0), 2),  # the group scan (4 bytes per group) above about 2,000 groups
 ]
 
 
