@@ -76,6 +76,7 @@ typedef enum { PA_LAYOUT_HND = 0, PA_LAYOUT_NHD = 1 } pa_kv_layout;
 #define PA_DEVERR_CONTEXT 4u  /* a context length < 0 or beyond the table / workspace was clamped */
 #define PA_DEVERR_PAIR 8u     /* a copy pair with an id outside [0, num_blocks) was skipped */
 #define PA_DEVERR_TIMEOUT 16u /* an internal wait ran past its limit; the results are undefined */
+#define PA_DEVERR_PAIR_ALIAS 32u /* a copy / swap pair racing with another pair was skipped (see pa_copy_blocks) */
 
 /*
  * Write each new token's K and V into the cache slot the block manager chose
@@ -169,6 +170,10 @@ pa_status pa_decode_split(void* out, const void* q, const void* k_cache, const v
  */
 #define PA_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
 
+/* PA_STATIC_SCRATCH_BYTES as the library was built (for bindings that cannot
+ * read the macro). Host only; no CUDA call. */
+size_t pa_static_scratch_bytes(void);
+
 /*
  * pa_decode_split without a workspace argument. The pages have no counterpart
  * to this call: it exists for callers that cannot allocate device memory at
@@ -181,15 +186,24 @@ pa_status pa_decode_split(void* out, const void* q, const void* k_cache, const v
  * inside the library instead. It calls no cudaMalloc, cudaFree or other
  * allocating routine.
  *
- *   - Size limit: pa_decode_split_workspace_bytes(num_seqs, num_heads,
- *     head_dim, max_context_len, partition_tokens) must not exceed
+ *   - Arguments are checked exactly as pa_decode_split checks them (same
+ *     statuses), then the size limit:
+ *     pa_decode_split_workspace_bytes(num_seqs, num_heads, head_dim,
+ *     max_context_len, partition_tokens) must not exceed
  *     PA_STATIC_SCRATCH_BYTES (e.g. 8 sequences x 64 heads x head_dim 128 fit
  *     up to 63 partitions, 32,256 tokens at 512-token partitions); a larger
  *     request returns PA_ERR_UNSUPPORTED and launches nothing -- use
  *     pa_decode_split with a workspace for it.
  *   - The first call on a device looks up the array's device address (once per
  *     device, with that device current); make that first call before any
- *     stream capture.
+ *     stream capture. With CUDA's lazy module loading (the default) that first
+ *     call can also be when the driver loads the library's device code and
+ *     commits the array's 16 MiB, so the "allocates nothing" guarantee holds
+ *     from the second call on: make one call (or any pa_* call that launches a
+ *     kernel) during set-up, outside the region that must not allocate.
+ *   - The address is cached per device for the life of the process; do not
+ *     use the library across cudaDeviceReset() (the same holds for the error
+ *     word every call reports into).
  *   - Every call, on every stream, shares the one array and leaves its
  *     contents behind: calls whose executions overlap on the GPU race and give
  *     undefined results. Nothing in the array needs to start at zero.
@@ -258,9 +272,16 @@ pa_status pa_decode_cascade(void* out, const void* q, const void* k_cache, const
  *                       (or NHD: the copy moves whole blocks, contiguous in both)
  *   block_pairs         int64 [num_pairs][2] (src, dst)
  *
- * The copy is bit-exact. Destinations must be distinct and no destination may
- * also be a source (the copies run in parallel). Pairs with an id outside
- * [0, num_blocks) are skipped and recorded.
+ * The copy is bit-exact. All pairs are copied in parallel, so destinations must
+ * be distinct and no destination may also be a source (its own pair's or
+ * another's). The kernel checks this on the device: every pair whose
+ * destination is another pair's destination or any pair's source, or whose
+ * source is another pair's destination, is skipped in every layer (neither K
+ * nor V is written) and PA_DEVERR_PAIR_ALIAS is recorded; the other pairs are
+ * copied. Pairs with an id outside [0, num_blocks) are skipped and recorded as
+ * PA_DEVERR_PAIR (and race with nothing). The check reads the whole pair list
+ * once per CTA, which is small next to the blocks for the few hundred pairs of
+ * a decode step; it grows as num_pairs^2.
  */
 pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers,
                          const int64_t* block_pairs, int num_pairs, int num_kv_heads, int head_dim,
@@ -319,8 +340,14 @@ pa_status pa_decode_split_fp8(void* out, const void* q, const void* k_cache, con
  *   block_pairs                 int64 [num_pairs][2] (src id, dst id), device
  *                               memory or pinned host memory
  *
- * Bit-exact. Destinations must be distinct and must not alias any source
- * block. Ids outside their pool are skipped and recorded (PA_DEVERR_PAIR).
+ * Bit-exact. Destinations must be distinct; checked on the device as for
+ * pa_copy_blocks (a pair whose destination is another pair's destination is
+ * skipped and recorded as PA_DEVERR_PAIR_ALIAS). Where a layer's source and
+ * destination pool are the same memory (the same pointer), ids of both sides
+ * name the same blocks and the copy-on-write rule applies in full: no
+ * destination may be any pair's source. Pools that overlap without being the
+ * same pointer are not supported. Ids outside their pool are skipped and
+ * recorded (PA_DEVERR_PAIR).
  */
 pa_status pa_swap_blocks(void* const* dst_k_caches, void* const* dst_v_caches,
                          const void* const* src_k_caches, const void* const* src_v_caches, int num_layers,
@@ -333,8 +360,22 @@ pa_status pa_swap_blocks(void* const* dst_k_caches, void* const* dst_v_caches,
  * work already queued on `stream` has finished. *error_bits (host) receives the
  * bits. Returns PA_ERR_OUT_OF_RANGE when any bit was set, PA_OK otherwise. It
  * synchronises `stream`.
+ *
+ * There is one error word per device, shared by every stream: the bits read
+ * are those set by any of the library's kernels that ran on the device since
+ * the last read, on whatever stream; kernels of other streams still running
+ * may set bits after the read. To attribute bits to one stream, synchronise
+ * the device's other streams first (or use one stream).
  */
 pa_status pa_get_error(uint32_t* error_bits, cudaStream_t stream);
+
+/*
+ * pa_get_error without the bits: waits for `stream`, reads and clears the
+ * calling device's error word, and returns PA_ERR_OUT_OF_RANGE if any bit was
+ * set (PA_OK otherwise; PA_ERR_CUDA if a CUDA call failed). The device-side
+ * range checks it reports are always compiled in, not only in debug builds.
+ */
+pa_status pa_debug_check(cudaStream_t stream);
 
 /*
  * Diagnostic of the bounded waits that every kernel uses on its mbarriers
@@ -354,7 +395,9 @@ pa_status pa_get_error(uint32_t* error_bits, cudaStream_t stream);
  */
 pa_status pa_check_wait_limit(uint64_t limit_ns, cudaStream_t stream);
 
-/* A static, human-readable name for a status. */
+/* A static, human-readable name for a status (never NULL). pa_status_str and
+ * pa_status_string are the same function under two names. */
+const char* pa_status_str(pa_status status);
 const char* pa_status_string(pa_status status);
 
 /* Library version, major * 10000 + minor * 100 + patch. */

@@ -28,6 +28,7 @@ __all__ = [
     "pa_decode_cascade_workspace_bytes", "pa_get_error", "pa_check_wait_limit",
     "pa_version", "PA_STATIC_SCRATCH_BYTES", "PA_LAYOUT_HND", "PA_LAYOUT_NHD",
     "PA_DEVERR_BLOCK_ID", "PA_DEVERR_SLOT", "PA_DEVERR_CONTEXT", "PA_DEVERR_PAIR", "PA_DEVERR_TIMEOUT",
+    "PA_DEVERR_PAIR_ALIAS", "pa_debug_check", "pa_status_str",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -37,7 +38,7 @@ PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_OUT_OF_RANGE, PA_ERR_CUDA 
 PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3 = 0, 1, 2, 3
 PA_LAYOUT_HND, PA_LAYOUT_NHD = 0, 1
 PA_DEVERR_BLOCK_ID, PA_DEVERR_SLOT, PA_DEVERR_CONTEXT, PA_DEVERR_PAIR, PA_DEVERR_TIMEOUT = 1, 2, 4, 8, 16
-PA_STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
+PA_DEVERR_PAIR_ALIAS = 32
 
 _lib = None
 
@@ -78,6 +79,11 @@ def library():
     lib.pa_check_wait_limit.argtypes = [ctypes.c_uint64, P]
     lib.pa_status_string.argtypes = [I]
     lib.pa_status_string.restype = ctypes.c_char_p
+    lib.pa_status_str.argtypes = [I]
+    lib.pa_status_str.restype = ctypes.c_char_p
+    lib.pa_debug_check.argtypes = [P]
+    lib.pa_static_scratch_bytes.argtypes = []
+    lib.pa_static_scratch_bytes.restype = SZ
     lib.pa_version.argtypes = []
     lib.pa_bm_create.argtypes = [I64, I, I]
     lib.pa_bm_create.restype = P
@@ -99,10 +105,18 @@ def library():
     lib.pa_bm_stats.restype = None
     for f in ("pa_reshape_and_cache", "pa_decode", "pa_decode_split", "pa_decode_split_static",
               "pa_copy_blocks", "pa_swap_blocks", "pa_reshape_and_cache_fp8", "pa_decode_fp8",
-              "pa_decode_split_fp8", "pa_decode_cascade", "pa_get_error", "pa_check_wait_limit", "pa_version"):
+              "pa_decode_split_fp8", "pa_decode_cascade", "pa_get_error", "pa_debug_check", "pa_check_wait_limit",
+              "pa_version"):
         getattr(lib, f).restype = I
     _lib = lib
     return lib
+
+
+def __getattr__(name):
+    # PA_STATIC_SCRATCH_BYTES is read from the library, so it cannot drift from the C macro
+    if name == "PA_STATIC_SCRATCH_BYTES":
+        return int(library().pa_static_scratch_bytes())
+    raise AttributeError(f"module {__name__!r} has no attribute {name!r}")
 
 
 def _torch():
@@ -379,6 +393,20 @@ def pa_get_error(stream=None) -> int:
     if st not in (PA_OK, PA_ERR_OUT_OF_RANGE):
         raise PAError("pa_get_error", st)
     return int(bits.value)
+
+
+def pa_debug_check(stream=None) -> int:
+    """Wait for the stream, read and clear the device error word; the status
+    (``PA_OK`` or ``PA_ERR_OUT_OF_RANGE`` = 3) is returned, other statuses raise."""
+    st = library().pa_debug_check(_stream(stream))
+    if st not in (PA_OK, PA_ERR_OUT_OF_RANGE):
+        raise PAError("pa_debug_check", st)
+    return int(st)
+
+
+def pa_status_str(status) -> str:
+    """The library's name for a status code."""
+    return library().pa_status_str(int(status)).decode()
 
 
 def pa_check_wait_limit(limit_ns, stream=None):

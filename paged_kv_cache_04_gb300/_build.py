@@ -18,7 +18,7 @@ LIB = os.path.join(HERE, "libpa.so")
 OBJDIR = os.path.join(HERE, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["pa_api.cu", "pa_cache.cu", "pa_decode_bf16.cu", "pa_decode_f16.cu", "pa_decode_f32.cu",
-           "pa_decode_fp8.cu", "pa_decode_d256.cu", "pa_cascade.cu", "pa_static.cu", "pa_diag.cu",
+           "pa_decode_fp8.cu", "pa_decode_d256.cu", "pa_decode_g8.cu", "pa_cascade.cu", "pa_static.cu", "pa_diag.cu",
            "pa_block_manager.cpp"]
 
 

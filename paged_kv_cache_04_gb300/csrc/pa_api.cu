@@ -138,6 +138,10 @@ pa_status dispatch_path(const CUtensorMap& km, const CUtensorMap& vm, const Deco
                         long long items, int mode, cudaStream_t st) {
   // group >= 4 on 16-bit or FP8 data: tensor cores; MHA: vector path with q in registers
   if constexpr (sizeof(DT) <= 2) {
+    // plain decode at groups of 5-8 merges in rounds (kPathMmaG8); split and suffix
+    // mode do not merge inside the CTA and take kPathMma at every group
+    if (p.group > kMergeHeads && mode == kModePlain)
+      return launch_decode<DT, QT, OT, D, kPathMmaG8, kModePlain>(km, vm, p, sms, items, st);
     if (p.group >= 4) return dispatch_mode<DT, QT, OT, D, kPathMma>(km, vm, p, sms, items, mode, st);
   }
   // (head_dim 256: q stays in shared memory; a lane's half of a 256-wide row in registers would spill)
@@ -334,6 +338,31 @@ extern "C" size_t pa_decode_split_workspace_bytes(int num_seqs, int num_heads, i
   return pa::align256(rows * head_dim * 4) + 2 * pa::align256(rows * 4);
 }
 
+namespace pa {
+// Every check of pa_decode_split except those on the workspace itself; *need
+// receives the workspace size (0 when num_seqs == 0).
+pa_status check_split_call(const void* out, const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                           int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                           pa_kv_layout layout, int64_t num_blocks, float scale, pa_dtype dtype, pa_dtype out_dtype,
+                           int max_context_len, int partition_tokens, size_t* need) {
+  DecodeArgs a{const_cast<void*>(out), q,         k_cache,      v_cache,  block_tables, max_blocks_per_seq,
+               context_lens,           num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+               (long long)num_blocks,  scale,     dtype,     out_dtype};
+  a.layout = layout;
+  *need = 0;
+  pa_status s = check_decode(a);
+  if (s != PA_OK) return s;
+  if (max_context_len < 0 || partition_tokens <= 0 || partition_tokens % block_size) return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PA_OK;
+  if (num_seqs > kSplitMaxSeqs) return PA_ERR_UNSUPPORTED;
+  const long long P = std::max(1LL, ((long long)max_context_len + partition_tokens - 1) / partition_tokens);
+  if ((long long)num_seqs * num_kv_heads * P > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+  *need = pa_decode_split_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len, partition_tokens);
+  return *need == 0 ? PA_ERR_INVALID_ARG : PA_OK;
+}
+}  // namespace pa
+
 extern "C" pa_status pa_decode_split(void* out, const void* q, const void* k_cache, const void* v_cache,
                                      const int32_t* block_tables, int max_blocks_per_seq,
                                      const int32_t* context_lens, int num_seqs, int num_heads, int num_kv_heads,
@@ -342,20 +371,17 @@ extern "C" pa_status pa_decode_split(void* out, const void* q, const void* k_cac
                                      int partition_tokens, void* workspace, size_t workspace_bytes,
                                      cudaStream_t stream) {
   using namespace pa;
+  size_t need = 0;
+  pa_status s = check_split_call(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                                 num_heads, num_kv_heads, head_dim, block_size, layout, num_blocks, scale, dtype,
+                                 out_dtype, max_context_len, partition_tokens, &need);
+  if (s != PA_OK || num_seqs == 0) return s;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < need) return PA_ERR_INVALID_ARG;
   DecodeArgs a{out,      q,         k_cache,      v_cache,  block_tables, max_blocks_per_seq,
-                     context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
-                     (long long)num_blocks, scale, dtype, out_dtype};
+               context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+               (long long)num_blocks, scale, dtype, out_dtype};
   a.layout = layout;
-  pa_status s = check_decode(a);
-  if (s != PA_OK) return s;
-  if (max_context_len < 0 || partition_tokens <= 0 || partition_tokens % block_size) return PA_ERR_INVALID_ARG;
-  if (num_seqs == 0) return PA_OK;
-  if (num_seqs > kSplitMaxSeqs) return PA_ERR_UNSUPPORTED;
-  const size_t need =
-      pa_decode_split_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len, partition_tokens);
-  if (!workspace || !aligned16(workspace) || workspace_bytes < need || need == 0) return PA_ERR_INVALID_ARG;
   const long long P = std::max(1LL, ((long long)max_context_len + partition_tokens - 1) / partition_tokens);
-  if ((long long)num_seqs * num_kv_heads * P > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
   return run_decode(a, true, partition_tokens, (int)P, workspace, stream);
 }
 
@@ -487,6 +513,11 @@ extern "C" pa_status pa_get_error(uint32_t* error_bits, cudaStream_t stream) {
   return host ? PA_ERR_OUT_OF_RANGE : PA_OK;
 }
 
+extern "C" pa_status pa_debug_check(cudaStream_t stream) {
+  uint32_t bits = 0;
+  return pa_get_error(&bits, stream);
+}
+
 extern "C" const char* pa_status_string(pa_status status) {
   switch (status) {
     case PA_OK: return "ok";
@@ -499,4 +530,6 @@ extern "C" const char* pa_status_string(pa_status status) {
   return "unknown status";
 }
 
-extern "C" int pa_version(void) { return 100; }
+extern "C" const char* pa_status_str(pa_status status) { return pa_status_string(status); }
+
+extern "C" int pa_version(void) { return 200; }

@@ -55,79 +55,115 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-constexpr int kMaxLayersPerLaunch = 64;
-struct LayerPtrs {
-  uint4* k[kMaxLayersPerLaunch];
-  uint4* v[kMaxLayersPerLaunch];
+constexpr int kMaxLayersPerLaunch = 32;
+// Per-layer pools of one launch: the source and destination of layer l's K and
+// V blocks (the same pools for copy-on-write, two pools for a swap).
+struct MovePtrs {
+  const uint4* src_k[kMaxLayersPerLaunch];
+  const uint4* src_v[kMaxLayersPerLaunch];
+  uint4* dst_k[kMaxLayersPerLaunch];
+  uint4* dst_v[kMaxLayersPerLaunch];
 };
 
-// grid = (pairs, layers, 2): one CTA copies one K or V block of one layer.
+// Whether pair `me` (src, dst) races with another pair of the list: two copies
+// writing one block, or one copy writing a block that another reads. With
+// same_pool (copy-on-write inside one pool, or a swap whose two pools are the
+// same memory) source and destination ids name the same blocks, so a
+// destination may also not be any pair's source (its own included). Pairs with
+// ids outside their pools are skipped by every CTA and race with nothing. All
+// threads of the CTA take part; every thread gets the same answer.
+__device__ __forceinline__ bool pair_races(const int64_t* __restrict__ pairs, int num_pairs, int me, long long src,
+                                           long long dst, long long src_blocks, long long dst_blocks,
+                                           bool same_pool) {
+  bool bad = same_pool && src == dst;
+  for (int q = threadIdx.x; q < num_pairs; q += blockDim.x) {
+    if (q == me) continue;
+    const long long sq = __ldg(pairs + 2 * (long long)q), dq = __ldg(pairs + 2 * (long long)q + 1);
+    if (sq < 0 || sq >= src_blocks || dq < 0 || dq >= dst_blocks) continue;
+    bad |= dq == dst;
+    if (same_pool) bad |= (sq == dst) | (dq == src);
+  }
+  return __syncthreads_or(bad) != 0;
+}
+
+// grid = (pairs, layer chunks, 2): one CTA moves the K (z = 0) or V (z = 1) block
+// of one pair for layers [y * layers_per_cta, ...) of the launch, from the source
+// pool to the destination pool (either may be pinned host memory, reached
+// directly through the unified address space). Every CTA first checks its pair
+// against the whole list, so a racing pair is skipped in all of its CTAs. The
+// first chunk's loads go out before that check (reading a racing pair's source
+// is harmless; only its stores are skipped), so the check's latency hides behind
+// them.
 template <int VPT>
 __global__ void __launch_bounds__(256)
-    copy_blocks_kernel(const LayerPtrs ptrs, const int64_t* __restrict__ pairs, long long num_blocks,
-                       int vpb, unsigned* err) {
+    move_blocks_kernel(const MovePtrs ptrs, const int64_t* __restrict__ pairs, int num_pairs, long long src_blocks,
+                       long long dst_blocks, int vpb, int num_layers, int layers_per_cta, int same_pool,
+                       unsigned* err) {
   pdl_begin();
-  const long long src = __ldg(pairs + 2 * (long long)blockIdx.x);
-  const long long dst = __ldg(pairs + 2 * (long long)blockIdx.x + 1);
-  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
-    if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) atomicOr(err, kErrPair);
+  const int me = blockIdx.x;
+  const long long src = __ldg(pairs + 2 * (long long)me);
+  const long long dst = __ldg(pairs + 2 * (long long)me + 1);
+  const bool first = threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
+  if (src < 0 || src >= src_blocks || dst < 0 || dst >= dst_blocks) {
+    if (first) atomicOr(err, kErrPair);
     return;
   }
-  uint4* base = blockIdx.z ? ptrs.v[blockIdx.y] : ptrs.k[blockIdx.y];
-  const uint4* s = base + src * vpb;
-  uint4* d = base + dst * vpb;
-  for (int i0 = threadIdx.x; i0 < vpb; i0 += 256 * VPT) {
-    uint4 r[VPT];
+  const int l0 = blockIdx.y * layers_per_cta, l1 = min(num_layers, l0 + layers_per_cta);
+  uint4 r[VPT];
+  auto load = [&](int l, int i0) {
+    const uint4* s = (blockIdx.z ? ptrs.src_v[l] : ptrs.src_k[l]) + src * vpb;
 #pragma unroll
     for (int u = 0; u < VPT; ++u) {
       const int i = i0 + u * 256;
       if (i < vpb) r[u] = __ldcs(s + i);
     }
+  };
+  auto store = [&](int l, int i0) {
+    uint4* d = (blockIdx.z ? ptrs.dst_v[l] : ptrs.dst_k[l]) + dst * vpb;
 #pragma unroll
     for (int u = 0; u < VPT; ++u) {
       const int i = i0 + u * 256;
       if (i < vpb) __stcs(d + i, r[u]);
+    }
+  };
+  load(l0, threadIdx.x);
+  if (pair_races(pairs, num_pairs, me, src, dst, src_blocks, dst_blocks, same_pool != 0)) {
+    if (first) atomicOr(err, kErrPairAlias);
+    return;
+  }
+  for (int l = l0; l < l1; ++l) {
+    for (int i0 = threadIdx.x; i0 < vpb; i0 += 256 * VPT) {
+      if (l != l0 || i0 != (int)threadIdx.x) load(l, i0);
+      store(l, i0);
     }
   }
 }
 
-constexpr int kMaxSwapLayers = 32;
-struct SwapPtrs {
-  const uint4* src_k[kMaxSwapLayers];
-  const uint4* src_v[kMaxSwapLayers];
-  uint4* dst_k[kMaxSwapLayers];
-  uint4* dst_v[kMaxSwapLayers];
-};
-
-// grid = (pairs, layers, 2): one CTA moves one K or V block of one layer from
-// the source pool to the destination pool (either may be pinned host memory,
-// reached directly through the unified address space).
-template <int VPT>
-__global__ void __launch_bounds__(256)
-    swap_blocks_kernel(const SwapPtrs ptrs, const int64_t* __restrict__ pairs, long long src_blocks,
-                       long long dst_blocks, int vpb, unsigned* err) {
-  pdl_begin();
-  const long long src = __ldg(pairs + 2 * (long long)blockIdx.x);
-  const long long dst = __ldg(pairs + 2 * (long long)blockIdx.x + 1);
-  if (src < 0 || src >= src_blocks || dst < 0 || dst >= dst_blocks) {
-    if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) atomicOr(err, kErrPair);
-    return;
-  }
-  const uint4* s = (blockIdx.z ? ptrs.src_v[blockIdx.y] : ptrs.src_k[blockIdx.y]) + src * vpb;
-  uint4* d = (blockIdx.z ? ptrs.dst_v[blockIdx.y] : ptrs.dst_k[blockIdx.y]) + dst * vpb;
-  for (int i0 = threadIdx.x; i0 < vpb; i0 += 256 * VPT) {
-    uint4 r[VPT];
-#pragma unroll
-    for (int u = 0; u < VPT; ++u) {
-      const int i = i0 + u * 256;
-      if (i < vpb) r[u] = __ldcs(s + i);
+// Launch the moves of `num_layers` layers in chunks of kMaxLayersPerLaunch. Each
+// CTA takes several layers of its pair when there are many CTAs, so that the
+// per-CTA pair check is paid once for many blocks (about two waves of eight
+// CTAs per SM).
+template <typename SK, typename SV, typename DK, typename DV>
+pa_status launch_moves(SK src_k, SV src_v, DK dst_k, DV dst_v, int num_layers, const int64_t* pairs,
+                       int num_pairs, long long src_blocks, long long dst_blocks, int vpb, bool same_pool, int sms,
+                       unsigned* err, cudaStream_t stream) {
+  for (int b = 0; b < num_layers; b += kMaxLayersPerLaunch) {
+    const int nl = std::min(kMaxLayersPerLaunch, num_layers - b);
+    MovePtrs ptrs;
+    for (int i = 0; i < kMaxLayersPerLaunch; ++i) {
+      ptrs.src_k[i] = i < nl ? static_cast<const uint4*>(src_k[b + i]) : nullptr;
+      ptrs.src_v[i] = i < nl ? static_cast<const uint4*>(src_v[b + i]) : nullptr;
+      ptrs.dst_k[i] = i < nl ? static_cast<uint4*>(dst_k[b + i]) : nullptr;
+      ptrs.dst_v[i] = i < nl ? static_cast<uint4*>(dst_v[b + i]) : nullptr;
     }
-#pragma unroll
-    for (int u = 0; u < VPT; ++u) {
-      const int i = i0 + u * 256;
-      if (i < vpb) __stcs(d + i, r[u]);
-    }
+    const long long all = (long long)num_pairs * nl * 2, target = (long long)sms * 16;
+    const int lpc = (int)std::max(1LL, std::min<long long>(nl, all / std::max(1LL, target)));
+    dim3 grid((unsigned)num_pairs, (unsigned)((nl + lpc - 1) / lpc), 2);
+    if (launch_pdl(move_blocks_kernel<8>, grid, dim3(256), 0, stream, ptrs, pairs, num_pairs, src_blocks,
+                   dst_blocks, vpb, nl, lpc, same_pool ? 1 : 0, err) != cudaSuccess)
+      return PA_ERR_CUDA;
   }
+  return PA_OK;
 }
 
 int esize(pa_dtype dt) { return dt == PA_F32 ? 4 : (dt == PA_FP8_E4M3 ? 1 : 2); }
@@ -230,19 +266,8 @@ extern "C" pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches
   pa_status st = device_state(&err, &sms);
   if (st != PA_OK) return st;
   const int vpb = (int)(block_bytes / 16);
-  for (int l0 = 0; l0 < num_layers; l0 += kMaxLayersPerLaunch) {
-    const int nl = std::min(kMaxLayersPerLaunch, num_layers - l0);
-    LayerPtrs ptrs;
-    for (int i = 0; i < kMaxLayersPerLaunch; ++i) {
-      ptrs.k[i] = i < nl ? static_cast<uint4*>(k_caches[l0 + i]) : nullptr;
-      ptrs.v[i] = i < nl ? static_cast<uint4*>(v_caches[l0 + i]) : nullptr;
-    }
-    dim3 grid((unsigned)num_pairs, (unsigned)nl, 2);
-    if (launch_pdl(copy_blocks_kernel<8>, grid, dim3(256), 0, stream, ptrs, block_pairs, (long long)num_blocks, vpb,
-                   err) != cudaSuccess)
-      return PA_ERR_CUDA;
-  }
-  return PA_OK;
+  return launch_moves(k_caches, v_caches, k_caches, v_caches, num_layers, block_pairs, num_pairs,
+                      (long long)num_blocks, (long long)num_blocks, vpb, true, sms, err, stream);
 }
 
 extern "C" pa_status pa_swap_blocks(void* const* dst_k_caches, void* const* dst_v_caches,
@@ -270,21 +295,12 @@ extern "C" pa_status pa_swap_blocks(void* const* dst_k_caches, void* const* dst_
   pa_status st = device_state(&err, &sms);
   if (st != PA_OK) return st;
   const int vpb = (int)(block_bytes / 16);
-  for (int l0 = 0; l0 < num_layers; l0 += kMaxSwapLayers) {
-    const int nl = std::min(kMaxSwapLayers, num_layers - l0);
-    SwapPtrs ptrs;
-    for (int i = 0; i < kMaxSwapLayers; ++i) {
-      ptrs.src_k[i] = i < nl ? static_cast<const uint4*>(src_k_caches[l0 + i]) : nullptr;
-      ptrs.src_v[i] = i < nl ? static_cast<const uint4*>(src_v_caches[l0 + i]) : nullptr;
-      ptrs.dst_k[i] = i < nl ? static_cast<uint4*>(dst_k_caches[l0 + i]) : nullptr;
-      ptrs.dst_v[i] = i < nl ? static_cast<uint4*>(dst_v_caches[l0 + i]) : nullptr;
-    }
-    dim3 grid((unsigned)num_pairs, (unsigned)nl, 2);
-    if (launch_pdl(swap_blocks_kernel<8>, grid, dim3(256), 0, stream, ptrs, block_pairs, (long long)src_num_blocks,
-                   (long long)dst_num_blocks, vpb, err) != cudaSuccess)
-      return PA_ERR_CUDA;
-  }
-  return PA_OK;
+  // ids name blocks of one id space only where a source and a destination pool are the same memory
+  bool same_pool = false;
+  for (int l = 0; l < num_layers; ++l)
+    same_pool |= dst_k_caches[l] == src_k_caches[l] || dst_v_caches[l] == src_v_caches[l];
+  return launch_moves(src_k_caches, src_v_caches, dst_k_caches, dst_v_caches, num_layers, block_pairs, num_pairs,
+                      (long long)src_num_blocks, (long long)dst_num_blocks, vpb, same_pool, sms, err, stream);
 }
 
 extern "C" pa_status pa_reshape_and_cache_fp8(const void* key, const void* value, void* k_cache, void* v_cache,

@@ -87,6 +87,18 @@ constexpr int kJobTokens = 16;        // tokens per TMA job
 constexpr int kPathVec = 0;     // lanes split head_dim, FFMA; any group, q staged in shared memory
 constexpr int kPathVecMha = 1;  // the same for group 1 (MHA), q held in registers
 constexpr int kPathMma = 2;     // group >= 4 on 16-bit data: mma.sync m16n8k16
+constexpr int kPathMmaG8 = 3;   // the same for groups of 5-8 in plain mode, merging heads in rounds
+__host__ __device__ constexpr bool is_mma_path(int path) { return path == kPathMma || path == kPathMmaG8; }
+
+// Plain mode merges the warps' fp32 partial outputs of an item through shared
+// memory. kPathMmaG8 merges at most kMergeHeads heads per round (a group of 8 in
+// two rounds), so its merge area stays W x 4 x head_dim floats: at group 8 the
+// whole-group area (16 KiB at head_dim 128) would leave room for one CTA per SM
+// instead of two. The other paths merge their whole group in one round.
+constexpr int kMergeHeads = 4;
+__host__ __device__ inline int merge_heads(int group, int path) {
+  return path == kPathMmaG8 && group > kMergeHeads ? kMergeHeads : group;
+}
 
 // What a launch writes.
 constexpr int kModePlain = 0;   // the attention output
@@ -157,12 +169,12 @@ __host__ __device__ inline SmemLayout make_layout(int W, int R, int D, int esize
   L.ok_off = off;
   off = round_up(off + W * R, 16);
   L.merge_off = off;
-  if (!split) off += W * group * D * 4 + W * kMaxGroup * 2 * 4;
+  if (!split) off += W * merge_heads(group, path) * D * 4 + W * kMaxGroup * 2 * 4;
   L.q_off = off;
   if (path == kPathVec) off += W * group * D * 4;            // fp32 q rows per warp
   if (path == kPathVecMha) off += round_up(W * 2 * D * qsize, 16);  // double-buffered raw q row per warp
   L.wts_off = off;
-  if (path != kPathMma) off += W * kJobTokens * 4;             // vector paths: one job's weights per warp
+  if (!is_mma_path(path)) off += W * kJobTokens * 4;          // vector paths: one job's weights per warp
   L.sched_off = off;
   if (split)
     off += (S + 1) * 4;
@@ -190,7 +202,7 @@ struct StageCfg {
   // tensor-core kernels fit 3 CTAs per SM by shared memory; saying so gives them
   // the registers of that occupancy (left alone, the compiler settles for 128
   // registers and spills in split mode). head_dim 256 runs two CTAs per SM.
-  static constexpr int MINB = E == 1 && PATH == kPathMma ? 3 : (D > 128 ? 2 : 0);
+  static constexpr int MINB = E == 1 && is_mma_path(PATH) ? 3 : (D > 128 ? 2 : 0);
 };
 
 struct Item {
@@ -301,7 +313,9 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
                         const DecodeParams p) {
   pdl_begin();
   using Cfg = StageCfg<DT, D, PATH>;
-  constexpr bool MMA = PATH == kPathMma;
+  constexpr bool MMA = is_mma_path(PATH);
+  constexpr bool ROUNDS = PATH == kPathMmaG8;  // plain mode, groups of 5-8: merge four heads per round
+  static_assert(!ROUNDS || MODE == kModePlain, "only plain mode merges inside the CTA");
   constexpr bool SPLIT = MODE == kModeSplit;
   constexpr bool SUFFIX = MODE == kModeSuffix;
   constexpr bool F8 = std::is_same<DT, fp8e4m3>::value;
@@ -313,7 +327,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
   // right after q K^T, its V tile after P V (two barriers per stage). Measured
   // +2.7% on the Llama batch; the same split in split mode, in the suffix pass
   // and on the MHA vector path was 2-4% slower, so those refill whole stages.
-  constexpr bool KV_SPLIT = PATH == kPathMma && !F8 && MODE == kModePlain;
+  constexpr bool KV_SPLIT = MMA && !F8 && MODE == kModePlain;
   // The 16-bit tensor-core paths land K and V on separate barriers in every
   // mode (split decode measured +2% with it); E4M3 (two jobs per step) and the
   // vector paths keep one barrier for both (two measured 1.5-2.5% slower on
@@ -336,8 +350,9 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
   const SmemLayout L = make_layout(W, R, D, E, (int)sizeof(QT), p.group, PATH, SPLIT, p.S);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars_off);
   volatile uint8_t* stage_ok = smem + L.ok_off;                        // [W][R]
-  float* mrg_o = reinterpret_cast<float*>(smem + L.merge_off);        // [W][group][D] (plain mode)
-  float* mrg_ml = mrg_o + W * p.group * D;                             // [W][kMaxGroup][2]
+  const int MH = merge_heads(p.group, PATH);                           // heads per merge round
+  float* mrg_o = reinterpret_cast<float*>(smem + L.merge_off);        // [W][MH][D] (plain mode)
+  float* mrg_ml = mrg_o + W * MH * D;                                  // [W][kMaxGroup][2]
   float* qs_all = reinterpret_cast<float*>(smem + L.q_off);            // [W][group][D] (vector path)
   uint8_t* qraw_all = smem + L.q_off;                                  // [W][2][D] raw (MHA path)
   float* wts_all = reinterpret_cast<float*>(smem + L.wts_off);         // [W][JT] (vector paths)
@@ -641,12 +656,14 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
       cursor_settle(ic);
     }
   };
-  // Plain mode: merge the W warps' partials of the current item and write it.
-  auto merge_and_write = [&](const Item& x) {
+  // Plain mode: merge the W warps' partials of heads h0 .. h0 + MH - 1 of the
+  // current item (at mrg_o[w][h - h0]) and write them.
+  auto merge_and_write = [&](const Item& x, int h0) {
     asm volatile("bar.sync 1, %0;" ::"n"(W * 32) : "memory");
     const int hq0 = x.kv * p.group;
-    for (int idx = tid; idx < p.group * D; idx += nthreads) {
-      const int h = idx / D, i = idx - h * D;
+    const int nh = min(MH, p.group - h0);
+    for (int idx = tid; idx < nh * D; idx += nthreads) {
+      const int hh = idx / D, i = idx - hh * D, h = h0 + hh;
       float M = NEG_INF;
 #pragma unroll
       for (int w = 0; w < W; ++w) {
@@ -659,7 +676,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
         if (l > 0.f) {
           const float f = exp2f(mrg_ml[(w * kMaxGroup + h) * 2 + 0] - M);
           Lsum = fmaf(l, f, Lsum);
-          O = fmaf(mrg_o[(w * p.group + h) * D + i], f, O);
+          O = fmaf(mrg_o[(w * MH + hh) * D + i], f, O);
         }
       }
       reinterpret_cast<OT*>(p.out)[((long long)x.s * p.H + hq0 + h) * D + i] =
@@ -981,21 +998,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
           }
         }
       } else {
-        float* mo = mrg_o + warp * p.group * D;
-        if (hA < p.group) {
-#pragma unroll
-          for (int mt = 0; mt < D / 16; ++mt) {
-            mo[hA * D + drow(mt, g)] = o[mt][0];
-            mo[hA * D + drow(mt, g + 8)] = o[mt][2];
-          }
-        }
-        if (hB < p.group) {
-#pragma unroll
-          for (int mt = 0; mt < D / 16; ++mt) {
-            mo[hB * D + drow(mt, g)] = o[mt][1];
-            mo[hB * D + drow(mt, g + 8)] = o[mt][3];
-          }
-        }
+        float* mo = mrg_o + warp * MH * D;
         if (g == 0) {
           float* ml = mrg_ml + warp * kMaxGroup * 2;
           ml[hA * 2 + 0] = m0;
@@ -1003,7 +1006,33 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
           ml[hB * 2 + 0] = m1;
           ml[hB * 2 + 1] = l1;
         }
-        merge_and_write(it);
+        // Heads [h0, h0 + MH) of this lane's pair (hA, hB) go to the merge area,
+        // then the CTA merges them. One round at groups of up to four; kPathMmaG8
+        // takes two rounds of four heads, lanes t4 = 0, 1 in the first and
+        // t4 = 2, 3 in the second.
+        auto stage_heads = [&](int h0) {
+          if (hA >= h0 && hA < h0 + MH && hA < p.group) {
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+              mo[(hA - h0) * D + drow(mt, g)] = o[mt][0];
+              mo[(hA - h0) * D + drow(mt, g + 8)] = o[mt][2];
+            }
+          }
+          if (hB >= h0 && hB < h0 + MH && hB < p.group) {
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+              mo[(hB - h0) * D + drow(mt, g)] = o[mt][1];
+              mo[(hB - h0) * D + drow(mt, g + 8)] = o[mt][3];
+            }
+          }
+          merge_and_write(it, h0);
+        };
+        if constexpr (ROUNDS) {
+          stage_heads(0);
+          stage_heads(kMergeHeads);
+        } else {
+          stage_heads(0);
+        }
       }
       have = have_next;
       it = nx;
@@ -1240,7 +1269,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
         }
         job_done();
       }
-      float* mo = mrg_o + warp * p.group * D;
+      float* mo = mrg_o + warp * MH * D;  // vector paths: MH = group, one merge round
       float* ml = mrg_ml + warp * kMaxGroup * 2;
 #pragma unroll
       for (int h = 0; h < GM; ++h) {
@@ -1268,7 +1297,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
           }
         }
       }
-      if (!WARP_PARTS) merge_and_write(it);
+      if (!WARP_PARTS) merge_and_write(it, 0);
     }
     if constexpr (MHA) cp_async_wait_all();
   }

@@ -22,6 +22,7 @@ enum : unsigned {
   kErrContext = 4u,    // a context length < 0 or longer than the table / workspace allows
   kErrPair = 8u,       // a copy pair outside [0, num_blocks)
   kErrTimeout = 16u,   // a wait on an mbarrier ran past its time limit
+  kErrPairAlias = 32u, // a copy / swap pair that races with another pair of the list
 };
 
 // A wait that should finish in microseconds gives up after this long.

@@ -10,6 +10,14 @@ namespace pa {
 
 struct DecodeParams;
 
+// Every argument check of pa_decode_split except those on the workspace itself
+// (pa_api.cu); *need receives the workspace size (0 for an empty batch).
+pa_status check_split_call(const void* out, const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                           int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                           pa_kv_layout layout, int64_t num_blocks, float scale, pa_dtype dtype, pa_dtype out_dtype,
+                           int max_context_len, int partition_tokens, size_t* need);
+
 // Per-device state, set up on the first call on a device: the device address
 // of the error word and the SM count. Returns PA_ERR_CUDA if CUDA fails.
 pa_status device_state(unsigned** err, int* num_sms);

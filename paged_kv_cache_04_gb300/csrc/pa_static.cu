@@ -9,6 +9,7 @@
 #include <mutex>
 
 #include "pa.h"
+#include "pa_internal.h"
 
 namespace {
 
@@ -37,19 +38,22 @@ pa_status scratch_address(void** out) {
 
 }  // namespace
 
+extern "C" size_t pa_static_scratch_bytes(void) { return (size_t)PA_STATIC_SCRATCH_BYTES; }
+
 extern "C" pa_status pa_decode_split_static(void* out, const void* q, const void* k_cache, const void* v_cache,
                                             const int32_t* block_tables, int max_blocks_per_seq,
                                             const int32_t* context_lens, int num_seqs, int num_heads,
                                             int num_kv_heads, int head_dim, int block_size, pa_kv_layout layout,
                                             int64_t num_blocks, float scale, pa_dtype dtype, pa_dtype out_dtype, int max_context_len,
                                             int partition_tokens, cudaStream_t stream) {
-  if (num_seqs == 0)  // nothing to compute: the regular entry point checks the rest and returns
-    return pa_decode_split(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
-                           num_heads, num_kv_heads, head_dim, block_size, layout, num_blocks, scale, dtype,
-                           out_dtype, max_context_len, partition_tokens, nullptr, 0, stream);
-  const size_t need =
-      pa_decode_split_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len, partition_tokens);
-  if (need == 0) return PA_ERR_INVALID_ARG;
+  // The same argument checks as pa_decode_split, in the same order, so that a bad
+  // call gets the same status from both; the size limit comes after them.
+  size_t need = 0;
+  const pa_status chk = pa::check_split_call(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                                             num_seqs, num_heads, num_kv_heads, head_dim, block_size, layout,
+                                             num_blocks, scale, dtype, out_dtype, max_context_len, partition_tokens,
+                                             &need);
+  if (chk != PA_OK || num_seqs == 0) return chk;
   if (need > (size_t)PA_STATIC_SCRATCH_BYTES) return PA_ERR_UNSUPPORTED;
   void* scratch = nullptr;
   const pa_status s = scratch_address(&scratch);

@@ -220,6 +220,16 @@ def llama8b(device="cpu", S=256, num_blocks=100_000, new_token=True, rotate=0) -
                                  device, new_token=new_token, rotate=rotate)
 
 
+def llama70b_short(device="cpu", S=256, num_blocks=100_000, new_token=True) -> Workload:
+    """Plain decode at a GQA group of 8: the Llama-3.1-70B head layout (64 q / 8 kv
+    heads, d 128, bf16, block 16) on the Llama-3.1-8B batch's lengths
+    (U[512, 4096], 256 sequences) over a 100k-block shuffled pool. The KV bytes
+    per token equal the 8B batch's (the same 8 kv heads); twice the query rows."""
+    ctx = uniform_lengths(S, 512, 4096, _gen(SEED_CTX)).tolist()
+    return batch_with_new_tokens("llama70b_short", S, 64, 8, 128, 16, torch.bfloat16, ctx, num_blocks,
+                                 device, new_token=new_token)
+
+
 def gemma_d256(device="cpu", S=256, num_blocks=50_000, new_token=True) -> Workload:
     """head_dim 256 with a group of 2 (16 q / 8 kv heads, the Gemma-2-9B layer
     shape), bf16, block 16: the Llama-3.1-8B batch's lengths (U[512, 4096]) and a
@@ -337,6 +347,7 @@ def to_nhd(wl: Workload) -> Workload:
 
 def by_name(name: str, device="cpu", **kw) -> Workload:
     table = {"tiny": tiny, "opt13b": opt13b, "llama8b": llama8b, "long70b": long70b, "gemma_d256": gemma_d256,
+             "llama70b_short": llama70b_short,
              "shared": shared_prefix,
              "shared_cow": lambda device="cpu", **k: shared_prefix(device, cow=True, **k)}
     return table[name](device=device, **kw)

@@ -107,3 +107,58 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(pa, "library_path", str(tmp_path / "missing.so"))
     with pytest.raises(pa.PAError):
         pa.library()
+
+
+def test_survey_boundary_names(lib_path):
+    """The boundary's names for the status string and the error-word check:
+    pa_status_str is pa_status_string under another name; pa_debug_check is
+    declared and exported."""
+    import paged_kv_cache_04_gb300 as pa
+    lib = pa.library()
+    names = declared_functions()
+    assert "pa_status_str" in names and "pa_debug_check" in names
+    for st in range(-1, 7):
+        assert lib.pa_status_str(st) == lib.pa_status_string(st)
+    assert pa.pa_status_str(0) == "ok"
+
+
+def test_static_scratch_size_matches_header(lib_path):
+    """The binding reads the scratch size from the library; the header's macro agrees."""
+    import paged_kv_cache_04_gb300 as pa
+    text = open(os.path.join(ROOT, "include", "pa.h")).read()
+    m = re.search(r"#define\s+PA_STATIC_SCRATCH_BYTES\s+\((\d+)u\s*\*\s*(\d+)u\s*\*\s*(\d+)u\)", text)
+    assert m, "macro not found"
+    macro = int(m.group(1)) * int(m.group(2)) * int(m.group(3))
+    assert pa.PA_STATIC_SCRATCH_BYTES == macro == int(pa.library().pa_static_scratch_bytes())
+
+
+def test_static_split_rejects_bad_arguments_like_the_workspace_call(lib_path):
+    """pa_decode_split_static runs pa_decode_split's argument checks first, so a
+    bad call gets the same status from both, even when it is also too large for
+    the scratch array (these calls return before any CUDA call)."""
+    import paged_kv_cache_04_gb300 as pa
+    lib = pa.library()
+    null = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(1 << 20)  # aligned, never dereferenced: the calls fail on the host
+    huge = 1 << 20  # max_context_len far beyond the scratch array
+    cases = [
+        # null q/out with sequences
+        (null, null, 8, 64, 8, 128, 16, huge, 512),
+        # partition not a multiple of the block size
+        (fake, fake, 8, 64, 8, 128, 16, huge, 500),
+        # more sequences than split mode takes
+        (fake, fake, 4096, 64, 8, 128, 16, huge, 512),
+        # unsupported head_dim
+        (fake, fake, 8, 64, 8, 96, 16, huge, 512),
+        # negative max_context_len
+        (fake, fake, 8, 64, 8, 128, 16, -1, 512),
+    ]
+    for out, q, S, H, G, d, B, mctx, T in cases:
+        a = lib.pa_decode_split(out, q, fake, fake, fake, 64, fake, S, H, G, d, B, 0, 1000, 1.0, 2, 2, mctx, T,
+                                fake, 1 << 40, null)
+        b = lib.pa_decode_split_static(out, q, fake, fake, fake, 64, fake, S, H, G, d, B, 0, 1000, 1.0, 2, 2,
+                                       mctx, T, null)
+        assert a == b != 0, (S, d, mctx, T, a, b)
+    # a valid call that is only too large: UNSUPPORTED from the static call alone
+    assert lib.pa_decode_split_static(fake, fake, fake, fake, fake, 1 << 16, fake, 8, 64, 8, 128, 16, 0, 1 << 20,
+                                      1.0, 2, 2, huge, 512, null) == 2

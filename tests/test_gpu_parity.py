@@ -86,6 +86,22 @@ def test_llama8b_full_size_sampled(pa, cuda_device):
     _no_device_errors(pa)
 
 
+def test_llama70b_short_full_size_sampled(pa, cuda_device):
+    """Plain decode at group 8 (64 q / 8 kv heads) on the benchmark's lengths and
+    pool, sampled sequences checked, with bf16 and fp32 output."""
+    wl = workloads.llama70b_short(device=cuda_device)
+    seqs = H.sample_seqs(wl, 12)
+    P = H.Pristine(wl, seqs)
+    out = H.gpu_step(pa, wl)
+    ref = P.decode()
+    H.check_close(out[seqs], ref, torch.bfloat16, "llama70b_short full")
+    o32 = torch.empty(wl.q.shape, dtype=torch.float32, device=cuda_device)
+    pa.pa_decode(o32, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale)
+    H.check_close(o32[seqs], ref, torch.float32, "llama70b_short full, fp32 out")
+    assert torch.equal(out, o32.to(torch.bfloat16)), "bf16 output must be the RNE of the fp32 output"
+    _no_device_errors(pa)
+
+
 def test_llama8b_full_size_cache_write_bit_exact(pa, cuda_device):
     wl = workloads.llama8b(device=cuda_device)
     k0, v0 = wl.k_cache.clone(), wl.v_cache.clone()
@@ -212,6 +228,9 @@ SHAPES = [
     (8, 8, 128, 16, torch.float16), (8, 4, 64, 32, torch.float16), (12, 4, 128, 16, torch.float16),
     (16, 4, 128, 16, torch.bfloat16), (32, 4, 64, 16, torch.bfloat16), (16, 2, 128, 32, torch.bfloat16),
     (40, 5, 128, 16, torch.bfloat16), (64, 8, 128, 32, torch.bfloat16), (6, 2, 64, 32, torch.bfloat16),
+    # groups of 5-7 and group 8 at head_dim 64: plain decode merges them in two rounds of four heads
+    (20, 4, 64, 16, torch.float16), (24, 4, 128, 32, torch.bfloat16), (28, 4, 128, 16, torch.float16),
+    (16, 2, 64, 32, torch.bfloat16),
 ]
 
 

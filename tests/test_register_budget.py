@@ -18,7 +18,7 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 CSRC = os.path.join(ROOT, "paged_kv_cache_04_gb300", "csrc")
-UNITS = ["pa_decode_bf16.cu", "pa_decode_f16.cu", "pa_decode_fp8.cu"]
+UNITS = ["pa_decode_bf16.cu", "pa_decode_f16.cu", "pa_decode_fp8.cu", "pa_decode_g8.cu"]
 THREADS = 128
 SM_REGS = 65536
 
@@ -63,14 +63,14 @@ def kernels(tmp_path_factory):
     return found
 
 
-PATH_MHA, PATH_MMA = 1, 2
+PATH_MHA, PATH_MMA, PATH_MMA_G8 = 1, 2, 3
 
 
 def expected_ctas(dt, D, path):
     """CTAs per SM that shared memory allows the measured head_dim-128 kernels."""
     if D != 128:
         return None
-    if path == PATH_MMA:
+    if path in (PATH_MMA, PATH_MMA_G8):
         return 3 if "fp8" in dt else 2
     if path == PATH_MHA and dt != "float":
         return 3
@@ -80,7 +80,8 @@ def expected_ctas(dt, D, path):
 def test_the_measured_kernels_were_found(kernels):
     keys = {(k[0], k[3], k[4], k[5]) for k in kernels}
     for want in [("__nv_bfloat16", 128, PATH_MMA, 0), ("__nv_bfloat16", 128, PATH_MMA, 1),
-                 ("__half", 128, PATH_MHA, 0), ("pa::fp8e4m3", 128, PATH_MMA, 0), ("pa::fp8e4m3", 128, PATH_MMA, 1)]:
+                 ("__half", 128, PATH_MHA, 0), ("pa::fp8e4m3", 128, PATH_MMA, 0), ("pa::fp8e4m3", 128, PATH_MMA, 1),
+                 ("__nv_bfloat16", 128, PATH_MMA_G8, 0), ("pa::fp8e4m3", 128, PATH_MMA_G8, 0)]:
         assert want in keys, (want, sorted(keys)[:8])
 
 

@@ -37,6 +37,11 @@ int main() {
         row<__nv_bfloat16, __nv_bfloat16, 128, kPathMma>("mma16_d128", g, sp, S);
         row<fp8e4m3, __nv_bfloat16, 128, kPathMma>("fp8_d128", g, sp, S);
         row<__nv_bfloat16, __nv_bfloat16, 256, kPathMma>("mma16_d256", g, sp, S);
+        if (!sp) {  // plain decode at groups of 5-8: merged four heads per round
+          row<__nv_bfloat16, __nv_bfloat16, 128, kPathMmaG8>("mma16g8_d128", g, sp, S);
+          row<fp8e4m3, __nv_bfloat16, 128, kPathMmaG8>("fp8g8_d128", g, sp, S);
+          row<__nv_bfloat16, __nv_bfloat16, 256, kPathMmaG8>("mma16g8_d256", g, sp, S);
+        }
         row<__half, __half, 128, kPathVecMha>("mha_d128", 1, sp, S);
         row<__nv_bfloat16, __nv_bfloat16, 256, kPathVec>("vec_d256", 2, sp, S);
       }
@@ -84,6 +89,10 @@ HOLDS = [
     (("mha_d128", 1, 0, 2048), 3),    # OPT-13B-shaped MHA
     (("mha_d128", 1, 1, 256), 3),
     (("mma16_d256", 4, 0, 2048), 2),  # head_dim 256: one stage per warp, two CTAs
+    (("mma16g8_d128", 8, 0, 256), 2),  # plain decode at group 8 (64 q / 8 kv heads): merge rounds
+    (("mma16g8_d128", 8, 0, 2048), 2),
+    (("fp8g8_d128", 8, 0, 256), 3),    # E4M3 plain decode at group 8
+    (("mma16g8_d256", 8, 0, 2048), 2),
     (("vec_d256", 2, 0, 2048), 2),
     (("tc_d128_m64", 512, 0, 0), 2),   # tcgen05 prefix pass, 33-64 rows per group
     (("tc_d128_m128", 2048, 0, 0), 2),  # 65-128 rows per group
@@ -91,14 +100,11 @@ HOLDS = [
 ]
 
 # Known cliffs, kept as strict expected failures so that a fix shows up here:
-# the fp32 merge area (warps x group x head_dim x 4 bytes) doubles at group 8;
 # the sort order (2 bytes per sequence) pushes E4M3 plain decode over the
 # three-CTA budget above about 750 sequences; the split schedule (4 bytes per
 # sequence) does the same to MHA split decode above about 1,900; the tcgen05
 # prefix pass's group scan costs its M = 64 form a CTA above about 2,000 groups.
 GAPS = [
-    (("mma16_d128", 8, 0, 256), 2),
-    (("fp8_d128", 8, 0, 256), 3),
     (("fp8_d128", 4, 0, 2048), 3),
     (("mha_d128", 1, 1, 2048), 3),
     (("tc_d128_m64", 2048, 0, 0), 2),  # the group scan (4 bytes per group) above about 2,000 groups

@@ -64,3 +64,24 @@ def test_static_scratch_rejects_oversize_requests(pa, cuda_device):
     assert e.value.status == 2  # PA_ERR_UNSUPPORTED, and nothing was launched:
     torch.cuda.synchronize()
     assert bool((out == 7.0).all())
+
+
+def test_static_call_allocates_no_device_memory(pa, cuda_device):
+    """After a first call (which may load the library's device code and commit
+    the array), a further call changes neither torch's allocator count nor the
+    device's free memory."""
+    T = 512
+    wl = workloads.long70b(device=cuda_device, S=4, lo=9000, hi=20000, new_token=False)
+    out = torch.empty(wl.q.shape, dtype=torch.float32, device=cuda_device)
+    args = (out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale, wl.max_context, T)
+    pa.pa_decode_split_static(*args)
+    torch.cuda.synchronize()
+    ref = out.clone()
+    alloc0 = torch.cuda.memory_allocated(cuda_device)
+    free0, _ = torch.cuda.mem_get_info(cuda_device)
+    pa.pa_decode_split_static(*args)
+    torch.cuda.synchronize()
+    assert torch.cuda.memory_allocated(cuda_device) == alloc0
+    free1, _ = torch.cuda.mem_get_info(cuda_device)
+    assert free1 == free0, (free0, free1)
+    assert torch.equal(out, ref)  # the same inputs give the same bits
