@@ -11,7 +11,14 @@ Prints one JSON line. ``value`` is the algorithmic HBM throughput of the step
 (K/V bytes of every attended token + q + out + the new rows written) over the
 device time; ``e2e`` is the same metric through the public Python API with the
 step's host inputs copied in from pinned memory and the output copied back
-inside the timed region.
+inside the timed region (overlapped with the neighbouring steps as a serving
+loop would, and ``e2e.serial`` with nothing overlapped). At one GPU the line
+also carries ``workloads``: each other configuration (tiny, OPT-13B MHA, the
+Llama batch over E4M3 codes, 70B-shaped GQA-8 on short contexts, the
+shared-prefix batches with plain and cascade decode, the 32K-128K contexts at
+block 16 and 32, the copy-on-write copies) device-timed on its own, with its
+attention call's roofline, clocks and a bounded oracle sample. ``--headline-only``
+skips them.
 
 ``--impl reference`` times the CPU oracle (the only reference this method has)
 on bounded samples of the same workload.
@@ -38,7 +45,6 @@ sys.path.insert(0, ROOT)
 METRIC = "paged decode attention KV GB/s (% of GB300 HBM peak) and seqs/s, 1 GPU"
 WORKLOAD = ("Llama-3.1-8B GQA decode layer: 256 seqs x (32 q / 8 kv heads, d 128), bf16, block 16, "
             "context U[512,4096], 100k-block shuffled pool; step = reshape_and_cache(256 new tokens) + decode")
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "pa_decode_llama8b.md")
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -57,9 +63,14 @@ def parse():
     ap.add_argument("--profile-case", choices=["split", "cascade", "cascade_x16", "mha"], default=None,
                     help="a small case of another path for ncu: split (2 seqs, 48K-64K tokens, 64 q / 8 kv), "
                          "cascade (32 prompts x 8 samples), mha (the OPT-13B batch)")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="skip the other configurations' entries ('workloads') of the default run")
+    ap.add_argument("--record-traffic", metavar="CSV", default=None,
+                    help="write profiles/pa_decode_llama8b.json from `ncu --page raw --csv` of the --profile case")
     ap.add_argument("--workload", default="llama8b",
                     choices=["llama8b", "tiny", "opt13b", "shared", "shared_cow", "long70b_b16", "long70b_b32",
                              "llama8b_fp8", "long70b_b16_fp8", "shared_cascade", "shared_cow_cascade", "gemma_d256",
+                             "llama70b_short", "llama70b_short_fp8",
                              "shared_x16", "shared_x16_cascade", "shared_x32", "shared_x32_cascade",
                              "llama8b_nhd", "llama8b_fp8_nhd", "long70b_b16_nhd", "shared_cascade_nhd",
                              "copy_blocks", "swap_out", "swap_in", "reshape", "reshape_prefill"],
@@ -181,17 +192,58 @@ def kernel_source_sha():
     return h.hexdigest()
 
 
+PROFILE_RECORD = os.path.join(ROOT, "profiles", "pa_decode_llama8b.json")
+
+
 def profiled_traffic():
-    """DRAM bytes per pa_decode launch from the committed ncu summary, if it matches the sources."""
+    """DRAM bytes per pa_decode launch of the benchmark batch, from the record that
+    ``--record-traffic`` wrote from an ncu capture, while it matches the kernel sources."""
     try:
-        text = open(PROFILE_SUMMARY).read()
-    except OSError:
+        with open(PROFILE_RECORD) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
         return None
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    s = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
-    if not m or not s or s.group(1) != kernel_source_sha():
+    if rec.get("source_sha256") != kernel_source_sha():
         return None
-    return float(m.group(1))
+    return {"bytes": float(rec["traffic_bytes_per_launch"]),
+            "source": f"ncu capture of the {rec['capture_case']} ({rec['scale']:.4f} x its per-launch traffic "
+                      f"scaled by algorithmic bytes), profiles/pa_decode_llama8b.json"}
+
+
+def record_traffic(csv_path):
+    """Write profiles/pa_decode_llama8b.json from ``ncu --page raw --csv`` of the profiling
+    case (``--profile``): its dram read + write bytes per launch, scaled to the benchmark
+    batch's launch by algorithmic bytes (traffic grows with the tokens read)."""
+    import csv
+    from paged_kv_cache_04_gb300 import roofline, workloads
+    rows = list(csv.reader(open(csv_path)))
+    head = rows[0]
+    data = [r for r in rows[2:] if r and "paged_decode_kernel" in ",".join(r)]
+    if not data:
+        raise SystemExit(f"no paged_decode_kernel row in {csv_path}")
+    r = data[-1]
+    col = {n: i for i, n in enumerate(head)}
+    unit_scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+    units = rows[1]
+
+    def val(name):
+        i = col[name]
+        return float(r[i].replace(",", "")) * unit_scale.get(units[i], 1)
+    small = workloads.llama8b(device="cpu", S=64, num_blocks=16_000)
+    full = workloads.llama8b(device="cpu")
+    small_bytes = roofline.decode_bytes(small.context_lens.tolist(), 32, 8, 128, 2)
+    full_bytes = roofline.decode_bytes(full.context_lens.tolist(), 32, 8, 128, 2)
+    traffic = val("dram__bytes_read.sum") + val("dram__bytes_write.sum")
+    rec = {"kernel": "paged_decode_kernel<bf16, bf16, bf16, 128, tensor-core path, plain mode>",
+           "capture_case": "64-sequence profiling case (bench.py --profile)",
+           "dram_bytes_per_launch_small": traffic, "algorithmic_bytes_small": small_bytes,
+           "scale": traffic / small_bytes, "algorithmic_bytes_full": full_bytes,
+           "traffic_bytes_per_launch": round(traffic / small_bytes * full_bytes),
+           "gpu_time_ns_small": val("gpu__time_duration.sum"), "source_sha256": kernel_source_sha(),
+           "csv": os.path.basename(csv_path)}
+    with open(PROFILE_RECORD, "w") as f:
+        json.dump(rec, f, indent=1)
+    print(json.dumps(rec))
 
 
 # ---------------------------------------------------------------------------
@@ -254,17 +306,23 @@ def run_ours(args, rank, world, local):
     clocks.start()
     time.sleep(0.3)
     K = args.steps
-    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     t0.record(stream)
     for i in range(K):
-        step(i, dec_ev[i])
+        step(i)
     t1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     ms_total = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    # The decode kernel's own launch time, from a second pass of the same steps with
+    # events around each decode call (kept out of the pass above: an event between the
+    # cache write and the decode stops the decode from being scheduled early).
+    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(K):
+        step(i, dec_ev[i])
+    torch.cuda.synchronize()
     dec_ms = [a.elapsed_time(b) for a, b in dec_ev]
 
     # end to end through the public API: pinned host inputs in, output back out
@@ -324,6 +382,32 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     barrier(world)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+
+    # The same end-to-end step with nothing overlapped: one stream, copy in -> cache
+    # write -> decode -> copy out, each step after the last (the latency of one step).
+    def serial_step(i):
+        j = i % 2
+        wl = batches[j]
+        h, d = host[j]
+        for k in d:
+            d[k].copy_(h[k], non_blocking=True)
+        pa.pa_reshape_and_cache(d["new_key"], d["new_value"], wl.k_cache, wl.v_cache, d["slot_mapping"])
+        pa.pa_decode(outs[j], d["q"], wl.k_cache, wl.v_cache, d["block_tables"], d["context_lens"], wl.scale)
+        h["out"].copy_(outs[j], non_blocking=True)
+
+    for i in range(3):
+        serial_step(i)
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    s0.record(stream)
+    for i in range(K2):
+        serial_step(i)
+    s1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    serial_ms = max_over_ranks(s0.elapsed_time(s1), world, dev)
     clk = clocks.stop()
     for j in range(2):  # the overlapped copies delivered each batch's output
         if not torch.equal(host[j][0]["out"], outs[j].cpu()):
@@ -363,20 +447,40 @@ def run_ours(args, rank, world, local):
         "seqs_per_s": round(world * S / (ms_step * 1e-3), 1),
         "kv_tokens_per_s": round(world * tokens / (ms_step * 1e-3), 1),
         "frac_of_hbm_peak": round(value / world / peak, 4),
+        "frac_of_nominal_peak": round(value / world / NOMINAL_HBM_GBS, 4),
         "roofline": {"kernel": "paged_decode_kernel (pa_decode)", "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": traffic, "algorithmic_bytes_per_launch": int(dec_bytes),
+                     "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4), "nominal_peak": NOMINAL_HBM_GBS,
+                     "traffic": traffic["bytes"] if traffic else None,
+                     "traffic_source": traffic["source"] if traffic else
+                     "null: no ncu capture of the current kernel sources",
+                     "algorithmic_bytes_per_launch": int(dec_bytes),
                      "avg_launch_ms": round(dec_avg, 5)},
         "e2e": {"value": round(world * (dec_bytes + rc_bytes) / (e2e_ms / K2 * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms / K2, 5), "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": 2 * K,
+                "d2h_bytes_per_step": int(d2h),
+                "how": "pinned host inputs up on one stream while the previous step computes, output down on a third",
+                "serial": {"value": round(world * (dec_bytes + rc_bytes) / (serial_ms / K2 * 1e-3) / 1e9, 1),
+                           "ms_per_step": round(serial_ms / K2, 5),
+                           "how": "one stream: copy in, cache write, decode, copy out, step after step"}},
+        "gpu_launches": 2 * K,  # the timed pass: one cache write and one decode per step
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(batches[0], args.cpu_seconds)
+        line["cpu_baseline"]["one_thread"] = cpu_baseline(batches[0], args.cpu_seconds / 4, threads=1)
+    if rank == 0 and world == 1 and not args.headline_only:
+        # the other configurations, each timed on its own after the headline (N = 1 only)
+        del batches, outs, host
+        torch.cuda.empty_cache()
+        extras = {}
+        for name in EXTRA_WORKLOADS:
+            extras[name] = measure_workload(name, max(10, min(30, K)), max(3, args.warmup),
+                                            None if args.no_cpu_baseline else 2.0, local)
+            torch.cuda.empty_cache()
+        line["workloads"] = extras
     return line
 
 
@@ -422,9 +526,9 @@ def sample_bytes(smp):
     return (roofline.decode_bytes(ctx, 32, 8, 128, 2) + roofline.reshape_and_cache_bytes(len(ctx), 8, 128, 2))
 
 
-def cpu_baseline(wl, seconds):
+def cpu_baseline(wl, seconds, threads=None):
     import oracle
-    threads = len(os.sched_getaffinity(0))
+    threads = threads or len(os.sched_getaffinity(0))
     n = 2
     while True:
         smp = oracle_sample(wl, list(range(n)))
@@ -437,7 +541,7 @@ def cpu_baseline(wl, seconds):
     return {"value": round(sample_bytes(smp) / dt / 1e9, 4), "unit": "GB/s", "cores": min(threads, oracle.max_threads()),
             "kind": "oracle", "seconds": round(dt, 2),
             "sample": f"first {n} of {wl.S} sequences of the same batch (all 32 heads, its new tokens written "
-                      f"first), float64 C oracle, OpenMP over (sequence, head)"}
+                      f"first), float64 C oracle, OpenMP over (sequence, head), {threads} thread(s)"}
 
 
 def run_reference(args, rank, world, local):
@@ -540,7 +644,7 @@ def time_steps(step, steps, warmup, flush):
     return statistics.mean(x.elapsed_time(y) for x, y in times)
 
 
-def run_cache_workload(args, name):
+def measure_cache_workload(name, steps, warmup, cpu_seconds=None, clocks_index=0):
     """The cache kernels on their own: CoW block copies, swap to and from pinned host
     memory, and the cache write at decode and at prefill size."""
     import numpy as np
@@ -556,13 +660,15 @@ def run_cache_workload(args, name):
     g = torch.Generator().manual_seed(0)
     line = {"workload": name}
     cpu = None
+    clocks = ClockSampler(clocks_index)
+    clocks.start()
     if name == "copy_blocks":
         wl = workloads.shared_prefix(device="cpu", cow=True)   # its 448 copy-on-write pairs and pool size
         pairs = wl.copy_pairs.to(dev)
         nb = wl.num_blocks
         kp = [torch.empty((nb, G, B, d), dtype=dt, device=dev) for _ in range(L)]
         vp = [torch.empty((nb, G, B, d), dtype=dt, device=dev) for _ in range(L)]
-        ms = time_steps(lambda: pa.pa_copy_blocks(kp, vp, pairs), args.steps, args.warmup, flush)
+        ms = time_steps(lambda: pa.pa_copy_blocks(kp, vp, pairs), steps, warmup, flush)
         byt = roofline.copy_blocks_bytes(pairs.shape[0], L, B, G, d, 2)
         # the 7 samples of a prompt all copy its one partial block: reads repeat through L2
         nsrc = len(set(wl.copy_pairs[:, 0].tolist()))
@@ -594,14 +700,14 @@ def run_cache_workload(args, name):
         else:
             pairs = torch.stack([dst, src], 1).to(dev)
             step = lambda: pa.pa_swap_blocks(dk, dv, hk, hv, pairs)  # noqa: E731
-        ms = time_steps(step, args.steps, args.warmup, flush)
+        ms = time_steps(step, steps, warmup, flush)
         byt = P * L * roofline.kv_block_bytes(B, G, d, 2)  # bytes moved across the host link
         # the same byte count as one contiguous copy over the same link, timed here
         dbuf = torch.empty(byt // 2, dtype=dt, device=dev)
         hbuf = torch.empty(byt // 2, dtype=dt).pin_memory()
         ref = (lambda: hbuf.copy_(dbuf, non_blocking=True)) if name == "swap_out" else \
             (lambda: dbuf.copy_(hbuf, non_blocking=True))
-        ref_ms = time_steps(ref, args.steps, args.warmup, flush)
+        ref_ms = time_steps(ref, steps, warmup, flush)
         line.update(desc=f"{P} blocks x {L} layers (K and V) {'device -> pinned host' if name == 'swap_out' else 'pinned host -> device'}, one launch",
                     bound="host link", contiguous_copy_GBps=round(byt / (ref_ms * 1e-3) / 1e9, 1),
                     frac_of_contiguous_copy=round(ref_ms / ms, 4))
@@ -613,7 +719,7 @@ def run_cache_workload(args, name):
         key = torch.randn((N, G, d), generator=g).to(dt).to(dev)
         val = torch.randn((N, G, d), generator=g).to(dt).to(dev)
         slots = torch.randperm(nb * B, generator=g)[:N].to(dev)
-        ms = time_steps(lambda: pa.pa_reshape_and_cache(key, val, kc, vc, slots), args.steps, args.warmup, flush)
+        ms = time_steps(lambda: pa.pa_reshape_and_cache(key, val, kc, vc, slots), steps, warmup, flush)
         byt = roofline.reshape_and_cache_bytes(N, G, d, 2)
         line.update(desc=f"{N} new tokens x 8 kv heads x 128 (bf16) into a 100k-block pool, random slots",
                     bound="hbm" if N > 1024 else "launch latency",
@@ -626,36 +732,44 @@ def run_cache_workload(args, name):
         cpu = {"value": round(roofline.reshape_and_cache_bytes(n, G, d, 2) / cdt / 1e9, 4), "unit": "GB/s",
                "cores": 1, "kind": "oracle", "seconds": round(cdt, 3),
                "sample": f"{n} tokens, numpy element copies"}
+    clk = clocks.stop()
     line.update(ms_per_step=round(ms, 5), algorithmic_GBps=round(byt / (ms * 1e-3) / 1e9, 1), bytes_per_step=byt,
-                l2="512 MiB buffer read between timed steps", device_errors=pa.pa_get_error())
-    if cpu is not None and not args.no_cpu_baseline:
+                frac_of_nominal_peak=round(byt / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
+                l2="512 MiB buffer read between timed steps", gpu_launches=steps,
+                clocks=clk, device_errors=pa.pa_get_error())
+    if cpu is not None and cpu_seconds:
         line["cpu_baseline"] = cpu
-    print(json.dumps(line), flush=True)
+    return line
 
 
-def run_workload(args):
-    """Device-timed step of one of the other workload shapes (single GPU)."""
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e nominal (~8 TB/s), reported beside the measured copy peak
+
+# The default run's other configurations, each a device-timed entry under "workloads"
+# in the one JSON line (N = 1 only): the pages' workload shapes (OPT-13B MHA, the
+# Llama-3.1-8B batch over E4M3 codes, 70B-shaped GQA-8 on short contexts, 64 prompts x 8
+# samples sharing 2048-token prefixes, 70B-shaped 32K-128K contexts) and the CoW copies.
+EXTRA_WORKLOADS = ("tiny", "opt13b", "llama8b_fp8", "llama70b_short", "shared", "shared_cascade", "shared_cow",
+                   "shared_cow_cascade", "long70b_b16", "long70b_b32", "copy_blocks")
+
+
+def build_workload(name, dev):
+    """(workload, split, partition) for a named bench workload (a _nhd suffix stores the pools NHD)."""
     import torch
+    from paged_kv_cache_04_gb300 import workloads
     import paged_kv_cache_04_gb300 as pa
-    from paged_kv_cache_04_gb300 import _build, roofline, workloads
-    _build.ensure_built()
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    if args.workload in ("copy_blocks", "swap_out", "swap_in", "reshape", "reshape_prefill"):
-        return run_cache_workload(args, args.workload)
-    nhd = args.workload.endswith("_nhd")
-    name = args.workload[:-4] if nhd else args.workload
+    nhd = name.endswith("_nhd")
+    base = name[:-4] if nhd else name
     split, T = False, None
-    if name == "tiny":
+    if base == "tiny":
         wl = workloads.tiny(device=dev)
-    elif name == "opt13b":
+    elif base == "opt13b":
         wl = workloads.opt13b(device=dev)
-    elif name.startswith("shared"):
+    elif base.startswith("shared"):
         # _x16: 32 prompts x 16 samples (64 query rows per group), _x32: 16 x 32 (128
         # rows), else 64 x 8 (32 rows); 512 sequences each
-        shape = {"prompts": 32, "samples": 16} if "_x16" in name else (
-            {"prompts": 16, "samples": 32} if "_x32" in name else {})
-        wl = workloads.shared_prefix(device=dev, cow=name.startswith("shared_cow"), **shape)
+        shape = {"prompts": 32, "samples": 16} if "_x16" in base else (
+            {"prompts": 16, "samples": 32} if "_x32" in base else {})
+        wl = workloads.shared_prefix(device=dev, cow=base.startswith("shared_cow"), **shape)
         # set-up: the CoW copies and every appended token, once; a timed step then
         # repeats the copies and writes each sample's newest token before decoding
         if wl.copy_pairs.numel():
@@ -665,26 +779,43 @@ def run_workload(args):
                              for s, c in enumerate(wl.context_lens.tolist())], dtype=torch.int64, device=dev)
         wl.slot_mapping = last
         wl.new_key, wl.new_value = wl.new_key[:wl.S].contiguous(), wl.new_value[:wl.S].contiguous()
-    elif name == "llama8b":  # the benchmark batch, device-timed here (its pool stored NHD)
+    elif base in ("llama8b", "llama8b_fp8"):
         wl = workloads.llama8b(device=dev)
-    elif name == "llama8b_fp8":
-        wl = workloads.to_fp8(workloads.llama8b(device=dev))
-    elif name == "gemma_d256":
+    elif base in ("llama70b_short", "llama70b_short_fp8"):
+        wl = workloads.llama70b_short(device=dev)
+    elif base == "gemma_d256":
         wl = workloads.gemma_d256(device=dev)
-    elif name.startswith("long70b"):
-        B = 32 if "b32" in name else 16
-        wl = workloads.long70b(device=dev, B=B)
-        if name.endswith("fp8"):
-            wl = workloads.to_fp8(wl)
+    elif base.startswith("long70b"):
+        wl = workloads.long70b(device=dev, B=32 if "b32" in base else 16)
         split, T = True, 512
     else:
-        raise ValueError(f"unknown workload {args.workload}")
+        raise ValueError(f"unknown workload {name}")
+    if base.endswith("fp8"):
+        wl = workloads.to_fp8(wl)
     if nhd:
         wl = workloads.to_nhd(wl)
-        torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    return wl, split, T
+
+
+def measure_workload(name, steps, warmup, cpu_seconds=None, clocks_index=0):
+    """Device-timed steps of one named workload (single GPU): a dict with the step time,
+    seqs/s, attended KV tokens/s, algorithmic GB/s against the measured and nominal HBM
+    peaks, the attention call's own roofline, the clocks seen and (with cpu_seconds) the
+    oracle on a bounded sample."""
+    import torch
+    import paged_kv_cache_04_gb300 as pa
+    from paged_kv_cache_04_gb300 import _build, roofline
+    _build.ensure_built()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if name in ("copy_blocks", "swap_out", "swap_in", "reshape", "reshape_prefill"):
+        return measure_cache_workload(name, steps, warmup, cpu_seconds, clocks_index)
+    wl, split, T = build_workload(name, dev)
+    base = name[:-4] if name.endswith("_nhd") else name
     lay = wl.layout
-    fp8 = name.endswith("fp8")
-    cascade = name.endswith("cascade")
+    fp8 = base.endswith("fp8")
+    cascade = base.endswith("cascade")
     ks, vs = wl.meta.get("k_scale", 1.0), wl.meta.get("v_scale", 1.0)
     if cascade:
         gs = torch.tensor(wl.meta["group_starts"], dtype=torch.int32, device=dev)
@@ -705,23 +836,17 @@ def run_workload(args):
     flush = torch.ones(128 * 1024 * 1024, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
     pairs = wl.copy_pairs if wl.copy_pairs is not None and wl.copy_pairs.numel() else None
+    launches = 0
 
-    def step():
+    def attend():
         if fp8:
-            pa.pa_reshape_and_cache_fp8(wl.new_key, wl.new_value, wl.k_cache, wl.v_cache, wl.slot_mapping, ks, vs,
-                                        layout=lay)
             if split:
                 pa.pa_decode_split_fp8(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens,
                                        wl.scale, ks, vs, max_ctx, T, ws, layout=lay)
             else:
                 pa.pa_decode_fp8(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale,
                                  ks, vs, layout=lay)
-            return
-        if pairs is not None:
-            pa.pa_copy_blocks([wl.k_cache], [wl.v_cache], pairs)
-        if wl.slot_mapping is not None:
-            pa.pa_reshape_and_cache(wl.new_key, wl.new_value, wl.k_cache, wl.v_cache, wl.slot_mapping, layout=lay)
-        if cascade:
+        elif cascade:
             pa.pa_decode_cascade(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale,
                                  gs, pl, gmax, pmax, max_ctx, T, ws, layout=lay)
         elif split:
@@ -730,21 +855,56 @@ def run_workload(args):
         else:
             pa.pa_decode(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale, layout=lay)
 
-    for _ in range(args.warmup):
+    # kernels one step launches: copies, cache write, then the attention call's launches
+    attend_launches = 3 if cascade and max(wl.meta["prefix_lens"]) > 0 else (2 if split or cascade else 1)
+    step_launches = attend_launches + (1 if wl.slot_mapping is not None else 0) + (1 if pairs is not None else 0)
+
+    def step(ev=None):
+        if pairs is not None:
+            pa.pa_copy_blocks([wl.k_cache], [wl.v_cache], pairs)
+        if wl.slot_mapping is not None:
+            if fp8:
+                pa.pa_reshape_and_cache_fp8(wl.new_key, wl.new_value, wl.k_cache, wl.v_cache, wl.slot_mapping,
+                                            ks, vs, layout=lay)
+            else:
+                pa.pa_reshape_and_cache(wl.new_key, wl.new_value, wl.k_cache, wl.v_cache, wl.slot_mapping,
+                                        layout=lay)
+        if ev is not None:
+            ev[0].record(stream)
+        attend()
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize()
-    times = []
-    # keep the GPU busy while the host queues every timed step, so no step waits on the host
-    torch.cuda._sleep(int(2e6 * (2 + args.steps)))
-    for _ in range(args.steps):
-        flush.sum()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        step()
-        b.record(stream)
-        times.append((a, b))
-    torch.cuda.synchronize()
-    ms = statistics.mean(x.elapsed_time(y) for x, y in times)
+    clocks = ClockSampler(clocks_index)
+    clocks.start()
+    time.sleep(0.2)
+
+    def timed(inner):
+        # inner: events around the attention call too (for its own roofline); they sit
+        # between the cache write and the attention launch and stop that launch from
+        # being scheduled early, so the step time comes from a loop without them
+        nonlocal launches
+        times = []
+        # keep the GPU busy while the host queues every timed step, so no step waits on the host
+        torch.cuda._sleep(int(2e6 * (2 + steps)))
+        for _ in range(steps):
+            flush.sum()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            ev[0].record(stream)
+            step((ev[1], ev[2]) if inner else None)
+            ev[3].record(stream)
+            times.append(ev)
+            launches += step_launches
+        torch.cuda.synchronize()
+        return (statistics.mean(e[0].elapsed_time(e[3]) for e in times),
+                statistics.mean(e[1].elapsed_time(e[2]) for e in times) if inner else None)
+
+    ms, _ = timed(False)
+    _, att_ms = timed(True)
+    clk = clocks.stop()
     e = wl.q.element_size()
     ke = wl.k_cache.element_size()
     ctx = wl.context_lens.tolist()
@@ -758,21 +918,47 @@ def run_workload(args):
     if pairs is not None:
         extra += roofline.copy_blocks_bytes(pairs.shape[0], 1, wl.B, wl.G, wl.d, e)
     unique = None
-    if name.startswith("shared"):
+    if base.startswith("shared"):
         unique = wl.meta["unique_tokens"] * roofline.kv_bytes_per_token(1, wl.G, wl.d, e) + 2 * wl.S * wl.H * wl.d * e
-    peak, _ = measured_hbm_peak()
-    line = {"workload": args.workload, "ms_per_step": round(ms, 5), "seqs_per_s": round(wl.S / (ms * 1e-3), 1),
+    peak, peak_kind = measured_hbm_peak()
+    gbps = (dec + extra) / (ms * 1e-3) / 1e9
+    att_bytes = unique if unique is not None else dec
+    att_gbps = att_bytes / (att_ms * 1e-3) / 1e9
+    kernel = {"plain": "paged_decode_kernel (pa_decode)", "fp8": "paged_decode_kernel over E4M3 codes (pa_decode_fp8)",
+              "split": "paged_decode_kernel split mode + lse_reduce (pa_decode_split, 2 launches)",
+              "split_fp8": "paged_decode_kernel split mode over E4M3 codes + lse_reduce (pa_decode_split_fp8)",
+              "cascade": "prefix pass + suffix pass + lse_reduce (pa_decode_cascade, 3 launches)"}[
+        "cascade" if cascade else ("split_fp8" if split and fp8 else ("split" if split else ("fp8" if fp8 else "plain")))]
+    line = {"workload": name, "seqs": wl.S, "q_heads": wl.H, "kv_heads": wl.G, "head_dim": wl.d, "block_size": wl.B,
+            "cache_dtype": "e4m3" if fp8 else str(wl.k_cache.dtype).replace("torch.", ""), "layout": lay,
+            "ms_per_step": round(ms, 5), "seqs_per_s": round(wl.S / (ms * 1e-3), 1),
             "kv_tokens_per_s": round(sum(ctx) / (ms * 1e-3), 1),
-            "algorithmic_GBps": round((dec + extra) / (ms * 1e-3) / 1e9, 1),
-            "frac_of_measured_peak": round((dec + extra) / (ms * 1e-3) / 1e9 / peak, 4),
-            "bytes_per_step": dec + extra, "l2": "512 MiB buffer read between timed steps",
+            "algorithmic_GBps": round(gbps, 1),
+            "frac_of_measured_peak": round(gbps / peak, 4),
+            "frac_of_nominal_peak": round(gbps / NOMINAL_HBM_GBS, 4),
+            "bytes_per_step": dec + extra,
+            "roofline": {"kernel": kernel, "bound": "hbm", "achieved": round(att_gbps, 1), "peak": peak,
+                         "peak_kind": peak_kind, "unit": "GB/s", "frac": round(att_gbps / peak, 4),
+                         "frac_of_nominal": round(att_gbps / NOMINAL_HBM_GBS, 4), "traffic": None,
+                         "algorithmic_bytes_per_launch": int(att_bytes), "avg_launch_ms": round(att_ms, 5),
+                         "bytes_counted": "unique K/V (each shared prefix block once) + q + out" if unique is not None
+                         else "K/V of every attended token + q + out"},
+            "l2": "512 MiB buffer read between timed steps", "gpu_launches": launches, "clocks": clk,
             "device_errors": pa.pa_get_error()}
-    if not args.no_cpu_baseline:
-        line["cpu_baseline"] = decode_oracle_baseline(wl, min(args.cpu_seconds, 5.0), fp8=fp8)
     if unique is not None:
+        line["logical_GBps"] = line["algorithmic_GBps"]
         line["unique_GBps"] = round((unique + extra) / (ms * 1e-3) / 1e9, 1)
         line["unique_frac_of_measured_peak"] = round((unique + extra) / (ms * 1e-3) / 1e9 / peak, 4)
         line["copy_pairs"] = 0 if pairs is None else int(pairs.shape[0])
+    if cpu_seconds:
+        line["cpu_baseline"] = decode_oracle_baseline(wl, cpu_seconds, fp8=fp8)
+    return line
+
+
+def run_workload(args):
+    """One device-timed line for one of the other workload shapes (single GPU)."""
+    line = measure_workload(args.workload, args.steps, args.warmup,
+                            None if args.no_cpu_baseline else min(args.cpu_seconds, 5.0))
     print(json.dumps(line), flush=True)
 
 
@@ -853,6 +1039,9 @@ def run_other_profile_case(args):
 
 def main():
     args = parse()
+    if args.record_traffic:
+        record_traffic(args.record_traffic)
+        return
     if args.profile or args.profile_fp8:
         run_profile_case(args)
         return
