@@ -171,7 +171,7 @@ def test_long70b_split_reduced_full(pa, cuda_device, B):
 @pytest.mark.parametrize("B", [16, 32])
 def test_long70b_full_size_sampled(pa, cuda_device, B):
     wl = workloads.long70b(device=cuda_device, B=B)
-    seqs = H.sample_seqs(wl, 2)  # the shortest and the longest context
+    seqs = H.sample_seqs(wl, 4)  # the shortest and the longest context and two more
     P = H.Pristine(wl, seqs)
     out = H.gpu_step(pa, wl, split=True)
     ref = P.decode()
