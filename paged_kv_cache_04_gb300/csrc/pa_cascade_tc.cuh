@@ -118,6 +118,32 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// 16 consecutive 32-bit columns of 16 lanes, twice (warp-collective, shape
+// 16x32bx2): threads 0-15 read lanes 0-15 of the warp's quarter at columns
+// taddr + j, threads 16-31 the same lanes at columns taddr + OFF + j (measured on
+// the GB300 with known values stored through the 32x32b shape).
+template <int OFF>
+__device__ __forceinline__ void tc_ld16x2(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16], %17;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr), "n"(OFF)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+template <int OFF>
+__device__ __forceinline__ void tc_st16x2(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x32bx2.x16.b32 [%0], %1, {%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17};" ::"r"(
+          taddr),
+      "n"(OFF), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
@@ -442,10 +468,17 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   } else {
     // -------------------------------- softmax --------------------------------
     const float NEG_INF = -__int_as_float(0x7f800000);
-    // the row this thread owns: an M = 64 accumulator keeps row 16 w + t in lane
-    // 32 w + t (lanes t >= 16 hold none), an M = 128 one keeps row 32 w + t in lane 32 w + t
-    const int row = MR == 64 ? 16 * warp + lane : 32 * warp + lane;
-    const bool has_row = MR == 128 || lane < 16;
+    // The row this thread owns. An M = 128 accumulator keeps row 32 w + t in lane
+    // 32 w + t: thread t of warp w takes that whole row. An M = 64 one keeps row
+    // 16 w + t in lane 32 w + t (t < 16) and nothing in lanes 16-31, so threads t
+    // and t + 16 share row 16 w + t (HALF): the 16x32bx2 loads give thread t its
+    // columns 0-15 and thread t + 16 its columns 16-31 (of a tile's 32 scores; of
+    // O, the first and second half of head_dim). The two halves exchange the row
+    // max per tile and the sum at the end of an item.
+    constexpr bool HALF = MR == 64;
+    constexpr int CW = HALF ? NT / 2 : NT;  // score columns per thread
+    const int half = HALF ? lane >> 4 : 0;
+    const int row = HALF ? 16 * warp + (lane & 15) : 32 * warp + lane;
     const uint32_t lane_addr = tbase + ((uint32_t)(32 * warp) << 16);
     // Q of an item into the Q tile: row r = member r / group, head r % group, by
     // cp.async (padding rows are zero); 128 threads, 16-byte chunks, 128-byte
@@ -499,42 +532,47 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         // before this tile's P V has read the stage
         const unsigned ok = job_ok[n % R];
         tc_fence_after();
-        uint32_t s[32];
-        tc_ld32(lane_addr + S_COL + b * NT, s);
+        uint32_t s[CW];
+        if constexpr (HALF)
+          tc_ld16x2<NT / 2>(lane_addr + S_COL + b * NT, s);
+        else
+          tc_ld32(lane_addr + S_COL + b * NT, s);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_free[b]);
-        // scores of this tile's real tokens, in base-2 units
+        // scores of this tile's real tokens (this thread's columns tok0 ..), in base-2 units
         const int nv = min(NT, it.t1 - (it.t0 + 2 * i * JT));
-        float z[32], t16[16];
+        const int tok0 = half * CW;
+        float z[CW], tm[CW / 2];
         if (nv == NT && ok == 3u) {  // every tile but an item's ragged or faulty last one
 #pragma unroll
-          for (int t = 0; t < 32; ++t) z[t] = __uint_as_float(s[t]) * p.scale_log2;
+          for (int t = 0; t < CW; ++t) z[t] = __uint_as_float(s[t]) * p.scale_log2;
         } else {
 #pragma unroll
-          for (int t = 0; t < 32; ++t) {
-            const bool real = t < nv && ((ok >> (t / JT)) & 1u);
+          for (int t = 0; t < CW; ++t) {
+            const bool real = tok0 + t < nv && ((ok >> ((tok0 + t) / JT)) & 1u);
             z[t] = real ? __uint_as_float(s[t]) * p.scale_log2 : NEG_INF;
           }
         }
 #pragma unroll
-        for (int e = 0; e < 16; ++e) t16[e] = fmaxf(z[e], z[e + 16]);  // the row max as a tree
+        for (int e = 0; e < CW / 2; ++e) tm[e] = fmaxf(z[e], z[e + CW / 2]);  // the row max as a tree
 #pragma unroll
-        for (int w = 8; w > 0; w >>= 1)
+        for (int w = CW / 4; w > 0; w >>= 1)
 #pragma unroll
-          for (int e = 0; e < w; ++e) t16[e] = fmaxf(t16[e], t16[e + w]);
-        const float mx = t16[0];
+          for (int e = 0; e < w; ++e) tm[e] = fmaxf(tm[e], tm[e + w]);
+        float mx = tm[0];
+        if constexpr (HALF) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));  // the other half of the row
         const bool move = mx > m_ref + kTcRescale || (m_ref == NEG_INF && mx > NEG_INF);
         const float m_new = move ? mx : m_ref;
         const float c = move ? exp2f(m_ref - m_new) : 1.f;
         const float msub = m_new == NEG_INF ? 0.f : m_new;
         l *= c;
         m_ref = m_new;
-        // this row's weights as hi + lo 16-bit parts
-        uint32_t hw[16], lw[16];
+        // this thread's weights as hi + lo 16-bit parts (l: this thread's columns' sum)
+        uint32_t hw[CW / 2], lw[CW / 2];
         float ls[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: short dependency chains
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
+        for (int e = 0; e < CW / 2; ++e) {
           const float w0 = ex2_ftz(z[2 * e] - msub), w1 = ex2_ftz(z[2 * e + 1] - msub);
           ls[e & 3] += w0 + w1;
           hw[e] = Mma<DT>::pack(w0, w1);
@@ -549,26 +587,37 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           stop = true;
           break;
         }
-        if (i > 0 && __any_sync(0xffffffffu, has_row && move)) {
+        if (i > 0 && __any_sync(0xffffffffu, move)) {
           tc_fence_after();
-          const float cr = has_row ? c : 1.f;
+          if constexpr (HALF) {  // thread t: columns [0, D/2) of its row, thread t + 16: [D/2, D)
 #pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t o[32];
-            tc_ld32(lane_addr + O_COL + c0, o);
+            for (int c0 = 0; c0 < D / 2; c0 += 16) {
+              uint32_t o[16];
+              tc_ld16x2<D / 2>(lane_addr + O_COL + c0, o);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * cr);
-            tc_st32(lane_addr + O_COL + c0, o);
+              for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * c);
+              tc_st16x2<D / 2>(lane_addr + O_COL + c0, o);
+            }
+          } else {
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t o[32];
+              tc_ld32(lane_addr + O_COL + c0, o);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * c);
+              tc_st32(lane_addr + O_COL + c0, o);
+            }
           }
         }
-        if (has_row) {  // chunks 0-3: hi weights of tokens 8 ch .. 8 ch + 7; chunks 4-7: lo
+        {  // chunks 0-3: hi weights of tokens 8 ch .. 8 ch + 7; chunks 4-7: lo (this thread's chunks)
           uint8_t* pr = smem + L.p_off + pb * (M * 128) + row * 128;
 #pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
+          for (int cc = 0; cc < CW / 8; ++cc) {
+            const int ch = half * (CW / 8) + cc;
             *reinterpret_cast<uint4*>(pr + ((ch ^ (row & 7)) << 4)) =
-                make_uint4(hw[4 * ch], hw[4 * ch + 1], hw[4 * ch + 2], hw[4 * ch + 3]);
+                make_uint4(hw[4 * cc], hw[4 * cc + 1], hw[4 * cc + 2], hw[4 * cc + 3]);
             *reinterpret_cast<uint4*>(pr + (((ch + 4) ^ (row & 7)) << 4)) =
-                make_uint4(lw[4 * ch], lw[4 * ch + 1], lw[4 * ch + 2], lw[4 * ch + 3]);
+                make_uint4(lw[4 * cc], lw[4 * cc + 1], lw[4 * cc + 2], lw[4 * cc + 3]);
           }
         }
         fence_proxy_async_smem();
@@ -581,23 +630,39 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       if (!wait_all(&pv_done[0], (n - 1) & 1)) break;
       tc_fence_after();
       if (have_next) issue_q(nx, 0);  // every score MMA of this item has read Q
-      const bool write = has_row && row < rows;
+      if constexpr (HALF) l += __shfl_xor_sync(0xffffffffu, l, 16);  // the row's two halves
+      const bool write = row < rows;
       const long long wrow = ((long long)(it.s0 + row / p.group) * p.H + it.kv * p.group + row % p.group) *
                                  p.max_partitions + it.part;
       const float inv = l > 0.f ? p.v_scale / l : 0.f;
+      if constexpr (HALF) {
 #pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t o[32];
-        tc_ld32(lane_addr + O_COL + c0, o);
-        if (write) {
-          float4* dst = reinterpret_cast<float4*>(p.ws_o + wrow * D + c0);
+        for (int c0 = 0; c0 < D / 2; c0 += 16) {
+          uint32_t o[16];
+          tc_ld16x2<D / 2>(lane_addr + O_COL + c0, o);
+          if (write) {
+            float4* dst = reinterpret_cast<float4*>(p.ws_o + wrow * D + half * (D / 2) + c0);
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            dst[e] = make_float4(__uint_as_float(o[4 * e]) * inv, __uint_as_float(o[4 * e + 1]) * inv,
-                                 __uint_as_float(o[4 * e + 2]) * inv, __uint_as_float(o[4 * e + 3]) * inv);
+            for (int e = 0; e < 4; ++e)
+              dst[e] = make_float4(__uint_as_float(o[4 * e]) * inv, __uint_as_float(o[4 * e + 1]) * inv,
+                                   __uint_as_float(o[4 * e + 2]) * inv, __uint_as_float(o[4 * e + 3]) * inv);
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          tc_ld32(lane_addr + O_COL + c0, o);
+          if (write) {
+            float4* dst = reinterpret_cast<float4*>(p.ws_o + wrow * D + c0);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              dst[e] = make_float4(__uint_as_float(o[4 * e]) * inv, __uint_as_float(o[4 * e + 1]) * inv,
+                                   __uint_as_float(o[4 * e + 2]) * inv, __uint_as_float(o[4 * e + 3]) * inv);
+          }
         }
       }
-      if (write) {
+      if (write && half == 0) {
         p.ws_m[wrow] = m_ref;
         p.ws_l[wrow] = l;
       }
