@@ -60,9 +60,10 @@ def parse():
                     help="run only the step's kernels on a 64-sequence batch of the same shape (for ncu)")
     ap.add_argument("--profile-fp8", action="store_true",
                     help="the same 64-sequence case with an E4M3 cache (for ncu)")
-    ap.add_argument("--profile-case", choices=["split", "cascade", "cascade_x16", "mha"], default=None,
+    ap.add_argument("--profile-case", choices=["split", "cascade", "cascade_x16", "mha", "g8"], default=None,
                     help="a small case of another path for ncu: split (2 seqs, 48K-64K tokens, 64 q / 8 kv), "
-                         "cascade (32 prompts x 8 samples), mha (the OPT-13B batch)")
+                         "cascade (32 prompts x 8 samples), mha (the OPT-13B batch), g8 (64 seqs of the "
+                         "64 q / 8 kv short-context batch, plain decode)")
     ap.add_argument("--headline-only", action="store_true",
                     help="skip the other configurations' entries ('workloads') of the default run")
     ap.add_argument("--record-traffic", metavar="CSV", default=None,
@@ -1004,6 +1005,8 @@ def run_other_profile_case(args):
         wl = workloads.shared_prefix(device=dev, prompts=32)
     elif name == "cascade_x16":  # 64 query rows per group: the tcgen05 prefix pass
         wl = workloads.shared_prefix(device=dev, prompts=16, samples=16)
+    elif name == "g8":  # plain decode at group 8 (merge in rounds): ~0.57 GB of K/V, 4.4x the L2
+        wl = workloads.llama70b_short(device=dev, S=64, num_blocks=16_000)
     else:
         wl = workloads.opt13b(device=dev)
     out = torch.empty_like(wl.q)
