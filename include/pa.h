@@ -225,7 +225,7 @@ pa_status pa_decode_split_static(void* out, const void* q, const void* k_cache, 
  * computed in three launches:
  *   1. prefix pass: each (group, kv head, partition of the prefix) attends all
  *      of the group's query rows at once, so a prefix block is read once per
- *      group instead of once per member (groups of more than 32 query rows run
+ *      group instead of once per member (groups of more than 16 query rows run
  *      it on tcgen05 tensor cores, M = 64 or 128 rows per tile);
  *   2. each sequence's own tokens [prefix, context) as one partial per
  *      (sequence, head), one warp per (sequence, kv head), longest first;

@@ -233,9 +233,12 @@ pa_status run_decode(const DecodeArgs& a, bool split, int partition, int max_par
       if (!mma_path &&
           (s = make_pool_map(&vsw, a.v_cache, a.dt, a.D, a.G, a.BS, a.num_blocks, a.layout)) != PA_OK)
         return s;
-      // Groups of 33-64 query rows fill the M = 64 tile of the tcgen05 pass and
-      // groups of 65-128 its M = 128 tile; up to 32 rows, the mma.sync pass (four
-      // warps of 8 rows) wastes no lane.
+      // Groups of 17-64 query rows take the M = 64 tile of the tcgen05 pass and
+      // groups of 65-128 its M = 128 tile; up to 16 rows, the mma.sync pass (four
+      // warps of 8 rows). The tcgen05 pass is bound by its per-tile chain, not by
+      // its rows, so at 32 rows (8 samples of a GQA-4 model) a half-empty M = 64
+      // tile still beats the mma.sync pass (3-3.5% per step on 64 prompts x 8
+      // samples, measured).
       const bool bf = a.dt == PA_BF16;
       if (c.rows > 64) {
         if (a.D == 128)
@@ -244,7 +247,7 @@ pa_status run_decode(const DecodeArgs& a, bool split, int partition, int max_par
         else
           s = bf ? launch_cascade_prefix_tc<__nv_bfloat16, 64, 128>(km, vsw, p, sms, pitems, st)
                  : launch_cascade_prefix_tc<__half, 64, 128>(km, vsw, p, sms, pitems, st);
-      } else if (c.rows > 8 * kCascadeConsumers) {
+      } else if (c.rows > 16) {
         if (a.D == 128)
           s = bf ? launch_cascade_prefix_tc<__nv_bfloat16, 128, 64>(km, vsw, p, sms, pitems, st)
                  : launch_cascade_prefix_tc<__half, 128, 64>(km, vsw, p, sms, pitems, st);

@@ -9,17 +9,19 @@
 // group's rows form the M side (64 or 128, padded) of real matrix products:
 //   S = Q K^T   M rows, N = 32 tokens, K = head_dim
 //   O += P V    M rows, N = head_dim, K = 32 tokens
-// Warp roles (192 threads):
-//   warps 0-3  softmax: each thread owns one query row (M = 64: thread t < 16 of
-//              warp w owns row 16 w + t, kept in tensor-memory lane 32 w + t;
-//              M = 128: thread t of warp w owns row 32 w + t, in that lane); it
-//              reads its row of S, keeps the running (max, sum), writes its row
-//              of P (16-bit hi + lo parts) to shared memory and, at the end of
-//              an item, reads its row of O;
+// Warp roles (224 threads):
+//   warps 0-3  softmax: each thread owns one query row, or half of one (M = 64:
+//              row 16 w + t of warp w sits in tensor-memory lane 32 w + t and
+//              threads t and t + 16 take its two column halves; M = 128:
+//              thread t of warp w owns row 32 w + t, in that lane); it reads
+//              its part of S, keeps the running (max, sum), writes its part of
+//              P (16-bit hi + lo parts) to shared memory and, at the end of an
+//              item, reads its part of O;
 //   warp 4     TMA producer: two 16-token jobs per stage (K and V, 128-byte
 //              swizzle), a ring of five stages (three for M = 128);
 //   warp 5     owns the tensor memory (allocation, release); its lane 0 issues
-//              every MMA and commits them to mbarriers.
+//              the score MMAs and commits them to mbarriers;
+//   warp 6     its lane 0 issues the P V MMAs and commits them.
 // S is double-buffered in tensor memory, so the scores of a tile are computed
 // while the softmax warps work on the one before; the softmax computes a
 // tile's weights before it waits for the last P V to release the P buffer.
@@ -39,10 +41,10 @@ namespace pa {
 
 constexpr int kTcMaxRows = 128;    // query rows of one group (members x heads) the pass takes
 constexpr int kTcTokens = 32;      // N of S, K of P V: tokens per stage (two TMA jobs)
-// M of the tiles is 64 (groups of 33-64 query rows) or 128 (65-128); the
+// M of the tiles is 64 (groups of 17-64 query rows) or 128 (65-128); the
 // larger Q tile of M = 128 leaves room for three stages instead of five.
 __host__ __device__ constexpr int tc_stages(int MR) { return MR == 64 ? 5 : 3; }
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 224;
 constexpr float kTcRescale = 8.f;
 
 struct TcLayout {
@@ -60,7 +62,7 @@ __host__ __device__ inline TcLayout tc_layout(int D, int num_groups, int MR) {
   L.stage_bytes = 2u * kTcTokens * D * 2;
   L.p_off = L.stage_off + tc_stages(MR) * L.stage_bytes;
   L.bar_off = L.p_off + MR * 128;
-  L.misc_off = L.bar_off + (2 * tc_stages(MR) + 12) * 8;
+  L.misc_off = L.bar_off + (2 * tc_stages(MR) + 13) * 8;
   L.sched_off = round_up(L.misc_off + 16, 16);
   L.total = round_up(L.sched_off + (num_groups + 1) * 4, 16) + 1024;
   return L;
@@ -80,6 +82,11 @@ __device__ __forceinline__ uint64_t tc_desc(uint32_t addr, uint32_t lbo, uint32_
   return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
+
+// The descriptor of addr + off, from the descriptor of addr: the start address
+// field is addr >> 4 in the low 14 bits, and shared-memory addresses stay below
+// 2^18, so adding off >> 4 (off a multiple of 16) never carries out of it.
+__device__ __forceinline__ uint64_t tc_desc_add(uint64_t desc, uint32_t off) { return desc + (off >> 4); }
 
 // Instruction descriptor of kind::f16 with an fp32 accumulator: operand format
 // (0 fp16, 1 bf16) for A and B, B MN-major or K-major, N >> 3, M >> 4.
@@ -232,7 +239,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   uint64_t* p_full = s_full + 6;      // [0]: P written -> MMA ([1] unused)
   uint64_t* pv_done = s_full + 8;     // [0]: P V done -> softmax (P free, O current; [1] unused)
   uint64_t* o_free = s_full + 10;     // O read at the end of an item -> MMA
-  uint64_t* fin = s_full + 11;        // every MMA done (teardown)
+  uint64_t* fin = s_full + 11;        // every score MMA done (teardown)
+  uint64_t* fin_pv = s_full + 12;     // every P V MMA done (teardown)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc_off + 4);
   // [R] bit j: job j of the stage comes from a block in the pool. Written before
@@ -255,6 +263,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     }
     mbar_init(o_free, 4);
     mbar_init(fin, 1);
+    mbar_init(fin_pv, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -392,80 +401,83 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       for (int m = first; m < n; ++m) mbar_wait_bounded(&full[m % R], (m / R) & 1, nullptr, p.err, kDrainLimitNs);
     }
     __syncwarp();
-  } else if (warp == 5) {
-    // ------------------------------ MMA issuer -------------------------------
+  } else if (warp == 5 || warp == 6) {
+    // ------------------------------ MMA issuers ------------------------------
+    // Lane 0 of warp 5 issues the score MMAs of every tile, lane 0 of warp 6 the
+    // P V MMAs: a tile's P V goes out as soon as its P is written, never behind
+    // the next tile's score MMAs. Each commit tracks the issuing thread's own
+    // MMAs. A tile's P V is issued after the softmax has read its S, so its S
+    // MMAs (which read the stage's K) have completed by then, and the commit of
+    // P V to empty[stage] frees the whole stage.
     if (lane == 0) {
       int n = 0;
       bool issued = false;
       PItem it;
-      // P V of tile m (the item's `first` tile overwrites O)
-      auto pv = [&](int m, bool first, int k) -> bool {
-        if (!mbar_wait_sleep(&p_full[0], m & 1, abort_flag, p.err, kWaitLimitNs)) return false;
-        if (first && k > 0 && !mbar_wait_sleep(o_free, (k - 1) & 1, abort_flag, p.err, kWaitLimitNs))
-          return false;
-        tc_fence_after();
-        const uint32_t vst = st_base + (m % R) * L.stage_bytes + TILE;
-        const uint32_t pbuf = p_base;
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {  // hi weights (K columns 0-31), then lo (32-63)
-#pragma unroll
-          for (int ks = 0; ks < NT / 16; ++ks) {
-            const uint64_t a = tc_desc(pbuf + (part * (NT / 16) + ks) * 32, 16, 1024);
-            const uint64_t b = tc_desc(vst + ks * 2048, REG_BYTES, 1024);
-            tc_mma(tbase + O_COL, a, b, ID_PV, !(first && part == 0 && ks == 0));
-          }
-        }
-        tc_commit(&pv_done[0]);
-        tc_commit(&empty[m % R]);
-        issued = true;
-        return true;
-      };
-      for (int k = 0; get(k, it); ++k) {
-        if (!mbar_wait_sleep(&q_full[0], k & 1, abort_flag, p.err, kWaitLimitNs)) break;
-        const int nt = num_tiles(it);
-        const uint32_t qa = q_base;
-        bool stop = false;
-        for (int i = 0; i < nt; ++i, ++n) {
-          const int stage = n % R, b = n & 1;
-          // the last tile's P V first when its P is already there: the sooner it
-          // runs, the sooner its stage is refilled
-          bool pv_pending = i > 0;
-          if (pv_pending && mbar_try_wait(&p_full[0], (n - 1) & 1)) {
-            if (!pv(n - 1, i == 1, k)) {
+      if (warp == 5) {
+        const uint64_t qdesc = tc_desc(q_base, 16, 1024);  // built once; the MMAs add offsets
+        for (int k = 0; get(k, it); ++k) {
+          if (!mbar_wait_sleep(&q_full[0], k & 1, abort_flag, p.err, kWaitLimitNs)) break;
+          const int nt = num_tiles(it);
+          bool stop = false;
+          for (int i = 0; i < nt; ++i, ++n) {
+            const int stage = n % R, b = n & 1;
+            if (!mbar_wait_sleep(&full[stage], (n / R) & 1, abort_flag, p.err, kWaitLimitNs) ||
+                !mbar_wait_sleep(&s_free[b], ((n >> 1) & 1) ^ 1, abort_flag, p.err, kWaitLimitNs)) {
               stop = true;
               break;
             }
-            pv_pending = false;
-          }
-          if (!mbar_wait_sleep(&full[stage], (n / R) & 1, abort_flag, p.err, kWaitLimitNs) ||
-              !mbar_wait_sleep(&s_free[b], ((n >> 1) & 1) ^ 1, abort_flag, p.err, kWaitLimitNs)) {
-            stop = true;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t kst = st_base + stage * L.stage_bytes;
+            tc_fence_after();
+            const uint64_t kdesc = tc_desc(st_base + stage * L.stage_bytes, 16, 1024);
 #pragma unroll
-          for (int ks = 0; ks < KSTEPS; ++ks) {
-            const uint64_t a = tc_desc(qa + (ks >> 2) * (M * 128) + (ks & 3) * 32, 16, 1024);
-            const uint64_t bd = tc_desc(kst + (ks >> 2) * REG_BYTES + (ks & 3) * 32, 16, 1024);
-            tc_mma(tbase + S_COL + b * NT, a, bd, ID_S, ks > 0);
+            for (int ks = 0; ks < KSTEPS; ++ks) {
+              const uint64_t a = tc_desc_add(qdesc, (ks >> 2) * (M * 128) + (ks & 3) * 32);
+              const uint64_t bd = tc_desc_add(kdesc, (ks >> 2) * REG_BYTES + (ks & 3) * 32);
+              tc_mma(tbase + S_COL + b * NT, a, bd, ID_S, ks > 0);
+            }
+            tc_commit(&s_full[b]);
+            issued = true;
           }
-          tc_commit(&s_full[b]);
-          issued = true;
-          if (pv_pending && !pv(n - 1, i == 1, k)) {
-            stop = true;
-            break;
-          }
+          if (stop) break;
         }
-        if (stop || !pv(n - 1, nt == 1, k)) break;
+      } else {
+        const uint64_t pdesc = tc_desc(p_base, 16, 1024);
+        for (int k = 0; get(k, it); ++k) {
+          const int nt = num_tiles(it);
+          bool stop = false;
+          for (int i = 0; i < nt; ++i, ++n) {
+            // the item's first tile overwrites O, once the softmax has read the last item's O
+            const bool first = i == 0;
+            if (!mbar_wait_sleep(&p_full[0], n & 1, abort_flag, p.err, kWaitLimitNs) ||
+                (first && k > 0 && !mbar_wait_sleep(o_free, (k - 1) & 1, abort_flag, p.err, kWaitLimitNs))) {
+              stop = true;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t vdesc = tc_desc(st_base + (n % R) * L.stage_bytes + TILE, REG_BYTES, 1024);
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {  // hi weights (K columns 0-31), then lo (32-63)
+#pragma unroll
+              for (int ks = 0; ks < NT / 16; ++ks) {
+                const uint64_t a = tc_desc_add(pdesc, (part * (NT / 16) + ks) * 32);
+                const uint64_t b = tc_desc_add(vdesc, ks * 2048);
+                tc_mma(tbase + O_COL, a, b, ID_PV, !(first && part == 0 && ks == 0));
+              }
+            }
+            tc_commit(&pv_done[0]);
+            tc_commit(&empty[n % R]);
+            issued = true;
+          }
+          if (stop) break;
+        }
       }
-      if (issued) {  // every MMA issued has completed before the tensor memory is released
-        tc_commit(fin);
-        mbar_wait_bounded(fin, 0, nullptr, p.err, kDrainLimitNs);
+      if (issued) {  // every MMA this thread issued has completed before the tensor memory is released
+        uint64_t* done = warp == 5 ? fin : fin_pv;
+        tc_commit(done);
+        mbar_wait_bounded(done, 0, nullptr, p.err, kDrainLimitNs);
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp < 4) {
     // -------------------------------- softmax --------------------------------
     const float NEG_INF = -__int_as_float(0x7f800000);
     // The row this thread owns. An M = 128 accumulator keeps row 32 w + t in lane

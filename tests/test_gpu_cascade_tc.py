@@ -1,8 +1,9 @@
-"""The tcgen05 prefix pass of pa_decode_cascade (groups of 33-128 query rows).
+"""The tcgen05 prefix pass of pa_decode_cascade (groups of 17-128 query rows).
 
-Groups of 16 samples x 4 query heads (or 8 x 8) fill the M = 64 tile, groups of
-32 x 4 (or 16 x 8) the M = 128 tile, so the shared-prefix decode runs its
-prefix pass on the fifth-generation tensor cores.
+Groups of 5-16 samples x 4 query heads (or 3-8 x 8) take the M = 64 tile,
+groups of 17-32 x 4 (or 9-16 x 8) the M = 128 tile, so the shared-prefix decode
+runs its prefix pass on the fifth-generation tensor cores; groups of up to 16
+rows take the mma.sync pass.
 Each case is checked against the oracle (which sees the pool before any kernel
 ran) and against plain pa_decode of the same batch: long prefixes (many tiles
 and several items per CTA), a last partition of one 16-token job, both block
@@ -52,6 +53,10 @@ CASES = [
     (12, 32, 8, 128, 16, torch.bfloat16, 777, "HND", True),    # 48 rows: a partly filled tile
     (16, 32, 8, 64, 16, torch.bfloat16, 1300, "HND", False),   # head_dim 64
     (16, 16, 4, 64, 32, torch.float16, 1500, "NHD", False),
+    (8, 32, 8, 128, 16, torch.bfloat16, 1100, "HND", True),    # 32 rows: the 64 x 8-sample batch's groups
+    (5, 32, 8, 128, 16, torch.float16, 900, "NHD", False),     # 20 rows
+    (17, 8, 8, 128, 16, torch.bfloat16, 700, "HND", False),    # MHA, 17 rows: the smallest M = 64 group
+    (4, 32, 8, 128, 32, torch.bfloat16, 800, "HND", True),     # 16 rows: the mma.sync pass
     # M = 128 tiles
     (32, 32, 8, 128, 16, torch.bfloat16, 1040, "HND", True),   # 128 rows
     (16, 64, 8, 128, 32, torch.float16, 1300, "NHD", False),   # 16 samples x group 8

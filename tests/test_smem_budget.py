@@ -94,7 +94,7 @@ HOLDS = [
     (("fp8g8_d128", 8, 0, 256), 3),    # E4M3 plain decode at group 8
     (("mma16g8_d256", 8, 0, 2048), 2),
     (("vec_d256", 2, 0, 2048), 2),
-    (("tc_d128_m64", 512, 0, 0), 2),   # tcgen05 prefix pass, 33-64 rows per group
+    (("tc_d128_m64", 512, 0, 0), 2),   # tcgen05 prefix pass, 17-64 rows per group
     (("tc_d128_m128", 2048, 0, 0), 2),  # 65-128 rows per group
     (("tc_d64_m64", 2048, 0, 0), 2),    # (tensor memory caps this kernel at two CTAs per SM)
 ]
