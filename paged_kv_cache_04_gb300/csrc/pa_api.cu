@@ -136,19 +136,30 @@ pa_status dispatch_mode(const CUtensorMap& km, const CUtensorMap& vm, const Deco
 template <typename DT, typename QT, typename OT, int D>
 pa_status dispatch_path(const CUtensorMap& km, const CUtensorMap& vm, const DecodeParams& p, int sms,
                         long long items, int mode, cudaStream_t st) {
-  // group >= 4 on 16-bit or FP8 data: tensor cores; MHA: vector path with q in registers
+  // Group >= 2 on 16-bit or FP8 data: tensor cores (groups of 2-3 leave most of
+  // the MMA's 8 head columns empty, yet issue far fewer instructions per job than
+  // lanes splitting head_dim: measured 0.98 against 0.76 of peak at group 2 and
+  // 0.97 against 0.57 at group 3 on 16-bit caches, 0.84 against 0.53 / 0.32 over
+  // E4M3, 1.13x at head_dim 256). MHA (group 1) stays on the vector path with q in
+  // registers, which measured 6% faster there (three CTAs per SM instead of two).
   if constexpr (sizeof(DT) <= 2) {
     // plain decode at groups of 5-8 merges in rounds (kPathMmaG8); split and suffix
     // mode do not merge inside the CTA and take kPathMma at every group
     if (p.group > kMergeHeads && mode == kModePlain)
       return launch_decode<DT, QT, OT, D, kPathMmaG8, kModePlain>(km, vm, p, sms, items, st);
-    if (p.group >= 4) return dispatch_mode<DT, QT, OT, D, kPathMma>(km, vm, p, sms, items, mode, st);
+    if (p.group >= 2) return dispatch_mode<DT, QT, OT, D, kPathMma>(km, vm, p, sms, items, mode, st);
+    // group 1 (head_dim 256: q stays in shared memory; a lane's half of a 256-wide
+    // row in registers would spill)
+    if constexpr (D <= 128)
+      return dispatch_mode<DT, QT, OT, D, kPathVecMha>(km, vm, p, sms, items, mode, st);
+    else
+      return dispatch_mode<DT, QT, OT, D, kPathVec>(km, vm, p, sms, items, mode, st);
+  } else {  // fp32 data: the vector paths at every group
+    if constexpr (D <= 128) {
+      if (p.group == 1) return dispatch_mode<DT, QT, OT, D, kPathVecMha>(km, vm, p, sms, items, mode, st);
+    }
+    return dispatch_mode<DT, QT, OT, D, kPathVec>(km, vm, p, sms, items, mode, st);
   }
-  // (head_dim 256: q stays in shared memory; a lane's half of a 256-wide row in registers would spill)
-  if constexpr (D <= 128) {
-    if (p.group == 1) return dispatch_mode<DT, QT, OT, D, kPathVecMha>(km, vm, p, sms, items, mode, st);
-  }
-  return dispatch_mode<DT, QT, OT, D, kPathVec>(km, vm, p, sms, items, mode, st);
 }
 
 template <typename DT, typename OT>
@@ -181,8 +192,8 @@ pa_status run_decode(const DecodeArgs& a, bool split, int partition, int max_par
   int sms = 0;
   pa_status s = device_state(&err, &sms);
   if (s != PA_OK) return s;
-  // tensor-core path (16-bit or FP8 data, group >= 4) or vector path: see dispatch_path
-  const bool mma_path = esize(a.dt) <= 2 && a.H / a.G >= 4;
+  // tensor-core path (16-bit or FP8 data, group >= 2) or vector path: see dispatch_path
+  const bool mma_path = esize(a.dt) <= 2 && a.H / a.G >= 2;
   CUtensorMap km, vm;
   if ((s = make_pool_map(&km, a.k_cache, a.dt, a.D, a.G, a.BS, a.num_blocks, a.layout)) != PA_OK) return s;
   if ((s = make_pool_map(&vm, a.v_cache, a.dt, a.D, a.G, a.BS, a.num_blocks, a.layout, mma_path)) != PA_OK)

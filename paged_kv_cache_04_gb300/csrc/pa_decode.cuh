@@ -38,10 +38,10 @@
 //     sequence's own tokens are dealt to single warps, which write one partial
 //     each into the slot after the prefix partitions;
 //   * a KV job is read once for all H / G query heads of its kv head: with a
-//     group of >= 4 heads on 16-bit or E4M3 data the step is a small dense
+//     group of >= 2 heads on 16-bit or E4M3 data the step is a small dense
 //     contraction and runs on mma.sync m16n8k16 (tokens x heads for q K^T, d x
 //     heads for P V; E4M3 codes are converted to fp16 on the way into the
-//     fragments); otherwise (MHA, group < 4, fp32) lanes split head_dim and use
+//     fragments); otherwise (MHA, fp32) lanes split head_dim and use
 //     FFMA, with V staged unswizzled so a token row sits at fixed offsets;
 //   * the softmax is online, in fp32, base 2, with warp shuffles for the maxima;
 //     the output accumulators are rescaled only when a running max grew; in
@@ -86,7 +86,7 @@ constexpr int kJobTokens = 16;        // tokens per TMA job
 // Compute paths of the decode kernel.
 constexpr int kPathVec = 0;     // lanes split head_dim, FFMA; any group, q staged in shared memory
 constexpr int kPathVecMha = 1;  // the same for group 1 (MHA), q held in registers
-constexpr int kPathMma = 2;     // group >= 4 on 16-bit data: mma.sync m16n8k16
+constexpr int kPathMma = 2;     // group >= 2 on 16-bit or E4M3 data: mma.sync m16n8k16
 constexpr int kPathMmaG8 = 3;   // the same for groups of 5-8 in plain mode, merging heads in rounds
 __host__ __device__ constexpr bool is_mma_path(int path) { return path == kPathMma || path == kPathMmaG8; }
 
@@ -687,7 +687,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
 
   Item it;
   if constexpr (MMA) {
-    // ---------------- tensor-core path: group >= 4, 16-bit data ----------------
+    // ---------------- tensor-core path: group >= 2, 16-bit or E4M3 data ----------------
     const int g = lane >> 2, t4 = lane & 3;
     uint32_t qf[D / 16][2], qn[D / 16][2];
     // FP8 caches permute head_dim inside each 64-wide slice so that a thread's

@@ -1,11 +1,9 @@
-// Decode-kernel instantiations for bf16 caches: the three compute paths, head_dim
-// 64/128, output in the cache type or fp32, plain, split and shared-prefix suffix mode.
+// Decode-kernel instantiations for bf16 caches, head_dim 64/128: the MHA vector
+// path (group 1) and the tensor-core path (groups 2-8; plain decode at groups 5-8
+// is in pa_decode_g8.cu), output in the cache type or fp32, plain, split and
+// shared-prefix suffix mode.
 #include "pa_decode_launch.cuh"
 
-PA_INSTANTIATE_DECODE(__nv_bfloat16, __nv_bfloat16, __nv_bfloat16, 64, pa::kPathVec)
-PA_INSTANTIATE_DECODE(__nv_bfloat16, __nv_bfloat16, float, 64, pa::kPathVec)
-PA_INSTANTIATE_SPLIT(__nv_bfloat16, __nv_bfloat16, 64, pa::kPathVec)
-PA_INSTANTIATE_SUFFIX(__nv_bfloat16, __nv_bfloat16, 64, pa::kPathVec)
 PA_INSTANTIATE_DECODE(__nv_bfloat16, __nv_bfloat16, __nv_bfloat16, 64, pa::kPathVecMha)
 PA_INSTANTIATE_DECODE(__nv_bfloat16, __nv_bfloat16, float, 64, pa::kPathVecMha)
 PA_INSTANTIATE_SPLIT(__nv_bfloat16, __nv_bfloat16, 64, pa::kPathVecMha)
@@ -14,10 +12,6 @@ PA_INSTANTIATE_DECODE(__nv_bfloat16, __nv_bfloat16, __nv_bfloat16, 64, pa::kPath
 PA_INSTANTIATE_DECODE(__nv_bfloat16, __nv_bfloat16, float, 64, pa::kPathMma)
 PA_INSTANTIATE_SPLIT(__nv_bfloat16, __nv_bfloat16, 64, pa::kPathMma)
 PA_INSTANTIATE_SUFFIX(__nv_bfloat16, __nv_bfloat16, 64, pa::kPathMma)
-PA_INSTANTIATE_DECODE(__nv_bfloat16, __nv_bfloat16, __nv_bfloat16, 128, pa::kPathVec)
-PA_INSTANTIATE_DECODE(__nv_bfloat16, __nv_bfloat16, float, 128, pa::kPathVec)
-PA_INSTANTIATE_SPLIT(__nv_bfloat16, __nv_bfloat16, 128, pa::kPathVec)
-PA_INSTANTIATE_SUFFIX(__nv_bfloat16, __nv_bfloat16, 128, pa::kPathVec)
 PA_INSTANTIATE_DECODE(__nv_bfloat16, __nv_bfloat16, __nv_bfloat16, 128, pa::kPathVecMha)
 PA_INSTANTIATE_DECODE(__nv_bfloat16, __nv_bfloat16, float, 128, pa::kPathVecMha)
 PA_INSTANTIATE_SPLIT(__nv_bfloat16, __nv_bfloat16, 128, pa::kPathVecMha)

@@ -1,7 +1,8 @@
 // Decode-kernel instantiations for head_dim 256 (bf16, fp16, fp32 caches): the
-// vector path (any group; q in shared memory) and, for 16-bit caches with a group
-// of >= 4, the tensor-core path; plain and split mode, and the reduce. The
-// shared-prefix suffix pass and the E4M3 caches stop at head_dim 128.
+// vector path (q in shared memory: MHA on 16-bit caches, every group on fp32) and,
+// for 16-bit caches with a group of >= 2, the tensor-core path; plain and split
+// mode, and the reduce. The shared-prefix suffix pass and the E4M3 caches stop at
+// head_dim 128.
 #include "pa_decode_launch.cuh"
 
 PA_INSTANTIATE_DECODE(__nv_bfloat16, __nv_bfloat16, __nv_bfloat16, 256, pa::kPathVec)

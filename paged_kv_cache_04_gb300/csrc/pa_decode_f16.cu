@@ -1,11 +1,9 @@
-// Decode-kernel instantiations for f16 caches: the three compute paths, head_dim
-// 64/128, output in the cache type or fp32, plain, split and shared-prefix suffix mode.
+// Decode-kernel instantiations for fp16 caches, head_dim 64/128: the MHA vector
+// path (group 1) and the tensor-core path (groups 2-8; plain decode at groups 5-8
+// is in pa_decode_g8.cu), output in the cache type or fp32, plain, split and
+// shared-prefix suffix mode.
 #include "pa_decode_launch.cuh"
 
-PA_INSTANTIATE_DECODE(__half, __half, __half, 64, pa::kPathVec)
-PA_INSTANTIATE_DECODE(__half, __half, float, 64, pa::kPathVec)
-PA_INSTANTIATE_SPLIT(__half, __half, 64, pa::kPathVec)
-PA_INSTANTIATE_SUFFIX(__half, __half, 64, pa::kPathVec)
 PA_INSTANTIATE_DECODE(__half, __half, __half, 64, pa::kPathVecMha)
 PA_INSTANTIATE_DECODE(__half, __half, float, 64, pa::kPathVecMha)
 PA_INSTANTIATE_SPLIT(__half, __half, 64, pa::kPathVecMha)
@@ -14,10 +12,6 @@ PA_INSTANTIATE_DECODE(__half, __half, __half, 64, pa::kPathMma)
 PA_INSTANTIATE_DECODE(__half, __half, float, 64, pa::kPathMma)
 PA_INSTANTIATE_SPLIT(__half, __half, 64, pa::kPathMma)
 PA_INSTANTIATE_SUFFIX(__half, __half, 64, pa::kPathMma)
-PA_INSTANTIATE_DECODE(__half, __half, __half, 128, pa::kPathVec)
-PA_INSTANTIATE_DECODE(__half, __half, float, 128, pa::kPathVec)
-PA_INSTANTIATE_SPLIT(__half, __half, 128, pa::kPathVec)
-PA_INSTANTIATE_SUFFIX(__half, __half, 128, pa::kPathVec)
 PA_INSTANTIATE_DECODE(__half, __half, __half, 128, pa::kPathVecMha)
 PA_INSTANTIATE_DECODE(__half, __half, float, 128, pa::kPathVecMha)
 PA_INSTANTIATE_SPLIT(__half, __half, 128, pa::kPathVecMha)
