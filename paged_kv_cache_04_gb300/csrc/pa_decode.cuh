@@ -18,11 +18,11 @@
 //     by TMA tensor copies (2-D over HND rows, 3-D for NHD; the box lands the
 //     same way) that complete on the stage's K and V mbarriers; the warp's lane
 //     0 issues the copy of the job R ahead each time it finishes one, so a warp
-//     always has R - 1 jobs in flight while it computes one (plain-mode tensor
-//     cores issue the K half as soon as q K^T has read the old one; a single
-//     producer warp
-//     feeding all four rings measured 45% slower: its serial block-table and
-//     context-length loads at item boundaries stall every ring at once);
+//     always has R - 1 jobs in flight while it computes one (R - 2 while it
+//     computes two: the tensor-core path of E4M3 and of 16-bit plain decode
+//     takes two jobs per softmax step; a single producer warp feeding all four
+//     rings measured 45% slower: its serial block-table and context-length
+//     loads at item boundaries stall every ring at once);
 //   * plain mode: a work item is (sequence, kv head); items are dealt to CTAs
 //     in a serpentine order, longest contexts first (ties in batch order), and
 //     an item's jobs go round-robin to the CTA's W warps, whose partial (max,
@@ -319,20 +319,29 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
   constexpr bool SPLIT = MODE == kModeSplit;
   constexpr bool SUFFIX = MODE == kModeSuffix;
   constexpr bool F8 = std::is_same<DT, fp8e4m3>::value;
-  constexpr bool PAIR = F8;  // tensor-core path: two jobs per softmax step
+  // Tensor-core path: two jobs per softmax step (one max / rescale per 32 tokens,
+  // two independent score chains in flight). E4M3 in every mode; 16-bit data in
+  // plain mode at head_dim <= 128, where it replaced the split refill below and,
+  // with one barrier per stage, measured 0.967 -> 0.993 of the copy peak on the
+  // Llama batch, 0.92 -> 0.95 at group 8, 1.2x on plain shared-prefix decode and
+  // +6-10% at head_dim 64 (A/B on one GPU); 16-bit split decode and the suffix
+  // pass gained nothing (0.942 vs 0.945; within 1%) and keep one job per step.
+  constexpr bool PAIR = F8 || (MMA && D <= 128 && MODE == kModePlain);
   // stale running max (see kLazyTau): plain mode, and E4M3 split mode (+2.8%
   // there; 16-bit split decode measured 6% slower with it)
   constexpr bool LAZY = MODE == kModePlain || (F8 && MODE == kModeSplit);
-  // Plain-mode tensor-core step on 16-bit data: a stage's K tile is refilled
-  // right after q K^T, its V tile after P V (two barriers per stage). Measured
-  // +2.7% on the Llama batch; the same split in split mode, in the suffix pass
-  // and on the MHA vector path was 2-4% slower, so those refill whole stages.
-  constexpr bool KV_SPLIT = MMA && !F8 && MODE == kModePlain;
-  // The 16-bit tensor-core paths land K and V on separate barriers in every
-  // mode (split decode measured +2% with it); E4M3 (two jobs per step) and the
-  // vector paths keep one barrier for both (two measured 1.5-2.5% slower on
-  // E4M3 and 1.4% on the one-stage head_dim-256 vector path).
-  constexpr bool TWO_BARS = MMA && !F8;
+  // A one-job tensor-core step on 16-bit data in plain mode (head_dim 256) refills
+  // a stage's K tile right after q K^T and its V tile after P V (two barriers per
+  // stage): +2.7% on the Llama batch when one job per step was the plain-mode
+  // form; the same split in split mode, in the suffix pass and on the MHA vector
+  // path was 2-4% slower, so those refill whole stages.
+  constexpr bool KV_SPLIT = MMA && !PAIR && MODE == kModePlain;
+  // The one-job 16-bit tensor-core steps land K and V on separate barriers
+  // (split decode measured +2% with it); the two-job steps (E4M3, 16-bit plain
+  // mode) and the vector paths keep one barrier for both (two measured 1.5-2.5%
+  // slower on E4M3, 0.5% on 16-bit plain decode, 1.4% on the one-stage
+  // head_dim-256 vector path).
+  constexpr bool TWO_BARS = MMA && !PAIR;
   static_assert(!KV_SPLIT || TWO_BARS, "a split refill needs a barrier per half");
   static_assert(!PAIR || StageCfg<DT, D, PATH>::R >= 2, "two jobs per step need two stages");
   using MT = typename std::conditional<F8, __half, DT>::type;  // tensor-core operand type
