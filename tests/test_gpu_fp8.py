@@ -44,7 +44,7 @@ def _oracle(wl_host_k, wl_host_v, wl, seqs=None):
 
 
 SHAPES = [("llama", 32, 8, torch.bfloat16), ("mha", 16, 16, torch.float16), ("g2", 8, 4, torch.bfloat16),
-          ("g8", 64, 8, torch.float16)]
+          ("g3", 12, 4, torch.float16), ("g6", 48, 8, torch.bfloat16), ("g8", 64, 8, torch.float16)]
 
 
 @pytest.mark.parametrize("name,Hq,G,qt", SHAPES, ids=[s[0] for s in SHAPES])
