@@ -478,8 +478,12 @@ def run_ours(args, rank, world, local):
         torch.cuda.empty_cache()
         extras = {}
         for name in EXTRA_WORKLOADS:
-            extras[name] = measure_workload(name, max(10, min(30, K)), max(3, args.warmup),
-                                            None if args.no_cpu_baseline else 2.0, local)
+            # one entry's failure is recorded in that entry; the headline and the others stand
+            try:
+                extras[name] = measure_workload(name, max(10, min(30, K)), max(3, args.warmup),
+                                                None if args.no_cpu_baseline else 2.0, local)
+            except Exception as e:  # noqa: BLE001
+                extras[name] = {"workload": name, "error": f"{type(e).__name__}: {e}"[:300]}
             torch.cuda.empty_cache()
         line["workloads"] = extras
     return line
