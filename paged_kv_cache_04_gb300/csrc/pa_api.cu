@@ -133,27 +133,42 @@ pa_status dispatch_mode(const CUtensorMap& km, const CUtensorMap& vm, const Deco
   return launch_decode<DT, QT, OT, D, PATH, kModePlain>(km, vm, p, sms, items, st);
 }
 
+// Whether a decode launch takes the tensor-core path (mma.sync; V staged with
+// the 128-byte swizzle) rather than a vector path (lanes split head_dim). A
+// group of >= 2 query heads per kv head on 16-bit or E4M3 data: tensor cores
+// (groups of 2-3 leave most of the MMA's 8 head columns empty, yet issue far
+// fewer instructions per job than the vector path: measured 0.98 against 0.76
+// of peak at group 2 and 0.97 against 0.57 at group 3 on 16-bit caches, 0.84
+// against 0.53 / 0.32 over E4M3, 1.13x at head_dim 256). MHA (group 1) takes
+// them over E4M3 caches (0.86 against 0.82) and in 16-bit split decode (0.97
+// against 0.90 on 32K-128K contexts); 16-bit plain and suffix-pass MHA keep the
+// vector path, which measured as fast or faster there (OPT-13B batch within 1%,
+// head_dim 64 +2%) at three CTAs per SM. fp32 data: vector paths.
+bool tensor_core_path(int esize_bytes, int group, int D, int mode) {
+  if (esize_bytes > 2) return false;
+  if (group >= 2 || esize_bytes == 1) return true;
+  return mode == kModeSplit && D <= 128;
+}
+
 template <typename DT, typename QT, typename OT, int D>
 pa_status dispatch_path(const CUtensorMap& km, const CUtensorMap& vm, const DecodeParams& p, int sms,
                         long long items, int mode, cudaStream_t st) {
-  // Group >= 2 on 16-bit or FP8 data: tensor cores (groups of 2-3 leave most of
-  // the MMA's 8 head columns empty, yet issue far fewer instructions per job than
-  // lanes splitting head_dim: measured 0.98 against 0.76 of peak at group 2 and
-  // 0.97 against 0.57 at group 3 on 16-bit caches, 0.84 against 0.53 / 0.32 over
-  // E4M3, 1.13x at head_dim 256). MHA (group 1) stays on the vector path with q in
-  // registers, which measured 6% faster there (three CTAs per SM instead of two).
+  // Tensor cores (see tensor_core_path) or the vector paths. Plain decode at
+  // groups of 5-8 merges in rounds (kPathMmaG8); split and suffix mode do not
+  // merge inside the CTA and take kPathMma at every group.
   if constexpr (sizeof(DT) <= 2) {
-    // plain decode at groups of 5-8 merges in rounds (kPathMmaG8); split and suffix
-    // mode do not merge inside the CTA and take kPathMma at every group
     if (p.group > kMergeHeads && mode == kModePlain)
       return launch_decode<DT, QT, OT, D, kPathMmaG8, kModePlain>(km, vm, p, sms, items, st);
-    if (p.group >= 2) return dispatch_mode<DT, QT, OT, D, kPathMma>(km, vm, p, sms, items, mode, st);
-    // group 1 (head_dim 256: q stays in shared memory; a lane's half of a 256-wide
-    // row in registers would spill)
-    if constexpr (D <= 128)
+    if (tensor_core_path(sizeof(DT), p.group, D, mode))
+      return dispatch_mode<DT, QT, OT, D, kPathMma>(km, vm, p, sms, items, mode, st);
+    if constexpr (sizeof(DT) == 1) {
+      return PA_ERR_UNSUPPORTED;  // (E4M3 always takes the tensor cores)
+    } else if constexpr (D <= 128) {
       return dispatch_mode<DT, QT, OT, D, kPathVecMha>(km, vm, p, sms, items, mode, st);
-    else
+    } else {
+      // head_dim 256: q stays in shared memory; a lane's half of a 256-wide row in registers would spill
       return dispatch_mode<DT, QT, OT, D, kPathVec>(km, vm, p, sms, items, mode, st);
+    }
   } else {  // fp32 data: the vector paths at every group
     if constexpr (D <= 128) {
       if (p.group == 1) return dispatch_mode<DT, QT, OT, D, kPathVecMha>(km, vm, p, sms, items, mode, st);
@@ -192,8 +207,9 @@ pa_status run_decode(const DecodeArgs& a, bool split, int partition, int max_par
   int sms = 0;
   pa_status s = device_state(&err, &sms);
   if (s != PA_OK) return s;
-  // tensor-core path (16-bit or FP8 data, group >= 2) or vector path: see dispatch_path
-  const bool mma_path = esize(a.dt) <= 2 && a.H / a.G >= 2;
+  // tensor-core path or vector path: see tensor_core_path (the mode is set below)
+  const int launch_mode = !split ? kModePlain : (c.group_starts ? kModeSuffix : kModeSplit);
+  const bool mma_path = tensor_core_path(esize(a.dt), a.H / a.G, a.D, launch_mode);
   CUtensorMap km, vm;
   if ((s = make_pool_map(&km, a.k_cache, a.dt, a.D, a.G, a.BS, a.num_blocks, a.layout)) != PA_OK) return s;
   if ((s = make_pool_map(&vm, a.v_cache, a.dt, a.D, a.G, a.BS, a.num_blocks, a.layout, mma_path)) != PA_OK)
@@ -229,7 +245,7 @@ pa_status run_decode(const DecodeArgs& a, bool split, int partition, int max_par
     p.ws_l = reinterpret_cast<float*>(static_cast<char*>(ws) + align256(o_bytes) + align256(m_bytes));
     if (!c.group_starts) items *= max_partitions;  // the suffix pass has one item per (sequence, kv head)
   }
-  const int mode = !split ? kModePlain : (c.group_starts ? kModeSuffix : kModeSplit);
+  const int mode = launch_mode;
   if (c.group_starts) {
     p.group_starts = c.group_starts;
     p.prefix_lens = c.prefix_lens;
