@@ -75,7 +75,7 @@ typedef enum { PA_LAYOUT_HND = 0, PA_LAYOUT_NHD = 1 } pa_kv_layout;
 #define PA_DEVERR_SLOT 2u     /* a slot outside [-1, num_blocks * block_size) was skipped */
 #define PA_DEVERR_CONTEXT 4u  /* a context length < 0 or beyond the table / workspace was clamped */
 #define PA_DEVERR_PAIR 8u     /* a copy pair with an id outside [0, num_blocks) was skipped */
-#define PA_DEVERR_TIMEOUT 16u /* an internal wait ran past its limit; the results are undefined */
+#define PA_DEVERR_TIMEOUT 16u /* an internal wait ran past its limit; the results are undefined (below) */
 #define PA_DEVERR_PAIR_ALIAS 32u /* a copy / swap pair racing with another pair was skipped (see pa_copy_blocks) */
 
 /*
@@ -368,6 +368,20 @@ pa_status pa_swap_blocks(void* const* dst_k_caches, void* const* dst_v_caches,
  * the device's other streams first (or use one stream).
  */
 pa_status pa_get_error(uint32_t* error_bits, cudaStream_t stream);
+
+/*
+ * PA_DEVERR_TIMEOUT: every wait inside a kernel (on the arrival of its own TMA
+ * copies or tensor-core results) gives up after 2 s of wall time instead of
+ * spinning forever; the kernel then stops, lets its copies in flight land and
+ * returns, and the CUDA context stays usable. On a healthy GPU these waits
+ * last microseconds, so the bit means the GPU was starved (time-sliced with
+ * other work, preempted for seconds) or faulty. The outputs of the launches
+ * that ran since the last read of the error word are then undefined; nothing
+ * else is: the attention calls only read the caches, and a copy or cache write
+ * that stopped early wrote some of its rows. Re-issuing the same calls on the
+ * same inputs recomputes them (cache writes and copies are idempotent for a
+ * well-formed slot mapping and pair list).
+ */
 
 /*
  * pa_get_error without the bits: waits for `stream`, reads and clears the
