@@ -160,14 +160,14 @@ __host__ __device__ inline unsigned round_up(unsigned x, unsigned a) { return (x
 
 // Shared-memory map, computed identically on the host (launch size) and device.
 __host__ __device__ inline SmemLayout make_layout(int W, int R, int D, int esize, int qsize, int group, int path,
-                                                  bool split, int S) {
+                                                  bool split, int S, int jps = 1) {
   SmemLayout L;
-  L.stage_bytes = 2u * kJobTokens * D * esize;
+  L.stage_bytes = jps * 2u * kJobTokens * D * esize;  // jps jobs of K and V tiles
   unsigned off = W * R * L.stage_bytes;
   L.bars_off = off;
   off += W * R * 16;  // per stage: K barrier, V barrier
   L.ok_off = off;
-  off = round_up(off + W * R, 16);
+  off = round_up(off + W * R * jps, 16);  // per job: its block id was in the pool
   L.merge_off = off;
   if (!split) off += W * merge_heads(group, path) * D * 4 + W * kMaxGroup * 2 * 4;
   L.q_off = off;
@@ -187,17 +187,26 @@ __host__ __device__ inline SmemLayout make_layout(int W, int R, int D, int esize
   return L;
 }
 
-template <typename DT, int D, int PATH>
+template <typename DT, int D, int PATH, int MODE = kModePlain>
 struct StageCfg {
   static constexpr int E = sizeof(DT);
   static constexpr int TILE = kJobTokens * D * E;  // one K (or V) job tile
-  static constexpr int kStage = 2 * TILE;
+  static constexpr int kJob = 2 * TILE;            // K and V of one job
   static constexpr int W = 4;
+  // Tensor-core steps of two jobs each (see the kernel): E4M3 in every mode,
+  // 16-bit data in plain mode at head_dim <= 128.
+  static constexpr bool PAIRED = is_mma_path(PATH) && D <= 128 && (E == 1 || MODE == kModePlain);
+  // Jobs of 4 KiB (E4M3 at head_dim 128, 16-bit data at 64) taken two per step
+  // also travel two per stage: one barrier, one wait and one refill for both.
+  // A copy-only build of the one-job-per-stage schedule topped out at 0.87-0.92
+  // of the copy peak with such jobs (0.998 with 8 KiB jobs): per-job overheads.
+  static constexpr int JPS = PAIRED && kJob <= 4096 ? 2 : 1;
   // The MHA path is bound by instruction latency with 2 CTAs per SM: two 8 KiB
   // stages per warp let 3 CTAs fit (50% more warps, the same bytes in flight).
   // head_dim 256 makes a job 16 KiB (16-bit) or 32 KiB (fp32): one stage per
-  // warp, so that two CTAs (eight warps) share an SM instead of one.
-  static constexpr int R = D > 128 ? 1 : (kStage <= 4096 ? 4 : (PATH == kPathVecMha ? 2 : 3));
+  // warp, so that two CTAs (eight warps) share an SM instead of one. Four 4 KiB
+  // jobs per warp: four stages, or two stages of two jobs.
+  static constexpr int R = (D > 128 ? 1 : (kJob <= 4096 ? 4 : (PATH == kPathVecMha ? 2 : 3))) / JPS;
   // Minimum CTAs per SM for the register allocator (0: unspecified). The E4M3
   // tensor-core kernels fit 3 CTAs per SM by shared memory; saying so gives them
   // the registers of that occupancy (left alone, the compiler settles for 128
@@ -308,11 +317,11 @@ struct Schedule {
 // DT: cache element type (float, __half, __nv_bfloat16 or fp8e4m3); QT: query
 // type (DT, or a 16-bit type over an FP8 cache); OT: output type.
 template <typename DT, typename QT, typename OT, int D, int PATH, int MODE>
-__global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D, PATH>::MINB)
+__global__ void __launch_bounds__(StageCfg<DT, D, PATH, MODE>::W * 32, StageCfg<DT, D, PATH, MODE>::MINB)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         const DecodeParams p) {
   pdl_begin();
-  using Cfg = StageCfg<DT, D, PATH>;
+  using Cfg = StageCfg<DT, D, PATH, MODE>;
   constexpr bool MMA = is_mma_path(PATH);
   constexpr bool ROUNDS = PATH == kPathMmaG8;  // plain mode, groups of 5-8: merge four heads per round
   static_assert(!ROUNDS || MODE == kModePlain, "only plain mode merges inside the CTA");
@@ -327,6 +336,8 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
   // +6-10% at head_dim 64 (A/B on one GPU); 16-bit split decode and the suffix
   // pass gained nothing (0.942 vs 0.945; within 1%) and keep one job per step.
   constexpr bool PAIR = F8 || (MMA && D <= 128 && MODE == kModePlain);
+  static_assert(PAIR == Cfg::PAIRED, "the stage configuration follows the step");
+  constexpr int JPS = Cfg::JPS;  // jobs per stage
   // stale running max (see kLazyTau): plain mode, and E4M3 split mode (+2.8%
   // there; 16-bit split decode measured 6% slower with it)
   constexpr bool LAZY = MODE == kModePlain || (F8 && MODE == kModeSplit);
@@ -343,7 +354,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
   // head_dim-256 vector path).
   constexpr bool TWO_BARS = MMA && !PAIR;
   static_assert(!KV_SPLIT || TWO_BARS, "a split refill needs a barrier per half");
-  static_assert(!PAIR || StageCfg<DT, D, PATH>::R >= 2, "two jobs per step need two stages");
+  static_assert(!PAIR || Cfg::R * JPS >= 2, "two jobs per step need two staged jobs");
   using MT = typename std::conditional<F8, __half, DT>::type;  // tensor-core operand type
   static_assert(!F8 || D % 64 == 0, "FP8 caches need head_dim a multiple of 64");
   constexpr int W = Cfg::W, R = Cfg::R, E = Cfg::E, TILE = Cfg::TILE, JT = kJobTokens;
@@ -356,9 +367,9 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
   extern __shared__ uint8_t smem_raw[];
   // TMA 128-byte swizzling needs 1024-byte aligned destinations: align the shared-window offset.
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const SmemLayout L = make_layout(W, R, D, E, (int)sizeof(QT), p.group, PATH, SPLIT, p.S);
+  const SmemLayout L = make_layout(W, R, D, E, (int)sizeof(QT), p.group, PATH, SPLIT, p.S, JPS);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars_off);
-  volatile uint8_t* stage_ok = smem + L.ok_off;                        // [W][R]
+  volatile uint8_t* stage_ok = smem + L.ok_off;                        // [W][R][JPS]
   const int MH = merge_heads(p.group, PATH);                           // heads per merge round
   float* mrg_o = reinterpret_cast<float*>(smem + L.merge_off);        // [W][MH][D] (plain mode)
   float* mrg_ml = mrg_o + W * MH * D;                                  // [W][kMaxGroup][2]
@@ -508,7 +519,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
   // ---- per-warp issue cursor over this warp's jobs ---------------------------
   uint8_t* my_stages = smem + warp * R * L.stage_bytes;
   uint64_t* my_bars = bars + warp * 2 * R;  // [0, R): K tiles, [R, 2R): V tiles
-  volatile uint8_t* my_ok = stage_ok + warp * R;
+  volatile uint8_t* my_ok = stage_ok + warp * R * JPS;
   // split mode: each warp owns whole partitions; suffix mode: each warp owns items
   constexpr bool WARP_PARTS = SPLIT || SUFFIX;
   // A warp that streams its own partition also asks L2 for the K and V tiles of
@@ -523,9 +534,10 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
   struct Cursor {
     int k, u, ue;
     long long phys;  // block-table entry of job u, loaded one job ahead of its issue
+    long long phys2; // JPS == 2: block-table entry of the warp's next job in the item (if has2)
     long long pf;    // PREFETCH: block-table entry of job u + PF_AHEAD in the same item, or -1
     Item it;
-    bool valid;
+    bool valid, has2;
   };
   auto cursor_range = [&](Cursor& c) {
     c.u = c.it.t0 / JT + (WARP_PARTS ? 0 : warp);
@@ -540,6 +552,11 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
     if (c.valid) {
       const int32_t* table = p.block_tables + (long long)c.it.s * p.max_blocks;
       c.phys = __ldg(table + ((c.u * JT) >> p.block_shift));
+      if constexpr (JPS == 2) {
+        const int u2 = c.u + job_step;
+        c.has2 = u2 < c.ue;
+        c.phys2 = c.has2 ? (long long)__ldg(table + ((u2 * JT) >> p.block_shift)) : -1;
+      }
       if constexpr (PREFETCH) {
         const int uf = c.u + PF_AHEAD;
         c.pf = !p.nhd && uf < c.ue ? (long long)__ldg(table + ((uf * JT) >> p.block_shift)) : -1;
@@ -603,15 +620,61 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
     }
   };
 
+  // JPS == 2: stage n % R takes the cursor's job and, when the item has one, the
+  // warp's next job (so an item's jobs pair up from its first one, as the
+  // consumer takes them); one barrier counts both. The cursor moves past both.
+  auto issue2 = [&](Cursor& c, int n) {
+    const int stage = n % R;
+    if (lane == 0) {
+      uint64_t* bar = &my_bars[stage];
+      uint8_t* base = my_stages + stage * L.stage_bytes;
+      const long long ph[2] = {c.phys, c.phys2};
+      bool ok[2];
+      unsigned bytes = 0;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const bool real = j == 0 || c.has2;
+        ok[j] = real && ph[j] >= 0 && ph[j] < p.num_blocks;
+        if (real && !ok[j]) atomicOr(p.err, kErrBlockId);  // skipped; the consumer skips the job
+        my_ok[stage * 2 + j] = ok[j] ? 1 : 0;
+        bytes += ok[j] ? 2u * TILE : 0u;
+      }
+      fence_proxy_async_smem();
+      if (bytes == 0) {
+        mbar_arrive(bar);  // complete the phase with no data
+      } else {
+        mbar_arrive_expect_tx(bar, bytes);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          if (!ok[j]) continue;
+          const int tok = (c.u + j * job_step) * JT;
+          const int r0 = tok - ((tok >> p.block_shift) << p.block_shift);
+          uint8_t* kdst = base + j * 2 * TILE;
+#pragma unroll
+          for (int rg = 0; rg < NREG; ++rg) {
+            tma_load_tile(kdst + rg * JT * 128, &kmap, p, rg * BOX_X, ph[j], c.it.kv, r0, bar);
+            tma_load_tile(kdst + TILE + rg * JT * 128, &vmap, p, rg * BOX_X, ph[j], c.it.kv, r0, bar);
+          }
+        }
+      }
+    }
+    c.u += (c.has2 ? 2 : 1) * job_step;
+    cursor_settle(c);
+  };
+
   fence_proxy_async_smem();  // generic writes to stage memory (sort counters) before TMA reuses it
   __syncthreads();            // barrier inits and schedule tables visible; stage memory free again
 
   int n_issue = 0;
 #pragma unroll 1
   for (int r = 0; r < R && ic.valid; ++r) {
-    issue(ic, n_issue++, kPartK | kPartV);
-    ic.u += job_step;
-    cursor_settle(ic);
+    if constexpr (JPS == 2) {
+      issue2(ic, n_issue++);
+    } else {
+      issue(ic, n_issue++, kPartK | kPartV);
+      ic.u += job_step;
+      cursor_settle(ic);
+    }
   }
 
   // ---- consume -----------------------------------------------------------------
@@ -660,9 +723,13 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
         }
       }
     } else if (ic.valid && !*abort_flag) {
-      issue(ic, n_issue++, kPartK | kPartV);
-      ic.u += job_step;
-      cursor_settle(ic);
+      if constexpr (JPS == 2) {
+        issue2(ic, n_issue++);
+      } else {
+        issue(ic, n_issue++, kPartK | kPartV);
+        ic.u += job_step;
+        cursor_settle(ic);
+      }
     }
   };
   // Plain mode: merge the W warps' partials of heads h0 .. h0 + MH - 1 of the
@@ -927,10 +994,22 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
         for (int u = ub; u < ue; u += 2 * job_step) {
           const bool two = u + job_step < ue;
           int sa = 0, sb = 0;
-          const bool oka = next_job(sa, 0);
-          const bool okb = two && next_job(sb, 1);
-          const uint8_t* ka = my_stages + sa * L.stage_bytes;
-          const uint8_t* kb = my_stages + sb * L.stage_bytes;
+          bool oka, okb;
+          const uint8_t *ka, *kb;
+          if constexpr (JPS == 2) {  // both jobs in one stage, behind one barrier
+            sa = n_done % R;
+            bool ok = mbar_wait_bounded(&my_bars[sa], (n_done / R) & 1, abort_flag, p.err, kWaitLimitNs);
+            ok = __all_sync(0xffffffffu, ok);
+            oka = ok && my_ok[sa * 2];
+            okb = ok && two && my_ok[sa * 2 + 1];
+            ka = my_stages + sa * L.stage_bytes;
+            kb = ka + 2 * TILE;
+          } else {
+            oka = next_job(sa, 0);
+            okb = two && next_job(sb, 1);
+            ka = my_stages + sa * L.stage_bytes;
+            kb = my_stages + sb * L.stage_bytes;
+          }
           const int nva = min(JT, it.t1 - u * JT), nvb = min(JT, it.t1 - (u + job_step) * JT);
           float z[2][4];
 #pragma unroll
@@ -943,7 +1022,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH>::W * 32, StageCfg<DT, D,
             if (okb) job_pv(kb, nvb, z[1]);
           }
           job_done();
-          if (two) job_done();
+          if (JPS == 1 && two) job_done();
         }
       } else {
 #pragma unroll 1

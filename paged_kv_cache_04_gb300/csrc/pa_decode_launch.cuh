@@ -11,10 +11,10 @@ namespace pa {
 template <typename DT, typename QT, typename OT, int D, int PATH, int MODE>
 pa_status launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                         int num_sms, long long max_items, cudaStream_t stream) {
-  using Cfg = StageCfg<DT, D, PATH>;
+  using Cfg = StageCfg<DT, D, PATH, MODE>;
   auto kern = paged_decode_kernel<DT, QT, OT, D, PATH, MODE>;
   const SmemLayout L =
-      make_layout(Cfg::W, Cfg::R, D, Cfg::E, (int)sizeof(QT), p.group, PATH, MODE == kModeSplit, p.S);
+      make_layout(Cfg::W, Cfg::R, D, Cfg::E, (int)sizeof(QT), p.group, PATH, MODE == kModeSplit, p.S, Cfg::JPS);
   if (L.total > 227u * 1024u) return PA_ERR_UNSUPPORTED;
 
   // Opt in to the dynamic shared memory once per device, and remember the

@@ -24,10 +24,14 @@ PROGRAM = r"""
 #include "pa_decode.cuh"
 #include "pa_cascade_tc.cuh"
 using namespace pa;
+template <typename C, typename QT, int D, int PATH>
+SmemLayout layout_of(int group, int split, int S) {
+  return make_layout(C::W, C::R, D, C::E, (int)sizeof(QT), group, PATH, split != 0, S, C::JPS);
+}
 template <typename DT, typename QT, int D, int PATH>
 void row(const char* name, int group, int split, int S) {
-  using C = StageCfg<DT, D, PATH>;
-  const SmemLayout L = make_layout(C::W, C::R, D, C::E, (int)sizeof(QT), group, PATH, split != 0, S);
+  const SmemLayout L = split ? layout_of<StageCfg<DT, D, PATH, kModeSplit>, QT, D, PATH>(group, 1, S)
+                             : layout_of<StageCfg<DT, D, PATH, kModePlain>, QT, D, PATH>(group, 0, S);
   printf("%s %d %d %d %u\n", name, group, split, S, L.total);
 }
 int main() {
