@@ -86,6 +86,25 @@ pa_status make_pool_map(CUtensorMap* map, const void* base, pa_dtype dt, int D, 
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
+// The TMA view of q [S][H][D] (16-bit) for the tcgen05 prefix pass: one box is
+// 64 columns of `group` consecutive heads (one kv head's queries) of
+// `members` consecutive sequences, rows in (sequence, head) order, 128-byte
+// swizzle; rows past the batch read as zeros.
+pa_status make_q_map(CUtensorMap* map, const void* q, pa_dtype dt, int D, int H, int S, int group, int members) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+  pa_status st = encoder(&enc);
+  if (st != PA_OK) return st;
+  if (members < 1 || members > 256 || group < 1 || group > 256) return PA_ERR_UNSUPPORTED;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)group, (cuuint32_t)members};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, dt == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                   const_cast<void*>(q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
 struct DecodeArgs {
   void* out;
   const void* q;
@@ -267,20 +286,24 @@ pa_status run_decode(const DecodeArgs& a, bool split, int partition, int max_par
       // tile still beats the mma.sync pass (3-3.5% per step on 64 prompts x 8
       // samples, measured).
       const bool bf = a.dt == PA_BF16;
+      CUtensorMap qm;
+      if (c.rows > 16 &&
+          (s = make_q_map(&qm, a.q, a.dt, a.D, a.H, a.S, p.group, (c.rows > 64 ? 128 : 64) / p.group)) != PA_OK)
+        return s;
       if (c.rows > 64) {
         if (a.D == 128)
-          s = bf ? launch_cascade_prefix_tc<__nv_bfloat16, 128, 128>(km, vsw, p, sms, pitems, st)
-                 : launch_cascade_prefix_tc<__half, 128, 128>(km, vsw, p, sms, pitems, st);
+          s = bf ? launch_cascade_prefix_tc<__nv_bfloat16, 128, 128>(km, vsw, qm, p, sms, pitems, st)
+                 : launch_cascade_prefix_tc<__half, 128, 128>(km, vsw, qm, p, sms, pitems, st);
         else
-          s = bf ? launch_cascade_prefix_tc<__nv_bfloat16, 64, 128>(km, vsw, p, sms, pitems, st)
-                 : launch_cascade_prefix_tc<__half, 64, 128>(km, vsw, p, sms, pitems, st);
+          s = bf ? launch_cascade_prefix_tc<__nv_bfloat16, 64, 128>(km, vsw, qm, p, sms, pitems, st)
+                 : launch_cascade_prefix_tc<__half, 64, 128>(km, vsw, qm, p, sms, pitems, st);
       } else if (c.rows > 16) {
         if (a.D == 128)
-          s = bf ? launch_cascade_prefix_tc<__nv_bfloat16, 128, 64>(km, vsw, p, sms, pitems, st)
-                 : launch_cascade_prefix_tc<__half, 128, 64>(km, vsw, p, sms, pitems, st);
+          s = bf ? launch_cascade_prefix_tc<__nv_bfloat16, 128, 64>(km, vsw, qm, p, sms, pitems, st)
+                 : launch_cascade_prefix_tc<__half, 128, 64>(km, vsw, qm, p, sms, pitems, st);
         else
-          s = bf ? launch_cascade_prefix_tc<__nv_bfloat16, 64, 64>(km, vsw, p, sms, pitems, st)
-                 : launch_cascade_prefix_tc<__half, 64, 64>(km, vsw, p, sms, pitems, st);
+          s = bf ? launch_cascade_prefix_tc<__nv_bfloat16, 64, 64>(km, vsw, qm, p, sms, pitems, st)
+                 : launch_cascade_prefix_tc<__half, 64, 64>(km, vsw, qm, p, sms, pitems, st);
       } else if (a.D == 128) {
         s = bf ? launch_cascade_prefix<__nv_bfloat16, 128, 1>(km, vsw, p, sms, pitems, st)
                : launch_cascade_prefix<__half, 128, 1>(km, vsw, p, sms, pitems, st);

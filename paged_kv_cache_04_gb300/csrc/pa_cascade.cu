@@ -51,8 +51,8 @@ pa_status launch_cascade_prefix(const CUtensorMap& kmap, const CUtensorMap& vmap
 }
 
 template <typename DT, int D, int MR>
-pa_status launch_cascade_prefix_tc(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
-                                   int num_sms, long long max_items, cudaStream_t stream) {
+pa_status launch_cascade_prefix_tc(const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& qmap,
+                                   const DecodeParams& p, int num_sms, long long max_items, cudaStream_t stream) {
   auto kern = cascade_prefix_tc_kernel<DT, D, MR>;
   const TcLayout L = tc_layout(D, p.num_groups, MR);
   if (L.total > 227u * 1024u) return PA_ERR_UNSUPPORTED;
@@ -88,14 +88,16 @@ pa_status launch_cascade_prefix_tc(const CUtensorMap& kmap, const CUtensorMap& v
   long long grid = (long long)num_sms * per_sm;
   if (max_items < grid) grid = max_items;
   if (grid <= 0) return PA_OK;
-  return launch_pdl(kern, dim3((unsigned)grid), dim3(kTcThreads), L.total, stream, kmap, vmap, p) == cudaSuccess
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(kTcThreads), L.total, stream, kmap, vmap, qmap, p) ==
+                 cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
 }
 
 #define PA_INSTANTIATE_CASCADE_TC(DT, D, MR)                                                                \
   template pa_status launch_cascade_prefix_tc<DT, D, MR>(const CUtensorMap&, const CUtensorMap&,               \
-                                                         const DecodeParams&, int, long long, cudaStream_t);
+                                                         const CUtensorMap&, const DecodeParams&, int, long long, \
+                                                         cudaStream_t);
 PA_INSTANTIATE_CASCADE_TC(__nv_bfloat16, 128, 64)
 PA_INSTANTIATE_CASCADE_TC(__nv_bfloat16, 128, 128)
 PA_INSTANTIATE_CASCADE_TC(__nv_bfloat16, 64, 64)

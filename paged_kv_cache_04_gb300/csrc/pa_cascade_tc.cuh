@@ -15,19 +15,23 @@
 //              threads t and t + 16 take its two column halves; M = 128:
 //              thread t of warp w owns row 32 w + t, in that lane); it reads
 //              its part of S, keeps the running (max, sum), writes its part of
-//              P (16-bit hi + lo parts) to shared memory and, at the end of an
+//              P (16-bit hi + lo parts) to tensor memory and, at the end of an
 //              item, reads its part of O;
 //   warp 4     TMA producer: two 16-token jobs per stage (K and V, 128-byte
-//              swizzle), a ring of five stages (three for M = 128);
+//              swizzle), a ring of five stages (four for M = 128);
 //   warp 5     owns the tensor memory (allocation, release); its lane 0 issues
-//              the score MMAs and commits them to mbarriers;
+//              the score MMAs and commits them to mbarriers, and loads an
+//              item's Q tile by TMA as soon as the last item's score MMAs have
+//              completed (so the tile is there before the softmax warps are
+//              done with the last item);
 //   warp 6     its lane 0 issues the P V MMAs and commits them.
-// S is double-buffered in tensor memory, so the scores of a tile are computed
-// while the softmax warps work on the one before; the softmax computes a
-// tile's weights before it waits for the last P V to release the P buffer.
-// (Shared memory goes to stages: with a per-stage life of several thousand
-// cycles, five stages measured faster than four with a second P buffer, or
-// three with a second Q tile.) The accumulator O is rescaled
+// S and P are double-buffered in tensor memory: the scores of a tile are
+// computed while the softmax warps work on the one before, and the softmax
+// writes a tile's weights while the P V of the one before runs. P is the A
+// operand of P V straight from tensor memory (a row of P sits in the lane of
+// its accumulator row, two 16-bit weights per column: checked on the GB300
+// against the same product with P in shared memory), so it costs no shared
+// memory and no proxy fence; shared memory goes to stages. The accumulator O is rescaled
 // lazily: a row's reference max moves only when a score exceeds it by more
 // than kTcRescale (log2 units); weights then stay below 2^kTcRescale and the
 // result is the same softmax (numerator and denominator share the reference).
@@ -42,26 +46,24 @@ namespace pa {
 constexpr int kTcMaxRows = 128;    // query rows of one group (members x heads) the pass takes
 constexpr int kTcTokens = 32;      // N of S, K of P V: tokens per stage (two TMA jobs)
 // M of the tiles is 64 (groups of 17-64 query rows) or 128 (65-128); the
-// larger Q tile of M = 128 leaves room for three stages instead of five.
-__host__ __device__ constexpr int tc_stages(int MR) { return MR == 64 ? 5 : 3; }
+// larger Q tile of M = 128 leaves room for four stages instead of five.
+__host__ __device__ constexpr int tc_stages(int MR) { return MR == 64 ? 5 : 4; }
 constexpr int kTcThreads = 224;
 constexpr float kTcRescale = 8.f;
 
 struct TcLayout {
-  unsigned q_bytes, stage_off, stage_bytes, p_off, bar_off, misc_off, sched_off, total;
+  unsigned q_bytes, stage_off, stage_bytes, bar_off, misc_off, sched_off, total;
 };
 
 // Offsets from the 1024-byte aligned base: the Q tile, the stages (K then V,
-// each [head_dim / 64 regions][32 tokens][128 B]), the P buffer ([M rows]
-// [128 B]: a row's 32 hi weights, then its 32 lo weights), mbarriers, the
+// each [head_dim / 64 regions][32 tokens][128 B]), mbarriers, the
 // tensor-memory base, the abort flag, per-stage job flags and the group scan.
 __host__ __device__ inline TcLayout tc_layout(int D, int num_groups, int MR) {
   TcLayout L;
   L.q_bytes = MR * D * 2;
   L.stage_off = L.q_bytes;
   L.stage_bytes = 2u * kTcTokens * D * 2;
-  L.p_off = L.stage_off + tc_stages(MR) * L.stage_bytes;
-  L.bar_off = L.p_off + MR * 128;
+  L.bar_off = L.stage_off + tc_stages(MR) * L.stage_bytes;
   L.misc_off = L.bar_off + (2 * tc_stages(MR) + 13) * 8;
   L.sched_off = round_up(L.misc_off + 16, 16);
   L.total = round_up(L.sched_off + (num_groups + 1) * 4, 16) + 1024;
@@ -102,6 +104,17 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, 
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+
+// The same with A in tensor memory at a_tmem: row m of A in the lane that holds
+// row m of an M-row accumulator, K elements two to a 32-bit column.
+__device__ __forceinline__ void tc_mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                              bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"((uint32_t)accumulate)
       : "memory");
 }
 
@@ -213,7 +226,7 @@ __device__ __forceinline__ void tma_load_zero_tile(void* dst, const CUtensorMap*
 template <typename DT, int D, int MR>
 __global__ void __launch_bounds__(kTcThreads, 2)
     cascade_prefix_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                             const DecodeParams p) {
+                             const __grid_constant__ CUtensorMap qmap, const DecodeParams p) {
   pdl_begin();
   static_assert(sizeof(DT) == 2 && (D == 64 || D == 128), "tensor-core prefix pass: 16-bit caches, head_dim 64/128");
   static_assert(MR == 64 || MR == 128, "tiles of 64 or 128 query rows");
@@ -222,8 +235,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   constexpr int TILE = NT * D * 2;        // K (or V) bytes of one stage
   constexpr int REG_BYTES = NT * 128;     // one region of a stage's K (or V): [32 tokens][128 B]
   constexpr int KSTEPS = D / 16;
-  constexpr uint32_t TCOLS = D + 2 * NT <= 128 ? 128u : 256u;  // O (D columns) + two S buffers
-  constexpr uint32_t O_COL = 0, S_COL = D;
+  // tensor-memory columns: O (D), two S buffers (NT each), two P buffers (NT each:
+  // a row's NT hi and NT lo weights, two to a column)
+  constexpr uint32_t TCOLS = 256u;
+  constexpr uint32_t O_COL = 0, S_COL = D, P_COL = D + 2 * NT;
+  static_assert(P_COL + 2 * NT <= TCOLS, "tensor-memory columns");
   constexpr uint32_t ID_S = tc_idesc<DT>(M, NT, false);
   constexpr uint32_t ID_PV = tc_idesc<DT>(M, D, true);
 
@@ -235,9 +251,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   uint64_t* empty = bars + R;         // [R] MMA (P V done) -> TMA
   uint64_t* s_full = bars + 2 * R;    // [2] S written -> softmax
   uint64_t* s_free = s_full + 2;      // [2] S read -> MMA
-  uint64_t* q_full = s_full + 4;      // [0]: the item's Q tile written -> MMA ([1] unused)
-  uint64_t* p_full = s_full + 6;      // [0]: P written -> MMA ([1] unused)
-  uint64_t* pv_done = s_full + 8;     // [0]: P V done -> softmax (P free, O current; [1] unused)
+  uint64_t* q_full = s_full + 4;      // the item's Q tile landed -> score MMAs
+  uint64_t* q_free = s_full + 5;      // the last item's score MMAs done -> Q tile reloaded
+  uint64_t* p_full = s_full + 6;      // [2] P written -> MMA
+  uint64_t* pv_done = s_full + 8;     // [2] P V done -> softmax (that P buffer free, O current)
   uint64_t* o_free = s_full + 10;     // O read at the end of an item -> MMA
   uint64_t* fin = s_full + 11;        // every score MMA done (teardown)
   uint64_t* fin_pv = s_full + 12;     // every P V MMA done (teardown)
@@ -257,7 +274,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
       mbar_init(&s_free[b], 4);
-      mbar_init(&q_full[b], 4);
+      mbar_init(&q_full[b], 1);  // q_full, q_free
       mbar_init(&p_full[b], 4);
       mbar_init(&pv_done[b], 1);
     }
@@ -270,7 +287,14 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   if (threadIdx.x == 32) {
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
+    prefetch_tensormap(&qmap);
   }
+  // Q rows past the box (group x (M / group) rows) stay zero; the box rows past
+  // the group's members hold other sequences' queries (or zeros past the batch):
+  // those rows' scores and outputs are computed and never written
+  for (int i = threadIdx.x; i < (int)(L.q_bytes / 16); i += kTcThreads)
+    reinterpret_cast<uint4*>(smem)[i] = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
   if (warp == 5) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                  "r"(TCOLS)
@@ -330,7 +354,6 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   auto num_tiles = [&](const PItem& it) { return ((it.t1 - it.t0 + JT - 1) / JT + 1) / 2; };
   const uint32_t q_base = smem_u32(smem);
   const uint32_t st_base = smem_u32(smem + L.stage_off);
-  const uint32_t p_base = smem_u32(smem + L.p_off);
 
   if (warp == 4) {
     // ------------------------------- producer -------------------------------
@@ -415,8 +438,22 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       PItem it;
       if (warp == 5) {
         const uint64_t qdesc = tc_desc(q_base, 16, 1024);  // built once; the MMAs add offsets
-        for (int k = 0; get(k, it); ++k) {
-          if (!mbar_wait_sleep(&q_full[0], k & 1, abort_flag, p.err, kWaitLimitNs)) break;
+        // an item's Q tile: rows member x group + head, from a box of (M / group)
+        // sequences x group heads of its kv head, one box per 64 columns
+        const int qrows = p.group * (M / p.group);
+        int q_loads = 0, q_landed = 0;  // Q copies issued, and waited for
+        auto load_q = [&](const PItem& x) {
+          ++q_loads;
+          mbar_arrive_expect_tx(q_full, (uint32_t)(qrows * D * 2));
+#pragma unroll
+          for (int rg = 0; rg < NREG; ++rg)
+            tma_load_3d(smem + rg * (M * 128), &qmap, rg * 64, x.kv * p.group, x.s0, q_full);
+        };
+        bool have = get(0, it);
+        if (have) load_q(it);
+        for (int k = 0; have; ++k) {
+          if (!mbar_wait_sleep(q_full, k & 1, abort_flag, p.err, kWaitLimitNs)) break;
+          ++q_landed;
           const int nt = num_tiles(it);
           bool stop = false;
           for (int i = 0; i < nt; ++i, ++n) {
@@ -438,32 +475,44 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             issued = true;
           }
           if (stop) break;
+          PItem nx;
+          const bool have_next = get(k + 1, nx);
+          if (have_next) {  // the next item's Q, once this item's score MMAs have read the tile
+            tc_commit(q_free);
+            if (!mbar_wait_sleep(q_free, k & 1, abort_flag, p.err, kWaitLimitNs)) break;
+            load_q(nx);
+          }
+          have = have_next;
+          it = nx;
         }
+        if (q_loads > q_landed)  // a Q copy still in flight after an abort lands before the block exits
+          mbar_wait_bounded(q_full, (q_loads - 1) & 1, nullptr, p.err, kDrainLimitNs);
       } else {
-        const uint64_t pdesc = tc_desc(p_base, 16, 1024);
         for (int k = 0; get(k, it); ++k) {
           const int nt = num_tiles(it);
           bool stop = false;
           for (int i = 0; i < nt; ++i, ++n) {
             // the item's first tile overwrites O, once the softmax has read the last item's O
             const bool first = i == 0;
-            if (!mbar_wait_sleep(&p_full[0], n & 1, abort_flag, p.err, kWaitLimitNs) ||
+            const int pb = n & 1;
+            if (!mbar_wait_sleep(&p_full[pb], (n >> 1) & 1, abort_flag, p.err, kWaitLimitNs) ||
                 (first && k > 0 && !mbar_wait_sleep(o_free, (k - 1) & 1, abort_flag, p.err, kWaitLimitNs))) {
               stop = true;
               break;
             }
             tc_fence_after();
             const uint64_t vdesc = tc_desc(st_base + (n % R) * L.stage_bytes + TILE, REG_BYTES, 1024);
+            // P buffer pb: columns 16 ks .. 16 ks + 7 hold the hi weights of tokens
+            // 16 ks .. 16 ks + 15, the next 8 columns their lo weights
 #pragma unroll
-            for (int part = 0; part < 2; ++part) {  // hi weights (K columns 0-31), then lo (32-63)
+            for (int ks = 0; ks < NT / 16; ++ks) {
+              const uint64_t b = tc_desc_add(vdesc, ks * 2048);
 #pragma unroll
-              for (int ks = 0; ks < NT / 16; ++ks) {
-                const uint64_t a = tc_desc_add(pdesc, (part * (NT / 16) + ks) * 32);
-                const uint64_t b = tc_desc_add(vdesc, ks * 2048);
-                tc_mma(tbase + O_COL, a, b, ID_PV, !(first && part == 0 && ks == 0));
-              }
+              for (int part = 0; part < 2; ++part)
+                tc_mma_tmem_a(tbase + O_COL, tbase + P_COL + pb * NT + ks * 16 + part * 8, b, ID_PV,
+                              !(first && part == 0 && ks == 0));
             }
-            tc_commit(&pv_done[0]);
+            tc_commit(&pv_done[pb]);
             tc_commit(&empty[n % R]);
             issued = true;
           }
@@ -492,30 +541,6 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     const int half = HALF ? lane >> 4 : 0;
     const int row = HALF ? 16 * warp + (lane & 15) : 32 * warp + lane;
     const uint32_t lane_addr = tbase + ((uint32_t)(32 * warp) << 16);
-    // Q of an item into the Q tile: row r = member r / group, head r % group, by
-    // cp.async (padding rows are zero); 128 threads, 16-byte chunks, 128-byte
-    // swizzle. finish_q waits for the copies and hands the tile to the MMA.
-    auto issue_q = [&](const PItem& x, int buf) {
-      uint8_t* q = smem + buf * L.q_bytes;
-      const int rows = x.members * p.group;
-      constexpr int CPR = D / 8;  // 16-byte chunks per row
-      for (int c = threadIdx.x; c < M * CPR; c += 128) {
-        const int r = c / CPR, ch = c % CPR;
-        uint8_t* dst = q + (ch >> 3) * (M * 128) + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
-        if (r < rows)
-          cp_async16(dst, reinterpret_cast<const DT*>(p.q) +
-                              ((long long)(x.s0 + r / p.group) * p.H + x.kv * p.group + r % p.group) * D + ch * 8);
-        else
-          *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-      }
-      cp_async_commit();
-    };
-    auto finish_q = [&](int buf) {
-      cp_async_wait_all();
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&q_full[buf]);
-    };
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
       const bool ok = mbar_wait_bounded(bar, parity, abort_flag, p.err, kWaitLimitNs);
       return __all_sync(0xffffffffu, ok);
@@ -523,10 +548,6 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     int n = 0;
     PItem it, nx;
     bool have = get(0, it);
-    if (have) {
-      issue_q(it, 0);
-      finish_q(0);
-    }
     for (int k = 0; have; ++k) {
       const bool have_next = get(k + 1, nx);
       const int rows = it.members * p.group;
@@ -593,13 +614,18 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           lw[e] = Mma<DT>::pack(w0 - r0, w1 - r1);
         }
         l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-        // P (and O, for a rescale) are free once the P V of tile n - 1 has completed
-        const int pb = 0;
-        if (n >= 1 && !wait_all(&pv_done[0], (n - 1) & 1)) {
+        // P buffer pb is free once the P V of tile n - 2 has completed; O is current
+        // (for a rescale) once that of tile n - 1 has
+        const int pb = n & 1;
+        if (n >= 2 && !wait_all(&pv_done[pb], ((n - 2) >> 1) & 1)) {
           stop = true;
           break;
         }
         if (i > 0 && __any_sync(0xffffffffu, move)) {
+          if (!wait_all(&pv_done[pb ^ 1], ((n - 1) >> 1) & 1)) {
+            stop = true;
+            break;
+          }
           tc_fence_after();
           if constexpr (HALF) {  // thread t: columns [0, D/2) of its row, thread t + 16: [D/2, D)
 #pragma unroll 1
@@ -621,27 +647,36 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             }
           }
         }
-        {  // chunks 0-3: hi weights of tokens 8 ch .. 8 ch + 7; chunks 4-7: lo (this thread's chunks)
-          uint8_t* pr = smem + L.p_off + pb * (M * 128) + row * 128;
+        // P into buffer pb: per 16 tokens, 8 columns of hi weights then 8 of lo (M = 64:
+        // thread t the first 16 columns of its row, thread t + 16 the next 16)
+        tc_fence_after();
+        if constexpr (HALF) {
+          uint32_t pw[16];
 #pragma unroll
-          for (int cc = 0; cc < CW / 8; ++cc) {
-            const int ch = half * (CW / 8) + cc;
-            *reinterpret_cast<uint4*>(pr + ((ch ^ (row & 7)) << 4)) =
-                make_uint4(hw[4 * cc], hw[4 * cc + 1], hw[4 * cc + 2], hw[4 * cc + 3]);
-            *reinterpret_cast<uint4*>(pr + (((ch + 4) ^ (row & 7)) << 4)) =
-                make_uint4(lw[4 * cc], lw[4 * cc + 1], lw[4 * cc + 2], lw[4 * cc + 3]);
+          for (int e = 0; e < 8; ++e) {
+            pw[e] = hw[e];
+            pw[8 + e] = lw[e];
           }
+          tc_st16x2<16>(lane_addr + P_COL + pb * NT, pw);
+        } else {
+          uint32_t pw[32];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            pw[e] = hw[e];
+            pw[8 + e] = lw[e];
+            pw[16 + e] = hw[8 + e];
+            pw[24 + e] = lw[8 + e];
+          }
+          tc_st32(lane_addr + P_COL + pb * NT, pw);
         }
-        fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[pb]);
       }
       if (stop) break;
       // the item's last P V, then this thread's row of O: normalised partial, max, sum
-      if (!wait_all(&pv_done[0], (n - 1) & 1)) break;
+      if (!wait_all(&pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1)) break;
       tc_fence_after();
-      if (have_next) issue_q(nx, 0);  // every score MMA of this item has read Q
       if constexpr (HALF) l += __shfl_xor_sync(0xffffffffu, l, 16);  // the row's two halves
       const bool write = row < rows;
       const long long wrow = ((long long)(it.s0 + row / p.group) * p.H + it.kv * p.group + row % p.group) *
@@ -681,11 +716,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(o_free);
-      if (have_next) finish_q(0);
       have = have_next;
       it = nx;
     }
-    cp_async_wait_all();  // no copy into shared memory outlives the block
   }
 
   // ---- teardown: every role has stopped; release the tensor memory ----------------

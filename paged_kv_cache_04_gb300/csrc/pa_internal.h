@@ -36,9 +36,10 @@ template <typename DT, int D, int NT>
 pa_status launch_cascade_prefix(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                                 int num_sms, long long max_items, cudaStream_t stream);
 
-// The same pass on tcgen05 tensor cores (pa_cascade.cu).
+// The same pass on tcgen05 tensor cores (pa_cascade.cu); qmap views q as
+// [S][H][D] with a box of MR / group sequences x group heads x 64 columns.
 template <typename DT, int D, int MR>
-pa_status launch_cascade_prefix_tc(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
-                                   int num_sms, long long max_items, cudaStream_t stream);
+pa_status launch_cascade_prefix_tc(const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& qmap,
+                                   const DecodeParams& p, int num_sms, long long max_items, cudaStream_t stream);
 
 }  // namespace pa
