@@ -9,7 +9,7 @@
 // group's rows form the M side (64 or 128, padded) of real matrix products:
 //   S = Q K^T   M rows, N = 32 tokens, K = head_dim
 //   O += P V    M rows, N = head_dim, K = 32 tokens
-// Warp roles (224 threads):
+// Warp roles (256 threads):
 //   warps 0-3  softmax: each thread owns one query row, or half of one (M = 64:
 //              row 16 w + t of warp w sits in tensor-memory lane 32 w + t and
 //              threads t and t + 16 take its two column halves; M = 128:
@@ -17,21 +17,28 @@
 //              its part of S, keeps the running (max, sum), writes its part of
 //              P (16-bit hi + lo parts) to tensor memory and, at the end of an
 //              item, reads its part of O;
-//   warp 4     TMA producer: two 16-token jobs per stage (K and V, 128-byte
-//              swizzle), a ring of five stages (four for M = 128);
+//   warp 4     K producer: TMA copies of two 16-token jobs' keys per slot
+//              (128-byte swizzle) into a ring of K slots; a slot is free once
+//              the softmax warps have read the tile's scores;
+//   warp 7     V producer: the same jobs' values into a ring of V slots; a slot
+//              is free once the tile's P V has completed (five K and five V
+//              slots measured 2-3% faster than four and six);
 //   warp 5     owns the tensor memory (allocation, release); its lane 0 issues
 //              the score MMAs and commits them to mbarriers, and loads an
 //              item's Q tile by TMA as soon as the last item's score MMAs have
 //              completed (so the tile is there before the softmax warps are
 //              done with the last item);
 //   warp 6     its lane 0 issues the P V MMAs and commits them.
+// Separate K and V rings keep every byte of shared memory busy: a K slot lives
+// from its copy to the score MMAs, a V slot from its copy to the P V, instead
+// of a combined stage living until the later of the two.
 // S and P are double-buffered in tensor memory: the scores of a tile are
 // computed while the softmax warps work on the one before, and the softmax
 // writes a tile's weights while the P V of the one before runs. P is the A
 // operand of P V straight from tensor memory (a row of P sits in the lane of
 // its accumulator row, two 16-bit weights per column: checked on the GB300
 // against the same product with P in shared memory), so it costs no shared
-// memory and no proxy fence; shared memory goes to stages. The accumulator O is rescaled
+// memory and no proxy fence; shared memory goes to K and V slots. The accumulator O is rescaled
 // lazily: a row's reference max moves only when a score exceeds it by more
 // than kTcRescale (log2 units); weights then stay below 2^kTcRescale and the
 // result is the same softmax (numerator and denominator share the reference).
@@ -44,27 +51,29 @@
 namespace pa {
 
 constexpr int kTcMaxRows = 128;    // query rows of one group (members x heads) the pass takes
-constexpr int kTcTokens = 32;      // N of S, K of P V: tokens per stage (two TMA jobs)
+constexpr int kTcTokens = 32;      // N of S, K of P V: tokens per slot (two TMA jobs)
 // M of the tiles is 64 (groups of 17-64 query rows) or 128 (65-128); the
-// larger Q tile of M = 128 leaves room for four stages instead of five.
-__host__ __device__ constexpr int tc_stages(int MR) { return MR == 64 ? 5 : 4; }
-constexpr int kTcThreads = 224;
+// larger Q tile of M = 128 leaves room for eight slots instead of ten.
+__host__ __device__ constexpr int tc_kslots(int MR) { return MR == 64 ? 5 : 4; }
+__host__ __device__ constexpr int tc_vslots(int MR) { return MR == 64 ? 5 : 4; }
+constexpr int kTcThreads = 256;
 constexpr float kTcRescale = 8.f;
 
 struct TcLayout {
-  unsigned q_bytes, stage_off, stage_bytes, bar_off, misc_off, sched_off, total;
+  unsigned q_bytes, k_off, v_off, slot_bytes, bar_off, misc_off, sched_off, total;
 };
 
-// Offsets from the 1024-byte aligned base: the Q tile, the stages (K then V,
-// each [head_dim / 64 regions][32 tokens][128 B]), mbarriers, the
-// tensor-memory base, the abort flag, per-stage job flags and the group scan.
+// Offsets from the 1024-byte aligned base: the Q tile, the K slots and the V
+// slots (each [head_dim / 64 regions][32 tokens][128 B]), mbarriers, the
+// tensor-memory base, the abort flag, per-K-slot job flags and the group scan.
 __host__ __device__ inline TcLayout tc_layout(int D, int num_groups, int MR) {
   TcLayout L;
   L.q_bytes = MR * D * 2;
-  L.stage_off = L.q_bytes;
-  L.stage_bytes = 2u * kTcTokens * D * 2;
-  L.bar_off = L.stage_off + tc_stages(MR) * L.stage_bytes;
-  L.misc_off = L.bar_off + (2 * tc_stages(MR) + 13) * 8;
+  L.slot_bytes = kTcTokens * D * 2;
+  L.k_off = L.q_bytes;
+  L.v_off = L.k_off + tc_kslots(MR) * L.slot_bytes;
+  L.bar_off = L.v_off + tc_vslots(MR) * L.slot_bytes;
+  L.misc_off = L.bar_off + (2 * tc_kslots(MR) + 2 * tc_vslots(MR) + 13) * 8;
   L.sched_off = round_up(L.misc_off + 16, 16);
   L.total = round_up(L.sched_off + (num_groups + 1) * 4, 16) + 1024;
   return L;
@@ -230,10 +239,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   pdl_begin();
   static_assert(sizeof(DT) == 2 && (D == 64 || D == 128), "tensor-core prefix pass: 16-bit caches, head_dim 64/128");
   static_assert(MR == 64 || MR == 128, "tiles of 64 or 128 query rows");
-  constexpr int R = tc_stages(MR), NT = kTcTokens, JT = kJobTokens, M = MR;
+  constexpr int RK = tc_kslots(MR), RV = tc_vslots(MR), NT = kTcTokens, JT = kJobTokens, M = MR;
   constexpr int NREG = D / 64;            // 128-byte regions of a row
-  constexpr int TILE = NT * D * 2;        // K (or V) bytes of one stage
-  constexpr int REG_BYTES = NT * 128;     // one region of a stage's K (or V): [32 tokens][128 B]
+  constexpr int TILE = NT * D * 2;        // K (or V) bytes of one slot
+  constexpr int REG_BYTES = NT * 128;     // one region of a slot: [32 tokens][128 B]
   constexpr int KSTEPS = D / 16;
   // tensor-memory columns: O (D), two S buffers (NT each), two P buffers (NT each:
   // a row's NT hi and NT lo weights, two to a column)
@@ -247,9 +256,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const TcLayout L = tc_layout(D, p.num_groups, MR);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
-  uint64_t* full = bars;              // [R] TMA -> MMA
-  uint64_t* empty = bars + R;         // [R] MMA (P V done) -> TMA
-  uint64_t* s_full = bars + 2 * R;    // [2] S written -> softmax
+  uint64_t* k_full = bars;                 // [RK] K copied -> score MMAs
+  uint64_t* k_empty = bars + RK;           // [RK] scores read by the softmax -> K producer
+  uint64_t* v_full = bars + 2 * RK;        // [RV] V copied -> P V MMAs
+  uint64_t* v_empty = bars + 2 * RK + RV;  // [RV] P V done -> V producer
+  uint64_t* s_full = bars + 2 * RK + 2 * RV;  // [2] S written -> softmax
   uint64_t* s_free = s_full + 2;      // [2] S read -> MMA
   uint64_t* q_full = s_full + 4;      // the item's Q tile landed -> score MMAs
   uint64_t* q_free = s_full + 5;      // the last item's score MMAs done -> Q tile reloaded
@@ -260,16 +271,21 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   uint64_t* fin_pv = s_full + 12;     // every P V MMA done (teardown)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc_off + 4);
-  // [R] bit j: job j of the stage comes from a block in the pool. Written before
-  // the producer's arrive on full[stage] and read after a wait on it.
+  // [RK] bit j: job j of the K slot comes from a block in the pool. Written before
+  // the K producer's arrive on k_full[slot] and read after a wait on it (the
+  // softmax releases the slot after reading it).
   volatile uint8_t* job_ok = smem + L.misc_off + 8;
   int* pstart = reinterpret_cast<int*>(smem + L.sched_off);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < R; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+    for (int i = 0; i < RK; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 4);
+    }
+    for (int i = 0; i < RV; ++i) {
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
@@ -353,12 +369,20 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   };
   auto num_tiles = [&](const PItem& it) { return ((it.t1 - it.t0 + JT - 1) / JT + 1) / 2; };
   const uint32_t q_base = smem_u32(smem);
-  const uint32_t st_base = smem_u32(smem + L.stage_off);
+  const uint32_t k_base = smem_u32(smem + L.k_off);
+  const uint32_t v_base = smem_u32(smem + L.v_off);
 
-  if (warp == 4) {
-    // ------------------------------- producer -------------------------------
-    // The warp reads the block ids of 32 jobs at a time (one per lane) and lane 0
-    // takes them by shuffle, so no table load waits between two tiles' copies.
+  if (warp == 4 || warp == 7) {
+    // ------------------------------- producers ------------------------------
+    // Warp 4 copies the keys, warp 7 the values of the same tiles, each into its
+    // own ring. A warp reads the block ids of 32 jobs at a time (one per lane) and
+    // lane 0 takes them by shuffle, so no table load waits between two copies.
+    const bool is_v = warp == 7;
+    const int R = is_v ? RV : RK;
+    uint64_t* full = is_v ? v_full : k_full;
+    uint64_t* empty = is_v ? v_empty : k_empty;
+    uint8_t* ring = smem + (is_v ? L.v_off : L.k_off);
+    const CUtensorMap* map = is_v ? &vmap : &kmap;
     int n = 0;
     PItem it;
     for (int k = 0; get(k, it); ++k) {
@@ -381,35 +405,36 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           ph[j] = __shfl_sync(0xffffffffu, wphys, ua + j - wbase);
           if (ua + j >= ue) ph[j] = -2;  // no such job in this item
         }
-        // lane 0 waits for the stage and announces its bytes; lanes 0 .. 4 NREG - 1
-        // then issue one box each (job j, K or V, region rg): a single thread
-        // issuing all of a tile's boxes in turn measured slower than the copy itself
-        const int stage = n % R;
+        // lane 0 waits for the slot and announces its bytes; lanes 0 .. 2 NREG - 1
+        // then issue one box each (job j, region rg): a single thread issuing all
+        // of a tile's boxes in turn measured slower than the copy itself
+        const int slot = n % R;
         int ok = 1;
         if (lane == 0) {
-          ok = mbar_wait_sleep(&empty[stage], ((n / R) & 1) ^ 1, abort_flag, p.err, kWaitLimitNs);
+          ok = mbar_wait_sleep(&empty[slot], ((n / R) & 1) ^ 1, abort_flag, p.err, kWaitLimitNs);
           if (ok) {
-            job_ok[stage] = (uint8_t)((ph[0] >= 0 && ph[0] < p.num_blocks ? 1 : 0) |
-                                      (ph[1] >= 0 && ph[1] < p.num_blocks ? 2 : 0));
+            if (!is_v) {
+              job_ok[slot] = (uint8_t)((ph[0] >= 0 && ph[0] < p.num_blocks ? 1 : 0) |
+                                       (ph[1] >= 0 && ph[1] < p.num_blocks ? 2 : 0));
 #pragma unroll
-            for (int j = 0; j < 2; ++j)
-              if (ph[j] != -2 && (ph[j] < 0 || ph[j] >= p.num_blocks)) atomicOr(p.err, kErrBlockId);
-            mbar_arrive_expect_tx(&full[stage], 2 * TILE);
+              for (int j = 0; j < 2; ++j)
+                if (ph[j] != -2 && (ph[j] < 0 || ph[j] >= p.num_blocks)) atomicOr(p.err, kErrBlockId);
+            }
+            mbar_arrive_expect_tx(&full[slot], TILE);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (ok && lane < 4 * NREG) {
-          const int j = lane / (2 * NREG), is_v = (lane / NREG) & 1, rg = lane % NREG;
+        if (ok && lane < 2 * NREG) {
+          const int j = lane / NREG, rg = lane % NREG;
           long long phys = j ? ph[1] : ph[0];  // (a select: no local-memory array)
           if (phys >= p.num_blocks) phys = -1;
           const int tok = (ua + j) * JT;
           const int r0 = tok - ((tok >> p.block_shift) << p.block_shift);
-          uint8_t* dst = smem + L.stage_off + stage * L.stage_bytes + is_v * TILE + rg * REG_BYTES + j * JT * 128;
-          const CUtensorMap* map = is_v ? &vmap : &kmap;
+          uint8_t* dst = ring + slot * L.slot_bytes + rg * REG_BYTES + j * JT * 128;
           if (phys >= 0)
-            tma_load_tile(dst, map, p, rg * 64, phys, it.kv, r0, &full[stage]);
+            tma_load_tile(dst, map, p, rg * 64, phys, it.kv, r0, &full[slot]);
           else  // absent or out-of-pool job: zeros (the softmax masks its tokens)
-            tma_load_zero_tile(dst, map, p, rg * 64, &full[stage]);
+            tma_load_zero_tile(dst, map, p, rg * 64, &full[slot]);
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) {
           stop = true;
@@ -429,9 +454,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     // Lane 0 of warp 5 issues the score MMAs of every tile, lane 0 of warp 6 the
     // P V MMAs: a tile's P V goes out as soon as its P is written, never behind
     // the next tile's score MMAs. Each commit tracks the issuing thread's own
-    // MMAs. A tile's P V is issued after the softmax has read its S, so its S
-    // MMAs (which read the stage's K) have completed by then, and the commit of
-    // P V to empty[stage] frees the whole stage.
+    // MMAs; the commit of a tile's P V to v_empty frees its V slot.
     if (lane == 0) {
       int n = 0;
       bool issued = false;
@@ -457,14 +480,14 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           const int nt = num_tiles(it);
           bool stop = false;
           for (int i = 0; i < nt; ++i, ++n) {
-            const int stage = n % R, b = n & 1;
-            if (!mbar_wait_sleep(&full[stage], (n / R) & 1, abort_flag, p.err, kWaitLimitNs) ||
+            const int slot = n % RK, b = n & 1;
+            if (!mbar_wait_sleep(&k_full[slot], (n / RK) & 1, abort_flag, p.err, kWaitLimitNs) ||
                 !mbar_wait_sleep(&s_free[b], ((n >> 1) & 1) ^ 1, abort_flag, p.err, kWaitLimitNs)) {
               stop = true;
               break;
             }
             tc_fence_after();
-            const uint64_t kdesc = tc_desc(st_base + stage * L.stage_bytes, 16, 1024);
+            const uint64_t kdesc = tc_desc(k_base + slot * L.slot_bytes, 16, 1024);
 #pragma unroll
             for (int ks = 0; ks < KSTEPS; ++ks) {
               const uint64_t a = tc_desc_add(qdesc, (ks >> 2) * (M * 128) + (ks & 3) * 32);
@@ -496,12 +519,13 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             const bool first = i == 0;
             const int pb = n & 1;
             if (!mbar_wait_sleep(&p_full[pb], (n >> 1) & 1, abort_flag, p.err, kWaitLimitNs) ||
+                !mbar_wait_sleep(&v_full[n % RV], (n / RV) & 1, abort_flag, p.err, kWaitLimitNs) ||
                 (first && k > 0 && !mbar_wait_sleep(o_free, (k - 1) & 1, abort_flag, p.err, kWaitLimitNs))) {
               stop = true;
               break;
             }
             tc_fence_after();
-            const uint64_t vdesc = tc_desc(st_base + (n % R) * L.stage_bytes + TILE, REG_BYTES, 1024);
+            const uint64_t vdesc = tc_desc(v_base + (n % RV) * L.slot_bytes, REG_BYTES, 1024);
             // P buffer pb: columns 16 ks .. 16 ks + 7 hold the hi weights of tokens
             // 16 ks .. 16 ks + 15, the next 8 columns their lo weights
 #pragma unroll
@@ -513,7 +537,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                               !(first && part == 0 && ks == 0));
             }
             tc_commit(&pv_done[pb]);
-            tc_commit(&empty[n % R]);
+            tc_commit(&v_empty[n % RV]);
             issued = true;
           }
           if (stop) break;
@@ -556,14 +580,15 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       bool stop = false;
       for (int i = 0; i < nt; ++i, ++n) {
         const int b = n & 1;
-        if (!wait_all(&s_full[b], (n >> 1) & 1) || !wait_all(&full[n % R], (n / R) & 1)) {
+        const int kslot = n % RK;
+        if (!wait_all(&s_full[b], (n >> 1) & 1) || !wait_all(&k_full[kslot], (n / RK) & 1)) {
           stop = true;
           break;
         }
         // the tile's jobs with a block in the pool (the producer zero-filled the
-        // others); full[stage] completed before S was computed and cannot move on
-        // before this tile's P V has read the stage
-        const unsigned ok = job_ok[n % R];
+        // others); k_full[kslot] completed before S was computed and cannot move on
+        // before these warps release the slot
+        const unsigned ok = job_ok[kslot];
         tc_fence_after();
         uint32_t s[CW];
         if constexpr (HALF)
@@ -572,7 +597,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           tc_ld32(lane_addr + S_COL + b * NT, s);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s_free[b]);
+        if (lane == 0) {
+          mbar_arrive(&s_free[b]);
+          mbar_arrive(&k_empty[kslot]);  // the score MMAs are done with the K slot
+        }
         // scores of this tile's real tokens (this thread's columns tok0 ..), in base-2 units
         const int nv = min(NT, it.t1 - (it.t0 + 2 * i * JT));
         const int tok0 = half * CW;
