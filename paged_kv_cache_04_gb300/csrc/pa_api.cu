@@ -48,15 +48,20 @@ pa_status encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
   return PA_OK;
 }
 
-// The TMA view of a KV pool. One box is 128 bytes of head_dim x 16 tokens of
-// one (block, kv head) tile (one job), staged with 128-byte swizzling.
-//   HND [num_blocks][G][B][D]: 2-D, rows = num_blocks * G * B of D elements;
-//   NHD [num_blocks][B][G][D]: 3-D (D, G, num_blocks * B), so a box takes one
-//   kv head of 16 consecutive tokens (rows G * D elements apart).
+// The TMA view of a KV pool. A box is 16 tokens of one (block, kv head) tile
+// (one job), staged in 128-byte column regions ([regions][16 rows][128 B]),
+// with 128-byte swizzling.
+//   HND [num_blocks][G][B][D]: rows = num_blocks * G * B of D elements;
+//   NHD [num_blocks][B][G][D]: (D, G, num_blocks * B), so a box takes one kv
+//   head of 16 consecutive tokens (rows G * D elements apart).
+//   regions: with a row wider than 128 bytes, a last dimension of extent
+//   D * e / 128 and stride 128 bytes lets one box take every region of the
+//   job (plain decode); without it a box is one region, placed by its column
+//   coordinate (split decode, the shared-prefix passes).
 //   swizzle: 128-byte swizzled stages (read by ldmatrix / by columns), or plain
 //   row-major stages (V of the vector paths, whose lanes read one row at a time).
 pa_status make_pool_map(CUtensorMap* map, const void* base, pa_dtype dt, int D, int G, int BS, long long num_blocks,
-                        pa_kv_layout layout, bool swizzle = true) {
+                        pa_kv_layout layout, bool swizzle, bool regions) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
   pa_status st = encoder(&enc);
   if (st != PA_OK) return st;
@@ -66,20 +71,30 @@ pa_status make_pool_map(CUtensorMap* map, const void* base, pa_dtype dt, int D, 
                                 : dt == PA_FP8_E4M3   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const bool nhd = layout == PA_LAYOUT_NHD;
-  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)(num_blocks * G * BS), 1};
-  cuuint64_t strides[2] = {(cuuint64_t)D * e, 0};
-  cuuint32_t box[3] = {(cuuint32_t)(128 / e), (cuuint32_t)kJobTokens, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
+  const int nreg = regions ? D * e / 128 : 1;
+  const bool rdim = nreg > 1;  // a region dimension after the row dimension(s)
+  cuuint64_t dims[4] = {(cuuint64_t)(rdim ? 128 / e : D), (cuuint64_t)(num_blocks * G * BS), 1, 1};
+  cuuint64_t strides[3] = {(cuuint64_t)D * e, 0, 0};
+  cuuint32_t box[4] = {(cuuint32_t)(128 / e), (cuuint32_t)kJobTokens, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  int rank = 2;
   if (nhd) {
     dims[1] = (cuuint64_t)G;
     dims[2] = (cuuint64_t)(num_blocks * BS);
     strides[1] = (cuuint64_t)G * D * e;
     box[1] = 1;
     box[2] = (cuuint32_t)kJobTokens;
+    rank = 3;
+  }
+  if (rdim) {
+    dims[rank] = (cuuint64_t)nreg;
+    strides[rank - 1] = 128;
+    box[rank] = (cuuint32_t)nreg;
+    ++rank;
   }
   // NHD rows of one kv head are G * D elements apart: promote only the 128 bytes a box reads, so a
   // 128-byte row does not drag its neighbour head's row into L2.
-  CUresult r = enc(map, t, nhd ? 3 : 2, const_cast<void*>(base), dims, strides, box, estr,
+  CUresult r = enc(map, t, rank, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                    nhd ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -230,8 +245,10 @@ pa_status run_decode(const DecodeArgs& a, bool split, int partition, int max_par
   const int launch_mode = !split ? kModePlain : (c.group_starts ? kModeSuffix : kModeSplit);
   const bool mma_path = tensor_core_path(esize(a.dt), a.H / a.G, a.D, launch_mode);
   CUtensorMap km, vm;
-  if ((s = make_pool_map(&km, a.k_cache, a.dt, a.D, a.G, a.BS, a.num_blocks, a.layout)) != PA_OK) return s;
-  if ((s = make_pool_map(&vm, a.v_cache, a.dt, a.D, a.G, a.BS, a.num_blocks, a.layout, mma_path)) != PA_OK)
+  const bool whole = launch_mode == kModePlain;  // one box per job tile (see tma_load_job)
+  if ((s = make_pool_map(&km, a.k_cache, a.dt, a.D, a.G, a.BS, a.num_blocks, a.layout, true, whole)) != PA_OK)
+    return s;
+  if ((s = make_pool_map(&vm, a.v_cache, a.dt, a.D, a.G, a.BS, a.num_blocks, a.layout, mma_path, whole)) != PA_OK)
     return s;
 
   DecodeParams p{};
@@ -275,9 +292,9 @@ pa_status run_decode(const DecodeArgs& a, bool split, int partition, int max_par
     p.prefix_limit = (int)(lim_ws < lim_bt ? lim_ws : lim_bt);
     if (c.prefix_slots > 0) {  // prefix pass: every group's query rows over its shared blocks
       const long long pitems = (long long)c.num_groups * a.G * c.prefix_slots;
-      CUtensorMap vsw = vm;  // the prefix pass reads V with ldmatrix: swizzled stages
+      CUtensorMap vsw = vm;  // the prefix passes read V from swizzled stages
       if (!mma_path &&
-          (s = make_pool_map(&vsw, a.v_cache, a.dt, a.D, a.G, a.BS, a.num_blocks, a.layout)) != PA_OK)
+          (s = make_pool_map(&vsw, a.v_cache, a.dt, a.D, a.G, a.BS, a.num_blocks, a.layout, true, false)) != PA_OK)
         return s;
       // Groups of 17-64 query rows take the M = 64 tile of the tcgen05 pass and
       // groups of 65-128 its M = 128 tile; up to 16 rows, the mma.sync pass (four

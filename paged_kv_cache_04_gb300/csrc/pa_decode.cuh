@@ -152,6 +152,34 @@ __device__ __forceinline__ void tma_load_tile(void* dst, const CUtensorMap* map,
     tma_load_2d(dst, map, x, (int)((phys * p.G + kv) << p.block_shift) + r0, bar);
 }
 
+// One job's K or V rows with all of head_dim in one box, for a pool map with a
+// region dimension (128-byte column regions as a third / fourth coordinate,
+// stride 128 bytes): the same [regions][16 rows][128 B] stage image as one box
+// per region, from one copy instead of several. Plain decode takes its tiles
+// this way (NHD batch +1%, OPT-13B MHA +1.3%); split decode measured 5% slower
+// with it (0.863 against 0.910 on 32K-128K contexts) and, like the suffix pass
+// (no change), keeps one box per region.
+__device__ __forceinline__ void tma_load_job(void* dst, const CUtensorMap* map, const DecodeParams& p,
+                                             long long phys, int kv, int r0, uint64_t* bar) {
+  if (p.nhd)
+    tma_load_4d(dst, map, 0, kv, (int)(phys << p.block_shift) + r0, 0, bar);
+  else
+    tma_load_3d(dst, map, 0, (int)((phys * p.G + kv) << p.block_shift) + r0, 0, bar);
+}
+
+// A job's tile of NREG 128-byte regions (BOX_X elements each): one box over a
+// map with a region dimension (WHOLE), else one box per region.
+template <int NREG, int BOX_X, bool WHOLE>
+__device__ __forceinline__ void tma_load_rows(uint8_t* dst, const CUtensorMap* map, const DecodeParams& p,
+                                              long long phys, int kv, int r0, uint64_t* bar) {
+  if constexpr (WHOLE && NREG > 1) {
+    tma_load_job(dst, map, p, phys, kv, r0, bar);
+  } else {
+#pragma unroll
+    for (int rg = 0; rg < NREG; ++rg) tma_load_tile(dst + rg * kJobTokens * 128, map, p, rg * BOX_X, phys, kv, r0, bar);
+  }
+}
+
 struct SmemLayout {
   unsigned stage_bytes, bars_off, ok_off, merge_off, q_off, wts_off, sched_off, misc_off, total;
 };
@@ -159,8 +187,10 @@ struct SmemLayout {
 __host__ __device__ inline unsigned round_up(unsigned x, unsigned a) { return (x + a - 1) / a * a; }
 
 // Shared-memory map, computed identically on the host (launch size) and device.
+// suffix: the shared-prefix suffix pass, which merges nothing inside the CTA
+// and keeps each sequence's first own token beside the sort order.
 __host__ __device__ inline SmemLayout make_layout(int W, int R, int D, int esize, int qsize, int group, int path,
-                                                  bool split, int S, int jps = 1) {
+                                                  bool split, int S, int jps = 1, bool suffix = false) {
   SmemLayout L;
   L.stage_bytes = jps * 2u * kJobTokens * D * esize;  // jps jobs of K and V tiles
   unsigned off = W * R * L.stage_bytes;
@@ -169,7 +199,7 @@ __host__ __device__ inline SmemLayout make_layout(int W, int R, int D, int esize
   L.ok_off = off;
   off = round_up(off + W * R * jps, 16);  // per job: its block id was in the pool
   L.merge_off = off;
-  if (!split) off += W * merge_heads(group, path) * D * 4 + W * kMaxGroup * 2 * 4;
+  if (!split && !suffix) off += W * merge_heads(group, path) * D * 4 + W * kMaxGroup * 2 * 4;
   L.q_off = off;
   if (path == kPathVec) off += W * group * D * 4;            // fp32 q rows per warp
   if (path == kPathVecMha) off += round_up(W * 2 * D * qsize, 16);  // double-buffered raw q row per warp
@@ -179,7 +209,7 @@ __host__ __device__ inline SmemLayout make_layout(int W, int R, int D, int esize
   if (split)
     off += (S + 1) * 4;
   else if (S <= kSortMaxSeqs)
-    off += S * 2;
+    off += S * 2 + (suffix ? round_up(S * 2, 16) - S * 2 + S * 4 : 0);  // order [, first own token]
   off = round_up(off, 16);
   L.misc_off = off;
   off += 16;
@@ -268,10 +298,20 @@ __device__ __forceinline__ int seq_start(const DecodeParams& p, int s, int ctx) 
   return st;
 }
 
+// Suffix pass: a row's prefix slots past its group's prefix partitions get a
+// zero sum, so the reduce merges slots [0, suffix_slot] without looking the
+// group up (the prefix pass writes the slots below; the reduce skips a zero
+// sum). rbase: the row's first slot; t0: the sequence's first own token; the
+// calling threads split the slots (thread i of n).
+__device__ __forceinline__ void clear_prefix_slots(const DecodeParams& p, long long rbase, int t0, int i, int n) {
+  for (int q = (t0 + p.partition - 1) / p.partition + i; q < p.suffix_slot; q += n) p.ws_l[rbase + q] = 0.f;
+}
+
 template <int MODE, int W>
 struct Schedule {
   const uint16_t* order;  // plain mode: sequences longest-first (nullptr: batch order)
   const int* pstart;      // split mode: first item of each sequence, [S + 1]
+  const int* sstart;      // suffix mode: each sequence's first own token (nullptr: look it up)
   int num_items;
 
   // k-th item of this CTA (serpentine deal over the grid), as seen by `warp`. The
@@ -307,7 +347,10 @@ struct Schedule {
     } else {
       it.s = order ? (int)order[qi] : qi;
       it.t1 = clamp_ctx(p, it.s, false);
-      it.t0 = MODE == kModeSuffix ? seq_start(p, it.s, it.t1) : 0;
+      if (MODE == kModeSuffix)
+        it.t0 = sstart ? min(sstart[it.s], it.t1) : seq_start(p, it.s, it.t1);
+      else
+        it.t0 = 0;
       it.part = MODE == kModeSuffix ? p.suffix_slot : 0;
     }
     return true;
@@ -359,15 +402,17 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH, MODE>::W * 32, StageCfg<
   static_assert(!F8 || D % 64 == 0, "FP8 caches need head_dim a multiple of 64");
   constexpr int W = Cfg::W, R = Cfg::R, E = Cfg::E, TILE = Cfg::TILE, JT = kJobTokens;
   constexpr int NCH = D * E / 16;     // 16-byte chunks per row
-  constexpr int NREG = D * E / 128;   // 128-byte column regions (one TMA box each)
-  constexpr int BOX_X = 128 / E;
+  constexpr int NREG = D * E / 128;   // 128-byte column regions
+  constexpr int BOX_X = 128 / E;      // elements of a region
+  // plain mode's pool maps carry a region dimension: one box per job tile
+  constexpr bool WHOLE_ROWS = MODE == kModePlain;
   static_assert(NREG >= 1 && D * E % 128 == 0, "head_dim * element size must be a multiple of 128 bytes");
   static_assert(!MMA || ((sizeof(DT) == 2 || F8) && D % 16 == 0), "mma path needs 16-bit or FP8 data");
 
   extern __shared__ uint8_t smem_raw[];
   // TMA 128-byte swizzling needs 1024-byte aligned destinations: align the shared-window offset.
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const SmemLayout L = make_layout(W, R, D, E, (int)sizeof(QT), p.group, PATH, SPLIT, p.S, JPS);
+  const SmemLayout L = make_layout(W, R, D, E, (int)sizeof(QT), p.group, PATH, SPLIT, p.S, JPS, SUFFIX);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars_off);
   volatile uint8_t* stage_ok = smem + L.ok_off;                        // [W][R][JPS]
   const int MH = merge_heads(p.group, PATH);                           // heads per merge round
@@ -395,6 +440,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH, MODE>::W * 32, StageCfg<
   Schedule<MODE, W> sch;
   sch.order = nullptr;
   sch.pstart = nullptr;
+  sch.sstart = nullptr;
   if (SPLIT) {
     int* pstart = reinterpret_cast<int*>(smem + L.sched_off);
     if (warp == 0) {
@@ -430,6 +476,9 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH, MODE>::W * 32, StageCfg<
       // stable counting sort of the sequences by length bucket, longest first
       constexpr bool FINE_ORDER = !MMA || F8 || SUFFIX;
       uint16_t* order = reinterpret_cast<uint16_t*>(smem + L.sched_off);
+      // suffix mode: each sequence's first own token (its group's prefix), found
+      // once here instead of by a search over the groups at every item
+      int* sstart = SUFFIX ? reinterpret_cast<int*>(smem + L.sched_off + round_up(p.S * 2, 16)) : nullptr;
       // kNumBuckets counters, then each sequence's bucket, in stage memory (at least
       // 32 KiB, free until the first copy): a bucket is computed once, by the whole
       // CTA (in suffix mode it takes a search over the groups)
@@ -467,9 +516,14 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH, MODE>::W * 32, StageCfg<
       auto bucket = [&](int s) {  // ascending bucket index = descending length
         // the suffix pass sorts by the sequence's own tokens, which are short: finer buckets
         const int c = clamp_ctx(p, s, false);
+        int st = 0;
+        if constexpr (SUFFIX) {
+          st = seq_start(p, s, c);
+          sstart[s] = st;
+        }
         // Paths that run below their share of the bandwidth (vector, FP8, the short
         // suffix items) balance better with the finer log-scale order.
-        const int key = FINE_ORDER ? min(length_key(SUFFIX ? c - seq_start(p, s, c) : c), kNumBuckets - 1)
+        const int key = FINE_ORDER ? min(length_key(c - st), kNumBuckets - 1)
                                    : min(c >> coarse_shift, kNumBuckets - 1);
         return kNumBuckets - 1 - key;
       };
@@ -511,6 +565,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH, MODE>::W * 32, StageCfg<
       }
       __syncthreads();
       sch.order = order;
+      sch.sstart = sstart;
     } else {
       __syncthreads();
     }
@@ -597,15 +652,11 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH, MODE>::W * 32, StageCfg<
         fence_proxy_async_smem();
         if (part & kPartK) {
           mbar_arrive_expect_tx(kbar, TWO_BARS ? TILE : 2 * TILE);
-#pragma unroll
-          for (int rg = 0; rg < NREG; ++rg)
-            tma_load_tile(kdst + rg * JT * 128, &kmap, p, rg * BOX_X, phys, c.it.kv, r0, kbar);
+          tma_load_rows<NREG, BOX_X, WHOLE_ROWS>(kdst, &kmap, p, phys, c.it.kv, r0, kbar);
         }
         if (part & kPartV) {
           if (TWO_BARS) mbar_arrive_expect_tx(vbar, TILE);
-#pragma unroll
-          for (int rg = 0; rg < NREG; ++rg)
-            tma_load_tile(vdst + rg * JT * 128, &vmap, p, rg * BOX_X, phys, c.it.kv, r0, vbar);
+          tma_load_rows<NREG, BOX_X, WHOLE_ROWS>(vdst, &vmap, p, phys, c.it.kv, r0, vbar);
         }
         if (PREFETCH && (part & kPartV)) {
           if (c.pf >= 0 && c.pf < p.num_blocks) {  // [pf][kv][rows of job u + PF_AHEAD]: 16 x D contiguous
@@ -650,11 +701,8 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH, MODE>::W * 32, StageCfg<
           const int tok = (c.u + j * job_step) * JT;
           const int r0 = tok - ((tok >> p.block_shift) << p.block_shift);
           uint8_t* kdst = base + j * 2 * TILE;
-#pragma unroll
-          for (int rg = 0; rg < NREG; ++rg) {
-            tma_load_tile(kdst + rg * JT * 128, &kmap, p, rg * BOX_X, ph[j], c.it.kv, r0, bar);
-            tma_load_tile(kdst + TILE + rg * JT * 128, &vmap, p, rg * BOX_X, ph[j], c.it.kv, r0, bar);
-          }
+          tma_load_rows<NREG, BOX_X, WHOLE_ROWS>(kdst, &kmap, p, ph[j], c.it.kv, r0, bar);
+          tma_load_rows<NREG, BOX_X, WHOLE_ROWS>(kdst + TILE, &vmap, p, ph[j], c.it.kv, r0, bar);
         }
       }
     }
@@ -1072,6 +1120,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH, MODE>::W * 32, StageCfg<
               p.ws_m[rowA] = m0;
               p.ws_l[rowA] = l0;
             }
+            if (SUFFIX) clear_prefix_slots(p, rowA - it.part, it.t0, g, 8);
           }
           if (hB < p.group) {
 #pragma unroll
@@ -1083,6 +1132,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH, MODE>::W * 32, StageCfg<
               p.ws_m[rowB] = m1;
               p.ws_l[rowB] = l1;
             }
+            if (SUFFIX) clear_prefix_slots(p, rowB - it.part, it.t0, g, 8);
           }
         }
       } else {
@@ -1375,6 +1425,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH, MODE>::W * 32, StageCfg<
               p.ws_m[row] = mr[h];
               p.ws_l[row] = l;
             }
+            if (SUFFIX) clear_prefix_slots(p, row - it.part, it.t0, lane, 32);
           }
         } else {
 #pragma unroll
@@ -1402,6 +1453,15 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH, MODE>::W * 32, StageCfg<
   __syncwarp();
 }
 
+// Slots the reduce merges for sequence s: split decode, the partitions of its
+// context; shared-prefix decode, slots [0, suffix_slot) of prefix partitions
+// (those past the group's prefix hold a zero sum, see clear_prefix_slots) and
+// slot suffix_slot of its own tokens.
+__device__ __forceinline__ int merged_slots(const DecodeParams& p, int s) {
+  if (p.group_starts != nullptr) return p.suffix_slot + 1;
+  return (clamp_ctx(p, s, true) + p.partition - 1) / p.partition;
+}
+
 // Pass 2 of split mode: merge the partitions of one (sequence, head) row with
 // log-sum-exp weights, M = max_p m_p, w_p = l_p * 2^(m_p - M),
 // out = sum_p w_p o_p / sum_p w_p. One CTA per row: thread (v, pg) owns float4
@@ -1421,15 +1481,8 @@ __global__ void __launch_bounds__(256) lse_reduce_kernel(const DecodeParams p) {
   const int s = row / p.H;
   const int tid = threadIdx.x;
   const float NEG_INF = -__int_as_float(0x7f800000);
-  const int c = clamp_ctx(p, s, !p.suffix_single);  // one suffix slot bounds no context length
-  int Pp = 0, st = 0;
-  if (p.group_starts != nullptr) {
-    st = seq_start(p, s, c);
-    Pp = (st + p.partition - 1) / p.partition;
-  }
-  const int Ps = p.suffix_single ? 1 : (c - st + p.partition - 1) / p.partition;
-  const int P = Pp + Ps;  // merged slots: [0, Pp) and [suffix_slot, suffix_slot + Ps)
-  auto slot = [&](int q) { return q < Pp ? q : p.suffix_slot + (q - Pp); };
+  const int P = merged_slots(p, s);
+  auto slot = [](int q) { return q; };
   const long long base = (long long)row * p.max_partitions;
   const int v = tid % VPR, pg = tid / VPR;
   const float4* src = reinterpret_cast<const float4*>(p.ws_o + base * D) + v;
@@ -1508,17 +1561,10 @@ __global__ void __launch_bounds__(256) lse_reduce_small_kernel(const DecodeParam
   if (row >= p.S * p.H) return;
   const int s = row / p.H;
   const float NEG_INF = -__int_as_float(0x7f800000);
-  const int c = clamp_ctx(p, s, !p.suffix_single);  // one suffix slot bounds no context length
-  int Pp = 0, st = 0;
-  if (p.group_starts != nullptr) {
-    st = seq_start(p, s, c);
-    Pp = (st + p.partition - 1) / p.partition;
-  }
-  const int Ps = p.suffix_single ? 1 : (c - st + p.partition - 1) / p.partition;
-  const int P = min(Pp + Ps, 32);
+  const int P = min(merged_slots(p, s), 32);
   const long long base = (long long)row * p.max_partitions;
   // lane q holds slot q's (max, sum)
-  const int sl = lane < Pp ? lane : p.suffix_slot + (lane - Pp);
+  const int sl = lane;
   const float lq = lane < P ? __ldg(p.ws_l + base + sl) : 0.f;
   const float mq = lane < P ? __ldg(p.ws_m + base + sl) : NEG_INF;
   float M = lq > 0.f ? mq : NEG_INF;

@@ -14,7 +14,8 @@ pa_status launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const 
   using Cfg = StageCfg<DT, D, PATH, MODE>;
   auto kern = paged_decode_kernel<DT, QT, OT, D, PATH, MODE>;
   const SmemLayout L =
-      make_layout(Cfg::W, Cfg::R, D, Cfg::E, (int)sizeof(QT), p.group, PATH, MODE == kModeSplit, p.S, Cfg::JPS);
+      make_layout(Cfg::W, Cfg::R, D, Cfg::E, (int)sizeof(QT), p.group, PATH, MODE == kModeSplit, p.S, Cfg::JPS,
+                  MODE == kModeSuffix);
   if (L.total > 227u * 1024u) return PA_ERR_UNSUPPORTED;
 
   // Opt in to the dynamic shared memory once per device, and remember the
