@@ -488,6 +488,19 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH, MODE>::W * 32, StageCfg<
       int* longest = shared_pairs + 1;
       for (int b = tid; b < kNumBuckets; b += nthreads) base[b] = 0;
       if (tid == 0) *shared_pairs = *longest = 0;
+      if constexpr (SUFFIX) {
+        // each sequence's first own token, its group's shared prefix: one pass over
+        // the groups (a search over the groups per sequence, by every CTA, measured
+        // 10 us of the 64 x 8-sample suffix pass); a sequence outside every group's
+        // range (group_starts off its contract) is looked up below
+        for (int s = tid; s < p.S; s += nthreads) sstart[s] = -1;
+        __syncthreads();
+        for (int g = tid; g < p.num_groups; g += nthreads) {
+          const int b = max(__ldg(p.group_starts + g), 0), e = min(__ldg(p.group_starts + g + 1), p.S);
+          const int st = group_prefix(p, g);
+          for (int s = b; s < e; ++s) sstart[s] = st;
+        }
+      }
       __syncthreads();
       // The 16-bit tensor-core path sorts in 16-token buckets, which balances the
       // CTAs best (0.937 -> 0.945 of peak on the Llama batch), unless neighbours in
@@ -518,7 +531,13 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH, MODE>::W * 32, StageCfg<
         const int c = clamp_ctx(p, s, false);
         int st = 0;
         if constexpr (SUFFIX) {
-          st = seq_start(p, s, c);
+          st = sstart[s];
+          if (st < 0) {
+            st = seq_start(p, s, c);
+          } else if (st > c) {  // as seq_start: a prefix longer than the context
+            atomicOr(p.err, kErrContext);
+            st = c;
+          }
           sstart[s] = st;
         }
         // Paths that run below their share of the bandwidth (vector, FP8, the short

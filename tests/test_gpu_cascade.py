@@ -18,7 +18,8 @@ def _cascade(pa, wl, group_starts, prefix_lens, out_dtype=None, T=512):
     pl = torch.tensor(prefix_lens, dtype=torch.int32, device=dev)
     sizes = [b - a for a, b in zip(group_starts[:-1], group_starts[1:])]
     mpre, mctx = max(prefix_lens), wl.max_context
-    ws = torch.empty(pa.pa_decode_cascade_workspace_bytes(wl.S, wl.H, wl.d, mpre, mctx, T), dtype=torch.uint8,
+    # poisoned (0x7f bytes: finite, huge sums and maxima): every slot the reduce merges must be written
+    ws = torch.full((pa.pa_decode_cascade_workspace_bytes(wl.S, wl.H, wl.d, mpre, mctx, T),), 0x7F, dtype=torch.uint8,
                      device=dev)
     out = torch.empty(wl.q.shape, dtype=out_dtype or wl.dtype, device=dev)
     pa.pa_decode_cascade(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale, gs, pl,

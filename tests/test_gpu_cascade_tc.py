@@ -30,7 +30,8 @@ def _cascade(pa, wl, out_dtype=torch.float32, T=256):
     pl = torch.tensor(pl_l, dtype=torch.int32, device=dev)
     gmax = max(b - a for a, b in zip(gs_l[:-1], gs_l[1:]))
     mpre, mctx = max(pl_l), wl.max_context
-    ws = torch.empty(pa.pa_decode_cascade_workspace_bytes(wl.S, wl.H, wl.d, mpre, mctx, T), dtype=torch.uint8,
+    # poisoned (0x7f bytes: finite, huge sums and maxima): every slot the reduce merges must be written
+    ws = torch.full((pa.pa_decode_cascade_workspace_bytes(wl.S, wl.H, wl.d, mpre, mctx, T),), 0x7F, dtype=torch.uint8,
                      device=dev)
     out = torch.empty(wl.q.shape, dtype=out_dtype, device=dev)
     pa.pa_decode_cascade(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale, gs, pl,

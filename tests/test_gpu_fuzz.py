@@ -105,7 +105,8 @@ def test_fuzz_cascade(pa, cuda_device, i):
     gs = torch.tensor(wl.meta["group_starts"], dtype=torch.int32, device=cuda_device)
     pl = torch.tensor(wl.meta["prefix_lens"], dtype=torch.int32, device=cuda_device)
     mpre, mctx, T = max(wl.meta["prefix_lens"]), wl.max_context, c["T"]
-    ws = torch.empty(pa.pa_decode_cascade_workspace_bytes(wl.S, wl.H, wl.d, mpre, mctx, T), dtype=torch.uint8,
+    # poisoned (0x7f bytes: finite, huge sums and maxima): every slot the reduce merges must be written
+    ws = torch.full((pa.pa_decode_cascade_workspace_bytes(wl.S, wl.H, wl.d, mpre, mctx, T),), 0x7F, dtype=torch.uint8,
                      device=cuda_device)
     out = torch.empty(wl.q.shape, dtype=torch.float32, device=cuda_device)
     pa.pa_decode_cascade(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale, gs, pl,
