@@ -482,11 +482,15 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH, MODE>::W * 32, StageCfg<
       // kNumBuckets counters, then each sequence's bucket, in stage memory (at least
       // 32 KiB, free until the first copy): a bucket is computed once, by the whole
       // CTA (in suffix mode it takes a search over the groups)
+      // bucket b's counter sits at b + b / 32, so that lane l's 32 consecutive
+      // buckets in the prefix pass fall in 32 different banks
+      constexpr int kBaseWords = kNumBuckets + kNumBuckets / 32;
+      auto bidx = [](int b) { return b + (b >> 5); };
       int* base = reinterpret_cast<int*>(smem);
-      uint16_t* keys = reinterpret_cast<uint16_t*>(smem + kNumBuckets * 4);
-      int* shared_pairs = reinterpret_cast<int*>(smem + kNumBuckets * 4 + kSortMaxSeqs * 2);
+      uint16_t* keys = reinterpret_cast<uint16_t*>(smem + kBaseWords * 4);
+      int* shared_pairs = reinterpret_cast<int*>(smem + kBaseWords * 4 + kSortMaxSeqs * 2);
       int* longest = shared_pairs + 1;
-      for (int b = tid; b < kNumBuckets; b += nthreads) base[b] = 0;
+      for (int b = tid; b < kBaseWords; b += nthreads) base[b] = 0;
       if (tid == 0) *shared_pairs = *longest = 0;
       if constexpr (SUFFIX) {
         // each sequence's first own token, its group's shared prefix: one pass over
@@ -514,12 +518,15 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH, MODE>::W * 32, StageCfg<
       if constexpr (!FINE_ORDER) {
         int local = 0, cmax = 0;
         for (int s = tid; s < p.S; s += nthreads) {
+          // the four loads go out together (a table's first entry is readable
+          // whatever the context length; it is compared only for two live rows)
+          const bool nxt = s + 1 < p.S;
+          const int32_t* row = p.block_tables + (long long)s * p.max_blocks;
           const int c = __ldg(p.context_lens + s);
+          const int c1 = nxt ? __ldg(p.context_lens + s + 1) : 0;
+          const int32_t b0 = __ldg(row), b1 = nxt ? __ldg(row + p.max_blocks) : -1;
           cmax = max(cmax, c);
-          if (s + 1 < p.S && c > 0 && __ldg(p.context_lens + s + 1) > 0) {
-            const int32_t* row = p.block_tables + (long long)s * p.max_blocks;
-            if (__ldg(row) == __ldg(row + p.max_blocks)) ++local;
-          }
+          if (nxt && c > 0 && c1 > 0 && b0 == b1) ++local;
         }
         if (local) atomicAdd(shared_pairs, local);
         if (cmax) atomicMax(longest, cmax);
@@ -549,14 +556,14 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH, MODE>::W * 32, StageCfg<
       for (int s = tid; s < p.S; s += nthreads) {
         const int b = bucket(s);
         keys[s] = (uint16_t)b;
-        atomicAdd(&base[b], 1);
+        atomicAdd(&base[bidx(b)], 1);
       }
       __syncthreads();
       if (warp == 0) {
         constexpr int PER = kNumBuckets / 32;
         int local = 0;
 #pragma unroll
-        for (int i = 0; i < PER; ++i) local += base[lane * PER + i];
+        for (int i = 0; i < PER; ++i) local += base[bidx(lane * PER + i)];
         int incl = local;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -566,8 +573,8 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH, MODE>::W * 32, StageCfg<
         int run = incl - local;
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
-          const int c = base[lane * PER + i];
-          base[lane * PER + i] = run;
+          const int c = base[bidx(lane * PER + i)];
+          base[bidx(lane * PER + i)] = run;
           run += c;
         }
         __syncwarp();
@@ -576,9 +583,9 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH, MODE>::W * 32, StageCfg<
           const int s = c0 + lane;
           const int key = s < p.S ? (int)keys[s] : -1 - lane;  // padding lanes: keys of their own
           const unsigned peers = __match_any_sync(0xffffffffu, key);
-          if (s < p.S) order[base[key] + __popc(peers & lt)] = (uint16_t)s;
+          if (s < p.S) order[base[bidx(key)] + __popc(peers & lt)] = (uint16_t)s;
           __syncwarp();
-          if (s < p.S && (peers & lt) == 0) base[key] += __popc(peers);
+          if (s < p.S && (peers & lt) == 0) base[bidx(key)] += __popc(peers);
           __syncwarp();
         }
       }
