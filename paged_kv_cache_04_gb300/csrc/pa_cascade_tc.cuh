@@ -38,10 +38,11 @@
 // operand of P V straight from tensor memory (a row of P sits in the lane of
 // its accumulator row, two 16-bit weights per column: checked on the GB300
 // against the same product with P in shared memory), so it costs no shared
-// memory and no proxy fence; shared memory goes to K and V slots. The accumulator O is rescaled
-// lazily: a row's reference max moves only when a score exceeds it by more
-// than kTcRescale (log2 units); weights then stay below 2^kTcRescale and the
-// result is the same softmax (numerator and denominator share the reference).
+// memory and no proxy fence; shared memory goes to K and V slots. The
+// accumulator O is rescaled lazily: a row's reference max moves only when a
+// score exceeds it by more than kTcRescale (log2 units); weights then stay
+// below 2^kTcRescale and the result is the same softmax (numerator and
+// denominator share the reference).
 // Every wait is time-bounded; on a timeout all roles stop, the copies and
 // MMAs in flight are waited for, and the tensor memory is released.
 #pragma once
