@@ -3,7 +3,8 @@
 Groups of 5-16 samples x 4 query heads (or 3-8 x 8) take the M = 64 tile,
 groups of 17-32 x 4 (or 9-16 x 8) the M = 128 tile, so the shared-prefix decode
 runs its prefix pass on the fifth-generation tensor cores; groups of up to 16
-rows take the mma.sync pass.
+rows take the mma.sync pass. Query groups of 3, 5, 6 and 7 heads leave the
+tile's Q box short of M rows (group x (M / group)).
 Each case is checked against the oracle (which sees the pool before any kernel
 ran) and against plain pa_decode of the same batch: long prefixes (many tiles
 and several items per CTA), a last partition of one 16-token job, both block
@@ -68,6 +69,12 @@ CASES = [
     (40, 8, 8, 128, 16, torch.bfloat16, 700, "HND", False),    # MHA, 40 rows (M = 64)
     (100, 8, 8, 128, 32, torch.float16, 500, "NHD", True),     # MHA, 100 rows (M = 128)
     (20, 16, 8, 128, 16, torch.bfloat16, 800, "HND", False),   # group 2, 40 rows
+    # groups that do not divide the tile: the Q box holds group x (M / group) rows
+    (8, 24, 8, 128, 16, torch.bfloat16, 900, "HND", False),    # group 3, 24 rows: a 63-row box
+    (30, 24, 8, 128, 16, torch.float16, 700, "NHD", True),     # group 3, 90 rows: a 126-row box (M = 128)
+    (10, 48, 8, 128, 16, torch.bfloat16, 800, "HND", False),   # group 6, 60 rows: a 60-row box
+    (7, 40, 8, 64, 16, torch.bfloat16, 600, "HND", True),      # group 5, 35 rows, head_dim 64
+    (18, 56, 8, 128, 32, torch.float16, 700, "HND", False),    # group 7, 126 rows (M = 128)
 ]
 
 
