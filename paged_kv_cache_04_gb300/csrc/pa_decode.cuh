@@ -68,6 +68,10 @@ constexpr int kMaxGroup = 8;          // query heads per kv head
 // log-sum-exp, m + log2 l, whichever reference m is.
 constexpr float kLazyTau = 8.f;
 constexpr int kSortMaxSeqs = 2048;    // longest-first ordering up to this batch size
+// The suffix pass keeps each sequence's first own token in shared memory up to
+// this batch size (4 bytes a sequence; above it, the MHA suffix pass would lose
+// its third CTA per SM), and searches the groups per item beyond.
+constexpr int kSuffixStartMaxSeqs = 1024;
 constexpr int kSplitMaxSeqs = 2048;   // split mode keeps per-sequence offsets in shared memory
 // Sort key of a length: about 8 log2(len) (the exponent and the top three
 // mantissa bits), so lengths within ~9% of each other share a bucket: fine
@@ -209,7 +213,7 @@ __host__ __device__ inline SmemLayout make_layout(int W, int R, int D, int esize
   if (split)
     off += (S + 1) * 4;
   else if (S <= kSortMaxSeqs)
-    off += S * 2 + (suffix ? round_up(S * 2, 16) - S * 2 + S * 4 : 0);  // order [, first own token]
+    off += S * 2 + (suffix && S <= kSuffixStartMaxSeqs ? round_up(S * 2, 16) - S * 2 + S * 4 : 0);  // order [, starts]
   off = round_up(off, 16);
   L.misc_off = off;
   off += 16;
@@ -478,7 +482,9 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH, MODE>::W * 32, StageCfg<
       uint16_t* order = reinterpret_cast<uint16_t*>(smem + L.sched_off);
       // suffix mode: each sequence's first own token (its group's prefix), found
       // once here instead of by a search over the groups at every item
-      int* sstart = SUFFIX ? reinterpret_cast<int*>(smem + L.sched_off + round_up(p.S * 2, 16)) : nullptr;
+      int* sstart = SUFFIX && p.S <= kSuffixStartMaxSeqs
+                        ? reinterpret_cast<int*>(smem + L.sched_off + round_up(p.S * 2, 16))
+                        : nullptr;
       // kNumBuckets counters, then each sequence's bucket, in stage memory (at least
       // 32 KiB, free until the first copy): a bucket is computed once, by the whole
       // CTA (in suffix mode it takes a search over the groups)
@@ -492,7 +498,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH, MODE>::W * 32, StageCfg<
       int* longest = shared_pairs + 1;
       for (int b = tid; b < kBaseWords; b += nthreads) base[b] = 0;
       if (tid == 0) *shared_pairs = *longest = 0;
-      if constexpr (SUFFIX) {
+      if (sstart != nullptr) {
         // each sequence's first own token, its group's shared prefix: one pass over
         // the groups (a search over the groups per sequence, by every CTA, measured
         // 10 us of the 64 x 8-sample suffix pass); a sequence outside every group's
@@ -538,14 +544,14 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH, MODE>::W * 32, StageCfg<
         const int c = clamp_ctx(p, s, false);
         int st = 0;
         if constexpr (SUFFIX) {
-          st = sstart[s];
+          st = sstart ? sstart[s] : -1;
           if (st < 0) {
             st = seq_start(p, s, c);
           } else if (st > c) {  // as seq_start: a prefix longer than the context
             atomicOr(p.err, kErrContext);
             st = c;
           }
-          sstart[s] = st;
+          if (sstart) sstart[s] = st;
         }
         // Paths that run below their share of the bandwidth (vector, FP8, the short
         // suffix items) balance better with the finer log-scale order.

@@ -80,3 +80,19 @@ def test_cascade_rejects_wide_groups(pa, cuda_device):
     wl = workloads.shared_prefix(device=cuda_device, prompts=1, samples=33, prefix=64, tail_hi=8)
     with pytest.raises(pa.PAError):
         _cascade(pa, wl, wl.meta["group_starts"], wl.meta["prefix_lens"])  # 33 x 4 rows > 128
+
+
+@pytest.mark.parametrize("heads", [(32, 8), (8, 8)], ids=["gqa4", "mha"])
+def test_cascade_batch_above_start_cache(pa, cuda_device, heads):
+    """More than 1,024 sequences: the suffix pass finds each sequence's first own
+    token by a search over the groups per item instead of its shared-memory copy."""
+    Hh, G = heads
+    prompts, samples = (65, 16) if Hh // G > 1 else (130, 8)
+    wl = workloads.shared_prefix(device=cuda_device, prompts=prompts, samples=samples, prefix=160, tail_hi=64,
+                                 H=Hh, G=G)
+    assert wl.S > 1024
+    ref = H.Pristine(wl).decode()
+    _writes(pa, wl)
+    out = _cascade(pa, wl, wl.meta["group_starts"], wl.meta["prefix_lens"], torch.float32, T=64)
+    H.check_close(out, ref, torch.float32, f"cascade S={wl.S}")
+    assert pa.pa_get_error() == 0

@@ -34,6 +34,14 @@ void row(const char* name, int group, int split, int S) {
                              : layout_of<StageCfg<DT, D, PATH, kModePlain>, QT, D, PATH>(group, 0, S);
   printf("%s %d %d %d %u\n", name, group, split, S, L.total);
 }
+// the shared-prefix suffix pass (split slot 2 in the key): no merge area, and
+// each sequence's first own token beside the sort order
+template <typename DT, typename QT, int D, int PATH>
+void row_suffix(const char* name, int group, int S) {
+  using C = StageCfg<DT, D, PATH, kModeSuffix>;
+  const SmemLayout L = make_layout(C::W, C::R, D, C::E, (int)sizeof(QT), group, PATH, false, S, C::JPS, true);
+  printf("%s %d 2 %d %u\n", name, group, S, L.total);
+}
 int main() {
   for (int S : {64, 256, 752, 2048})
     for (int sp : {0, 1})
@@ -49,6 +57,11 @@ int main() {
         row<__half, __half, 128, kPathVecMha>("mha_d128", 1, sp, S);
         row<__nv_bfloat16, __nv_bfloat16, 256, kPathVec>("vec_d256", 2, sp, S);
       }
+  for (int S : {512, 1024, 2048}) {
+    row_suffix<__nv_bfloat16, __nv_bfloat16, 128, kPathMma>("sfx_mma16_d128", 4, S);
+    row_suffix<__nv_bfloat16, __nv_bfloat16, 64, kPathMma>("sfx_mma16_d64", 4, S);
+    row_suffix<__half, __half, 128, kPathVecMha>("sfx_mha_d128", 1, S);
+  }
   // the tcgen05 prefix pass of shared-prefix decode: (groups) in the group slot
   for (int D : {64, 128})
     for (int MR : {64, 128})
@@ -98,6 +111,10 @@ HOLDS = [
     (("fp8g8_d128", 8, 0, 256), 3),    # E4M3 plain decode at group 8
     (("mma16g8_d256", 8, 0, 2048), 2),
     (("vec_d256", 2, 0, 2048), 2),
+    (("sfx_mma16_d128", 4, 2, 512), 2),   # shared-prefix suffix pass (the 64 x 8-sample batch)
+    (("sfx_mma16_d128", 4, 2, 2048), 2),
+    (("sfx_mha_d128", 1, 2, 1024), 3),   # (each sequence's first own token kept up to 1,024)
+    (("sfx_mha_d128", 1, 2, 2048), 3),
     (("tc_d128_m64", 512, 0, 0), 2),   # tcgen05 prefix pass, 17-64 rows per group
     (("tc_d128_m64", 2048, 0, 0), 2),
     (("tc_d128_m128", 2048, 0, 0), 2),  # 65-128 rows per group
