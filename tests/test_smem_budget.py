@@ -126,7 +126,7 @@ HOLDS = [
 # three-CTA budget above about 750 sequences; the split schedule (4 bytes per
 # sequence) does the same to MHA split decode above about 1,900. (The tcgen05
 # prefix pass's group scan, 4 bytes per group, keeps two CTAs per SM up to
-# about 4,000 groups.)
+# about 4,000 groups; the cascade call takes at most 2,048.)
 GAPS = [
     (("fp8_d128", 4, 0, 2048), 3),
     (("mha_d128", 1, 1, 2048), 3),
