@@ -245,9 +245,11 @@ pa_status pa_decode_split_static(void* out, const void* q, const void* k_cache, 
  * The tokens of a group's prefix are read through the block table of its
  * first member. 16-bit caches only; num_seqs and num_groups at most 2048.
  * Workspace: pa_decode_cascade_workspace_bytes(...) bytes, laid out as for
- * pa_decode_split with P = ceil(max_prefix_len / T) + 1 slots: the prefix
- * partitions, then one slot for each sequence's own tokens (max_context_len is
- * accepted for symmetry with pa_decode_split and bounds nothing).
+ * pa_decode_split with P = ceil(max_prefix_len / T) + 1 slots (the prefix
+ * partitions, then one slot for each sequence's own tokens; max_context_len is
+ * accepted for symmetry with pa_decode_split and bounds nothing), followed by
+ * num_seqs x 6 bytes (256-byte aligned) where the prefix pass leaves the
+ * suffix pass its schedule. Its contents need no initialisation.
  */
 size_t pa_decode_cascade_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_prefix_len,
                                          int max_context_len, int partition_tokens);

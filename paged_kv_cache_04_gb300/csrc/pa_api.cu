@@ -279,6 +279,12 @@ pa_status run_decode(const DecodeArgs& a, bool split, int partition, int max_par
     p.ws_o = static_cast<float*>(ws);
     p.ws_m = reinterpret_cast<float*>(static_cast<char*>(ws) + align256(o_bytes));
     p.ws_l = reinterpret_cast<float*>(static_cast<char*>(ws) + align256(o_bytes) + align256(m_bytes));
+    if (c.group_starts && c.prefix_slots > 0 && c.rows > 16 && a.S <= kSuffixStartMaxSeqs) {
+      // the tcgen05 prefix pass computes the suffix pass's schedule (suffix_schedule)
+      char* sched = static_cast<char*>(ws) + align256(o_bytes) + 2 * align256(m_bytes);
+      p.sfx_order = reinterpret_cast<uint16_t*>(sched);
+      p.sfx_start = reinterpret_cast<int*>(sched + align256((size_t)a.S * 2));
+    }
     if (!c.group_starts) items *= max_partitions;  // the suffix pass has one item per (sequence, kv head)
   }
   const int mode = launch_mode;
@@ -524,7 +530,10 @@ extern "C" size_t pa_decode_cascade_workspace_bytes(int num_seqs, int num_heads,
     return 0;
   const long long P = ((long long)max_prefix_len + partition_tokens - 1) / partition_tokens + 1;
   const size_t rows = (size_t)num_seqs * num_heads * P;
-  return pa::align256(rows * head_dim * 4) + 2 * pa::align256(rows * 4);
+  // then the suffix pass's schedule: the sequence order (2 bytes each) and their
+  // first own tokens (4 bytes each)
+  return pa::align256(rows * head_dim * 4) + 2 * pa::align256(rows * 4) + pa::align256((size_t)num_seqs * 2) +
+         pa::align256((size_t)num_seqs * 4);
 }
 
 extern "C" pa_status pa_decode_cascade(void* out, const void* q, const void* k_cache, const void* v_cache,

@@ -756,6 +756,24 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   tc_fence_after();
   if (warp == 5)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(TCOLS) : "memory");
+
+  // The suffix pass's schedule (sequence order and first own tokens), computed
+  // once here instead of by every CTA of the suffix pass: by the CTA with the
+  // fewest items (when the items do not divide evenly over the grid it has a
+  // round to spare). Shared memory is free: every copy has landed.
+  if (p.sfx_order != nullptr && !*abort_flag) {
+    const int grid = (int)gridDim.x, rem = num_items % grid, last = num_items / grid;
+    const int sorter = (rem == 0 || (last & 1) == 0) ? grid - 1 : 0;  // the serpentine's last round
+    if ((int)blockIdx.x == sorter) {
+      uint16_t* order = reinterpret_cast<uint16_t*>(smem + kSortScratchBytes);
+      int* sstart = reinterpret_cast<int*>(smem + kSortScratchBytes + round_up(p.S * 2, 16));
+      suffix_schedule(p, smem, order, sstart, threadIdx.x, kTcThreads);
+      for (int s = threadIdx.x; s < p.S; s += kTcThreads) {
+        p.sfx_order[s] = order[s];
+        p.sfx_start[s] = sstart[s];
+      }
+    }
+  }
 }
 
 }  // namespace pa

@@ -141,6 +141,12 @@ struct DecodeParams {
   const void* k_cache;          // the pools (for L2 prefetches of whole HND tiles)
   const void* v_cache;
   unsigned* err;
+  // Shared-prefix decode with the tcgen05 prefix pass (S <= kSuffixStartMaxSeqs):
+  // the suffix pass's schedule in the workspace, written by one CTA of the prefix
+  // pass (suffix_schedule) and read by every CTA of the suffix pass; null: the
+  // suffix pass sorts for itself.
+  uint16_t* sfx_order;          // [S] sequences, longest own length first
+  int* sfx_start;               // [S] each sequence's first own token
 };
 
 // TMA copy of 16 rows (tokens r0 .. r0 + 15 of physical block phys, kv head kv)
@@ -309,6 +315,92 @@ __device__ __forceinline__ int seq_start(const DecodeParams& p, int s, int ctx) 
 // calling threads split the slots (thread i of n).
 __device__ __forceinline__ void clear_prefix_slots(const DecodeParams& p, long long rbase, int t0, int i, int n) {
   for (int q = (t0 + p.partition - 1) / p.partition + i; q < p.suffix_slot; q += n) p.ws_l[rbase + q] = 0.f;
+}
+
+// ---- the stable counting sort of the sequences (every mode's schedule) --------
+// Scratch: kNumBuckets counters (bucket b's at b + b / 32, so that lane l's 32
+// consecutive buckets in the prefix pass fall in 32 different banks), then each
+// sequence's bucket; order[] receives the sequences by ascending bucket, ties in
+// batch order. Every thread of the block calls it; warp 0 ranks.
+constexpr int kSortBaseWords = kNumBuckets + kNumBuckets / 32;
+constexpr unsigned kSortScratchBytes = kSortBaseWords * 4 + kSortMaxSeqs * 2;
+__device__ __forceinline__ int sort_bidx(int b) { return b + (b >> 5); }
+
+template <typename BucketFn>
+__device__ __forceinline__ void stable_sort_sequences(int S, uint8_t* scratch, uint16_t* order, BucketFn bucket_of,
+                                                      int tid, int nthreads) {
+  int* base = reinterpret_cast<int*>(scratch);
+  uint16_t* keys = reinterpret_cast<uint16_t*>(scratch + kSortBaseWords * 4);
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int b = tid; b < kSortBaseWords; b += nthreads) base[b] = 0;
+  __syncthreads();
+  for (int s = tid; s < S; s += nthreads) {
+    const int b = bucket_of(s);
+    keys[s] = (uint16_t)b;
+    atomicAdd(&base[sort_bidx(b)], 1);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    constexpr int PER = kNumBuckets / 32;
+    int local = 0;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) local += base[sort_bidx(lane * PER + i)];
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int c = base[sort_bidx(lane * PER + i)];
+      base[sort_bidx(lane * PER + i)] = run;
+      run += c;
+    }
+    __syncwarp();
+    const unsigned lt = (1u << lane) - 1u;
+    for (int c0 = 0; c0 < S; c0 += 32) {
+      const int s = c0 + lane;
+      const int key = s < S ? (int)keys[s] : -1 - lane;  // padding lanes: keys of their own
+      const unsigned peers = __match_any_sync(0xffffffffu, key);
+      if (s < S) order[base[sort_bidx(key)] + __popc(peers & lt)] = (uint16_t)s;
+      __syncwarp();
+      if (s < S && (peers & lt) == 0) base[sort_bidx(key)] += __popc(peers);
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+}
+
+// The shared-prefix suffix pass's schedule (S <= kSuffixStartMaxSeqs): sstart[s],
+// each sequence's first own token (its group's shared prefix, from one pass over
+// the groups' member ranges; a sequence outside every range, with group_starts
+// off its contract, is looked up), and order[], the sequences by descending own
+// length (buckets of about 8 log2(length): the short suffix items balance better
+// with the finer log-scale order). Every thread of the block calls it.
+static __device__ __noinline__ void suffix_schedule(const DecodeParams& p, uint8_t* scratch, uint16_t* order, int* sstart,
+                                             int tid, int nthreads) {
+  for (int s = tid; s < p.S; s += nthreads) sstart[s] = -1;
+  __syncthreads();
+  for (int g = tid; g < p.num_groups; g += nthreads) {
+    const int b = max(__ldg(p.group_starts + g), 0), e = min(__ldg(p.group_starts + g + 1), p.S);
+    const int st = group_prefix(p, g);
+    for (int s = b; s < e; ++s) sstart[s] = st;
+  }
+  __syncthreads();
+  stable_sort_sequences(p.S, scratch, order, [&](int s) {
+    const int c = clamp_ctx(p, s, false);
+    int st = sstart[s];
+    if (st < 0) {
+      st = seq_start(p, s, c);
+    } else if (st > c) {  // as seq_start: a prefix longer than the context
+      atomicOr(p.err, kErrContext);
+      st = c;
+    }
+    sstart[s] = st;
+    return kNumBuckets - 1 - min(length_key(c - st), kNumBuckets - 1);
+  }, tid, nthreads);
 }
 
 template <int MODE, int W>
@@ -485,117 +577,71 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH, MODE>::W * 32, StageCfg<
       int* sstart = SUFFIX && p.S <= kSuffixStartMaxSeqs
                         ? reinterpret_cast<int*>(smem + L.sched_off + round_up(p.S * 2, 16))
                         : nullptr;
-      // kNumBuckets counters, then each sequence's bucket, in stage memory (at least
-      // 32 KiB, free until the first copy): a bucket is computed once, by the whole
-      // CTA (in suffix mode it takes a search over the groups)
-      // bucket b's counter sits at b + b / 32, so that lane l's 32 consecutive
-      // buckets in the prefix pass fall in 32 different banks
-      constexpr int kBaseWords = kNumBuckets + kNumBuckets / 32;
-      auto bidx = [](int b) { return b + (b >> 5); };
-      int* base = reinterpret_cast<int*>(smem);
-      uint16_t* keys = reinterpret_cast<uint16_t*>(smem + kBaseWords * 4);
-      int* shared_pairs = reinterpret_cast<int*>(smem + kBaseWords * 4 + kSortMaxSeqs * 2);
+      // the counters and buckets in stage memory (at least 32 KiB, free until the
+      // first copy); the shared-pair check's two counters after them
+      int* shared_pairs = reinterpret_cast<int*>(smem + kSortScratchBytes);
       int* longest = shared_pairs + 1;
-      for (int b = tid; b < kBaseWords; b += nthreads) base[b] = 0;
-      if (tid == 0) *shared_pairs = *longest = 0;
-      if (sstart != nullptr) {
-        // each sequence's first own token, its group's shared prefix: one pass over
-        // the groups (a search over the groups per sequence, by every CTA, measured
-        // 10 us of the 64 x 8-sample suffix pass); a sequence outside every group's
-        // range (group_starts off its contract) is looked up below
-        for (int s = tid; s < p.S; s += nthreads) sstart[s] = -1;
-        __syncthreads();
-        for (int g = tid; g < p.num_groups; g += nthreads) {
-          const int b = max(__ldg(p.group_starts + g), 0), e = min(__ldg(p.group_starts + g + 1), p.S);
-          const int st = group_prefix(p, g);
-          for (int s = b; s < e; ++s) sstart[s] = st;
-        }
-      }
-      __syncthreads();
-      // The 16-bit tensor-core path sorts in 16-token buckets, which balances the
-      // CTAs best (0.937 -> 0.945 of peak on the Llama batch), unless neighbours in
-      // the batch share their first physical block (samples or beams of one prompt,
-      // at least one pair in eight): then 512-token buckets keep a prompt's members
-      // together, so its shared blocks are read while they are still in L2 (fine
-      // buckets measured 10% slower there).
-      // (Longer contexts widen the fine buckets so that the longest still gets a
-      // bucket of its own.)
-      int coarse_shift = 9;
-      if constexpr (!FINE_ORDER) {
-        int local = 0, cmax = 0;
-        for (int s = tid; s < p.S; s += nthreads) {
-          // the four loads go out together (a table's first entry is readable
-          // whatever the context length; it is compared only for two live rows)
-          const bool nxt = s + 1 < p.S;
-          const int32_t* row = p.block_tables + (long long)s * p.max_blocks;
-          const int c = __ldg(p.context_lens + s);
-          const int c1 = nxt ? __ldg(p.context_lens + s + 1) : 0;
-          const int32_t b0 = __ldg(row), b1 = nxt ? __ldg(row + p.max_blocks) : -1;
-          cmax = max(cmax, c);
-          if (nxt && c > 0 && c1 > 0 && b0 == b1) ++local;
-        }
-        if (local) atomicAdd(shared_pairs, local);
-        if (cmax) atomicMax(longest, cmax);
-        __syncthreads();
-        if (*shared_pairs * 8 < p.S) coarse_shift = max(4, 32 - __clz(max(*longest, 1)) - 10);
-      }
-      auto bucket = [&](int s) {  // ascending bucket index = descending length
-        // the suffix pass sorts by the sequence's own tokens, which are short: finer buckets
-        const int c = clamp_ctx(p, s, false);
-        int st = 0;
-        if constexpr (SUFFIX) {
-          st = sstart ? sstart[s] : -1;
-          if (st < 0) {
-            st = seq_start(p, s, c);
-          } else if (st > c) {  // as seq_start: a prefix longer than the context
-            atomicOr(p.err, kErrContext);
-            st = c;
+      bool sorted = false;
+      if constexpr (SUFFIX) {
+        if (sstart != nullptr) {
+          if (p.sfx_order != nullptr) {
+            // the schedule one CTA of the tcgen05 prefix pass wrote: checked, then
+            // used (a value out of range, left by a prefix pass that stopped early,
+            // and this CTA sorts for itself)
+            int bad = 0;
+            for (int s = tid; s < p.S; s += nthreads) {
+              const int o = __ldg(p.sfx_order + s), st = __ldg(p.sfx_start + s);
+              order[s] = (uint16_t)o;
+              sstart[s] = st;
+              bad |= (o >= p.S || st < 0) ? 1 : 0;
+            }
+            sorted = !__syncthreads_or(bad);
           }
-          if (sstart) sstart[s] = st;
-        }
-        // Paths that run below their share of the bandwidth (vector, FP8, the short
-        // suffix items) balance better with the finer log-scale order.
-        const int key = FINE_ORDER ? min(length_key(c - st), kNumBuckets - 1)
-                                   : min(c >> coarse_shift, kNumBuckets - 1);
-        return kNumBuckets - 1 - key;
-      };
-      for (int s = tid; s < p.S; s += nthreads) {
-        const int b = bucket(s);
-        keys[s] = (uint16_t)b;
-        atomicAdd(&base[bidx(b)], 1);
-      }
-      __syncthreads();
-      if (warp == 0) {
-        constexpr int PER = kNumBuckets / 32;
-        int local = 0;
-#pragma unroll
-        for (int i = 0; i < PER; ++i) local += base[bidx(lane * PER + i)];
-        int incl = local;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int v = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += v;
-        }
-        int run = incl - local;
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-          const int c = base[bidx(lane * PER + i)];
-          base[bidx(lane * PER + i)] = run;
-          run += c;
-        }
-        __syncwarp();
-        const unsigned lt = (1u << lane) - 1u;
-        for (int c0 = 0; c0 < p.S; c0 += 32) {
-          const int s = c0 + lane;
-          const int key = s < p.S ? (int)keys[s] : -1 - lane;  // padding lanes: keys of their own
-          const unsigned peers = __match_any_sync(0xffffffffu, key);
-          if (s < p.S) order[base[bidx(key)] + __popc(peers & lt)] = (uint16_t)s;
-          __syncwarp();
-          if (s < p.S && (peers & lt) == 0) base[bidx(key)] += __popc(peers);
-          __syncwarp();
+          if (!sorted) suffix_schedule(p, smem, order, sstart, tid, nthreads);
+          sorted = true;
         }
       }
-      __syncthreads();
+      if (!sorted) {
+        // The 16-bit tensor-core path sorts in 16-token buckets, which balances the
+        // CTAs best (0.937 -> 0.945 of peak on the Llama batch), unless neighbours in
+        // the batch share their first physical block (samples or beams of one prompt,
+        // at least one pair in eight): then 512-token buckets keep a prompt's members
+        // together, so its shared blocks are read while they are still in L2 (fine
+        // buckets measured 10% slower there).
+        // (Longer contexts widen the fine buckets so that the longest still gets a
+        // bucket of its own.)
+        int coarse_shift = 9;
+        if constexpr (!FINE_ORDER) {
+          if (tid == 0) *shared_pairs = *longest = 0;
+          __syncthreads();
+          int local = 0, cmax = 0;
+          for (int s = tid; s < p.S; s += nthreads) {
+            // the four loads go out together (a table's first entry is readable
+            // whatever the context length; it is compared only for two live rows)
+            const bool nxt = s + 1 < p.S;
+            const int32_t* row = p.block_tables + (long long)s * p.max_blocks;
+            const int c = __ldg(p.context_lens + s);
+            const int c1 = nxt ? __ldg(p.context_lens + s + 1) : 0;
+            const int32_t b0 = __ldg(row), b1 = nxt ? __ldg(row + p.max_blocks) : -1;
+            cmax = max(cmax, c);
+            if (nxt && c > 0 && c1 > 0 && b0 == b1) ++local;
+          }
+          if (local) atomicAdd(shared_pairs, local);
+          if (cmax) atomicMax(longest, cmax);
+          __syncthreads();
+          if (*shared_pairs * 8 < p.S) coarse_shift = max(4, 32 - __clz(max(*longest, 1)) - 10);
+        }
+        stable_sort_sequences(p.S, smem, order, [&](int s) {  // ascending bucket = descending length
+          const int c = clamp_ctx(p, s, false);
+          // Paths that run below their share of the bandwidth (vector, FP8, the short
+          // suffix items, here above the start cache's batch size) balance better
+          // with the finer log-scale order.
+          const int st = SUFFIX ? seq_start(p, s, c) : 0;
+          const int key = FINE_ORDER ? min(length_key(c - st), kNumBuckets - 1)
+                                     : min(c >> coarse_shift, kNumBuckets - 1);
+          return kNumBuckets - 1 - key;
+        }, tid, nthreads);
+      }
       sch.order = order;
       sch.sstart = sstart;
     } else {
