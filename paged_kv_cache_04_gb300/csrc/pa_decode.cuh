@@ -147,6 +147,9 @@ struct DecodeParams {
   // suffix pass sorts for itself.
   uint16_t* sfx_order;          // [S] sequences, longest own length first
   int* sfx_start;               // [S] each sequence's first own token
+  // Plain mode: entries of the longest-first order a CTA keeps in shared memory,
+  // one per item of its own (at least ceil(S G / grid)); set by the launcher.
+  int order_cap;
 };
 
 // TMA copy of 16 rows (tokens r0 .. r0 + 15 of physical block phys, kv head kv)
@@ -199,8 +202,10 @@ __host__ __device__ inline unsigned round_up(unsigned x, unsigned a) { return (x
 // Shared-memory map, computed identically on the host (launch size) and device.
 // suffix: the shared-prefix suffix pass, which merges nothing inside the CTA
 // and keeps each sequence's first own token beside the sort order.
+// order_cap: plain mode's entries of the sort order per CTA (-1: the whole batch).
 __host__ __device__ inline SmemLayout make_layout(int W, int R, int D, int esize, int qsize, int group, int path,
-                                                  bool split, int S, int jps = 1, bool suffix = false) {
+                                                  bool split, int S, int jps = 1, bool suffix = false,
+                                                  int order_cap = -1) {
   SmemLayout L;
   L.stage_bytes = jps * 2u * kJobTokens * D * esize;  // jps jobs of K and V tiles
   unsigned off = W * R * L.stage_bytes;
@@ -218,13 +223,25 @@ __host__ __device__ inline SmemLayout make_layout(int W, int R, int D, int esize
   L.sched_off = off;
   if (split)
     off += (S + 1) * 4;
+  else if (S <= kSortMaxSeqs && suffix)
+    off += S * 2 + (S <= kSuffixStartMaxSeqs ? round_up(S * 2, 16) - S * 2 + S * 4 : 0);  // order [, starts]
   else if (S <= kSortMaxSeqs)
-    off += S * 2 + (suffix && S <= kSuffixStartMaxSeqs ? round_up(S * 2, 16) - S * 2 + S * 4 : 0);  // order [, starts]
+    off += (order_cap >= 0 ? order_cap : S) * 2;  // the sequences of this CTA's items
   off = round_up(off, 16);
   L.misc_off = off;
   off += 16;
   L.total = off + 1024;  // slack to align the dynamic window to 1024 bytes
   return L;
+}
+
+// Entries of the sort order a plain-mode CTA keeps: the launcher's grid holds at
+// least min(num_sms, S G) CTAs, so no CTA deals itself more than this many items.
+// (Capped at S, the whole order's size: a CTA with more items than that, at more
+// than num_sms kv heads, takes the batch order.)
+__host__ __device__ inline int plain_order_cap(int S, int G, int num_sms) {
+  const long long items = (long long)S * G;
+  const long long cap = items <= num_sms ? 1 : (items + num_sms - 1) / num_sms;
+  return (int)(cap < S ? cap : (S > 1 ? S : 1));
 }
 
 template <typename DT, int D, int PATH, int MODE = kModePlain>
@@ -321,14 +338,16 @@ __device__ __forceinline__ void clear_prefix_slots(const DecodeParams& p, long l
 // Scratch: kNumBuckets counters (bucket b's at b + b / 32, so that lane l's 32
 // consecutive buckets in the prefix pass fall in 32 different banks), then each
 // sequence's bucket; order[] receives the sequences by ascending bucket, ties in
-// batch order. Every thread of the block calls it; warp 0 ranks.
+// batch order. Every thread of the block calls it; warp 0 ranks, then runs
+// after_rank(lane) (order[] complete and visible to warp 0), before the block's
+// closing barrier.
 constexpr int kSortBaseWords = kNumBuckets + kNumBuckets / 32;
 constexpr unsigned kSortScratchBytes = kSortBaseWords * 4 + kSortMaxSeqs * 2;
 __device__ __forceinline__ int sort_bidx(int b) { return b + (b >> 5); }
 
-template <typename BucketFn>
+template <typename BucketFn, typename AfterRank>
 __device__ __forceinline__ void stable_sort_sequences(int S, uint8_t* scratch, uint16_t* order, BucketFn bucket_of,
-                                                      int tid, int nthreads) {
+                                                      int tid, int nthreads, AfterRank after_rank) {
   int* base = reinterpret_cast<int*>(scratch);
   uint16_t* keys = reinterpret_cast<uint16_t*>(scratch + kSortBaseWords * 4);
   const int warp = tid >> 5, lane = tid & 31;
@@ -369,8 +388,15 @@ __device__ __forceinline__ void stable_sort_sequences(int S, uint8_t* scratch, u
       if (s < S && (peers & lt) == 0) base[sort_bidx(key)] += __popc(peers);
       __syncwarp();
     }
+    after_rank(lane);
   }
   __syncthreads();
+}
+
+template <typename BucketFn>
+__device__ __forceinline__ void stable_sort_sequences(int S, uint8_t* scratch, uint16_t* order, BucketFn bucket_of,
+                                                      int tid, int nthreads) {
+  stable_sort_sequences(S, scratch, order, bucket_of, tid, nthreads, [](int) {});
 }
 
 // The shared-prefix suffix pass's schedule (S <= kSuffixStartMaxSeqs): sstart[s],
@@ -441,7 +467,7 @@ struct Schedule {
         it.t0 = it.t1 = 0;
       }
     } else {
-      it.s = order ? (int)order[qi] : qi;
+      it.s = order ? (int)order[MODE == kModePlain ? k : qi] : qi;  // plain mode: the CTA's own list
       it.t1 = clamp_ctx(p, it.s, false);
       if (MODE == kModeSuffix)
         it.t0 = sstart ? min(sstart[it.s], it.t1) : seq_start(p, it.s, it.t1);
@@ -508,7 +534,9 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH, MODE>::W * 32, StageCfg<
   extern __shared__ uint8_t smem_raw[];
   // TMA 128-byte swizzling needs 1024-byte aligned destinations: align the shared-window offset.
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const SmemLayout L = make_layout(W, R, D, E, (int)sizeof(QT), p.group, PATH, SPLIT, p.S, JPS, SUFFIX);
+  const SmemLayout L = make_layout(W, R, D, E, (int)sizeof(QT), p.group, PATH, SPLIT, p.S, JPS, SUFFIX, p.order_cap);
+  static_assert(W * R * JPS * Cfg::kJob >= kSortScratchBytes + 16 + 2 * kSortMaxSeqs,
+                "the sort's scratch and the whole batch's order fit in the stage memory");
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars_off);
   volatile uint8_t* stage_ok = smem + L.ok_off;                        // [W][R][JPS]
   const int MH = merge_heads(p.group, PATH);                           // heads per merge round
@@ -568,9 +596,13 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH, MODE>::W * 32, StageCfg<
     sch.num_items = pstart[p.S] * p.G;
   } else {
     sch.num_items = p.S * p.G;
-    if (p.S <= kSortMaxSeqs) {
+    // plain mode: the most items the serpentine deal gives one CTA
+    const int kmax = (sch.num_items + (int)gridDim.x - 1) / (int)gridDim.x;
+    if (p.S <= kSortMaxSeqs && (SUFFIX || kmax <= p.order_cap)) {
       // stable counting sort of the sequences by length bucket, longest first
       constexpr bool FINE_ORDER = !MMA || F8 || SUFFIX;
+      // (plain mode: order[k] is the sequence of this CTA's k-th item; the suffix
+      // pass, which deals to warps, keeps the whole order)
       uint16_t* order = reinterpret_cast<uint16_t*>(smem + L.sched_off);
       // suffix mode: each sequence's first own token (its group's prefix), found
       // once here instead of by a search over the groups at every item
@@ -631,7 +663,11 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH, MODE>::W * 32, StageCfg<
           __syncthreads();
           if (*shared_pairs * 8 < p.S) coarse_shift = max(4, 32 - __clz(max(*longest, 1)) - 10);
         }
-        stable_sort_sequences(p.S, smem, order, [&](int s) {  // ascending bucket = descending length
+        // Plain mode ranks the whole batch in stage memory, after the sort's
+        // scratch, and keeps only its own items' sequences (order_cap entries
+        // instead of S: three E4M3 CTAs per SM still fit at 2,048 sequences).
+        uint16_t* ranked = SUFFIX ? order : reinterpret_cast<uint16_t*>(smem + kSortScratchBytes + 16);
+        stable_sort_sequences(p.S, smem, ranked, [&](int s) {  // ascending bucket = descending length
           const int c = clamp_ctx(p, s, false);
           // Paths that run below their share of the bandwidth (vector, FP8, the short
           // suffix items, here above the start cache's batch size) balance better
@@ -640,7 +676,14 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH, MODE>::W * 32, StageCfg<
           const int key = FINE_ORDER ? min(length_key(c - st), kNumBuckets - 1)
                                      : min(c >> coarse_shift, kNumBuckets - 1);
           return kNumBuckets - 1 - key;
-        }, tid, nthreads);
+        }, tid, nthreads, [&](int ln) {
+          if constexpr (!SUFFIX) {
+            for (int k = ln; k < kmax; k += 32) {
+              const int i = k * (int)gridDim.x + ((k & 1) ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x);
+              if (i < sch.num_items) order[k] = ranked[i / p.G];
+            }
+          }
+        });
       }
       sch.order = order;
       sch.sstart = sstart;

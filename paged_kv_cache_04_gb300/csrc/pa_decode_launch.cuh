@@ -13,9 +13,11 @@ pa_status launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const 
                         int num_sms, long long max_items, cudaStream_t stream) {
   using Cfg = StageCfg<DT, D, PATH, MODE>;
   auto kern = paged_decode_kernel<DT, QT, OT, D, PATH, MODE>;
+  DecodeParams q = p;
+  q.order_cap = MODE == kModePlain ? plain_order_cap(p.S, p.G, num_sms) : 0;
   const SmemLayout L =
       make_layout(Cfg::W, Cfg::R, D, Cfg::E, (int)sizeof(QT), p.group, PATH, MODE == kModeSplit, p.S, Cfg::JPS,
-                  MODE == kModeSuffix);
+                  MODE == kModeSuffix, q.order_cap);
   if (L.total > 227u * 1024u) return PA_ERR_UNSUPPORTED;
 
   // Opt in to the dynamic shared memory once per device, and remember the
@@ -49,7 +51,7 @@ pa_status launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const 
   const long long ctas = MODE == kModeSuffix ? (max_items + Cfg::W - 1) / Cfg::W : max_items;
   if (ctas < grid) grid = ctas;
   if (grid <= 0) return PA_OK;
-  return launch_pdl(kern, dim3((unsigned)grid), dim3(Cfg::W * 32), L.total, stream, kmap, vmap, p) == cudaSuccess
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(Cfg::W * 32), L.total, stream, kmap, vmap, q) == cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
 }

@@ -50,7 +50,8 @@ def gpu_step(pa, wl, out_dtype=None, split=False, partition=None, workspace=None
     if wl.slot_mapping is not None:
         pa.pa_reshape_and_cache(wl.new_key, wl.new_value, wl.k_cache, wl.v_cache, wl.slot_mapping,
                                 stream=stream, layout=wl.layout)
-    out = torch.empty(wl.q.shape, dtype=out_dtype or wl.dtype, device=wl.q.device)
+    # NaN in every output row first: a row that no kernel wrote fails check_close
+    out = torch.full(wl.q.shape, float("nan"), dtype=out_dtype or wl.dtype, device=wl.q.device)
     if split:
         T = partition or wl.partition_tokens or 512
         mctx = wl.max_context

@@ -79,6 +79,25 @@ def test_fp8_full_size_llama_sampled(pa, cuda_device):
     assert pa.pa_get_error() == 0
 
 
+def test_fp8_large_batch_every_sequence(pa, cuda_device):
+    """2,048 sequences, the largest batch the kernel orders longest first, where
+    E4M3 plain decode still runs three CTAs per SM (each CTA keeps the order of
+    its own items only): every sequence against the oracle, the output filled
+    with NaN first so that an item dealt to no CTA shows."""
+    S = 2048
+    ctx = [int(x) for x in torch.randint(1, 97, (S,), generator=torch.Generator().manual_seed(11))]
+    nb = sum(-(-c // 16) for c in ctx) + 9
+    wl = workloads.to_fp8(workloads.batch_with_new_tokens("f8big", S, 32, 8, 128, 16, torch.bfloat16, ctx, nb,
+                                                          cuda_device))
+    ref, _, _ = _oracle(wl.k_cache.cpu().numpy(), wl.v_cache.cpu().numpy(), wl)
+    ks, vs = wl.meta["k_scale"], wl.meta["v_scale"]
+    pa.pa_reshape_and_cache_fp8(wl.new_key, wl.new_value, wl.k_cache, wl.v_cache, wl.slot_mapping, ks, vs)
+    out = torch.full(wl.q.shape, float("nan"), dtype=torch.float32, device=cuda_device)
+    pa.pa_decode_fp8(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale, ks, vs)
+    H.check_close(out, ref, torch.float32, "fp8 S=2048")
+    assert pa.pa_get_error() == 0
+
+
 def test_fp8_cache_write_bit_exact_all_dtypes(pa, cuda_device):
     g = torch.Generator(device=cuda_device).manual_seed(3)
     for dt in (torch.float32, torch.float16, torch.bfloat16):

@@ -328,13 +328,15 @@ def test_non_default_stream(pa, cuda_device):
 @pytest.mark.parametrize("S", [2048, 2500])
 def test_large_batches(pa, cuda_device, S):
     """2048 sequences (the largest batch the kernel orders longest first) and 2500
-    (above it: batch order); results must not depend on the order."""
+    (above it: batch order); results must not depend on the order. At 2048 the
+    tensor-core case checks every sequence: each CTA keeps the order of its own
+    items only, so an item dealt to no CTA would leave its rows unwritten (NaN)."""
     ctx = [int(x) for x in torch.randint(1, 200, (S,), generator=torch.Generator().manual_seed(3))]
     nb = sum(-(-c // 16) for c in ctx) + 10
     for Hh, G in ((8, 2), (32, 8)):  # vector path and tensor-core path
         wl = workloads.batch_with_new_tokens("big", S, Hh, G, 64, 16, torch.bfloat16, ctx, nb, cuda_device,
                                              new_token=False)
-        seqs = H.sample_seqs(wl, 40)
+        seqs = list(range(S)) if S == 2048 and Hh == 32 else H.sample_seqs(wl, 40)
         ref = H.Pristine(wl, seqs).decode()
         out = H.gpu_step(pa, wl, out_dtype=torch.float32)
         H.check_close(out[seqs], ref, torch.float32, f"S={S} H={Hh} G={G}")
