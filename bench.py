@@ -60,7 +60,8 @@ def parse():
                     help="run only the step's kernels on a 64-sequence batch of the same shape (for ncu)")
     ap.add_argument("--profile-fp8", action="store_true",
                     help="the same 64-sequence case with an E4M3 cache (for ncu)")
-    ap.add_argument("--profile-case", choices=["split", "cascade", "cascade_x16", "mha", "g8"], default=None,
+    ap.add_argument("--profile-case", choices=["split", "cascade", "cascade_x16", "mha", "g8", "copy", "reshape"],
+                    default=None,
                     help="a small case of another path for ncu: split (2 seqs, 48K-64K tokens, 64 q / 8 kv), "
                          "cascade (32 prompts x 8 samples), mha (the OPT-13B batch), g8 (64 seqs of the "
                          "64 q / 8 kv short-context batch, plain decode)")
@@ -995,6 +996,46 @@ def run_profile_case(args):
                       "source_sha256": kernel_source_sha(), "device_errors": pa.pa_get_error()}))
 
 
+def run_cache_profile_case(args, name, dev):
+    """The cache kernels on small cases for ncu. copy: the copy-on-write workload's 448
+    pairs remapped into a compact pool of the 512 blocks they touch, 16 layers (537 MB
+    of unique bytes per launch, 1.1 GB of pools); reshape: 32,768 new tokens into a
+    20,000-block pool at random slots (268 MB per launch, 1.3 GB of pools)."""
+    import torch
+    import paged_kv_cache_04_gb300 as pa
+    from paged_kv_cache_04_gb300 import roofline, workloads
+    G, B, d, dt = 8, 16, 128, torch.bfloat16
+    g = torch.Generator(device=dev).manual_seed(0)
+    if name == "copy":
+        L = 16
+        pairs = workloads.shared_prefix(device="cpu", cow=True).copy_pairs
+        blocks = sorted(set(pairs.flatten().tolist()))
+        remap = {b: i for i, b in enumerate(blocks)}
+        cp = torch.tensor([[remap[int(a)], remap[int(b)]] for a, b in pairs.tolist()], dtype=torch.int64,
+                          device=dev)
+        nb, P = len(blocks), int(pairs.shape[0])
+        kp = [torch.randn((nb, G, B, d), generator=g, device=dev).to(dt) for _ in range(L)]
+        vp = [torch.randn((nb, G, B, d), generator=g, device=dev).to(dt) for _ in range(L)]
+        step = lambda: pa.pa_copy_blocks(kp, vp, cp)  # noqa: E731
+        nsrc = len(set(pairs[:, 0].tolist()))
+        info = {"pairs": P, "distinct_sources": nsrc, "layers": L, "pool_blocks": nb,
+                "bytes_per_launch": roofline.copy_blocks_bytes(P, L, B, G, d, 2),
+                "unique_bytes_per_launch": (nsrc + P) * L * roofline.kv_block_bytes(B, G, d, 2)}
+    else:
+        N, nb = 32 * 1024, 20_000
+        kc = torch.empty((nb, G, B, d), dtype=dt, device=dev)
+        vc = torch.empty((nb, G, B, d), dtype=dt, device=dev)
+        key = torch.randn((N, G, d), generator=g, device=dev).to(dt)
+        val = torch.randn((N, G, d), generator=g, device=dev).to(dt)
+        slots = torch.randperm(nb * B, generator=g, device=dev)[:N]
+        step = lambda: pa.pa_reshape_and_cache(key, val, kc, vc, slots)  # noqa: E731
+        info = {"tokens": N, "pool_blocks": nb, "bytes_per_launch": roofline.reshape_and_cache_bytes(N, G, d, 2)}
+    for _ in range(args.warmup + args.steps):
+        step()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": name, **info, "device_errors": pa.pa_get_error()}))
+
+
 def run_other_profile_case(args):
     """Small cases (K/V still larger than L2) of the split, shared-prefix and MHA paths, for ncu."""
     import torch
@@ -1003,6 +1044,9 @@ def run_other_profile_case(args):
     _build.ensure_built()
     dev = torch.device("cuda", 0)
     name = args.profile_case
+    if name in ("copy", "reshape"):
+        run_cache_profile_case(args, name, dev)
+        return
     if name == "split":
         wl = workloads.long70b(device=dev, S=2, lo=48_000, hi=64_000)
     elif name == "cascade":

@@ -343,6 +343,22 @@ def test_large_batches(pa, cuda_device, S):
     _no_device_errors(pa)
 
 
+@pytest.mark.parametrize("G", [200, 512])
+def test_many_kv_heads(pa, cuda_device, G):
+    """More kv heads than SMs: each CTA keeps the sort order of its own items, at
+    most S entries. With 200 heads that still holds every CTA's items (sorted);
+    with 512 a CTA is dealt more items than that and the kernel runs the batch
+    in batch order. Every sequence against the oracle."""
+    S = 64
+    ctx = [int(x) for x in torch.randint(1, 120, (S,), generator=torch.Generator().manual_seed(5))]
+    nb = sum(-(-c // 16) for c in ctx) + 4
+    wl = workloads.batch_with_new_tokens("heads", S, G, G, 64, 16, torch.float16, ctx, nb, cuda_device)
+    ref = H.Pristine(wl).decode()
+    out = H.gpu_step(pa, wl, out_dtype=torch.float32)
+    H.check_close(out, ref, torch.float32, f"G={G}")
+    _no_device_errors(pa)
+
+
 def test_all_contexts_empty(pa, cuda_device):
     """A batch in which no sequence has a token yet: every output row is zero, plain and split."""
     wl = workloads.batch_with_new_tokens("empty", 6, 32, 8, 128, 16, torch.bfloat16, [0] * 6, 8, cuda_device,

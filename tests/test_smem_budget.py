@@ -13,6 +13,7 @@ import re
 import shutil
 import subprocess
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -71,6 +72,10 @@ int main() {
     for (int MR : {64, 128})
       for (int g : {32, 512, 2048})
         printf("tc_d%d_m%d %d 0 0 %u\n", D, MR, g, tc_layout(D, g, MR).total);
+  // plain mode's per-CTA order capacity: (S, kv heads) in the group and S slots
+  for (int S : {1, 2, 7, 64, 151, 152, 153, 256, 1000, 2048})
+    for (int G : {1, 2, 8, 40, 152, 153, 512})
+      printf("cap %d 0 %d %d\n", G, S, plain_order_cap(S, G, 152));
 }
 """
 
@@ -89,6 +94,10 @@ def totals(tmp_path_factory):
     out = subprocess.run([str(exe)], check=True, capture_output=True, text=True, timeout=60).stdout
     res = {}
     for line in out.splitlines():
+        if line.startswith("cap "):
+            _, g, _, S, cap = line.split()
+            res[("cap", int(g), int(S))] = int(cap)
+            continue
         name, g, sp, S, total = line.split()
         res[(name, int(g), int(sp), int(S))] = int(total)
     return res
@@ -148,5 +157,30 @@ def test_known_occupancy_gaps(totals, key, want):
 
 
 def test_no_layout_exceeds_the_per_cta_limit(totals):
-    over = {k: v for k, v in totals.items() if v > 227 * 1024}
+    over = {k: v for k, v in totals.items() if k[0] != "cap" and v > 227 * 1024}
     assert not over, over
+
+
+def _serpentine_items(S, G, grid):
+    """Items of each CTA under the kernel's deal (item k*grid + b for even k,
+    k*grid + grid - 1 - b for odd k), counted by brute force."""
+    i = np.arange(S * G)
+    k, pos = i // grid, i % grid
+    cta = np.where(k % 2 == 0, pos, grid - 1 - pos)
+    return int(np.bincount(cta, minlength=grid).max())
+
+
+def test_plain_order_capacity_covers_every_grid(totals):
+    """The per-CTA order holds every item a CTA is dealt, for every grid the
+    launcher can pick (152 SMs x 1-3 CTAs, capped at the item count), except
+    past S entries, where the kernel takes the batch order instead."""
+    caps = {k[1:]: v for k, v in totals.items() if k[0] == "cap"}
+    assert caps
+    for (G, S), cap in caps.items():
+        assert 1 <= cap <= max(S, 1)
+        for per_sm in (1, 2, 3):
+            grid = min(152 * per_sm, S * G)
+            need = _serpentine_items(S, G, grid)
+            assert need == -(-(S * G) // grid)
+            if cap < S or G <= 152:
+                assert need <= cap, (S, G, grid, need, cap)
