@@ -431,7 +431,9 @@ static __device__ __noinline__ void suffix_schedule(const DecodeParams& p, uint8
 
 template <int MODE, int W>
 struct Schedule {
-  const uint16_t* order;  // plain mode: sequences longest-first (nullptr: batch order)
+  // plain mode: the sequence of this CTA's k-th item; suffix mode: the sequences
+  // longest-first (nullptr: batch order)
+  const uint16_t* order;
   const int* pstart;      // split mode: first item of each sequence, [S + 1]
   const int* sstart;      // suffix mode: each sequence's first own token (nullptr: look it up)
   int num_items;
