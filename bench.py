@@ -75,6 +75,7 @@ def parse():
                              "llama70b_short", "llama70b_short_fp8",
                              "shared_x16", "shared_x16_cascade", "shared_x32", "shared_x32_cascade",
                              "llama8b_nhd", "llama8b_fp8_nhd", "long70b_b16_nhd", "shared_cascade_nhd",
+                             "llama8b_s2048", "llama8b_s2048_fp8",
                              "copy_blocks", "swap_out", "swap_in", "reshape", "reshape_prefill"],
                     help="the other workload shapes give a device-timed line of their own (no e2e / CPU legs); "
                          "a _nhd suffix stores the pools NHD")
@@ -787,6 +788,8 @@ def build_workload(name, dev):
         wl.new_key, wl.new_value = wl.new_key[:wl.S].contiguous(), wl.new_value[:wl.S].contiguous()
     elif base in ("llama8b", "llama8b_fp8"):
         wl = workloads.llama8b(device=dev)
+    elif base in ("llama8b_s2048", "llama8b_s2048_fp8"):  # the same shape and lengths, 2,048 sequences
+        wl = workloads.llama8b(device=dev, S=2048, num_blocks=320_000)
     elif base in ("llama70b_short", "llama70b_short_fp8"):
         wl = workloads.llama70b_short(device=dev)
     elif base == "gemma_d256":
