@@ -217,7 +217,7 @@ __host__ __device__ inline SmemLayout make_layout(int W, int R, int D, int esize
   if (!split && !suffix) off += W * merge_heads(group, path) * D * 4 + W * kMaxGroup * 2 * 4;
   L.q_off = off;
   if (path == kPathVec) off += W * group * D * 4;            // fp32 q rows per warp
-  if (path == kPathVecMha) off += round_up(W * 2 * D * qsize, 16);  // double-buffered raw q row per warp
+  if (path == kPathVecMha) off += round_up(W * D * qsize, 16);  // raw q row per warp
   L.wts_off = off;
   if (!is_mma_path(path)) off += W * kJobTokens * 4;          // vector paths: one job's weights per warp
   L.sched_off = off;
@@ -545,7 +545,7 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH, MODE>::W * 32, StageCfg<
   float* mrg_o = reinterpret_cast<float*>(smem + L.merge_off);        // [W][MH][D] (plain mode)
   float* mrg_ml = mrg_o + W * MH * D;                                  // [W][kMaxGroup][2]
   float* qs_all = reinterpret_cast<float*>(smem + L.q_off);            // [W][group][D] (vector path)
-  uint8_t* qraw_all = smem + L.q_off;                                  // [W][2][D] raw (MHA path)
+  uint8_t* qraw_all = smem + L.q_off;                                  // [W][D] raw (MHA path)
   float* wts_all = reinterpret_cast<float*>(smem + L.wts_off);         // [W][JT] (vector paths)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc_off);
 
@@ -1310,32 +1310,32 @@ __global__ void __launch_bounds__(StageCfg<DT, D, PATH, MODE>::W * 32, StageCfg<
     constexpr int QE = (int)sizeof(QT);
     constexpr int QCH = D * QE / 16;         // 16-byte chunks of one q row
     float* qs = qs_all + warp * p.group * D;
-    uint8_t* qraw = qraw_all + warp * 2 * D * QE;
+    uint8_t* qraw = qraw_all + warp * D * QE;
     const int t = lane % JT, part = lane / JT;
     float qreg[MHA ? CPL * EPC : 1];  // MHA: this lane's half of the q row
-    auto fetch_q_raw = [&](const Item& x, int buf) {  // MHA: next q row -> shared memory, async
+    // MHA: an item's q row -> shared memory, async. One buffer a warp: the row is
+    // read into registers (qreg) before the next item's row is fetched into it.
+    auto fetch_q_raw = [&](const Item& x) {
       const uint8_t* src = reinterpret_cast<const uint8_t*>(p.q) + ((long long)x.s * p.H + x.kv) * D * QE;
-      for (int c = lane; c < QCH; c += 32) cp_async16(qraw + buf * D * QE + c * 16, src + c * 16);
+      for (int c = lane; c < QCH; c += 32) cp_async16(qraw + c * 16, src + c * 16);
       cp_async_commit();
     };
-    int qbuf = 0;
     if constexpr (MHA) {
-      if (sch.get(p, 0, warp, it)) fetch_q_raw(it, 0);
+      if (sch.get(p, 0, warp, it)) fetch_q_raw(it);
     }
 #pragma unroll 1
     for (int k = 0; sch.get(p, k, warp, it); ++k) {
       if constexpr (MHA) {
         cp_async_wait_all();
         __syncwarp();
-        const QT* qr = reinterpret_cast<const QT*>(qraw + qbuf * D * QE);
+        const QT* qr = reinterpret_cast<const QT*>(qraw);
 #pragma unroll
         for (int c = 0; c < CPL; ++c)
 #pragma unroll
           for (int e = 0; e < EPC; ++e) qreg[c * EPC + e] = to_f32(qr[(part * CPL + c) * EPC + e]);
-        __syncwarp();
+        __syncwarp();  // every lane has its part of the row before the next one lands
         Item nx;
-        if (sch.get(p, k + 1, warp, nx)) fetch_q_raw(nx, qbuf ^ 1);
-        qbuf ^= 1;
+        if (sch.get(p, k + 1, warp, nx)) fetch_q_raw(nx);
       } else {
         const QT* qrow = reinterpret_cast<const QT*>(p.q) + ((long long)it.s * p.H + it.kv * p.group) * D;
         for (int i = lane; i < p.group * D; i += 32) qs[i] = to_f32(qrow[i]);
