@@ -381,6 +381,21 @@ def test_one_long_sequence_plain(pa, cuda_device):
     _no_device_errors(pa)
 
 
+def test_mha_split_at_the_batch_limit(pa, cuda_device):
+    """MHA split decode at 2,048 sequences, the largest batch split mode takes
+    (the tensor-core path at group 1, its per-sequence schedule in shared
+    memory): every sequence against the oracle, several partitions each, the
+    output filled with NaN first."""
+    S = 2048
+    ctx = [int(x) for x in torch.randint(1, 160, (S,), generator=torch.Generator().manual_seed(9))]
+    nb = sum(-(-c // 16) for c in ctx) + 4
+    wl = workloads.batch_with_new_tokens("mha_split", S, 8, 8, 128, 16, torch.float16, ctx, nb, cuda_device)
+    ref = H.Pristine(wl).decode()
+    out = H.gpu_step(pa, wl, out_dtype=torch.float32, split=True, partition=32)
+    H.check_close(out, ref, torch.float32, "MHA split S=2048")
+    _no_device_errors(pa)
+
+
 def test_split_rejects_batches_above_its_limit(pa, cuda_device):
     S = 2049
     wl = workloads.batch_with_new_tokens("wide", S, 8, 8, 64, 16, torch.bfloat16, [3] * S, S + 2, cuda_device,

@@ -50,7 +50,7 @@ void row_suffix(const char* name, int group, int S) {
 int main() {
   for (int S : {64, 256, 752, 2048})
     for (int sp : {0, 1})
-      for (int g : {4, 8}) {
+      for (int g : {1, 4, 8}) {
         row<__nv_bfloat16, __nv_bfloat16, 128, kPathMma>("mma16_d128", g, sp, S);
         row<fp8e4m3, __nv_bfloat16, 128, kPathMma>("fp8_d128", g, sp, S);
         row<__nv_bfloat16, __nv_bfloat16, 256, kPathMma>("mma16_d256", g, sp, S);
@@ -59,7 +59,8 @@ int main() {
           row<fp8e4m3, __nv_bfloat16, 128, kPathMmaG8>("fp8g8_d128", g, sp, S);
           row<__nv_bfloat16, __nv_bfloat16, 256, kPathMmaG8>("mma16g8_d256", g, sp, S);
         }
-        row<__half, __half, 128, kPathVecMha>("mha_d128", 1, sp, S);
+        // (16-bit MHA split decode takes the tensor cores: the mma16 split rows at group 1)
+        if (!sp) row<__half, __half, 128, kPathVecMha>("mha_d128", 1, sp, S);
         row<__nv_bfloat16, __nv_bfloat16, 256, kPathVec>("vec_d256", 2, sp, S);
       }
   for (int S : {512, 1024, 2048}) {
@@ -118,8 +119,7 @@ HOLDS = [
     (("fp8_d128", 4, 0, 2048), 3),    # (the order of its own items only, not the batch's)
     (("fp8_d128", 8, 1, 2048), 3),    # E4M3 split decode
     (("mha_d128", 1, 0, 2048), 3),    # OPT-13B-shaped MHA
-    (("mha_d128", 1, 1, 256), 3),
-    (("mha_d128", 1, 1, 2048), 3),    # (one raw q row per warp: the split schedule still fits)
+    (("mma16_d128", 1, 1, 2048), 2),  # 16-bit MHA split decode (the tensor-core path at group 1)
     (("mma16_d256", 4, 0, 2048), 2),  # head_dim 256: one stage per warp, two CTAs
     (("mma16g8_d128", 8, 0, 256), 2),  # plain decode at group 8 (64 q / 8 kv heads): merge rounds
     (("mma16g8_d128", 8, 0, 2048), 2),
